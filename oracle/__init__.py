@@ -1,0 +1,138 @@
+"""fp64 CPU oracle for the bidirectional selective scan -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The product path (the CUDA library and
+its binding) never imports, links or runs anything here, and this package
+shares no code with it: the only module both sides use is ``workloads`` (seeded
+input generation, no scan arithmetic).
+
+Contents:
+  * ``vssm_oracle.c`` -- the recurrence written out in plain C, fp64, OpenMP
+    over (batch, channel) rows. See its header for the equations and the pages
+    they follow.
+  * ``quadform.py`` -- the SSD page's quadratic (matrix) form, NumPy, used only
+    to pin the recurrence on tiny inputs.
+  * ``scan()`` below -- ctypes binding of the C oracle.
+
+Pins (in ``tests/test_oracle_pins.py``): the quadratic form, a hand-worked
+two-step example from the SSD page's linear-form section, closed forms for
+A = 0 (prefix sum), vanishing decay, Δ = 0 and C = 0, L = 1, the
+backward-equals-flipped-forward invariant, folded-equals-per-segment, the
+silu gate against scipy's logistic function, linearity in x, and a mutation
+test that plants mistakes in a copy of the C source.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "vssm_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+DIR_FWD, DIR_BWD, DIR_BOTH = 1, 2, 3
+
+
+def compile_c(src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the C oracle (or a copy of it) into a shared library."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+           "-o", out, src, "-lm"]
+    subprocess.run(cmd, check=True, capture_output=True)
+    return out
+
+
+def build(force: bool = False) -> str:
+    if force or not os.path.exists(_LIB_PATH) or (
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+        compile_c()
+    return _LIB_PATH
+
+
+def load_library(path: str):
+    lib = ctypes.CDLL(path)
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib.oracle_scan.restype = ctypes.c_int
+    lib.oracle_scan.argtypes = [dp] * 12 + [ctypes.c_long] * 4 + [
+        ctypes.c_int, ctypes.c_long, ctypes.c_int]
+    lib.oracle_max_threads.restype = ctypes.c_int
+    return lib
+
+
+def _get_lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = load_library(build())
+    return _lib
+
+
+def max_threads() -> int:
+    return int(_get_lib().oracle_max_threads())
+
+
+def _as_f64(a):
+    if a is None:
+        return None, None
+    arr = np.ascontiguousarray(a, dtype=np.float64)
+    return arr, arr.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def scan(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None,
+         B_bwd=None, C_bwd=None, dirs: int = DIR_BOTH, seg_len: int = 0,
+         nthreads: int = 0, lib=None) -> np.ndarray:
+    """Run the fp64 oracle. Arrays may be any float dtype; they are widened to
+    float64 exactly. Shapes: x, delta, z (batch, dim, L); B, C (batch, L, N);
+    A (dim, N); D (dim,). Returns out (batch, dim, L) float64."""
+    lib = lib or _get_lib()
+    x = np.asarray(x)
+    batch, dim, L = x.shape
+    N = np.asarray(B).shape[-1]
+    if A_fwd is None and A_bwd is None:
+        raise ValueError("need A for the selected direction(s)")
+    keep = []
+    ptrs = []
+    for a in (x, delta, z, B, C, B_bwd, C_bwd, A_fwd, A_bwd, D_fwd, D_bwd):
+        arr, p = _as_f64(a)
+        keep.append(arr)
+        ptrs.append(p)
+    out = np.empty((batch, dim, L), dtype=np.float64)
+    pout = out.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+    rc = lib.oracle_scan(*ptrs, pout, batch, dim, L, N, int(dirs), int(seg_len),
+                         int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_scan rejected its arguments (status {rc})")
+    return out
+
+
+def scan_inputs(inp, dirs: Optional[int] = None, seg_len: Optional[int] = None,
+                nthreads: int = 0) -> np.ndarray:
+    """Oracle on a ``workloads.Inputs`` set (its exact, possibly bf16-rounded
+    values)."""
+    wl = inp.wl
+    return scan(inp.x, inp.delta, inp.A_fwd, inp.A_bwd, inp.B, inp.C,
+                inp.D_fwd, inp.D_bwd, inp.z,
+                dirs=wl.dirs if dirs is None else dirs,
+                seg_len=wl.seg_len if seg_len is None else seg_len,
+                nthreads=nthreads)
+
+
+def scan_rows(inp, rows, nthreads: int = 0) -> np.ndarray:
+    """Oracle outputs of selected (b, d) rows only: returns (len(rows), L)."""
+    wl = inp.wl
+    out = np.empty((len(rows), wl.seqlen), dtype=np.float64)
+    for i, (b, d) in enumerate(rows):
+        sl = (slice(b, b + 1), slice(d, d + 1))
+        out[i] = scan(inp.x[sl], inp.delta[sl], inp.A_fwd[d:d + 1], inp.A_bwd[d:d + 1],
+                      inp.B[b:b + 1], inp.C[b:b + 1], inp.D_fwd[d:d + 1],
+                      inp.D_bwd[d:d + 1], inp.z[sl], dirs=wl.dirs,
+                      seg_len=wl.seg_len, nthreads=nthreads)[0, 0]
+    return out

@@ -1,0 +1,152 @@
+/*
+ * fp64 CPU oracle for the bidirectional selective scan (S6) -- TEST
+ * INFRASTRUCTURE ONLY. Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg may load this. It shares no code with the CUDA path.
+ *
+ * What it computes, for every batch b and channel d (one "row"), written as
+ * the plain definition with no blocking, fusion or reordering:
+ *
+ *   Discretisation (VSSD page, §4.1.2 "连续→离散化"): the decay is
+ *     Abar_t = exp(delta_t * A[d][n]) and the input matrix is taken in its
+ *     first-order form Bbar_t ≈ delta_t * B_t (the page's "≈ΔB").
+ *   Recurrence (VSSD page, §4.2.1.3 "SSD的线性形式"):
+ *     h_t = Abar_t * h_{t-1} + delta_t * B_t * x_t,   h_{-1} = 0
+ *     y_t = sum_n C_t[n] * h_t[n] + D[d] * x_t
+ *   Backward direction (Vim page, §2.2 "双向状态空间建模": the backward path
+ *     runs along the reversed order): the same recurrence walked from
+ *     t = L-1 down to 0 with its own A and D, h_L = 0.
+ *   Combination: y = y_fwd + y_bwd (each direction adds its own D-skip),
+ *     then gated: out_t = y_t * silu(z_t), silu(z) = z / (1 + exp(-z)).
+ *   Batch folding with periodic state reset (SF-Mamba page, "批量折叠与周期性
+ *     状态重置"): on a folded sequence of segments of seg_len tokens the
+ *     discrete decay is set to 0 at every segment start, i.e. at
+ *     t mod seg_len == 0 going forward; going backward the segment start is
+ *     t mod seg_len == seg_len - 1. There h_t = delta_t * B_t * x_t.
+ *
+ * No hidden state is returned (SF-Mamba page, "实现优化": hidden-state output
+ * suppressed at inference).
+ *
+ * Layouts (row-major, last index fastest): x, delta, z, out: [batch][dim][L];
+ * B, C (and B_bwd, C_bwd): [batch][L][N]; A: [dim][N]; D: [dim].
+ */
+#include <math.h>
+#include <stdlib.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL (-1)
+#define ORACLE_ENOMEM (-2)
+
+int oracle_version(void) { return 1; }
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* One direction over one row. `rev` = 0 walks t upward, 1 walks downward.
+ * Adds y_t into acc[t]. */
+static void scan_row_direction(const double *xr, const double *dtr,
+                               const double *Bb, const double *Cb,
+                               const double *Ad, double Dd,
+                               long L, long N, int rev, long seg_len,
+                               double *h, double *acc)
+{
+    for (long n = 0; n < N; ++n) h[n] = 0.0;
+    for (long k = 0; k < L; ++k) {
+        const long t = rev ? (L - 1 - k) : k;
+        const double dt = dtr[t];
+        const double xt = xr[t];
+        const double *Bt = Bb + t * N;
+        const double *Ct = Cb + t * N;
+        int reset = 0;
+        if (seg_len > 0)
+            reset = rev ? (t % seg_len == seg_len - 1) : (t % seg_len == 0);
+        double y = 0.0;
+        for (long n = 0; n < N; ++n) {
+            const double abar = reset ? 0.0 : exp(dt * Ad[n]);
+            h[n] = abar * h[n] + dt * Bt[n] * xt;
+            y += Ct[n] * h[n];
+        }
+        acc[t] += y + Dd * xt;
+    }
+}
+
+/*
+ * dirs: bit 0 = forward, bit 1 = backward (at least one set).
+ * seg_len: 0 = plain sequences; > 0 = folded with reset every seg_len tokens
+ *          (with the backward bit set, L must be a multiple of seg_len).
+ * z, D_fwd, D_bwd may be NULL (no gate / zero skip). B_bwd, C_bwd may be NULL
+ * (backward shares B, C). nthreads <= 0 uses the OpenMP default.
+ */
+int oracle_scan(const double *x, const double *delta, const double *z,
+                const double *B, const double *C,
+                const double *B_bwd, const double *C_bwd,
+                const double *A_fwd, const double *A_bwd,
+                const double *D_fwd, const double *D_bwd,
+                double *out,
+                long batch, long dim, long L, long N,
+                int dirs, long seg_len, int nthreads)
+{
+    if (!x || !delta || !B || !C || !out) return ORACLE_EINVAL;
+    if (batch < 0 || dim < 0 || L < 0 || N <= 0) return ORACLE_EINVAL;
+    if (dirs < 1 || dirs > 3) return ORACLE_EINVAL;
+    if ((dirs & 1) && !A_fwd) return ORACLE_EINVAL;
+    if ((dirs & 2) && !A_bwd) return ORACLE_EINVAL;
+    if (seg_len < 0) return ORACLE_EINVAL;
+    if (seg_len > 0 && (dirs & 2) && L % seg_len != 0) return ORACLE_EINVAL;
+    if (!B_bwd) B_bwd = B;
+    if (!C_bwd) C_bwd = C;
+
+    const long rows = batch * dim;
+    int err = ORACLE_OK;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        double *h = (double *)malloc(sizeof(double) * (size_t)N);
+        double *acc = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        if (!h || !acc) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            err = ORACLE_ENOMEM;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 4)
+#endif
+            for (long r = 0; r < rows; ++r) {
+                const long b = r / dim, d = r % dim;
+                const double *xr = x + r * L;
+                const double *dtr = delta + r * L;
+                for (long t = 0; t < L; ++t) acc[t] = 0.0;
+                if (dirs & 1)
+                    scan_row_direction(xr, dtr, B + b * L * N, C + b * L * N,
+                                       A_fwd + d * N, D_fwd ? D_fwd[d] : 0.0,
+                                       L, N, 0, seg_len, h, acc);
+                if (dirs & 2)
+                    scan_row_direction(xr, dtr, B_bwd + b * L * N, C_bwd + b * L * N,
+                                       A_bwd + d * N, D_bwd ? D_bwd[d] : 0.0,
+                                       L, N, 1, seg_len, h, acc);
+                double *outr = out + r * L;
+                for (long t = 0; t < L; ++t) {
+                    double g = 1.0;
+                    if (z) {
+                        const double zt = z[r * L + t];
+                        g = zt / (1.0 + exp(-zt));
+                    }
+                    outr[t] = acc[t] * g;
+                }
+            }
+        }
+        free(h);
+        free(acc);
+    }
+    return err;
+}

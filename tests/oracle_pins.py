@@ -1,0 +1,244 @@
+"""Pins for the fp64 oracle, written as functions of a loaded oracle library so
+that the same checks can run against deliberately broken copies of the C
+source (see test_oracle_pins.test_planted_mistakes_are_caught).
+
+Every check compares the oracle with something other than itself: a value
+worked by hand from the pages, a closed form, a second formulation (the SSD
+quadratic form), or an invariant the pages state.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+from scipy.special import expit
+
+import oracle
+from oracle import quadform
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rand_problem(rng, batch, dim, L, N, gate=True, A_scale=1.0):
+    x = rng.standard_normal((batch, dim, L))
+    delta = np.log1p(np.exp(rng.normal(-1.0, 0.5, size=(batch, dim, L))))
+    z = rng.standard_normal((batch, dim, L)) if gate else None
+    B = rng.standard_normal((batch, L, N)) / np.sqrt(N)
+    C = rng.standard_normal((batch, L, N)) / np.sqrt(N)
+    A_f = -np.exp(rng.uniform(np.log(0.5), np.log(16), size=(dim, N))) * A_scale
+    A_b = -np.exp(rng.uniform(np.log(0.5), np.log(16), size=(dim, N))) * A_scale
+    D_f = rng.standard_normal(dim)
+    D_b = rng.standard_normal(dim)
+    return dict(x=x, delta=delta, z=z, B=B, C=C, A_fwd=A_f, A_bwd=A_b,
+                D_fwd=D_f, D_bwd=D_b)
+
+
+def _run(lib, p, **kw):
+    return oracle.scan(p["x"], p["delta"], p["A_fwd"], p["A_bwd"], p["B"], p["C"],
+                       p["D_fwd"], p["D_bwd"], p["z"], lib=lib, **kw)
+
+
+def _close(a, b, tol):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    scale = max(1.0, float(np.max(np.abs(b))) if b.size else 1.0)
+    return bool(np.all(np.isfinite(a))) and float(np.max(np.abs(a - b), initial=0.0)) <= tol * scale
+
+
+def read_golden(name="ssd_linear_form_worked_example.txt"):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = line.split(":", 1)
+            vals[k.strip()] = np.array([float(t) for t in v.split()])
+    return vals
+
+
+# ---------------------------------------------------------------- the pins
+
+def pin_worked_example(lib):
+    g = read_golden()
+    x = g["x"].reshape(1, 1, -1)
+    L = x.shape[-1]
+    delta = np.ones_like(x)
+    A = np.array([[np.log(g["abar"][0])]])
+    B = np.full((1, L, 1), g["dbx_scale"][0])
+    C = np.ones((1, L, 1))
+    ok = True
+    for key, dirs, seg in (("fwd", 1, 0), ("bwd", 2, 0), ("fwd_fold2", 1, 2), ("bwd_fold2", 2, 2)):
+        out = oracle.scan(x, delta, A, A, B, C, None, None, None, dirs=dirs,
+                          seg_len=seg, lib=lib)
+        ok &= _close(out[0, 0], g[key], 1e-12)
+    return ok
+
+
+def pin_quadratic_form(lib):
+    rng = np.random.default_rng(11)
+    ok = True
+    for L, N, dirs, seg in ((1, 1, 3, 0), (5, 4, 1, 0), (7, 3, 2, 0), (17, 4, 3, 0),
+                            (12, 2, 3, 4), (13, 3, 1, 5), (40, 4, 3, 8)):
+        p = _rand_problem(rng, 2, 3, L, N)
+        got = _run(lib, p, dirs=dirs, seg_len=seg)
+        ref = quadform.scan(p["x"], p["delta"], p["A_fwd"], p["A_bwd"], p["B"], p["C"],
+                            p["D_fwd"], p["D_bwd"], p["z"], dirs=dirs, seg_len=seg)
+        ok &= _close(got, ref, 1e-12)
+    return ok
+
+
+def pin_A_zero_prefix_sum(lib):
+    """A = 0: every decay is exactly 1, so h_t is the running sum of
+    delta_s B_s x_s (a textbook prefix sum)."""
+    rng = np.random.default_rng(12)
+    p = _rand_problem(rng, 2, 3, 33, 4, gate=False)
+    p["A_fwd"] = np.zeros_like(p["A_fwd"])
+    p["A_bwd"] = np.zeros_like(p["A_bwd"])
+    got = _run(lib, p, dirs=3)
+    ref = np.empty_like(got)
+    for b in range(2):
+        for d in range(3):
+            u = (p["delta"][b, d] * p["x"][b, d])[:, None] * p["B"][b]     # (L, N)
+            hf = np.cumsum(u, axis=0)
+            hb = np.cumsum(u[::-1], axis=0)[::-1]
+            ref[b, d] = (np.sum(p["C"][b] * hf, axis=1) + np.sum(p["C"][b] * hb, axis=1)
+                         + (p["D_fwd"][d] + p["D_bwd"][d]) * p["x"][b, d])
+    return _close(got, ref, 1e-12)
+
+
+def pin_vanishing_decay(lib):
+    """Decay exactly 0 (exp underflows): h_t = delta_t B_t x_t, so
+    y_t = (C_t . B_t) delta_t x_t + D x_t in each direction."""
+    rng = np.random.default_rng(13)
+    p = _rand_problem(rng, 1, 4, 9, 4, gate=False)
+    p["A_fwd"] = np.full_like(p["A_fwd"], -1e308)
+    p["A_bwd"] = np.full_like(p["A_bwd"], -1e308)
+    got = _run(lib, p, dirs=3)
+    cb = np.sum(p["C"][0] * p["B"][0], axis=1)
+    ref = (2 * cb[None, :] * p["delta"][0] * p["x"][0]
+           + (p["D_fwd"] + p["D_bwd"])[:, None] * p["x"][0])
+    return _close(got[0], ref, 1e-12)
+
+
+def pin_zero_input_paths(lib):
+    """delta = 0 or C = 0 leaves only the skip: out = (D_f + D_b) x silu(z)."""
+    rng = np.random.default_rng(14)
+    ok = True
+    for which in ("delta", "C"):
+        p = _rand_problem(rng, 2, 3, 10, 4)
+        p[which] = np.zeros_like(p[which])
+        got = _run(lib, p, dirs=3)
+        ref = ((p["D_fwd"] + p["D_bwd"])[None, :, None] * p["x"]
+               * p["z"] * expit(p["z"]))
+        ok &= _close(got, ref, 1e-12)
+    return ok
+
+
+def pin_single_token(lib):
+    """L = 1: y = (C . B) delta x + D x per direction (no history)."""
+    rng = np.random.default_rng(15)
+    p = _rand_problem(rng, 3, 5, 1, 4, gate=False)
+    got = _run(lib, p, dirs=3)
+    cb = np.sum(p["C"][:, 0, :] * p["B"][:, 0, :], axis=1)          # (batch,)
+    ref = (2 * cb[:, None, None] * p["delta"] * p["x"]
+           + (p["D_fwd"] + p["D_bwd"])[None, :, None] * p["x"])
+    return _close(got, ref, 1e-12)
+
+
+def pin_backward_is_flipped_forward(lib):
+    """Vim page §2.2: the backward path is the forward scan of the reversed
+    sequence (with the backward A, D)."""
+    rng = np.random.default_rng(16)
+    p = _rand_problem(rng, 2, 3, 23, 4)
+    bwd = _run(lib, p, dirs=2)
+    q = dict(p)
+    for k in ("x", "delta", "z"):
+        q[k] = p[k][:, :, ::-1]
+    for k in ("B", "C"):
+        q[k] = p[k][:, ::-1, :]
+    q["A_fwd"], q["D_fwd"] = p["A_bwd"], p["D_bwd"]
+    fwd_of_flip = _run(lib, q, dirs=1)
+    return _close(bwd, fwd_of_flip[:, :, ::-1], 1e-13)
+
+
+def pin_folded_equals_segments(lib):
+    """SF-Mamba page: the folded output equals the unfolded output. Fold B2
+    sequences of T tokens into one row with a reset every T tokens."""
+    rng = np.random.default_rng(17)
+    ok = True
+    T, B2, dim, N = 6, 5, 3, 4
+    p = _rand_problem(rng, B2, dim, T, N)           # B2 independent sequences
+    for dirs in (1, 2, 3):
+        ref = _run(lib, p, dirs=dirs)                # (B2, dim, T)
+        f = {}
+        for k in ("x", "delta", "z"):                # (1, dim, B2*T)
+            f[k] = p[k].transpose(1, 0, 2).reshape(1, dim, B2 * T)
+        for k in ("B", "C"):                         # (1, B2*T, N)
+            f[k] = p[k].reshape(1, B2 * T, N)
+        for k in ("A_fwd", "A_bwd", "D_fwd", "D_bwd"):
+            f[k] = p[k]
+        got = _run(lib, f, dirs=dirs, seg_len=T)
+        ok &= _close(got.reshape(dim, B2, T).transpose(1, 0, 2), ref, 1e-13)
+    return ok
+
+
+def pin_reset_first_token(lib):
+    """A reset at t = 0 of every segment gives h_t = delta_t B_t x_t there."""
+    rng = np.random.default_rng(18)
+    p = _rand_problem(rng, 1, 2, 12, 4, gate=False)
+    p["D_fwd"] = np.zeros_like(p["D_fwd"])
+    got = _run(lib, p, dirs=1, seg_len=4)
+    ok = True
+    for t in (0, 4, 8):
+        cb = np.sum(p["C"][0, t] * p["B"][0, t])
+        ok &= _close(got[0, :, t], cb * p["delta"][0, :, t] * p["x"][0, :, t], 1e-13)
+    return ok
+
+
+def pin_gate(lib):
+    """out = y * z * sigmoid(z): compare to the ungated run times scipy's
+    logistic function; z = 0 gives exactly 0."""
+    rng = np.random.default_rng(19)
+    p = _rand_problem(rng, 2, 3, 8, 4)
+    gated = _run(lib, p, dirs=3)
+    q = dict(p)
+    q["z"] = None
+    plain = _run(lib, q, dirs=3)
+    ok = _close(gated, plain * p["z"] * expit(p["z"]), 1e-13)
+    q["z"] = np.zeros_like(p["z"])
+    ok &= bool(np.all(_run(lib, q, dirs=3) == 0.0))
+    return ok
+
+
+def pin_linearity(lib):
+    """For fixed delta, B, C, z the scan is linear in x."""
+    rng = np.random.default_rng(20)
+    p = _rand_problem(rng, 2, 3, 15, 4)
+    x1, x2 = p["x"], rng.standard_normal(p["x"].shape)
+    a, b = 0.7, -1.3
+    q = dict(p)
+    y1 = _run(lib, p, dirs=3)
+    q["x"] = x2
+    y2 = _run(lib, q, dirs=3)
+    q["x"] = a * x1 + b * x2
+    y3 = _run(lib, q, dirs=3)
+    return _close(y3, a * y1 + b * y2, 1e-12)
+
+
+PINS = [pin_worked_example, pin_quadratic_form, pin_A_zero_prefix_sum,
+        pin_vanishing_decay, pin_zero_input_paths, pin_single_token,
+        pin_backward_is_flipped_forward, pin_folded_equals_segments,
+        pin_reset_first_token, pin_gate, pin_linearity]
+
+
+def failing_pins(lib):
+    failed = []
+    for pin in PINS:
+        try:
+            ok = pin(lib)
+        except Exception:  # a crash or a rejected call counts as a failure
+            ok = False
+        if not ok:
+            failed.append(pin.__name__)
+    return failed

@@ -1,0 +1,83 @@
+"""The fp64 oracle against its pins (CPU only)."""
+import os
+import shutil
+import tempfile
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle_pins as P
+from workloads import WORKLOADS, make_inputs
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return oracle.load_library(oracle.build())
+
+
+@pytest.mark.parametrize("pin", P.PINS, ids=lambda f: f.__name__)
+def test_pin(lib, pin):
+    assert pin(lib)
+
+
+# Plausible mistakes, each planted in a copy of the C source. Every one must
+# make at least one pin fail, which shows the pins can tell them apart from
+# the correct recurrence.
+MUTANTS = {
+    "dropped_D_skip": ("acc[t] += y + Dd * xt;", "acc[t] += y;"),
+    "exp_sign": ("exp(dt * Ad[n])", "exp(-dt * Ad[n])"),
+    "B_C_swapped": ("dt * Bt[n] * xt", "dt * Ct[n] * xt"),
+    "dropped_delta_in_input": ("dt * Bt[n] * xt", "Bt[n] * xt"),
+    "output_before_update": (
+        "h[n] = abar * h[n] + dt * Bt[n] * xt;\n            y += Ct[n] * h[n];",
+        "y += Ct[n] * h[n];\n            h[n] = abar * h[n] + dt * Bt[n] * xt;"),
+    "backward_not_reversed": ("rev ? (L - 1 - k) : k", "k"),
+    "fwd_reset_off_by_one": ("(t % seg_len == 0)", "(t % seg_len == 1)"),
+    "bwd_reset_at_fwd_start": ("(t % seg_len == seg_len - 1)", "(t % seg_len == 0)"),
+    "gate_sign": ("zt / (1.0 + exp(-zt))", "zt / (1.0 + exp(zt))"),
+    "bwd_uses_fwd_A": ("A_bwd + d * N", "A_fwd + d * N"),
+    "state_not_reset_between_rows": ("for (long n = 0; n < N; ++n) h[n] = 0.0;", ""),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistakes_are_caught(name):
+    old, new = MUTANTS[name]
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "vssm_oracle.c")).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    tmp = tempfile.mkdtemp(prefix="oracle_mutant_")
+    try:
+        path = os.path.join(tmp, "mutant.c")
+        with open(path, "w") as f:
+            f.write(src.replace(old, new))
+        lib = oracle.load_library(oracle.compile_c(path, os.path.join(tmp, "libmutant.so")))
+        assert P.failing_pins(lib), f"no pin caught the planted mistake {name}"
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
+
+
+def test_thread_count_does_not_change_results(lib):
+    inp = make_inputs(WORKLOADS["vim_ti_224"], seed=3)
+    a = oracle.scan_inputs(inp, nthreads=1)
+    b = oracle.scan_inputs(inp, nthreads=4)
+    assert np.array_equal(a, b)
+
+
+def test_rejects_bad_arguments(lib):
+    x = np.zeros((1, 1, 6))
+    A = -np.ones((1, 2))
+    B = np.zeros((1, 6, 2))
+    with pytest.raises(ValueError):   # backward folded needs L % seg_len == 0
+        oracle.scan(x, x, A, A, B, B, dirs=3, seg_len=4)
+    with pytest.raises(ValueError):
+        oracle.scan(x, x, A, A, B, B, dirs=0)
+
+
+def test_scan_rows_matches_full(lib):
+    inp = make_inputs(WORKLOADS["vim_ti_224"].scaled(batch=2, dim=8, seqlen=19), seed=5)
+    full = oracle.scan_inputs(inp)
+    rows = [(0, 3), (1, 7), (1, 0)]
+    sub = oracle.scan_rows(inp, rows)
+    for i, (b, d) in enumerate(rows):
+        assert np.array_equal(sub[i], full[b, d])
