@@ -1,0 +1,467 @@
+#!/usr/bin/env python
+"""Benchmark: bidirectional selective scan on one B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one scan of the whole workload (default vim_s_224: Vim-S at 224^2,
+batch 128, 197 tokens, 768 channels, 16 states, bf16 I/O, both directions,
+silu gate). Prints ONE JSON line (rank 0). ``value`` is algorithmic GB/s of
+the whole job (inputs resident in HBM); ``e2e`` is the same metric with the
+host<->device copies of every step's inputs and output inside the timed
+region; ``roofline`` relates the scan kernel to the bound that limits it.
+
+Under torchrun (N > 1) every rank scans its own full workload (weak scaling,
+no collective on the data path: rows are independent); the timed region is
+bracketed by barriers and the slowest rank's time is used.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead
+(a bounded sample of the same workload per step).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import (DIR_BOTH, DIR_BWD, DIR_FWD, ORDER, WORKLOADS,  # noqa: E402
+                       algorithmic_bytes, exp_count, make_inputs)
+
+METRIC = "bidir selective-scan GB/s and Gtoken·ch/s, % of HBM roofline, 1×B300"
+L2_BYTES = 126 * 1024 * 1024
+SMS = 148
+MAX_SM_MHZ = 2032.0
+EX2_PER_CLK_SM = 32        # MUFU ex2.approx.f32 per clock per SM, measured on B300
+FMA_PER_CLK_SM = 128       # fp32 FMA-pipe lane operations per clock per SM
+FALLBACK_HBM_GBS = 6400.0
+SPEC_HBM_GBS = 8000.0
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--workload", default="vim_s_224", choices=ORDER)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target CPU time of the oracle sample")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def dist_init(backend):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def reduce_max(value: float) -> float:
+    """Max of a float over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput under weak scaling: all ranks' units / slowest time."""
+    return units_per_rank * world / max_seconds
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler(threading.Thread):
+    """Samples the SM clock and the clock-event reasons through NVML."""
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, uuid: str, period_s: float = 0.004):
+        super().__init__(daemon=True)
+        self.samples = []
+        self.period = period_s
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as e:  # report, never fake
+            self.err = repr(e)
+
+    def sample(self):
+        nv = self.nv
+        try:
+            reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+        except AttributeError:
+            reasons = nv.nvmlDeviceGetCurrentClocksThrottleReasons(self.h)
+        self.samples.append((nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM), int(reasons)))
+
+    def run(self):
+        while not self._stop.is_set():
+            self.sample()
+            time.sleep(self.period)
+
+    def stop(self):
+        self._stop.set()
+        self.join(timeout=2)
+
+    def summary(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": self.err}
+        mhz = [m for m, _ in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        names = [n for b, n in self.REASONS.items() if bits & b and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": self.max_mhz, "reasons": names, "samples": len(mhz)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def source_sha() -> str:
+    csrc = os.path.join(ROOT, "bidirectional_selective_scan_vssm_b300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    path = os.path.join(PROFILES, "ncu_dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("source_sha") != source_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+
+def oracle_sample_run(wl, inp, target_s):
+    """Time the fp64 oracle (as it stands) on a slice of the workload sized to
+    about target_s seconds. Returns (tokch, seconds, threads, description)."""
+    import oracle
+    threads = oracle.max_threads()
+
+    def slice_inputs(nb, nd):
+        s = (slice(0, nb), slice(0, nd))
+        return dict(x=np.asarray(inp.x[s], np.float64), delta=np.asarray(inp.delta[s], np.float64),
+                    z=np.asarray(inp.z[s], np.float64), B=np.asarray(inp.B[:nb], np.float64),
+                    C=np.asarray(inp.C[:nb], np.float64), A_fwd=inp.A_fwd[:nd].astype(np.float64),
+                    A_bwd=inp.A_bwd[:nd].astype(np.float64), D_fwd=inp.D_fwd[:nd].astype(np.float64),
+                    D_bwd=inp.D_bwd[:nd].astype(np.float64))
+
+    def run(a):
+        t0 = time.perf_counter()
+        oracle.scan(a["x"], a["delta"], a["A_fwd"], a["A_bwd"], a["B"], a["C"], a["D_fwd"],
+                    a["D_bwd"], a["z"], dirs=wl.dirs, seg_len=wl.seg_len)
+        return time.perf_counter() - t0
+
+    # calibrate on a few channels of one batch entry
+    nd0 = min(wl.dim, max(threads, 16))
+    t_cal = run(slice_inputs(1, nd0))
+    per_row = t_cal / nd0
+    rows = max(1, int(target_s / max(per_row, 1e-9)))
+    nb = min(wl.batch, max(1, rows // wl.dim))
+    nd = wl.dim if nb > 1 or rows >= wl.dim else min(wl.dim, rows)
+    a = slice_inputs(nb, nd)
+    secs = run(a)
+    desc = (f"{nb} of {wl.batch} batch entries x {nd} of {wl.dim} channels x {wl.seqlen} tokens "
+            f"({nb * nd * wl.seqlen} token-channels), fp64, {threads} OpenMP threads")
+    return nb * nd * wl.seqlen, secs, threads, desc
+
+
+def run_reference(args):
+    rank, world = dist_init("gloo")
+    if rank != 0:
+        return
+    wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl, seed=0)
+    per_step = min(10.0, max(0.2, 150.0 / max(1, args.steps + args.warmup)))
+    bpt = algorithmic_bytes(wl) / wl.tokch
+    for _ in range(args.warmup):
+        oracle_sample_run(wl, inp, per_step)
+    tot_tok, tot_s, desc, threads = 0, 0.0, "", 0
+    for _ in range(args.steps):
+        tok, s, threads, desc = oracle_sample_run(wl, inp, per_step)
+        tot_tok += tok
+        tot_s += s
+    gbs = tot_tok * bpt / tot_s / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot_s / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(wl, "n/a (CPU)"),
+        "gtokch_per_s": round(tot_tok / tot_s / 1e9, 6),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": desc + " per step", "cpu": cpu_model()},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(wl, l2_note):
+    return {"workload": wl.name, "batch": wl.batch, "seqlen": wl.seqlen, "dim": wl.dim,
+            "dstate": wl.dstate, "io_dtype": wl.dtype,
+            "dirs": {DIR_FWD: "fwd", DIR_BWD: "bwd", DIR_BOTH: "both"}[wl.dirs],
+            "seg_len": wl.seg_len or None, "gate": "silu(z)", "l2": l2_note,
+            "description": wl.description}
+
+
+# ------------------------------------------------------------------ GPU leg
+
+def run_ours(args):
+    import torch
+    import bidirectional_selective_scan_vssm_b300 as vssm
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU path)")
+    torch.cuda.set_device(local)
+    dist_init("nccl")
+    dev = torch.device("cuda", local)
+    wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl, seed=rank)
+    set_bytes = algorithmic_bytes(wl)
+
+    def upload(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    base = {k: upload(inp.storage(k)) for k in ("x", "delta", "z", "B", "C")}
+    for k in ("A_fwd", "A_bwd", "D_fwd", "D_bwd"):
+        base[k] = torch.from_numpy(getattr(inp, k)).to(dev)
+    nsets = int(min(64, max(2, math.ceil(3 * L2_BYTES / set_bytes))))
+    sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(nsets - 1)]
+    outs = [torch.empty_like(base["x"]) for _ in range(nsets)]
+    total = nsets * set_bytes
+    l2_note = (f"{nsets} rotating input/output sets, {total / 2**20:.0f} MiB "
+               f"{'>' if total > L2_BYTES else '<='} 126 MiB L2")
+
+    stream = torch.cuda.current_stream(dev)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    seg = wl.seg_len
+    fn = vssm.lib.vssm_scan_folded if seg else vssm.lib.vssm_scan_bidir
+    argsets = []
+    ws = None
+    for s, o in zip(sets, outs):
+        a = vssm.make_args(s["x"], s["delta"], s["A_fwd"], s["A_bwd"], s["B"], s["C"],
+                           s["D_fwd"], s["D_bwd"], s["z"], o, dirs=wl.dirs)
+        need = vssm.workspace_size(a, seg)
+        if need and ws is None:
+            ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        if need:
+            a.workspace, a.workspace_bytes = ws.data_ptr(), need
+        argsets.append(a)
+
+    def launch(i):
+        a = ctypes.byref(argsets[i % nsets])
+        st = fn(a, seg, sptr) if seg else fn(a, sptr)
+        if st != 0:
+            raise RuntimeError(vssm.lib.vssm_last_error().decode())
+
+    for i in range(args.warmup):
+        launch(i)
+    torch.cuda.synchronize()
+
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(str(torch.cuda.get_device_properties(dev).uuid)
+                           if str(torch.cuda.get_device_properties(dev).uuid).startswith("GPU-")
+                           else "GPU-" + str(torch.cuda.get_device_properties(dev).uuid))
+    barrier()
+    torch.cuda.synchronize()
+    if sampler.ok:
+        sampler.sample()
+        sampler.start()
+    start.record(stream)
+    for i in range(args.steps):
+        ev_b[i].record(stream)
+        launch(i)
+        ev_e[i].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    if sampler.ok:
+        sampler.stop()
+    region_s = reduce_max(start.elapsed_time(end) / 1e3)
+    kern_ms = [b.elapsed_time(e) for b, e in zip(ev_b, ev_e)]
+    kern_avg_s = statistics.fmean(kern_ms) / 1e3
+
+    gbs = aggregate(set_bytes * args.steps, world, region_s) / 1e9
+    gtok = aggregate(wl.tokch * args.steps, world, region_s) / 1e9
+    peaks, peaks_kind = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    clocks = sampler.summary()
+
+    # Roofline of the scan kernel: the exp unit and the fp32 FMA pipe both
+    # allow 32 state updates per clock per SM (1 ex2 + 4 fp32 ops each).
+    upd = exp_count(wl)
+    ach = upd / kern_avg_s / 1e9
+    peak_upd = EX2_PER_CLK_SM * SMS * MAX_SM_MHZ * 1e6 / 1e9
+    kern_gbs = set_bytes / kern_avg_s / 1e9
+    med = clocks.get("sm_mhz")
+    roofline = {
+        "bound": "alu", "achieved": round(ach, 2), "peak": round(peak_upd, 2),
+        "unit": "Gupdate/s", "frac": round(ach / peak_upd, 4),
+        "traffic": ncu_traffic(wl.name),
+        "update": "one (token, channel, state, direction) recurrence step: 1 MUFU ex2 + 4 fp32 FMA-pipe ops",
+        "peak_basis": f"{EX2_PER_CLK_SM} ex2/clk/SM (and {FMA_PER_CLK_SM}/4 FMA-pipe updates/clk/SM) "
+                      f"x {SMS} SMs x {MAX_SM_MHZ:.0f} MHz max SM clock",
+        "frac_at_median_clock": round(ach / (peak_upd * med / MAX_SM_MHZ), 4) if med else None,
+        "kernel_avg_us": round(kern_avg_s * 1e6, 3),
+        "kernel_hbm_gbs": round(kern_gbs, 1),
+        "hbm_frac": round(kern_gbs / hbm_peak, 4),
+        "hbm_peak_gbs": hbm_peak, "hbm_peak_kind": peaks_kind,
+        "hbm_frac_spec_8tbs": round(kern_gbs / SPEC_HBM_GBS, 4),
+        "algorithmic_bytes_per_launch": set_bytes,
+    }
+
+    # ---- end to end through the public API: pinned host -> device, scan, -> host
+    e2e = None
+    if args.e2e_steps > 0:
+        host = {k: v.cpu().pin_memory() for k, v in base.items()}
+        dst = {k: torch.empty_like(v) for k, v in base.items()}
+        out_h = torch.empty(base["x"].shape, dtype=base["x"].dtype).pin_memory()
+        out_d = torch.empty_like(base["x"])
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = out_h.numel() * out_h.element_size()
+
+        def e2e_step():
+            for k in host:
+                dst[k].copy_(host[k], non_blocking=True)
+            kw = dict(D_fwd=dst["D_fwd"], D_bwd=dst["D_bwd"], z=dst["z"], dirs=wl.dirs,
+                      out=out_d, workspace=ws)
+            if seg:
+                vssm.scan_folded(dst["x"], dst["delta"], dst["A_fwd"], dst["A_bwd"], dst["B"],
+                                 dst["C"], seg_len=seg, **kw)
+            else:
+                vssm.scan_bidir(dst["x"], dst["delta"], dst["A_fwd"], dst["A_bwd"], dst["B"],
+                                dst["C"], **kw)
+            out_h.copy_(out_d, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_s = reduce_max(e0.elapsed_time(e1) / 1e3)
+        e2e = {"value": round(aggregate(set_bytes * args.e2e_steps, world, e2e_s) / 1e9, 3),
+               "unit": "GB/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": args.e2e_steps,
+               "gtokch_per_s": round(aggregate(wl.tokch * args.e2e_steps, world, e2e_s) / 1e9, 4)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tok, secs, threads, desc = oracle_sample_run(wl, inp, args.cpu_seconds)
+        cpu = {"value": round(tok * (set_bytes / wl.tokch) / secs / 1e9, 5), "unit": "GB/s",
+               "cores": threads, "kind": "oracle", "sample": desc,
+               "gtokch_per_s": round(tok / secs / 1e9, 6), "cpu": cpu_model()}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(region_s / args.steps * 1e3, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": workload_config(wl, l2_note),
+            "gtokch_per_s": round(gtok, 4),
+            "hbm_frac_of_measured": round(gbs / world / hbm_peak, 4),
+            "hbm_frac_of_spec_8tbs": round(gbs / world / SPEC_HBM_GBS, 4),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clocks, "gpu_launches": args.steps,
+            "kernel_source_sha": source_sha(),
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

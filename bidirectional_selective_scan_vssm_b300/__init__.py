@@ -1,0 +1,197 @@
+"""Bidirectional selective scan (S6) on NVIDIA B300 -- Python binding.
+
+A thin ctypes layer over the C ABI in ``include/vssm.h`` (library
+``libvssm.so`` built in-tree by ``build.py``). It only marshals arguments:
+every step of the scan runs in the CUDA kernels. PyTorch supplies device
+memory and streams. There is no CPU fallback: importing this package fails
+if the library is missing, and the scan functions refuse CPU tensors.
+
+    out = scan_bidir(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z)
+    out = scan_folded(x, delta, A_fwd, None, B, C, D_fwd, None, z, seg_len=51,
+                      dirs=DIR_FWD)
+
+Shapes: x, delta, z, out (batch, dim, L); B, C (batch, L, N); A (dim, N)
+float32; D (dim,) float32. x, delta, z, B, C share one dtype (float32 or
+bfloat16), which is also the output dtype.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+
+DIR_FWD, DIR_BWD, DIR_BOTH = 1, 2, 3
+VSSM_F32, VSSM_BF16 = 0, 1
+STATUS = {0: "VSSM_OK", -1: "VSSM_ERR_INVALID_ARG", -2: "VSSM_ERR_UNSUPPORTED",
+          -3: "VSSM_ERR_MISALIGNED", -4: "VSSM_ERR_CUDA", -6: "VSSM_ERR_WORKSPACE"}
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libvssm.so")
+EXPORTS = ["vssm_scan_bidir", "vssm_scan_folded", "vssm_scan_workspace_size",
+           "vssm_status_string", "vssm_last_error", "vssm_version"]
+
+
+class ScanArgs(ctypes.Structure):
+    """Mirror of ``vssm_scan_args`` (include/vssm.h)."""
+    _fields_ = [
+        ("x", ctypes.c_void_p), ("delta", ctypes.c_void_p), ("z", ctypes.c_void_p),
+        ("B", ctypes.c_void_p), ("C", ctypes.c_void_p),
+        ("B_bwd", ctypes.c_void_p), ("C_bwd", ctypes.c_void_p),
+        ("A_fwd", ctypes.c_void_p), ("A_bwd", ctypes.c_void_p),
+        ("D_fwd", ctypes.c_void_p), ("D_bwd", ctypes.c_void_p),
+        ("out", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("batch", ctypes.c_int), ("dim", ctypes.c_int), ("seqlen", ctypes.c_int),
+        ("dstate", ctypes.c_int), ("dtype", ctypes.c_int), ("dir_flags", ctypes.c_uint),
+    ]
+
+
+class VssmError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python bidirectional_selective_scan_vssm_b300/build.py` (needs nvcc)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER(ScanArgs)
+    lib.vssm_scan_bidir.argtypes = [P, ctypes.c_void_p]
+    lib.vssm_scan_bidir.restype = ctypes.c_int
+    lib.vssm_scan_folded.argtypes = [P, ctypes.c_int, ctypes.c_void_p]
+    lib.vssm_scan_folded.restype = ctypes.c_int
+    lib.vssm_scan_workspace_size.argtypes = [P, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
+    lib.vssm_scan_workspace_size.restype = ctypes.c_int
+    lib.vssm_status_string.argtypes = [ctypes.c_int]
+    lib.vssm_status_string.restype = ctypes.c_char_p
+    lib.vssm_last_error.argtypes = []
+    lib.vssm_last_error.restype = ctypes.c_char_p
+    lib.vssm_version.argtypes = []
+    lib.vssm_version.restype = ctypes.c_int
+    return lib
+
+
+lib = _load()
+
+
+def _check(status: int):
+    if status != 0:
+        raise VssmError(status, lib.vssm_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _dev_tensor(name, t, dtype=None, shape=None, device=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, out=None,
+              B_bwd=None, C_bwd=None, dirs: int = DIR_BOTH) -> ScanArgs:
+    """Validate tensors and fill a ``vssm_scan_args`` (no workspace yet)."""
+    x = _dev_tensor("x", x)
+    if x.dtype not in (torch.float32, torch.bfloat16) or x.dim() != 3:
+        raise TypeError("x must be a 3-D float32 or bfloat16 tensor (batch, dim, L)")
+    batch, dim, L = x.shape
+    N = B.shape[-1]
+    dev, dt = x.device, x.dtype
+    _dev_tensor("delta", delta, dt, x.shape, dev)
+    _dev_tensor("z", z, dt, x.shape, dev)
+    _dev_tensor("out", out, dt, x.shape, dev)
+    for n, t in (("B", B), ("C", C), ("B_bwd", B_bwd), ("C_bwd", C_bwd)):
+        _dev_tensor(n, t, dt, (batch, L, N), dev)
+    for n, t in (("A_fwd", A_fwd), ("A_bwd", A_bwd)):
+        _dev_tensor(n, t, torch.float32, (dim, N), dev)
+    for n, t in (("D_fwd", D_fwd), ("D_bwd", D_bwd)):
+        _dev_tensor(n, t, torch.float32, (dim,), dev)
+    a = ScanArgs()
+    a.x, a.delta, a.z = _ptr(x), _ptr(delta), _ptr(z)
+    a.B, a.C, a.B_bwd, a.C_bwd = _ptr(B), _ptr(C), _ptr(B_bwd), _ptr(C_bwd)
+    a.A_fwd, a.A_bwd, a.D_fwd, a.D_bwd = _ptr(A_fwd), _ptr(A_bwd), _ptr(D_fwd), _ptr(D_bwd)
+    a.out = _ptr(out)
+    a.batch, a.dim, a.seqlen, a.dstate = batch, dim, L, N
+    a.dtype = VSSM_F32 if dt == torch.float32 else VSSM_BF16
+    a.dir_flags = dirs
+    return a
+
+
+def workspace_size(a: ScanArgs, seg_len: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib.vssm_scan_workspace_size(ctypes.byref(a), seg_len, ctypes.byref(n)))
+    return int(n.value)
+
+
+_ws_cache = {}
+
+
+def _workspace(device: torch.device, stream, nbytes: int) -> Optional[torch.Tensor]:
+    """A scratch buffer per (device, stream), grown on demand (device memory
+    via torch). Calls on one stream run in order, so they can share it."""
+    if nbytes == 0:
+        return None
+    key = (device, stream.cuda_stream)
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def _launch(fn, a: ScanArgs, seg_len: Optional[int], device, workspace, stream):
+    need = workspace_size(a, seg_len or 0)
+    stream = stream if stream is not None else torch.cuda.current_stream(device)
+    if workspace is None:
+        workspace = _workspace(device, stream, need)
+    if workspace is not None:
+        a.workspace = workspace.data_ptr()
+        a.workspace_bytes = workspace.numel() * workspace.element_size()
+    s = stream.cuda_stream
+    if seg_len is None:
+        _check(fn(ctypes.byref(a), ctypes.c_void_p(s)))
+    else:
+        _check(fn(ctypes.byref(a), int(seg_len), ctypes.c_void_p(s)))
+
+
+def scan_bidir(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None,
+               dirs: int = DIR_BOTH, out=None, B_bwd=None, C_bwd=None,
+               stream: Optional[torch.cuda.Stream] = None, workspace=None) -> torch.Tensor:
+    """Selective scan over independent sequences (``vssm_scan_bidir``)."""
+    if out is None:
+        out = torch.empty_like(x)
+    a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, out, B_bwd, C_bwd, dirs)
+    _launch(lib.vssm_scan_bidir, a, None, x.device, workspace, stream)
+    return out
+
+
+def scan_folded(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *,
+                seg_len: int, dirs: int = DIR_FWD, out=None, B_bwd=None, C_bwd=None,
+                stream: Optional[torch.cuda.Stream] = None, workspace=None) -> torch.Tensor:
+    """Batch-folded scan with a state reset every ``seg_len`` tokens
+    (``vssm_scan_folded``)."""
+    if out is None:
+        out = torch.empty_like(x)
+    a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, out, B_bwd, C_bwd, dirs)
+    _launch(lib.vssm_scan_folded, a, seg_len, x.device, workspace, stream)
+    return out
+
+
+def version() -> int:
+    return int(lib.vssm_version())

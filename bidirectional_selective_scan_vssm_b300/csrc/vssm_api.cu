@@ -1,0 +1,250 @@
+// C ABI of the selective-scan library (declared in include/vssm.h):
+// argument validation, variant selection and launch on the caller's stream.
+#include <algorithm>
+#include <atomic>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "scan_kernel.cuh"
+#include "vssm.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int status, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int status, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return status;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb)
+{
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+// Launch plan for one call.
+struct Plan {
+    int dirs = 0;          // 1, 2 or 3
+    int pieces = 1;        // token ranges per (b, d)
+    int piece_len = 0;     // tokens per range
+    bool ysmem = false;    // y-buffer in shared memory
+    int ypitch = 0;        // floats per channel of the shared y-buffer
+    size_t workspace = 0;  // bytes of global y-buffer needed
+    long long ctas = 0;
+};
+
+constexpr int kBidirR = 32, kBidirG = 2;     // 128 threads: 64 forward, 64 backward
+constexpr int kOneDirR = 64, kOneDirG = 2;   // 128 threads
+constexpr int kYSmemMaxBytes = 48 * 1024;    // shared y-buffer budget per CTA
+constexpr int kTargetCtas = 148 * 8;         // enough CTAs to fill 148 SMs
+
+int make_plan(const vssm_scan_args *a, int seg_len, Plan *pl)
+{
+    const unsigned dirs = a->dir_flags;
+    pl->dirs = (int)dirs;
+    const int R = (dirs == 3) ? kBidirR : kOneDirR;
+    const long long dblocks = (a->dim + R - 1) / R;
+    pl->pieces = 1;
+    pl->piece_len = a->seqlen;
+    if (seg_len > 0 && a->seqlen > 0) {
+        // Split each folded row at segment boundaries so that the grid has
+        // enough CTAs; every piece starts on a reset, so pieces are independent.
+        const long long nseg = (a->seqlen + seg_len - 1) / seg_len;
+        long long want = (kTargetCtas + (long long)a->batch * dblocks - 1) /
+                         std::max<long long>(1, (long long)a->batch * dblocks);
+        want = std::max<long long>(1, std::min<long long>(want, nseg));
+        const long long per = (nseg + want - 1) / want;        // segments per piece
+        pl->pieces = (int)((nseg + per - 1) / per);
+        pl->piece_len = (int)(per * seg_len);
+    }
+    pl->ctas = (long long)a->batch * pl->pieces * dblocks;
+    pl->ysmem = false;
+    pl->workspace = 0;
+    if (dirs == 3) {
+        const int lv = std::min(a->seqlen, pl->piece_len);
+        const int pitch = lv | 1;                              // odd: rows hit distinct banks
+        if ((long long)R * pitch * 4 <= kYSmemMaxBytes) {
+            pl->ysmem = true;
+            pl->ypitch = pitch;
+        } else {
+            pl->workspace = (size_t)a->batch * a->dim * a->seqlen * sizeof(float);
+        }
+    }
+    return VSSM_OK;
+}
+
+int validate(const vssm_scan_args *a, int seg_len, bool folded)
+{
+    if (!a) return fail(VSSM_ERR_INVALID_ARG, "args is NULL");
+    if (a->batch < 0 || a->dim < 0 || a->seqlen < 0)
+        return fail(VSSM_ERR_INVALID_ARG, "negative size (batch=%d dim=%d seqlen=%d)",
+                    a->batch, a->dim, a->seqlen);
+    if (a->dstate < 1 || a->dstate > vssm::kMaxState)
+        return fail(VSSM_ERR_UNSUPPORTED, "dstate=%d outside 1..%d", a->dstate, vssm::kMaxState);
+    if (a->dtype != VSSM_F32 && a->dtype != VSSM_BF16)
+        return fail(VSSM_ERR_UNSUPPORTED, "unknown dtype %d", a->dtype);
+    if (a->dir_flags < 1 || a->dir_flags > 3)
+        return fail(VSSM_ERR_INVALID_ARG, "dir_flags=%u: need VSSM_DIR_FWD and/or VSSM_DIR_BWD",
+                    a->dir_flags);
+    if (folded) {
+        if (seg_len < 1) return fail(VSSM_ERR_INVALID_ARG, "seg_len=%d must be >= 1", seg_len);
+        if ((a->dir_flags & VSSM_DIR_BWD) && a->seqlen % seg_len != 0)
+            return fail(VSSM_ERR_INVALID_ARG,
+                        "backward folded scan needs seqlen (%d) to be a multiple of seg_len (%d)",
+                        a->seqlen, seg_len);
+    }
+    const long long tok = (long long)a->batch * a->dim * a->seqlen;
+    if (tok == 0) return VSSM_OK;
+    if (!a->x || !a->delta || !a->B || !a->C || !a->out)
+        return fail(VSSM_ERR_INVALID_ARG, "x, delta, B, C and out are required");
+    if ((a->dir_flags & VSSM_DIR_FWD) && !a->A_fwd)
+        return fail(VSSM_ERR_INVALID_ARG, "A_fwd is required for the forward direction");
+    if ((a->dir_flags & VSSM_DIR_BWD) && !a->A_bwd)
+        return fail(VSSM_ERR_INVALID_ARG, "A_bwd is required for the backward direction");
+    const void *ptrs[] = {a->x, a->delta, a->z, a->B, a->C, a->B_bwd, a->C_bwd, a->A_fwd,
+                          a->A_bwd, a->D_fwd, a->D_bwd, a->out, a->workspace};
+    const char *names[] = {"x", "delta", "z", "B", "C", "B_bwd", "C_bwd", "A_fwd",
+                           "A_bwd", "D_fwd", "D_bwd", "out", "workspace"};
+    for (int i = 0; i < 13; ++i)
+        if (ptrs[i] && !aligned16(ptrs[i]))
+            return fail(VSSM_ERR_MISALIGNED, "%s=%p is not 16-byte aligned", names[i], ptrs[i]);
+    const size_t es = a->dtype == VSSM_F32 ? 4 : 2;
+    const size_t nact = (size_t)tok * es;
+    const size_t nbc = (size_t)a->batch * a->seqlen * a->dstate * es;
+    const size_t npar = (size_t)a->dim * a->dstate * 4;
+    const struct { const void *p; size_t n; const char *name; } ins[] = {
+        {a->x, nact, "x"}, {a->delta, nact, "delta"}, {a->z, nact, "z"},
+        {a->B, nbc, "B"}, {a->C, nbc, "C"}, {a->B_bwd, nbc, "B_bwd"}, {a->C_bwd, nbc, "C_bwd"},
+        {a->A_fwd, npar, "A_fwd"}, {a->A_bwd, npar, "A_bwd"},
+        {a->D_fwd, (size_t)a->dim * 4, "D_fwd"}, {a->D_bwd, (size_t)a->dim * 4, "D_bwd"},
+        {a->workspace, a->workspace_bytes, "workspace"}};
+    for (const auto &in : ins)
+        if (overlaps(a->out, nact, in.p, in.n))
+            return fail(VSSM_ERR_INVALID_ARG, "out overlaps %s", in.name);
+    if (a->workspace && overlaps(a->workspace, a->workspace_bytes, a->x, nact))
+        return fail(VSSM_ERR_INVALID_ARG, "workspace overlaps x");
+    return VSSM_OK;
+}
+
+template <typename T, int DIRS, int R, int G, bool YSMEM>
+int launch_variant(const vssm::ScanParams &p, const Plan &pl, cudaStream_t stream)
+{
+    constexpr int NDIR = DIRS == 3 ? 2 : 1;
+    const size_t smem = sizeof(float) * ((size_t)NDIR * vssm::DirBlock<R>::kFloats +
+                                         (YSMEM ? (size_t)R * p.ypitch : 0));
+    auto kern = vssm::scan_kernel<T, DIRS, R, G, YSMEM>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess)
+        return fail(VSSM_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    kern<<<(unsigned)pl.ctas, NDIR * R * G, smem, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    return VSSM_OK;
+}
+
+template <typename T>
+int launch_typed(const vssm::ScanParams &p, const Plan &pl, cudaStream_t s)
+{
+    switch (pl.dirs) {
+    case 1: return launch_variant<T, 1, kOneDirR, kOneDirG, false>(p, pl, s);
+    case 2: return launch_variant<T, 2, kOneDirR, kOneDirG, false>(p, pl, s);
+    default:
+        return pl.ysmem ? launch_variant<T, 3, kBidirR, kBidirG, true>(p, pl, s)
+                        : launch_variant<T, 3, kBidirR, kBidirG, false>(p, pl, s);
+    }
+}
+
+int run(const vssm_scan_args *a, int seg_len, bool folded, void *stream)
+{
+    int st = validate(a, seg_len, folded);
+    if (st != VSSM_OK) return st;
+    if ((long long)a->batch * a->dim * a->seqlen == 0) return VSSM_OK;
+    Plan pl;
+    make_plan(a, folded ? seg_len : 0, &pl);
+    if (pl.ctas > 0x7fffffffLL) return fail(VSSM_ERR_UNSUPPORTED, "problem too large for one grid");
+    if (pl.workspace > 0 && (!a->workspace || a->workspace_bytes < pl.workspace))
+        return fail(VSSM_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", pl.workspace,
+                    a->workspace ? a->workspace_bytes : (size_t)0);
+    vssm::ScanParams p{};
+    p.x = a->x;
+    p.delta = a->delta;
+    p.z = a->z;
+    p.B[0] = a->B;
+    p.C[0] = a->C;
+    p.B[1] = a->B_bwd ? a->B_bwd : a->B;
+    p.C[1] = a->C_bwd ? a->C_bwd : a->C;
+    p.A[0] = a->A_fwd;
+    p.A[1] = a->A_bwd;
+    p.D[0] = a->D_fwd;
+    p.D[1] = a->D_bwd;
+    p.out = a->out;
+    p.ybuf = pl.workspace ? static_cast<float *>(a->workspace) : nullptr;
+    p.batch = a->batch;
+    p.dim = a->dim;
+    p.L = a->seqlen;
+    p.N = a->dstate;
+    p.seg_len = folded ? seg_len : 0;
+    p.pieces = pl.pieces;
+    p.piece_len = pl.piece_len;
+    p.ypitch = pl.ypitch;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return a->dtype == VSSM_F32 ? launch_typed<float>(p, pl, s)
+                                : launch_typed<__nv_bfloat16>(p, pl, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+int vssm_scan_workspace_size(const vssm_scan_args *a, int seg_len, size_t *bytes)
+{
+    if (!a || !bytes) return fail(VSSM_ERR_INVALID_ARG, "args or bytes is NULL");
+    if (a->batch < 0 || a->dim < 0 || a->seqlen < 0 || a->dir_flags < 1 || a->dir_flags > 3 ||
+        seg_len < 0)
+        return fail(VSSM_ERR_INVALID_ARG, "invalid sizes or dir_flags");
+    Plan pl;
+    make_plan(a, seg_len, &pl);
+    *bytes = pl.workspace;
+    return VSSM_OK;
+}
+
+int vssm_scan_bidir(const vssm_scan_args *a, void *stream) { return run(a, 0, false, stream); }
+
+int vssm_scan_folded(const vssm_scan_args *a, int seg_len, void *stream)
+{
+    return run(a, seg_len, true, stream);
+}
+
+const char *vssm_status_string(int status)
+{
+    switch (status) {
+    case VSSM_OK: return "ok";
+    case VSSM_ERR_INVALID_ARG: return "invalid argument";
+    case VSSM_ERR_UNSUPPORTED: return "unsupported configuration";
+    case VSSM_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case VSSM_ERR_CUDA: return "CUDA runtime error";
+    case VSSM_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+    }
+}
+
+const char *vssm_last_error(void) { return g_last_error.c_str(); }
+
+int vssm_version(void) { return VSSM_VERSION; }
+
+}  // extern "C"

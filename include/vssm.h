@@ -1,0 +1,130 @@
+/*
+ * vssm.h -- C ABI of the bidirectional selective-scan (S6) library for
+ * NVIDIA B300 (sm_103a).
+ *
+ * The operation (for every batch b and channel d, states n = 0..N-1):
+ *
+ *   decay      Abar_t[n] = exp(delta_t * A[d][n])         VSSD page, §4.1.2
+ *   recurrence h_t[n] = Abar_t[n] * h_{t-1}[n] + delta_t * B_t[n] * x_t
+ *              y_t    = sum_n C_t[n] * h_t[n] + D[d] * x_t  VSSD page, §4.2.1.3
+ *   backward   the same recurrence over t = L-1 .. 0 with its own A and D
+ *                                                           Vim page, §2.2
+ *   output     out_t = (y_fwd_t + y_bwd_t) * silu(z_t),  silu(z) = z * sigmoid(z)
+ *   folded     with seg_len > 0 the decay is 0 at every segment start
+ *              (t mod seg_len == 0 forward, == seg_len-1 backward), so
+ *              segments concatenated along t never exchange state
+ *                                  SF-Mamba page, "批量折叠与周期性状态重置"
+ *
+ * The first-order input term delta*B (the pages' "≈ΔB") is used; the state
+ * starts at zero in each direction and is never returned.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *    allocates nothing and keeps no pointer after the call returns.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL = the legacy default stream). A return of VSSM_OK means the kernel
+ *    was enqueued; execution errors surface at the caller's next
+ *    synchronisation, as for any CUDA launch.
+ *  - Arguments are validated on the host BEFORE anything is launched; an
+ *    invalid call launches nothing and returns a negative vssm_status. The
+ *    text of the last error on the calling thread is vssm_last_error().
+ *  - Layouts (row-major, last index fastest):
+ *      x, delta, z, out : [batch][dim][seqlen]
+ *      B, C, B_bwd, C_bwd: [batch][seqlen][dstate]
+ *      A_fwd, A_bwd     : [dim][dstate]   float32
+ *      D_fwd, D_bwd     : [dim]           float32
+ *    x, delta, z, B, C, B_bwd, C_bwd and out all have the element type
+ *    `dtype`; arithmetic and the state are float32 in both cases, and out is
+ *    rounded once (round to nearest even) when stored.
+ *  - Every pointer must be 16-byte aligned (torch allocations are).
+ *  - `out` must not overlap any input or the workspace.
+ */
+#ifndef VSSM_H
+#define VSSM_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define VSSM_VERSION 100 /* 1.0.0 */
+
+typedef enum {
+    VSSM_OK = 0,
+    VSSM_ERR_INVALID_ARG = -1,   /* null/negative/inconsistent argument        */
+    VSSM_ERR_UNSUPPORTED = -2,   /* e.g. dstate > 16, unknown dtype            */
+    VSSM_ERR_MISALIGNED = -3,    /* a pointer is not 16-byte aligned           */
+    VSSM_ERR_CUDA = -4,          /* the CUDA runtime refused the launch        */
+    VSSM_ERR_WORKSPACE = -6      /* workspace missing or smaller than required */
+} vssm_status;
+
+typedef enum { VSSM_F32 = 0, VSSM_BF16 = 1 } vssm_dtype;
+
+enum { VSSM_DIR_FWD = 1, VSSM_DIR_BWD = 2, VSSM_DIR_BOTH = 3 };
+
+typedef struct {
+    const void *x;          /* [batch][dim][seqlen]                      required */
+    const void *delta;      /* [batch][dim][seqlen], the step Δ (already
+                               positive, e.g. after softplus)            required */
+    const void *z;          /* [batch][dim][seqlen] gate input; NULL = no gate    */
+    const void *B;          /* [batch][seqlen][dstate]                   required */
+    const void *C;          /* [batch][seqlen][dstate]                   required */
+    const void *B_bwd;      /* backward B; NULL = use B                           */
+    const void *C_bwd;      /* backward C; NULL = use C                           */
+    const float *A_fwd;     /* [dim][dstate]; required if the FWD bit is set      */
+    const float *A_bwd;     /* [dim][dstate]; required if the BWD bit is set      */
+    const float *D_fwd;     /* [dim] skip weight; NULL = 0                        */
+    const float *D_bwd;     /* [dim] skip weight; NULL = 0                        */
+    void *out;              /* [batch][dim][seqlen] output               required */
+    void *workspace;        /* device scratch, see vssm_scan_workspace_size()     */
+    size_t workspace_bytes; /* size of `workspace` in bytes                       */
+    int batch, dim, seqlen; /* >= 0; an empty problem is a no-op                  */
+    int dstate;             /* 1..16                                              */
+    int dtype;              /* vssm_dtype                                         */
+    unsigned dir_flags;     /* VSSM_DIR_FWD | VSSM_DIR_BWD (at least one)         */
+} vssm_scan_args;
+
+/*
+ * Bytes of device workspace the call with these arguments needs (0 when it
+ * needs none). With both directions, the direction that reaches a token first
+ * leaves its partial output there until the other direction arrives; short
+ * rows keep that buffer in shared memory and need no workspace. The
+ * workspace holds nothing between calls. seg_len as in vssm_scan_folded
+ * (0 for vssm_scan_bidir). Only `batch`, `dim`, `seqlen`, `dstate`, `dtype`
+ * and `dir_flags` of `a` are read.
+ */
+int vssm_scan_workspace_size(const vssm_scan_args *a, int seg_len, size_t *bytes);
+
+/*
+ * Bidirectional (or single-direction, by dir_flags) selective scan over
+ * independent sequences of seqlen tokens. Vim page §2.2 and §3.1; VSSD page
+ * §4.1.2 and §4.2.1.3.
+ */
+int vssm_scan_bidir(const vssm_scan_args *a, void *stream);
+
+/*
+ * Batch-folded scan: each row of seqlen tokens is a concatenation of
+ * segments of seg_len tokens with the state reset at every segment start
+ * (SF-Mamba page, "批量折叠与周期性状态重置"; folded tensor Z' of shape
+ * B1 x D x (B2*T)). The caller folds (B2 sequences of T tokens become one row
+ * of B2*T tokens) and unfolds; the kernel receives the folded tensors.
+ * seg_len >= 1. Forward-only calls accept a partial last segment; when the
+ * BWD bit is set, seqlen must be a multiple of seg_len (else
+ * VSSM_ERR_INVALID_ARG).
+ */
+int vssm_scan_folded(const vssm_scan_args *a, int seg_len, void *stream);
+
+/* Static text for a vssm_status value. */
+const char *vssm_status_string(int status);
+
+/* Text of the last failed call on this thread ("" if none). */
+const char *vssm_last_error(void);
+
+/* VSSM_VERSION of the loaded library. */
+int vssm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VSSM_H */
