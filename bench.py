@@ -52,7 +52,7 @@ PROFILES = os.path.join(ROOT, "profiles")
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--steps", type=int, default=5000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--workload", default="vim_s_224", choices=ORDER)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -103,30 +103,40 @@ def aggregate(units_per_rank: float, world: int, max_seconds: float) -> float:
 
 # ------------------------------------------------------------------ clocks
 
-class ClockSampler(threading.Thread):
-    """Samples the SM clock and the clock-event reasons through NVML."""
+class ClockSampler:
+    """Samples the SM clock and the clock-event reasons of one GPU during the
+    timed region, through NVML when importable, else a streaming nvidia-smi."""
     REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
                0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
                0x100: "display_clock_setting"}
 
-    def __init__(self, uuid: str, period_s: float = 0.004):
-        super().__init__(daemon=True)
+    def __init__(self, uuid: str, period_ms: int = 20):
+        self.uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        self.period_ms = period_ms
         self.samples = []
-        self.period = period_s
-        self.ok = False
+        self.max_mhz = None
+        self.err = None
+        self.source = None
         self._stop = threading.Event()
+        self._thread = None
+        self._proc = None
         try:
             import pynvml
             pynvml.nvmlInit()
             self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
+            self.h = pynvml.nvmlDeviceGetHandleByUUID(self.uuid)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception as e:  # report, never fake
-            self.err = repr(e)
+            self.source = "nvml"
+        except Exception as e:
+            self.nv = None
+            self.err = f"nvml: {e!r}"
 
-    def sample(self):
+    @property
+    def ok(self):
+        return True
+
+    def _nvml_sample(self):
         nv = self.nv
         try:
             reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
@@ -134,25 +144,74 @@ class ClockSampler(threading.Thread):
             reasons = nv.nvmlDeviceGetCurrentClocksThrottleReasons(self.h)
         self.samples.append((nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM), int(reasons)))
 
-    def run(self):
+    def _nvml_loop(self):
         while not self._stop.is_set():
-            self.sample()
-            time.sleep(self.period)
+            self._nvml_sample()
+            time.sleep(self.period_ms / 1000)
+
+    def _smi_loop(self):
+        for line in self._proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 3:
+                continue
+            try:
+                mhz, mx = float(parts[0]), float(parts[1])
+                reasons = int(parts[2], 16)
+            except ValueError:
+                continue
+            self.max_mhz = mx
+            self.samples.append((mhz, reasons))
+            if self._stop.is_set():
+                break
+
+    def start(self):
+        """Begin sampling; returns once the first sample has arrived (or failed)."""
+        if self.nv is not None:
+            self._nvml_sample()
+            self._thread = threading.Thread(target=self._nvml_loop, daemon=True)
+            self._thread.start()
+            return
+        import subprocess
+        try:
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.uuid,
+                 "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", f"-lms={self.period_ms}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError as e:
+            self.err = (self.err or "") + f"; nvidia-smi: {e!r}"
+            return
+        self.source = "nvidia-smi"
+        self._thread = threading.Thread(target=self._smi_loop, daemon=True)
+        self._thread.start()
+        t0 = time.time()
+        while not self.samples and time.time() - t0 < 10:
+            time.sleep(0.01)
 
     def stop(self):
         self._stop.set()
-        self.join(timeout=2)
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except Exception:
+                self._proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
 
-    def summary(self):
-        if not self.ok:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": self.err}
-        mhz = [m for m, _ in self.samples]
+    def summary(self, first_in_region: int = 0):
+        """Median SM clock and the union of the reasons over the samples taken
+        from index first_in_region on (the timed region)."""
+        smp = self.samples[first_in_region:] or self.samples[-1:]
+        if not smp:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
+                    "error": self.err or "no samples"}
         bits = 0
-        for _, r in self.samples:
+        for _, r in smp:
             bits |= r
         names = [n for b, n in self.REASONS.items() if bits & b and n != "gpu_idle"]
-        return {"sm_mhz": statistics.median(mhz) if mhz else None,
-                "sm_max_mhz": self.max_mhz, "reasons": names, "samples": len(mhz)}
+        return {"sm_mhz": statistics.median(m for m, _ in smp), "sm_max_mhz": self.max_mhz,
+                "reasons": names, "samples": len(smp), "source": self.source}
 
 
 # ------------------------------------------------------------------ helpers
@@ -335,14 +394,11 @@ def run_ours(args):
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(str(torch.cuda.get_device_properties(dev).uuid)
-                           if str(torch.cuda.get_device_properties(dev).uuid).startswith("GPU-")
-                           else "GPU-" + str(torch.cuda.get_device_properties(dev).uuid))
+    sampler = ClockSampler(str(torch.cuda.get_device_properties(dev).uuid))
+    sampler.start()
     barrier()
     torch.cuda.synchronize()
-    if sampler.ok:
-        sampler.sample()
-        sampler.start()
+    first_sample = len(sampler.samples)
     start.record(stream)
     for i in range(args.steps):
         ev_b[i].record(stream)
@@ -351,8 +407,7 @@ def run_ours(args):
     end.record(stream)
     torch.cuda.synchronize()
     barrier()
-    if sampler.ok:
-        sampler.stop()
+    sampler.stop()
     region_s = reduce_max(start.elapsed_time(end) / 1e3)
     kern_ms = [b.elapsed_time(e) for b, e in zip(ev_b, ev_e)]
     kern_avg_s = statistics.fmean(kern_ms) / 1e3
@@ -361,7 +416,7 @@ def run_ours(args):
     gtok = aggregate(wl.tokch * args.steps, world, region_s) / 1e9
     peaks, peaks_kind = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    clocks = sampler.summary()
+    clocks = sampler.summary(first_sample)
 
     # Roofline of the scan kernel: the exp unit and the fp32 FMA pipe both
     # allow 32 state updates per clock per SM (1 ex2 + 4 fp32 ops each).

@@ -26,11 +26,12 @@ import torch
 DIR_FWD, DIR_BWD, DIR_BOTH = 1, 2, 3
 VSSM_F32, VSSM_BF16 = 0, 1
 STATUS = {0: "VSSM_OK", -1: "VSSM_ERR_INVALID_ARG", -2: "VSSM_ERR_UNSUPPORTED",
-          -3: "VSSM_ERR_MISALIGNED", -4: "VSSM_ERR_CUDA", -6: "VSSM_ERR_WORKSPACE"}
+          -3: "VSSM_ERR_MISALIGNED", -4: "VSSM_ERR_CUDA", -5: "VSSM_ERR_TIMEOUT",
+          -6: "VSSM_ERR_WORKSPACE"}
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libvssm.so")
 EXPORTS = ["vssm_scan_bidir", "vssm_scan_folded", "vssm_scan_workspace_size",
-           "vssm_status_string", "vssm_last_error", "vssm_version"]
+           "vssm_device_error", "vssm_status_string", "vssm_last_error", "vssm_version"]
 
 
 class ScanArgs(ctypes.Structure):
@@ -71,6 +72,8 @@ def _load():
     lib.vssm_status_string.restype = ctypes.c_char_p
     lib.vssm_last_error.argtypes = []
     lib.vssm_last_error.restype = ctypes.c_char_p
+    lib.vssm_device_error.argtypes = [ctypes.c_void_p]
+    lib.vssm_device_error.restype = ctypes.c_int
     lib.vssm_version.argtypes = []
     lib.vssm_version.restype = ctypes.c_int
     return lib
@@ -191,6 +194,13 @@ def scan_folded(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *,
     a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, out, B_bwd, C_bwd, dirs)
     _launch(lib.vssm_scan_folded, a, seg_len, x.device, workspace, stream)
     return out
+
+
+def device_error(stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Synchronise ``stream`` and raise VssmError(VSSM_ERR_TIMEOUT) if a scan
+    kernel stopped on an expired device-side wait since the last check."""
+    stream = stream if stream is not None else torch.cuda.current_stream()
+    _check(lib.vssm_device_error(ctypes.c_void_p(stream.cuda_stream)))
 
 
 def version() -> int:

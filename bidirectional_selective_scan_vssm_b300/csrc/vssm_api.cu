@@ -8,8 +8,15 @@
 #include <cstring>
 #include <string>
 
+#include <mutex>
+
 #include "scan_kernel.cuh"
+#include "scan_warp.cuh"
 #include "vssm.h"
+
+// Device error word written by kernels whose bounded waits expire (one per
+// device that loads the library).
+__device__ unsigned g_vssm_device_error;
 
 namespace {
 
@@ -38,6 +45,11 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb)
 
 // Launch plan for one call.
 struct Plan {
+    bool warp = false;     // warp-per-channel-group kernel (N = 16) vs general kernel
+    int G = 1;             // lanes per channel (warp kernel)
+    int W = 4;             // warps per CTA (warp kernel)
+    int rgroups = 0;       // channel groups per (batch, piece) (warp kernel)
+    long long ngroups = 0; // channel groups x pieces x batch (warp kernel)
     int dirs = 0;          // 1, 2 or 3
     int pieces = 1;        // token ranges per (b, d)
     int piece_len = 0;     // tokens per range
@@ -52,8 +64,70 @@ constexpr int kOneDirR = 64, kOneDirG = 2;   // 128 threads
 constexpr int kYSmemMaxBytes = 48 * 1024;    // shared y-buffer budget per CTA
 constexpr int kTargetCtas = 148 * 8;         // enough CTAs to fill 148 SMs
 
+constexpr int kWarpTargetWarps = 148 * 8;      // warps that fill 148 SMs at 8 warps each
+
+template <typename T>
+int warp_bytes(int G)
+{
+    switch (G) {
+    case 1: return vssm::WarpLayout<T, 1>::kWarpBytes;
+    case 2: return vssm::WarpLayout<T, 2>::kWarpBytes;
+    default: return vssm::WarpLayout<T, 4>::kWarpBytes;
+    }
+}
+
+constexpr int warps_per_cta(int G) { return G == 4 ? 8 : 4; }
+
+// Plan for the warp kernel (dstate == 16).
+void make_warp_plan(const vssm_scan_args *a, int seg_len, Plan *pl)
+{
+    const unsigned dirs = a->dir_flags;
+    const int ndir = dirs == 3 ? 2 : 1;
+    pl->warp = true;
+    pl->dirs = (int)dirs;
+    const long long nseg = seg_len > 0 ? (a->seqlen + seg_len - 1) / seg_len : 1;
+    // Smallest G (most states per lane) that still yields enough warps;
+    // folded sequences are first split into independent pieces.
+    int G = 4;
+    for (int g : {1, 2, 4}) {
+        const long long rg = (a->dim + 32 / g - 1) / (32 / g);
+        long long pieces = 1;
+        if (seg_len > 0) {
+            const long long per_piece_warps = (long long)a->batch * rg * ndir;
+            pieces = std::min<long long>(nseg, std::max<long long>(
+                1, (kWarpTargetWarps + per_piece_warps - 1) / std::max<long long>(1, per_piece_warps)));
+        }
+        if ((long long)a->batch * rg * pieces * ndir >= kWarpTargetWarps * 3 / 4 || g == 4) {
+            G = g;
+            break;
+        }
+    }
+    pl->G = G;
+    pl->W = warps_per_cta(G);
+    const int rpw = 32 / G;
+    pl->rgroups = (a->dim + rpw - 1) / rpw;
+    pl->pieces = 1;
+    pl->piece_len = a->seqlen;
+    if (seg_len > 0 && a->seqlen > 0) {
+        const long long per_piece_warps = (long long)a->batch * pl->rgroups * ndir;
+        long long want = (kWarpTargetWarps + per_piece_warps - 1) / std::max<long long>(1, per_piece_warps);
+        want = std::max<long long>(1, std::min<long long>(want, nseg));
+        const long long per = (nseg + want - 1) / want;        // segments per piece
+        pl->pieces = (int)((nseg + per - 1) / per);
+        pl->piece_len = (int)(per * seg_len);
+    }
+    pl->ngroups = (long long)a->batch * pl->pieces * pl->rgroups;
+    const int gpc = pl->W / ndir;
+    pl->ctas = (pl->ngroups + gpc - 1) / gpc;
+    pl->workspace = dirs == 3 ? (size_t)pl->ngroups * pl->piece_len * rpw * sizeof(float) : 0;
+}
+
 int make_plan(const vssm_scan_args *a, int seg_len, Plan *pl)
 {
+    if (a->dstate == vssm::kMaxState) {
+        make_warp_plan(a, seg_len, pl);
+        return VSSM_OK;
+    }
     const unsigned dirs = a->dir_flags;
     pl->dirs = (int)dirs;
     const int R = (dirs == 3) ? kBidirR : kOneDirR;
@@ -157,6 +231,57 @@ int launch_variant(const vssm::ScanParams &p, const Plan &pl, cudaStream_t strea
     return VSSM_OK;
 }
 
+// Address of this device's error word (looked up once per device).
+unsigned *device_error_word()
+{
+    static std::mutex mu;
+    static unsigned *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_vssm_device_error) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<unsigned *>(ptr);
+    }
+    return addr[dev];
+}
+
+template <typename T, int G, int DIRS>
+int launch_warp_variant(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t stream)
+{
+    constexpr int W = warps_per_cta(G);
+    const size_t smem = (size_t)W * vssm::WarpLayout<T, G>::kWarpBytes;
+    auto kern = vssm::warp_scan_kernel<T, G, DIRS, W>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return fail(VSSM_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    kern<<<(unsigned)pl.ctas, W * 32, smem, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    return VSSM_OK;
+}
+
+template <typename T, int G>
+int launch_warp_dirs(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t s)
+{
+    switch (pl.dirs) {
+    case 1: return launch_warp_variant<T, G, 1>(p, pl, s);
+    case 2: return launch_warp_variant<T, G, 2>(p, pl, s);
+    default: return launch_warp_variant<T, G, 3>(p, pl, s);
+    }
+}
+
+template <typename T>
+int launch_warp(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t s)
+{
+    switch (pl.G) {
+    case 1: return launch_warp_dirs<T, 1>(p, pl, s);
+    case 2: return launch_warp_dirs<T, 2>(p, pl, s);
+    default: return launch_warp_dirs<T, 4>(p, pl, s);
+    }
+}
+
 template <typename T>
 int launch_typed(const vssm::ScanParams &p, const Plan &pl, cudaStream_t s)
 {
@@ -180,6 +305,35 @@ int run(const vssm_scan_args *a, int seg_len, bool folded, void *stream)
     if (pl.workspace > 0 && (!a->workspace || a->workspace_bytes < pl.workspace))
         return fail(VSSM_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", pl.workspace,
                     a->workspace ? a->workspace_bytes : (size_t)0);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (pl.warp) {
+        vssm::WarpScanParams w{};
+        w.x = a->x;
+        w.delta = a->delta;
+        w.z = a->z;
+        w.B[0] = a->B;
+        w.C[0] = a->C;
+        w.B[1] = a->B_bwd ? a->B_bwd : a->B;
+        w.C[1] = a->C_bwd ? a->C_bwd : a->C;
+        w.A[0] = a->A_fwd;
+        w.A[1] = a->A_bwd;
+        w.D[0] = a->D_fwd;
+        w.D[1] = a->D_bwd;
+        w.out = a->out;
+        w.ybuf = pl.workspace ? static_cast<float *>(a->workspace) : nullptr;
+        w.err = device_error_word();
+        if (!w.err) return fail(VSSM_ERR_CUDA, "cannot locate the device error word");
+        w.total = (long long)a->batch * a->dim * a->seqlen;
+        w.batch = a->batch;
+        w.dim = a->dim;
+        w.L = a->seqlen;
+        w.seg_len = folded ? seg_len : 0;
+        w.pieces = pl.pieces;
+        w.piece_len = pl.piece_len;
+        w.rgroups = pl.rgroups;
+        w.ngroups = pl.ngroups;
+        return a->dtype == VSSM_F32 ? launch_warp<float>(w, pl, s) : launch_warp<__nv_bfloat16>(w, pl, s);
+    }
     vssm::ScanParams p{};
     p.x = a->x;
     p.delta = a->delta;
@@ -202,7 +356,6 @@ int run(const vssm_scan_args *a, int seg_len, bool folded, void *stream)
     p.pieces = pl.pieces;
     p.piece_len = pl.piece_len;
     p.ypitch = pl.ypitch;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     return a->dtype == VSSM_F32 ? launch_typed<float>(p, pl, s)
                                 : launch_typed<__nv_bfloat16>(p, pl, s);
 }
@@ -230,6 +383,19 @@ int vssm_scan_folded(const vssm_scan_args *a, int seg_len, void *stream)
     return run(a, seg_len, true, stream);
 }
 
+int vssm_device_error(void *stream)
+{
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+    unsigned word = 0, zero = 0;
+    e = cudaMemcpyFromSymbol(&word, g_vssm_device_error, sizeof word);
+    if (e == cudaSuccess && word) e = cudaMemcpyToSymbol(g_vssm_device_error, &zero, sizeof zero);
+    if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "error word: %s", cudaGetErrorString(e));
+    if (word & vssm::kErrTimeout)
+        return fail(VSSM_ERR_TIMEOUT, "a device-side wait exceeded its limit; results are invalid");
+    return VSSM_OK;
+}
+
 const char *vssm_status_string(int status)
 {
     switch (status) {
@@ -238,6 +404,7 @@ const char *vssm_status_string(int status)
     case VSSM_ERR_UNSUPPORTED: return "unsupported configuration";
     case VSSM_ERR_MISALIGNED: return "pointer not 16-byte aligned";
     case VSSM_ERR_CUDA: return "CUDA runtime error";
+    case VSSM_ERR_TIMEOUT: return "device-side wait timed out";
     case VSSM_ERR_WORKSPACE: return "workspace missing or too small";
     default: return "unknown status";
     }

@@ -56,6 +56,7 @@ typedef enum {
     VSSM_ERR_UNSUPPORTED = -2,   /* e.g. dstate > 16, unknown dtype            */
     VSSM_ERR_MISALIGNED = -3,    /* a pointer is not 16-byte aligned           */
     VSSM_ERR_CUDA = -4,          /* the CUDA runtime refused the launch        */
+    VSSM_ERR_TIMEOUT = -5,       /* a bounded device-side wait expired         */
     VSSM_ERR_WORKSPACE = -6      /* workspace missing or smaller than required */
 } vssm_status;
 
@@ -88,9 +89,11 @@ typedef struct {
 /*
  * Bytes of device workspace the call with these arguments needs (0 when it
  * needs none). With both directions, the direction that reaches a token first
- * leaves its partial output there until the other direction arrives; short
- * rows keep that buffer in shared memory and need no workspace. The
- * workspace holds nothing between calls. seg_len as in vssm_scan_folded
+ * leaves its partial output (fp32, one per token and channel) there until the
+ * other direction arrives; a single direction needs no workspace, and with
+ * dstate != 16 short rows keep that buffer in shared memory. The workspace
+ * holds nothing between calls, and two calls in flight at the same time must
+ * not share one. seg_len as in vssm_scan_folded
  * (0 for vssm_scan_bidir). Only `batch`, `dim`, `seqlen`, `dstate`, `dtype`
  * and `dir_flags` of `a` are read.
  */
@@ -114,6 +117,15 @@ int vssm_scan_bidir(const vssm_scan_args *a, void *stream);
  * VSSM_ERR_INVALID_ARG).
  */
 int vssm_scan_folded(const vssm_scan_args *a, int seg_len, void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears this device's error word.
+ * Returns VSSM_ERR_TIMEOUT if a kernel launched by this library since the
+ * last check stopped because one of its bounded waits (for a bulk copy or for
+ * its partner warp; limit 1 s) expired -- its output is then invalid -- and
+ * VSSM_OK otherwise. The kernels never trap and never wait without a limit.
+ */
+int vssm_device_error(void *stream);
 
 /* Static text for a vssm_status value. */
 const char *vssm_status_string(int status);

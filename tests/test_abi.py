@@ -90,9 +90,18 @@ def test_workspace_required_for_long_rows(v):
     assert _call(v, a) == -6                                     # too small
 
 
-def test_short_rows_need_no_workspace(v):
-    a = _args(v, seqlen=197, dim=768, batch=128)
+def test_workspace_sizes(v):
     n = ctypes.c_size_t(123)
+    # general kernel (dstate != 16): short rows keep the y-buffer in shared memory
+    a = _args(v, seqlen=197, dim=768, batch=128, dstate=8)
+    assert v.lib.vssm_scan_workspace_size(ctypes.byref(a), 0, ctypes.byref(n)) == 0
+    assert n.value == 0
+    # warp kernel (dstate == 16): one fp32 partial output per token and channel
+    a = _args(v, seqlen=197, dim=768, batch=128)
+    assert v.lib.vssm_scan_workspace_size(ctypes.byref(a), 0, ctypes.byref(n)) == 0
+    assert n.value == 128 * 768 * 197 * 4
+    # a single direction needs none
+    a = _args(v, seqlen=197, dim=768, batch=128, dir_flags=1)
     assert v.lib.vssm_scan_workspace_size(ctypes.byref(a), 0, ctypes.byref(n)) == 0
     assert n.value == 0
 
