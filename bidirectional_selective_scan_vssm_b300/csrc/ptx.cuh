@@ -72,6 +72,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
     return true;
 }
 
+// Per-thread 16-byte async copy global -> shared (L2-cached only). Bytes past
+// src_bytes (1..16) are zero-filled; dst and src must be 16-byte aligned.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Wait until at most N of this thread's committed copy groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Global -> shared bulk copy; completion is signalled on `bar` as transaction
 // bytes. dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
@@ -98,6 +116,13 @@ __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.w
 
 // Wait until every committed bulk store has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Order this thread's generic-proxy global-memory accesses with later
+// async-proxy (bulk copy) accesses of the same data.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (bulk copy) reads of them.
@@ -133,10 +158,53 @@ __device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c)
     return d;
 }
 
+__device__ __forceinline__ f2 add2(f2 a, f2 b)
+{
+    f2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d.v) : "l"(a.v), "l"(b.v));
+    return d;
+}
+
 __device__ __forceinline__ f2 mul2(f2 a, f2 b)
 {
     f2 d;
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d.v) : "l"(a.v), "l"(b.v));
+    return d;
+}
+
+// Two fp32 pairs from 16 bytes of shared memory (16-byte aligned), kept as
+// 64-bit registers so they feed packed instructions without repacking.
+__device__ __forceinline__ void lds_2xf2(const void *p, f2 &a, f2 &b)
+{
+    asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a.v), "=l"(b.v) : "r"(smem_addr(p)));
+}
+
+// (2^x.lo, 2^x.hi) of a pair, with the products a*b computed first: the
+// argument, both MUFU results and the result pair stay in one register pair.
+__device__ __forceinline__ f2 ex2_mul2(f2 a, f2 b)
+{
+    f2 d;
+    asm("{\n\t.reg .b64 t;\n\t.reg .f32 lo, hi;\n\t"
+        "mul.rn.f32x2 t, %1, %2;\n\t"
+        "mov.b64 {lo, hi}, t;\n\t"
+        "ex2.approx.ftz.f32 lo, lo;\n\t"
+        "ex2.approx.ftz.f32 hi, hi;\n\t"
+        "mov.b64 %0, {lo, hi};\n\t}"
+        : "=l"(d.v) : "l"(a.v), "l"(b.v));
+    return d;
+}
+
+// Same with a*b + c as the argument.
+__device__ __forceinline__ f2 ex2_fma2(f2 a, f2 b, f2 c)
+{
+    f2 d;
+    asm("{\n\t.reg .b64 t;\n\t.reg .f32 lo, hi;\n\t"
+        "fma.rn.f32x2 t, %1, %2, %3;\n\t"
+        "mov.b64 {lo, hi}, t;\n\t"
+        "ex2.approx.ftz.f32 lo, lo;\n\t"
+        "ex2.approx.ftz.f32 hi, hi;\n\t"
+        "mov.b64 %0, {lo, hi};\n\t}"
+        : "=l"(d.v) : "l"(a.v), "l"(b.v), "l"(c.v));
     return d;
 }
 

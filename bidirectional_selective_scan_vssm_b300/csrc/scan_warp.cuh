@@ -9,28 +9,31 @@
 //  * One warp scans one direction of one group. Lane (r, g) = (lane/G, lane%G)
 //    holds states g*NS .. g*NS+NS-1 (NS = 16/G) of channel d0+r in fp32
 //    registers and walks the tokens one at a time (Vim page §2.2: forward in
-//    spatial order, backward in reverse). The recurrence per state and token
-//    (VSSD page §4.1.2, §4.2.1.3) is
+//    spatial order, backward in reverse). Per state and token (VSSD page
+//    §4.1.2, §4.2.1.3):
 //        h = 2^(delta*A*log2e + lambda) * h + (delta*x) * B,   y += C*h
-//    where lambda = -inf at a folded segment start (decay forced to 0) and 0
+//    with lambda = -inf at a folded segment start (decay forced to 0) and 0
 //    elsewhere. Two states share each packed f32x2 instruction.
 //  * Both directions: the two warps of a pair own the same group and meet in
 //    the middle. Phase 0: forward walks the first half up, backward the second
-//    half down, each writing its y (no skip) to the workspace y-buffer with
-//    bulk stores. Phase 1: each walks the other half, bulk-loads the partner's
-//    y, adds the skip (D_fwd + D_bwd) * x, applies silu(z) and stores out.
+//    half down, each storing its y (no skip) to the workspace y-buffer.
+//    Phase 1: each walks the other half, adds the partner's y and the skip
+//    (D_fwd + D_bwd) * x, applies silu(z) and writes the output.
 //
-// Data movement per warp and chunk of kTC tokens: the warp's lanes issue 1-D
-// bulk async copies (TMA engine) of each channel's delta, x (and z) span and
-// of B_t, C_t into a kStages-deep shared-memory ring, completion tracked by
-// one mbarrier per stage. The warp then converts the chunk with lane = token
-// (reads along a channel, conflict-free) into a [token][channel] float4
-// (delta, delta*x, x, z) table and an fp32 B/C/lambda table, so that the scan
-// with lane = channel reads one float4 per token and broadcast B/C. Inputs are
-// read from HBM once and the state never leaves registers.
+// Data movement per warp and chunk of kTC tokens: every lane copies the
+// 16-byte blocks that cover its own channel's delta, x (and z) span into a
+// row slot of a kStages-deep shared-memory ring with per-thread async copies
+// (the tensor's final partial block is zero-filled past its end); B_t, C_t and
+// the partner's y are copied the same way, one block per lane. The scan lanes
+// read delta/x/z straight from their row slots (rows staggered across banks);
+// B/C are widened once per chunk into an fp32 table read by broadcast.
+// Outputs go to a small tile and leave with row-contiguous stores; partial y
+// leaves directly, one coalesced row of RPW values per token. Inputs are read
+// from HBM once and the state never leaves registers.
 //
-// Every wait is bounded (kWaitLimitNs); on expiry the kernel sets a bit in the
-// device error word and the warp stops.
+// The only wait on another warp (the pair rendezvous) is bounded
+// (kWaitLimitNs); on expiry the kernel sets a bit in the device error word
+// and the warp stops.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -42,8 +45,7 @@
 namespace vssm {
 
 constexpr int kTC = 16;          // tokens per chunk
-constexpr int kStages = 2;       // depth of the bulk-copy ring
-constexpr int kBCPitch = 36;     // floats per token: B[16], C[16], lambda, pad
+constexpr int kStages = 2;       // depth of the copy ring
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s
 constexpr unsigned kErrTimeout = 1u;
 
@@ -65,29 +67,39 @@ struct WarpLayout {
     static constexpr int RPW = 32 / G;            // channels per warp
     static constexpr int NS = 16 / G;             // states per lane
     static constexpr int ES = (int)sizeof(T);
-    // bytes per channel span: kTC elements plus up to 16-ES bytes of lead-in
-    // to the 16-byte aligned copy start
-    static constexpr int BOXB = ((16 - ES) + kTC * ES + 15) / 16 * 16;
+    // bytes per row slot: kTC elements plus up to 16-ES bytes of lead-in to
+    // the 16-byte aligned copy start
+    static constexpr int SLOT = ((16 - ES) + kTC * ES + 15) / 16 * 16;
+    // rows are staggered by 16 bytes every 8 rows so that rows r and r+8 fall
+    // on different bank groups
+    static constexpr int ROWB = RPW * SLOT + 16 * ((RPW - 1) >> 3) + 16;
     // one ring stage (bytes)
     static constexpr int oD = 0;
-    static constexpr int oX = oD + RPW * BOXB;
-    static constexpr int oZ = oX + RPW * BOXB;
-    static constexpr int oB = oZ + RPW * BOXB;
+    static constexpr int oX = oD + ROWB;
+    static constexpr int oZ = oX + ROWB;
+    static constexpr int oB = oZ + ROWB;
     static constexpr int oC = oB + kTC * 16 * ES;
     static constexpr int oPY = oC + kTC * 16 * ES;
-    static constexpr int kStageBytes = oPY + kTC * RPW * 4;
+    static constexpr int kStageBytes = (oPY + kTC * RPW * 4 + 15) / 16 * 16;
     // one warp's region (bytes)
-    static constexpr int CP = RPW + 1;            // float4 pitch of the converted table
-    static constexpr int oConv = kStages * kStageBytes;
-    static constexpr int oBC = oConv + kTC * CP * 16;
-    static constexpr int oYS = oBC + kTC * kBCPitch * 4;
-    static constexpr int oBar = oYS + kTC * RPW * 4;
-    static constexpr int kWarpBytes = (oBar + 8 * (kStages + 1) + 127) / 128 * 128;
-    static_assert(BOXB % 16 == 0 && kStageBytes % 16 == 0 && oBar % 16 == 0, "alignment");
+    static constexpr int oBC = kStages * kStageBytes;   // fp32 [kTC][32]: B[16], C[16]
+    // output tile [RPW][OTP] in the output type; the pitch makes the scan's
+    // column writes (one row per lane) land on distinct banks
+    static constexpr int OTP = ES == 2 ? kTC + 2 : kTC + 1;
+    static constexpr int oOT = oBC + kTC * 32 * 4;
+    static constexpr int oBar = (oOT + RPW * OTP * ES + 15) / 16 * 16;
+    static constexpr int kWarpBytes = (oBar + 16 + 127) / 128 * 128;
+    static_assert(SLOT % 16 == 0 && ROWB % 16 == 0 && kStageBytes % 16 == 0 && oBar % 16 == 0,
+                  "alignment");
+
+    __device__ static constexpr int row_off(int r) { return r * SLOT + 16 * (r >> 3); }
 };
 
 __device__ __forceinline__ float ld_as_f32(const float *p) { return *p; }
-__device__ __forceinline__ float ld_as_f32(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+__device__ __forceinline__ float ld_as_f32(const __nv_bfloat16 *p)
+{
+    return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short *>(p)) << 16);
+}
 __device__ __forceinline__ void st_from_f32(float *p, float v) { *p = v; }
 __device__ __forceinline__ void st_from_f32(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
 
@@ -127,223 +139,189 @@ __device__ __forceinline__ float silu_f32(float z)
 template <typename T, int G, int DIRS, int W>
 struct WarpScan {
     using Lay = WarpLayout<T, G>;
-    static constexpr int RPW = Lay::RPW, NS = Lay::NS, CP = Lay::CP;
+    static constexpr int RPW = Lay::RPW, NS = Lay::NS, ES = Lay::ES;
     static constexpr int NDIR = (DIRS == 3) ? 2 : 1;
 
     const WarpScanParams &p;
     unsigned char *wsm;          // this warp's shared region
-    uint64_t *full;              // kStages mbarriers
     uint64_t *pairbar;           // pair rendezvous (both directions)
-    int lane, dir;
+    int lane, dir, r, g;
     long long grp;
     int b, d0, ta, tb;
-    bool ok;                     // false once a wait has timed out
-    uint32_t inflight;           // bit s: stage s has copies issued and not yet waited for
-    uint32_t parity;             // bit s: parity of stage s's next completion
+    bool ok;                     // false once the pair rendezvous has timed out
+    uint32_t lane_emod;          // (element index of (b, d0+r, 0)) mod 16
+    long long lane_erow;         // element index of (b, d0+r, 0)
+    const char *rowp[3];         // this lane's row (b, d0+r, 0) of delta, x, z
+    T *out_row0;                 // output row (b, d0, 0)
 
     __device__ WarpScan(const WarpScanParams &p_) : p(p_) {}
 
     __device__ __forceinline__ unsigned char *stage(int s) const { return wsm + s * Lay::kStageBytes; }
 
-    __device__ __forceinline__ const T *arr(int a) const
+    // Byte offset of token c0 inside its 16-byte block (tensor bases are
+    // 16-byte aligned).
+    __device__ __forceinline__ uint32_t lead_of(uint32_t emod, int c0) const
     {
-        return static_cast<const T *>(a == 0 ? p.delta : (a == 1 ? p.x : p.z));
+        return ((emod + (uint32_t)c0) * ES) & 15u;
     }
 
-    // Bytes of a channel span copied by bulk copy: a full box unless the box
-    // would run past the end of the tensor (then whole 16-byte blocks only).
-    __device__ __forceinline__ uint32_t box_bytes(const T *base, const char *a0) const
-    {
-        const char *tend = reinterpret_cast<const char *>(base + p.total);
-        if (a0 + Lay::BOXB <= tend) return Lay::BOXB;
-        return (uint32_t)((tend - a0) & ~(ptrdiff_t)15);
-    }
-
-    // Issue the bulk copies of chunk [c0, c1) into ring stage s.
+    // Copy chunk [c0, c1) into ring stage s and commit it as one group. Each
+    // row span is copied from the 16-byte boundary at or before token c0 in
+    // whole blocks; a block that would run past the end of the tensor (only
+    // on its final row) is zero-filled past the end instead of read.
     __device__ void issue(int s, int c0, int c1, bool fin)
     {
         unsigned char *st = stage(s);
         const int len = c1 - c0;
-        const bool hasZ = fin && p.z != nullptr;
-        const int narr = hasZ ? 3 : 2;
-        for (int j = lane; j < narr * RPW; j += 32) {
-            const int a = j / RPW, rr = j % RPW;
-            const int d = d0 + rr;
-            if (d >= p.dim) continue;
-            const T *base = arr(a);
-            const char *src = reinterpret_cast<const char *>(base + ((long long)b * p.dim + d) * p.L + c0);
-            const char *a0 = reinterpret_cast<const char *>(reinterpret_cast<uintptr_t>(src) & ~(uintptr_t)15);
-            const uint32_t bytes = box_bytes(base, a0);
-            if (bytes) {
-                mbar_expect_tx(&full[s], bytes);
-                bulk_g2s(st + (a == 0 ? Lay::oD : a == 1 ? Lay::oX : Lay::oZ) + rr * Lay::BOXB, a0, bytes,
-                         &full[s]);
+        if ((G == 1 || g == 0) && d0 + r < p.dim) {
+            const uint32_t lead = lead_of(lane_emod, c0);
+            const int nblk = (int)((lead + (uint32_t)(len * ES) + 15u) >> 4);
+            const long long avail = (p.total - lane_erow - c0) * ES + lead;   // bytes to tensor end
+            const int narr = (fin && p.z != nullptr) ? 3 : 2;
+            const long long off = (long long)c0 * ES - lead;
+            unsigned char *dst = st + Lay::row_off(r);
+            if (avail >= 16 * nblk) {             // every block lies inside the tensor
+                for (int a = 0; a < narr; ++a)
+                    for (int k = 0; k < nblk; ++k)
+                        cp_async16(dst + a * Lay::ROWB + 16 * k, rowp[a] + off + 16 * k, 16u);
+            } else {                              // the tensor's final row: clip the last block
+                for (int a = 0; a < narr; ++a)
+                    for (int k = 0; k < nblk; ++k) {
+                        const long long rem = avail - 16 * k;
+                        cp_async16(dst + a * Lay::ROWB + 16 * k, rowp[a] + off + 16 * k,
+                                   rem >= 16 ? 16u : (uint32_t)rem);
+                    }
             }
         }
-        if (lane == 0 || lane == 1) {
-            const T *src = static_cast<const T *>(lane == 0 ? p.B[dir] : p.C[dir]) + ((long long)b * p.L + c0) * 16;
-            const uint32_t bytes = (uint32_t)(len * 16 * Lay::ES);
-            mbar_expect_tx(&full[s], bytes);
-            bulk_g2s(st + (lane == 0 ? Lay::oB : Lay::oC), src, bytes, &full[s]);
+        {   // B and C: len*ES blocks each, contiguous
+            const int nb = len * ES;
+            const long long boff = ((long long)b * p.L + c0) * 16 * ES;
+            const char *srcB = static_cast<const char *>(p.B[dir]) + boff;
+            const char *srcC = static_cast<const char *>(p.C[dir]) + boff;
+            for (int j = lane; j < nb; j += 32) {
+                cp_async16(st + Lay::oB + 16 * j, srcB + 16 * j, 16u);
+                cp_async16(st + Lay::oC + 16 * j, srcC + 16 * j, 16u);
+            }
         }
-        if (DIRS == 3 && fin && lane == 2) {
-            const float *src = p.ybuf + (grp * p.piece_len + (c0 - ta)) * RPW;
-            const uint32_t bytes = (uint32_t)(len * RPW * 4);
-            mbar_expect_tx(&full[s], bytes);
-            bulk_g2s(st + Lay::oPY, src, bytes, &full[s]);
+        if (DIRS == 3 && fin) {   // partner's partial y, len rows of RPW floats
+            const int nb = len * RPW / 4;
+            const char *src = reinterpret_cast<const char *>(p.ybuf + (grp * p.piece_len + (c0 - ta)) * RPW);
+            for (int j = lane; j < nb; j += 32) cp_async16(st + Lay::oPY + 16 * j, src + 16 * j, 16u);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full[s]);
-        inflight |= 1u << s;
+        cp_async_commit();
     }
 
-    // Wait for stage s (bounded). Records a timeout in the error word.
-    __device__ bool wait_stage(int s)
-    {
-        const bool done = mbar_wait(&full[s], (parity >> s) & 1u, kWaitLimitNs);
-        const bool all = __all_sync(0xffffffffu, done);
-        if (all) {
-            parity ^= 1u << s;
-            inflight &= ~(1u << s);
-        } else if (lane == 0) {
-            atomicOr(p.err, kErrTimeout);
-        }
-        return all;
-    }
-
-    // Convert ring stage s (chunk [c0, c1)) into the float4 table and the B/C table.
-    __device__ void convert(int s, int c0, int c1, bool fin)
+    // Widen the chunk's B_t, C_t into the fp32 table (lane = token x {B, C}).
+    __device__ void widen_bc(int s, int len)
     {
         const unsigned char *st = stage(s);
-        const int len = c1 - c0;
-        float4 *conv = reinterpret_cast<float4 *>(wsm + Lay::oConv);
         float *bc = reinterpret_cast<float *>(wsm + Lay::oBC);
-        const bool hasZ = fin && p.z != nullptr;
-        const int i = lane & 15;
-        const int hsel = lane >> 4;
-#pragma unroll 4
-        for (int rr0 = 0; rr0 < RPW; rr0 += 2) {
-            const int rr = rr0 + hsel;
-            const int d = d0 + rr;
-            float dv = 0.f, xv = 0.f, zv = 0.f;
-            if (i < len && d < p.dim) {
-                const long long e = ((long long)b * p.dim + d) * p.L + c0 + i;
-                const uintptr_t s0 = reinterpret_cast<uintptr_t>(static_cast<const T *>(p.delta) +
-                                                                 (e - i));
-                const uint32_t o = (uint32_t)(s0 & 15u) + (uint32_t)(i * Lay::ES);   // byte in box
-                const T *dbase = static_cast<const T *>(p.delta);
-                const char *a0 = reinterpret_cast<const char *>(s0 & ~(uintptr_t)15);
-                // all activation tensors share the element offset and 16-byte alignment
-                if (o + Lay::ES <= box_bytes(dbase, a0)) {
-                    const int ro = rr * Lay::BOXB + (int)o;
-                    dv = ld_as_f32(reinterpret_cast<const T *>(st + Lay::oD + ro));
-                    xv = ld_as_f32(reinterpret_cast<const T *>(st + Lay::oX + ro));
-                    if (hasZ) zv = ld_as_f32(reinterpret_cast<const T *>(st + Lay::oZ + ro));
-                } else {   // tail of the tensor not covered by whole 16-byte blocks
-                    dv = ld_as_f32(static_cast<const T *>(p.delta) + e);
-                    xv = ld_as_f32(static_cast<const T *>(p.x) + e);
-                    if (hasZ) zv = ld_as_f32(static_cast<const T *>(p.z) + e);
-                }
-            }
-            conv[i * CP + rr] = make_float4(dv, dv * xv, xv, zv);
-        }
-        {
-            const int t2 = lane >> 1, part = lane & 1;     // token, 0: B / 1: C
-            float v[16];
-            if (t2 < len) {
-                load16_f32(reinterpret_cast<const T *>(st + (part ? Lay::oC : Lay::oB)) + t2 * 16, v);
-            } else {
+        const int t2 = lane >> 1, part = lane & 1;
+        float v[16];
+        if (t2 < len) {
+            load16_f32(reinterpret_cast<const T *>(st + (part ? Lay::oC : Lay::oB)) + t2 * 16, v);
+        } else {
 #pragma unroll
-                for (int n = 0; n < 16; ++n) v[n] = 0.f;
-            }
-            float4 *dst = reinterpret_cast<float4 *>(bc + t2 * kBCPitch + part * 16);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            if (part == 0) {
-                float lam = 0.f;
-                if (p.seg_len > 0 && t2 < len) {
-                    const int ph = (c0 + t2) % p.seg_len;
-                    if (ph == (dir == 0 ? 0 : p.seg_len - 1)) lam = -__int_as_float(0x7f800000);
-                }
-                bc[t2 * kBCPitch + 32] = lam;
-            }
+            for (int n = 0; n < 16; ++n) v[n] = 0.f;
         }
+        float4 *dst = reinterpret_cast<float4 *>(bc + t2 * 32 + part * 16);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         __syncwarp();
     }
 
-    // Scan the converted chunk. FIN: last phase (emit output), else partial y.
-    template <int DIR, bool FIN>
-    __device__ __forceinline__ void scan_chunk(f2 (&h)[NS / 2], const f2 (&Ap)[NS / 2], float Dsum,
-                                               bool hasZ, int s)
+    // Bit i set: token c0+i starts a folded segment in this warp's direction.
+    __device__ __forceinline__ uint32_t reset_mask(int c0, int len) const
     {
-        const float4 *conv = reinterpret_cast<const float4 *>(wsm + Lay::oConv);
-        float4 *convw = reinterpret_cast<float4 *>(wsm + Lay::oConv);
+        if (p.seg_len <= 0) return 0u;
+        uint32_t m = 0;
+        const int start = dir == 0 ? 0 : p.seg_len - 1;
+        int ph = c0 % p.seg_len;
+        for (int i = 0; i < len; ++i) {
+            if (ph == start) m |= 1u << i;
+            ph = (ph + 1 == p.seg_len) ? 0 : ph + 1;
+        }
+        return m;
+    }
+
+    // Scan the staged chunk. FIN: last phase (emit output), else partial y.
+    // SEG: folded sequence (segment-start decay forced to 0). Tokens at or
+    // past len (a partial chunk) get delta = x = 0, which leaves h unchanged.
+    template <int DIR, bool FIN, bool SEG, bool GATE>
+    __device__ __forceinline__ void scan_chunk(f2 (&h)[NS / 2], const f2 (&Ap)[NS / 2], float Dsum,
+                                               int s, int c0, int len, uint32_t rmask)
+    {
+        const unsigned char *st = stage(s);
         const float *bc = reinterpret_cast<const float *>(wsm + Lay::oBC);
-        float *ys = reinterpret_cast<float *>(wsm + Lay::oYS);
-        const float *py = reinterpret_cast<const float *>(stage(s) + Lay::oPY);
-        const int r = lane / G, g = lane % G;
+        T *ot = reinterpret_cast<T *>(wsm + Lay::oOT) + r * Lay::OTP;
+        const float *py = reinterpret_cast<const float *>(st + Lay::oPY);
+        float *yrow = (DIRS == 3 && !FIN) ? p.ybuf + (grp * p.piece_len + (c0 - ta)) * RPW + r : nullptr;
+        const uint32_t lead = lead_of(lane_emod, c0);
+        const T *rd = reinterpret_cast<const T *>(st + Lay::oD + Lay::row_off(r) + lead);
+        const T *rx = reinterpret_cast<const T *>(st + Lay::oX + Lay::row_off(r) + lead);
+        const T *rz = reinterpret_cast<const T *>(st + Lay::oZ + Lay::row_off(r) + lead);
+        const int n4 = (len + 3) & ~3;     // tokens visited: len rounded up to the unroll
+#pragma unroll 1
+        for (int k0 = 0; k0 < n4; k0 += 4) {
 #pragma unroll
-        for (int k = 0; k < kTC; ++k) {
-            const int i = (DIR == 0) ? k : (kTC - 1 - k);
-            const float4 v = conv[i * CP + r];
-            const float *bcp = bc + i * kBCPitch;
-            const float lam = bcp[32];
-            const f2 dd = pack2(v.x, v.x), ll = pack2(lam, lam), uu = pack2(v.y, v.y);
-            f2 ya = pack2(0.f, 0.f), yb = pack2(0.f, 0.f);
+            for (int j = 0; j < 4; ++j) {
+                const int i = (DIR == 0) ? (k0 + j) : (n4 - 1 - k0 - j);
+                const uint32_t keep = (uint32_t)((i - len) >> 31);     // all ones if i < len
+                const float dtv = __uint_as_float(__float_as_uint(ld_as_f32(rd + i)) & keep);
+                const float xv = __uint_as_float(__float_as_uint(ld_as_f32(rx + i)) & keep);
+                const float dx = dtv * xv;
+                const f2 dd = pack2(dtv, dtv), uu = pack2(dx, dx);
+                const float *bcp = bc + i * 32;
+                f2 ya = pack2(0.f, 0.f), yb = pack2(0.f, 0.f);
+                f2 ll = pack2(0.f, 0.f);
+                if (SEG) {                        // -inf at a segment start, else 0
+                    const float lam = __uint_as_float(0xff800000u & (0u - ((rmask >> i) & 1u)));
+                    ll = pack2(lam, lam);
+                }
 #pragma unroll
-            for (int q = 0; q < NS / 4; ++q) {
-                const float4 Bq = *reinterpret_cast<const float4 *>(bcp + g * NS + 4 * q);
-                const float4 Cq = *reinterpret_cast<const float4 *>(bcp + 16 + g * NS + 4 * q);
-                const float2 a0 = unpack2(fma2(dd, Ap[2 * q], ll));
-                const float2 a1 = unpack2(fma2(dd, Ap[2 * q + 1], ll));
-                const f2 e0 = pack2(ex2_mufu(a0.x), ex2_mufu(a0.y));
-                const f2 e1 = pack2(ex2_mufu(a1.x), ex2_mufu(a1.y));
-                h[2 * q] = fma2(e0, h[2 * q], mul2(uu, pack2(Bq.x, Bq.y)));
-                h[2 * q + 1] = fma2(e1, h[2 * q + 1], mul2(uu, pack2(Bq.z, Bq.w)));
-                ya = fma2(pack2(Cq.x, Cq.y), h[2 * q], ya);
-                yb = fma2(pack2(Cq.z, Cq.w), h[2 * q + 1], yb);
-            }
-            const float2 y2a = unpack2(ya), y2b = unpack2(yb);
-            float y = (y2a.x + y2a.y) + (y2b.x + y2b.y);
-            if (G >= 2) y += __shfl_xor_sync(0xffffffffu, y, 1);
-            if (G >= 4) y += __shfl_xor_sync(0xffffffffu, y, 2);
-            if (!FIN) {
-                if (g == 0) ys[i * RPW + r] = y;
-            } else {
-                float tot = y + fmaf(Dsum, v.z, (DIRS == 3) ? py[i * RPW + r] : 0.f);
-                if (hasZ) tot *= silu_f32(v.w);
-                if (g == 0) convw[i * CP + r].x = tot;
+                for (int q = 0; q < NS / 4; ++q) {
+                    f2 B0, B1, C0, C1;
+                    lds_2xf2(bcp + g * NS + 4 * q, B0, B1);
+                    lds_2xf2(bcp + 16 + g * NS + 4 * q, C0, C1);
+                    const f2 e0 = SEG ? ex2_fma2(dd, Ap[2 * q], ll) : ex2_mul2(dd, Ap[2 * q]);
+                    const f2 e1 = SEG ? ex2_fma2(dd, Ap[2 * q + 1], ll) : ex2_mul2(dd, Ap[2 * q + 1]);
+                    h[2 * q] = fma2(e0, h[2 * q], mul2(uu, B0));
+                    h[2 * q + 1] = fma2(e1, h[2 * q + 1], mul2(uu, B1));
+                    ya = fma2(C0, h[2 * q], ya);
+                    yb = fma2(C1, h[2 * q + 1], yb);
+                }
+                const float2 y2 = unpack2(add2(ya, yb));
+                float y = y2.x + y2.y;
+                if (G >= 2) y += __shfl_xor_sync(0xffffffffu, y, 1);
+                if (G >= 4) y += __shfl_xor_sync(0xffffffffu, y, 2);
+                if (!FIN) {
+                    if (DIRS == 3 && g == 0 && i < len) yrow[i * RPW] = y;
+                } else {
+                    float tot = y + fmaf(Dsum, xv, (DIRS == 3) ? py[i * RPW + r] : 0.f);
+                    if (GATE) tot *= silu_f32(ld_as_f32(rz + i));
+                    if (g == 0) st_from_f32(ot + i, tot);
+                }
             }
         }
         __syncwarp();
     }
 
-    // Store the chunk's outputs (lane = token, two channels per instruction).
+    // Write the chunk's outputs from the output tile with row-contiguous
+    // stores: lane = token within the chunk, 32/kTC rows per pass.
     __device__ void store_out(int c0, int c1)
     {
-        const float4 *conv = reinterpret_cast<const float4 *>(wsm + Lay::oConv);
-        T *out = static_cast<T *>(p.out);
+        const T *ot = reinterpret_cast<const T *>(wsm + Lay::oOT);
+        constexpr int RPI = 32 / kTC;                 // rows per pass
         const int len = c1 - c0;
-        const int i = lane & 15, hsel = lane >> 4;
+        const int i = lane % kTC, sub = lane / kTC;
+        const int rows = min(RPW, p.dim - d0);
+        T *op = out_row0 + (long long)sub * p.L + c0 + i;
+        const long long step = (long long)RPI * p.L;
+        if (i < len) {
 #pragma unroll 4
-        for (int rr0 = 0; rr0 < RPW; rr0 += 2) {
-            const int rr = rr0 + hsel;
-            const int d = d0 + rr;
-            if (i < len && d < p.dim)
-                st_from_f32(out + ((long long)b * p.dim + d) * p.L + c0 + i, conv[i * CP + rr].x);
+            for (int rr = sub; rr < rows; rr += RPI, op += step) *op = ot[rr * Lay::OTP + i];
         }
-    }
-
-    // Bulk-store the chunk's partial y to the y-buffer.
-    __device__ void store_partial(int c0, int c1)
-    {
-        float *ys = reinterpret_cast<float *>(wsm + Lay::oYS);
-        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-            bulk_s2g(p.ybuf + (grp * p.piece_len + (c0 - ta)) * RPW, ys, (uint32_t)((c1 - c0) * RPW * 4));
-            bulk_commit();
-        }
     }
 
     __device__ void chunk_range(int k, int lo, int hi, int &c0, int &c1) const
@@ -357,10 +335,17 @@ struct WarpScan {
         }
     }
 
+    template <bool FIN, bool SEG, bool GATE>
+    __device__ __forceinline__ void scan_dispatch(f2 (&h)[NS / 2], const f2 (&Ap)[NS / 2], float Dsum,
+                                                  int s, int c0, int len, uint32_t rmask)
+    {
+        if (dir == 0) scan_chunk<0, FIN, SEG, GATE>(h, Ap, Dsum, s, c0, len, rmask);
+        else scan_chunk<1, FIN, SEG, GATE>(h, Ap, Dsum, s, c0, len, rmask);
+    }
+
     __device__ void run()
     {
         // ---- per-lane parameters
-        const int r = lane / G, g = lane % G;
         const int d = d0 + r;
         const bool active = d < p.dim;
         constexpr float kLog2e = 1.4426950408889634f;
@@ -382,11 +367,12 @@ struct WarpScan {
             }
         }
         const bool hasZ = p.z != nullptr;
+        const bool seg = p.seg_len > 0;
 
         const int Lv = tb - ta;
         const int H = (DIRS == 3) ? (Lv + 1) / 2 : Lv;
         const int nphase = (DIRS == 3) ? 2 : 1;
-        uint32_t kk = 0;   // chunks consumed so far (ring position)
+        uint32_t kk = 0;   // ring position
         for (int phase = 0; phase < nphase && ok; ++phase) {
             const bool fin = (phase == nphase - 1);
             int lo, hi;
@@ -399,48 +385,53 @@ struct WarpScan {
                 hi = tb;
             }
             const int nk = (hi - lo + kTC - 1) / kTC;
-            for (int k = 0; k < kStages && k < nk; ++k) {
-                int c0, c1;
-                chunk_range(k, lo, hi, c0, c1);
-                issue((kk + k) % kStages, c0, c1, fin);
+            // One copy group per ring slot in flight (empty groups past the end
+            // keep the group count uniform).
+            for (int k = 0; k < kStages; ++k) {
+                if (k < nk) {
+                    int c0, c1;
+                    chunk_range(k, lo, hi, c0, c1);
+                    issue((kk + k) % kStages, c0, c1, fin);
+                } else {
+                    cp_async_commit();
+                }
             }
             for (int k = 0; k < nk; ++k, ++kk) {
                 const int s = kk % kStages;
                 int c0, c1;
                 chunk_range(k, lo, hi, c0, c1);
-                if (!wait_stage(s)) {
-                    ok = false;
-                    break;
-                }
-                convert(s, c0, c1, fin);
-                if (!fin) {                      // the staging buffer of the previous bulk store
-                    if (lane == 0) bulk_wait_read();
-                    __syncwarp();
-                }
-                if (dir == 0) {
-                    if (fin) scan_chunk<0, true>(h, Ap, Dsum, hasZ, s);
-                    else scan_chunk<0, false>(h, Ap, Dsum, hasZ, s);
+                cp_async_wait<kStages - 1>();
+                __syncwarp();
+                const int len = c1 - c0;
+                widen_bc(s, len);
+                const uint32_t rmask = reset_mask(c0, len);
+                if (fin) {
+                    if (seg) {
+                        if (hasZ) scan_dispatch<true, true, true>(h, Ap, Dsum, s, c0, len, rmask);
+                        else scan_dispatch<true, true, false>(h, Ap, Dsum, s, c0, len, rmask);
+                    } else {
+                        if (hasZ) scan_dispatch<true, false, true>(h, Ap, Dsum, s, c0, len, rmask);
+                        else scan_dispatch<true, false, false>(h, Ap, Dsum, s, c0, len, rmask);
+                    }
+                    store_out(c0, c1);
                 } else {
-                    if (fin) scan_chunk<1, true>(h, Ap, Dsum, hasZ, s);
-                    else scan_chunk<1, false>(h, Ap, Dsum, hasZ, s);
+                    if (seg) scan_dispatch<false, true, false>(h, Ap, Dsum, s, c0, len, rmask);
+                    else scan_dispatch<false, false, false>(h, Ap, Dsum, s, c0, len, rmask);
                 }
                 if (k + kStages < nk) {
                     int n0, n1;
                     chunk_range(k + kStages, lo, hi, n0, n1);
                     issue(s, n0, n1, fin);
+                } else {
+                    cp_async_commit();
                 }
-                if (fin) store_out(c0, c1);
-                else store_partial(c0, c1);
-                __syncwarp();
             }
+            cp_async_wait<0>();
             if (DIRS == 3 && phase == 0) {
                 // Partial y fully written before the partner reads it.
-                if (lane == 0) {
-                    bulk_wait_all();
-                    __threadfence();
-                    mbar_arrive(pairbar);
-                }
+                __threadfence();
                 __syncwarp();
+                if (lane == 0) mbar_arrive(pairbar);
                 bool met = mbar_wait(pairbar, 0, kWaitLimitNs);
                 if (!__all_sync(0xffffffffu, met)) {
                     if (lane == 0) atomicOr(p.err, kErrTimeout);
@@ -448,18 +439,25 @@ struct WarpScan {
                 }
             }
         }
-        if (!ok) {
-            // Let copies already issued land before the warp's shared memory
-            // goes away (each wait again bounded).
-            for (int s = 0; s < kStages; ++s)
-                if (inflight & (1u << s)) (void)mbar_wait(&full[s], (parity >> s) & 1u, kWaitLimitNs);
-        }
-        if (lane == 0) bulk_wait_all();
+        cp_async_wait<0>();
     }
 };
 
+// CTAs per SM that the shared-memory footprint allows; used as the register
+// budget hint so that registers never limit residency below it.
+template <typename T, int G, int W>
+constexpr int warp_scan_min_blocks()
+{
+    return (227 * 1024) / (W * WarpLayout<T, G>::kWarpBytes) < 1
+               ? 1
+               : ((227 * 1024) / (W * WarpLayout<T, G>::kWarpBytes) > 8
+                      ? 8
+                      : (227 * 1024) / (W * WarpLayout<T, G>::kWarpBytes));
+}
+
 template <typename T, int G, int DIRS, int W>
-__global__ void __launch_bounds__(W * 32) warp_scan_kernel(const WarpScanParams p)
+__global__ void __launch_bounds__(W * 32, (warp_scan_min_blocks<T, G, W>()))
+warp_scan_kernel(const WarpScanParams p)
 {
     using Lay = WarpLayout<T, G>;
     constexpr int NDIR = (DIRS == 3) ? 2 : 1;
@@ -468,17 +466,14 @@ __global__ void __launch_bounds__(W * 32) warp_scan_kernel(const WarpScanParams 
     const int warp = threadIdx.x >> 5;
     WarpScan<T, G, DIRS, W> ws(p);
     ws.lane = threadIdx.x & 31;
+    ws.r = ws.lane / G;
+    ws.g = ws.lane % G;
     ws.wsm = smem_raw + warp * Lay::kWarpBytes;
-    ws.full = reinterpret_cast<uint64_t *>(ws.wsm + Lay::oBar);
-    ws.pairbar = reinterpret_cast<uint64_t *>(smem_raw + (warp - warp % NDIR) * Lay::kWarpBytes + Lay::oBar) +
-                 kStages;
+    ws.pairbar = reinterpret_cast<uint64_t *>(smem_raw + (warp - warp % NDIR) * Lay::kWarpBytes + Lay::oBar);
     ws.dir = (DIRS == 3) ? (warp % 2) : (DIRS == 1 ? 0 : 1);
     ws.ok = true;
-    ws.inflight = 0;
-    ws.parity = 0;
-    if (ws.lane == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&ws.full[s], 1);
-        if (DIRS == 3 && warp % 2 == 0) mbar_init(ws.pairbar, 2);
+    if (DIRS == 3 && ws.lane == 0 && warp % 2 == 0) {
+        mbar_init(ws.pairbar, 2);
         fence_mbar_init();
     }
     __syncthreads();
@@ -492,6 +487,13 @@ __global__ void __launch_bounds__(W * 32) warp_scan_kernel(const WarpScanParams 
     ws.d0 = rg * Lay::RPW;
     ws.ta = piece * p.piece_len;
     ws.tb = min(p.L, ws.ta + p.piece_len);
+    const long long e0 = ((long long)ws.b * p.dim + ws.d0) * p.L;
+    ws.lane_erow = e0 + (long long)ws.r * p.L;
+    ws.lane_emod = (uint32_t)(ws.lane_erow & 15);
+    ws.rowp[0] = static_cast<const char *>(p.delta) + ws.lane_erow * Lay::ES;
+    ws.rowp[1] = static_cast<const char *>(p.x) + ws.lane_erow * Lay::ES;
+    ws.rowp[2] = p.z ? static_cast<const char *>(p.z) + ws.lane_erow * Lay::ES : nullptr;
+    ws.out_row0 = static_cast<T *>(p.out) + e0;
     ws.run();
 }
 

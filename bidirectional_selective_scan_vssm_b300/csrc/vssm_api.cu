@@ -76,7 +76,7 @@ int warp_bytes(int G)
     }
 }
 
-constexpr int warps_per_cta(int G) { return G == 4 ? 8 : 4; }
+constexpr int warps_per_cta(int G) { return G == 4 ? 8 : (G == 2 ? 4 : 2); }
 
 // Plan for the warp kernel (dstate == 16).
 void make_warp_plan(const vssm_scan_args *a, int seg_len, Plan *pl)
