@@ -46,6 +46,10 @@ namespace vssm {
 
 constexpr int kTC = 16;          // tokens per chunk
 constexpr int kStages = 2;       // depth of the copy ring
+#ifndef VSSM_SCAN_UNROLL
+#define VSSM_SCAN_UNROLL 2
+#endif
+constexpr int kUnroll = VSSM_SCAN_UNROLL;   // tokens per unrolled scan step
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s
 constexpr unsigned kErrTimeout = 1u;
 
@@ -86,7 +90,8 @@ struct WarpLayout {
     // output tile [RPW][OTP] in the output type; the pitch makes the scan's
     // column writes (one row per lane) land on distinct banks
     static constexpr int OTP = ES == 2 ? kTC + 2 : kTC + 1;
-    static constexpr int oOT = oBC + kTC * 32 * 4;
+    static constexpr int oYS = oBC + kTC * 32 * 4;      // fp32 [kTC][RPW] partial y
+    static constexpr int oOT = oYS + kTC * RPW * 4;
     static constexpr int oBar = (oOT + RPW * OTP * ES + 15) / 16 * 16;
     static constexpr int kWarpBytes = (oBar + 16 + 127) / 128 * 128;
     static_assert(SLOT % 16 == 0 && ROWB % 16 == 0 && kStageBytes % 16 == 0 && oBar % 16 == 0,
@@ -131,8 +136,17 @@ __device__ __forceinline__ void load16_f32(const __nv_bfloat16 *src, float *dst)
     }
 }
 
+// silu(z) = z * sigmoid(z). For fp32 outputs: z / (1 + 2^(-z*log2e)). For
+// 16-bit outputs the identity z*sigmoid(z) = h + h*tanh(h), h = z/2, needs one
+// MUFU operation instead of two; tanh.approx's error (about 2^-11 relative)
+// stays below the output's own rounding (2^-9).
+template <typename T>
 __device__ __forceinline__ float silu_f32(float z)
 {
+    if (sizeof(T) == 2) {
+        const float hz = 0.5f * z;
+        return fmaf(hz, tanh_mufu(hz), hz);
+    }
     return __fdividef(z, 1.0f + ex2_mufu(-1.4426950408889634f * z));
 }
 
@@ -245,8 +259,9 @@ struct WarpScan {
     }
 
     // Scan the staged chunk. FIN: last phase (emit output), else partial y.
-    // SEG: folded sequence (segment-start decay forced to 0). Tokens at or
-    // past len (a partial chunk) get delta = x = 0, which leaves h unchanged.
+    // SEG: folded sequence (segment-start decay forced to 0). Tokens past len
+    // up to the unroll multiple read delta = x = 0 (zero_tail), which leaves
+    // h unchanged.
     template <int DIR, bool FIN, bool SEG, bool GATE>
     __device__ __forceinline__ void scan_chunk(f2 (&h)[NS / 2], const f2 (&Ap)[NS / 2], float Dsum,
                                                int s, int c0, int len, uint32_t rmask)
@@ -255,20 +270,19 @@ struct WarpScan {
         const float *bc = reinterpret_cast<const float *>(wsm + Lay::oBC);
         T *ot = reinterpret_cast<T *>(wsm + Lay::oOT) + r * Lay::OTP;
         const float *py = reinterpret_cast<const float *>(st + Lay::oPY);
-        float *yrow = (DIRS == 3 && !FIN) ? p.ybuf + (grp * p.piece_len + (c0 - ta)) * RPW + r : nullptr;
+        float *ys = reinterpret_cast<float *>(wsm + Lay::oYS);
         const uint32_t lead = lead_of(lane_emod, c0);
         const T *rd = reinterpret_cast<const T *>(st + Lay::oD + Lay::row_off(r) + lead);
         const T *rx = reinterpret_cast<const T *>(st + Lay::oX + Lay::row_off(r) + lead);
         const T *rz = reinterpret_cast<const T *>(st + Lay::oZ + Lay::row_off(r) + lead);
-        const int n4 = (len + 3) & ~3;     // tokens visited: len rounded up to the unroll
+        const int n4 = (len + kUnroll - 1) / kUnroll * kUnroll;   // len rounded up to the unroll
 #pragma unroll 1
-        for (int k0 = 0; k0 < n4; k0 += 4) {
+        for (int k0 = 0; k0 < n4; k0 += kUnroll) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < kUnroll; ++j) {
                 const int i = (DIR == 0) ? (k0 + j) : (n4 - 1 - k0 - j);
-                const uint32_t keep = (uint32_t)((i - len) >> 31);     // all ones if i < len
-                const float dtv = __uint_as_float(__float_as_uint(ld_as_f32(rd + i)) & keep);
-                const float xv = __uint_as_float(__float_as_uint(ld_as_f32(rx + i)) & keep);
+                const float dtv = ld_as_f32(rd + i);
+                const float xv = ld_as_f32(rx + i);
                 const float dx = dtv * xv;
                 const f2 dd = pack2(dtv, dtv), uu = pack2(dx, dx);
                 const float *bcp = bc + i * 32;
@@ -294,16 +308,48 @@ struct WarpScan {
                 float y = y2.x + y2.y;
                 if (G >= 2) y += __shfl_xor_sync(0xffffffffu, y, 1);
                 if (G >= 4) y += __shfl_xor_sync(0xffffffffu, y, 2);
+                // (all G lanes of a channel hold the same y and store it alike)
                 if (!FIN) {
-                    if (DIRS == 3 && g == 0 && i < len) yrow[i * RPW] = y;
+                    if (DIRS == 3) ys[i * RPW + r] = y;
                 } else {
                     float tot = y + fmaf(Dsum, xv, (DIRS == 3) ? py[i * RPW + r] : 0.f);
-                    if (GATE) tot *= silu_f32(ld_as_f32(rz + i));
-                    if (g == 0) st_from_f32(ot + i, tot);
+                    if (GATE) tot *= silu_f32<T>(ld_as_f32(rz + i));
+                    st_from_f32(ot + i, tot);
                 }
             }
         }
         __syncwarp();
+    }
+
+    // Zero delta and x of the tokens between len and the unroll multiple in
+    // this lane's row slot (only for a partial chunk).
+    __device__ void zero_tail(int s, int c0, int len)
+    {
+        const int n4 = (len + kUnroll - 1) / kUnroll * kUnroll;
+        if (n4 != len && (G == 1 || g == 0)) {
+            unsigned char *st = stage(s);
+            const uint32_t lead = lead_of(lane_emod, c0);
+            T *rd = reinterpret_cast<T *>(st + Lay::oD + Lay::row_off(r) + lead);
+            T *rx = reinterpret_cast<T *>(st + Lay::oX + Lay::row_off(r) + lead);
+            for (int i = len; i < n4; ++i) {
+                rd[i] = T(0.f);
+                rx[i] = T(0.f);
+            }
+        }
+        __syncwarp();
+    }
+
+    // Bulk-store the chunk's partial y (rows c0..c1-1 of RPW floats) to the
+    // y-buffer.
+    __device__ void store_partial(int c0, int c1)
+    {
+        float *ys = reinterpret_cast<float *>(wsm + Lay::oYS);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            bulk_s2g(p.ybuf + (grp * p.piece_len + (c0 - ta)) * RPW, ys, (uint32_t)((c1 - c0) * RPW * 4));
+            bulk_commit();
+        }
     }
 
     // Write the chunk's outputs from the output tile with row-contiguous
@@ -403,8 +449,13 @@ struct WarpScan {
                 cp_async_wait<kStages - 1>();
                 __syncwarp();
                 const int len = c1 - c0;
+                zero_tail(s, c0, len);
                 widen_bc(s, len);
                 const uint32_t rmask = reset_mask(c0, len);
+                if (DIRS == 3 && !fin) {          // ys is free once the previous bulk store read it
+                    if (lane == 0) bulk_wait_read();
+                    __syncwarp();
+                }
                 if (fin) {
                     if (seg) {
                         if (hasZ) scan_dispatch<true, true, true>(h, Ap, Dsum, s, c0, len, rmask);
@@ -417,6 +468,7 @@ struct WarpScan {
                 } else {
                     if (seg) scan_dispatch<false, true, false>(h, Ap, Dsum, s, c0, len, rmask);
                     else scan_dispatch<false, false, false>(h, Ap, Dsum, s, c0, len, rmask);
+                    if (DIRS == 3) store_partial(c0, c1);
                 }
                 if (k + kStages < nk) {
                     int n0, n1;
@@ -429,6 +481,7 @@ struct WarpScan {
             cp_async_wait<0>();
             if (DIRS == 3 && phase == 0) {
                 // Partial y fully written before the partner reads it.
+                if (lane == 0) bulk_wait_all();
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(pairbar);
@@ -440,6 +493,7 @@ struct WarpScan {
             }
         }
         cp_async_wait<0>();
+        if (lane == 0) bulk_wait_all();
     }
 };
 
