@@ -30,8 +30,10 @@ STATUS = {0: "VSSM_OK", -1: "VSSM_ERR_INVALID_ARG", -2: "VSSM_ERR_UNSUPPORTED",
           -6: "VSSM_ERR_WORKSPACE"}
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libvssm.so")
-EXPORTS = ["vssm_scan_bidir", "vssm_scan_folded", "vssm_scan_workspace_size",
-           "vssm_device_error", "vssm_status_string", "vssm_last_error", "vssm_version"]
+EXPORTS = ["vssm_scan_bidir", "vssm_scan_bidir_noalloc", "vssm_scan_folded",
+           "vssm_scan_workspace_size", "vssm_device_error", "vssm_status_string",
+           "vssm_last_error", "vssm_version"]
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class ScanArgs(ctypes.Structure):
@@ -64,6 +66,8 @@ def _load():
     P = ctypes.POINTER(ScanArgs)
     lib.vssm_scan_bidir.argtypes = [P, ctypes.c_void_p]
     lib.vssm_scan_bidir.restype = ctypes.c_int
+    lib.vssm_scan_bidir_noalloc.argtypes = [P, ctypes.c_void_p]
+    lib.vssm_scan_bidir_noalloc.restype = ctypes.c_int
     lib.vssm_scan_folded.argtypes = [P, ctypes.c_int, ctypes.c_void_p]
     lib.vssm_scan_folded.restype = ctypes.c_int
     lib.vssm_scan_workspace_size.argtypes = [P, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
@@ -181,6 +185,21 @@ def scan_bidir(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None,
         out = torch.empty_like(x)
     a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, out, B_bwd, C_bwd, dirs)
     _launch(lib.vssm_scan_bidir, a, None, x.device, workspace, stream)
+    return out
+
+
+def scan_bidir_noalloc(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None,
+                       dirs: int = DIR_BOTH, out=None, B_bwd=None, C_bwd=None,
+                       stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """``vssm_scan_bidir_noalloc``: the same scan as :func:`scan_bidir` with the
+    library's built-in scratch instead of a workspace (for callers that cannot
+    allocate device memory; calls share the scratch, so keep them on one
+    stream). ``out`` is allocated here only when not given."""
+    if out is None:
+        out = torch.empty_like(x)
+    a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, out, B_bwd, C_bwd, dirs)
+    stream = stream if stream is not None else torch.cuda.current_stream(x.device)
+    _check(lib.vssm_scan_bidir_noalloc(ctypes.byref(a), ctypes.c_void_p(stream.cuda_stream)))
     return out
 
 

@@ -18,6 +18,11 @@
 // device that loads the library).
 __device__ unsigned g_vssm_device_error;
 
+// Built-in scratch of vssm_scan_bidir_noalloc: stands in for the caller's
+// workspace. Every device that loads the library holds it until the process
+// exits; host code reaches it only through noalloc_scratch() below.
+static __device__ __align__(256) unsigned char g_vssm_noalloc_scratch[VSSM_NOALLOC_SCRATCH_BYTES];
+
 namespace {
 
 thread_local std::string g_last_error;
@@ -247,6 +252,32 @@ unsigned *device_error_word()
     return addr[dev];
 }
 
+// Device address of this device's built-in scratch, looked up once per
+// device with that device current. In host code the array's name is only a
+// host-side handle, so kernels are given this address instead.
+void *noalloc_scratch()
+{
+    static std::mutex mu;
+    static void *addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        fail(VSSM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_vssm_noalloc_scratch);
+        if (e != cudaSuccess) {
+            fail(VSSM_ERR_CUDA, "cudaGetSymbolAddress(built-in scratch): %s", cudaGetErrorString(e));
+            return nullptr;
+        }
+        addr[dev] = ptr;
+    }
+    return addr[dev];
+}
+
 template <typename T, int G, int DIRS>
 int launch_warp_variant(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t stream)
 {
@@ -377,6 +408,28 @@ int vssm_scan_workspace_size(const vssm_scan_args *a, int seg_len, size_t *bytes
 }
 
 int vssm_scan_bidir(const vssm_scan_args *a, void *stream) { return run(a, 0, false, stream); }
+
+int vssm_scan_bidir_noalloc(const vssm_scan_args *a, void *stream)
+{
+    if (!a) return fail(VSSM_ERR_INVALID_ARG, "args is NULL");
+    vssm_scan_args b = *a;                 // the caller's workspace fields are ignored
+    b.workspace = nullptr;
+    b.workspace_bytes = 0;
+    size_t need = 0;
+    const int st = vssm_scan_workspace_size(&b, 0, &need);
+    if (st != VSSM_OK) return st;
+    if (need > VSSM_NOALLOC_SCRATCH_BYTES)
+        return fail(VSSM_ERR_UNSUPPORTED,
+                    "vssm_scan_bidir_noalloc: this call needs %zu bytes of scratch but the built-in "
+                    "scratch holds %zu (VSSM_NOALLOC_SCRATCH_BYTES); use vssm_scan_bidir with a workspace",
+                    need, (size_t)VSSM_NOALLOC_SCRATCH_BYTES);
+    if (need > 0) {
+        b.workspace = noalloc_scratch();
+        if (!b.workspace) return VSSM_ERR_CUDA;
+        b.workspace_bytes = VSSM_NOALLOC_SCRATCH_BYTES;
+    }
+    return run(&b, 0, false, stream);
+}
 
 int vssm_scan_folded(const vssm_scan_args *a, int seg_len, void *stream)
 {

@@ -107,6 +107,44 @@ int vssm_scan_workspace_size(const vssm_scan_args *a, int seg_len, size_t *bytes
 int vssm_scan_bidir(const vssm_scan_args *a, void *stream);
 
 /*
+ * Bytes of the built-in scratch that vssm_scan_bidir_noalloc uses (16 MiB).
+ * A call needs as much scratch as vssm_scan_workspace_size reports for it;
+ * for bidirectional calls with dstate 16 that is 4 bytes per token and
+ * channel (rounded up to whole 32-channel groups), so up to about 4.19
+ * million token-channels fit.
+ */
+#define VSSM_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * vssm_scan_bidir for callers that cannot allocate device memory. (The pages
+ * have no counterpart to this: it only changes where the scratch lives.)
+ *
+ * vssm_scan_bidir needs a device workspace from its caller for bidirectional
+ * calls. Some callers cannot provide one: a plain C or embedded host program
+ * with no device allocator of its own, or a serving loop that must not call
+ * cudaMalloc once it is running (an allocation can synchronise the device or
+ * fail under memory pressure). This entry point computes exactly what
+ * vssm_scan_bidir computes, with the same arguments and layouts, but takes
+ * its scratch from an array of VSSM_NOALLOC_SCRATCH_BYTES that the library
+ * holds in device memory on every device that loads it, until the process
+ * exits. It allocates nothing, and a->workspace and a->workspace_bytes are
+ * ignored. The caller still owns all inputs and the output.
+ *
+ *  - A call that would need more than VSSM_NOALLOC_SCRATCH_BYTES of scratch
+ *    is rejected with VSSM_ERR_UNSUPPORTED before anything is launched (see
+ *    vssm_last_error()); pass a workspace to vssm_scan_bidir instead.
+ *  - The first call on a device looks up the scratch's device address
+ *    (cudaGetSymbolAddress, with that device current). Make that first call
+ *    before any stream capture on that device.
+ *  - All calls share the one array, and it keeps the last call's contents.
+ *    Nothing in it has to start at zero: a call writes every scratch value
+ *    before it reads it. Calls that overlap on the GPU (on different streams,
+ *    or issued from different host threads without ordering) race on the
+ *    scratch and give wrong results; order them on one stream.
+ */
+int vssm_scan_bidir_noalloc(const vssm_scan_args *a, void *stream);
+
+/*
  * Batch-folded scan: each row of seqlen tokens is a concatenation of
  * segments of seg_len tokens with the state reset at every segment start
  * (SF-Mamba page, "批量折叠与周期性状态重置"; folded tensor Z' of shape
