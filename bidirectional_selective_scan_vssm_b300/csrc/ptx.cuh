@@ -81,6 +81,14 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t 
                  : "memory");
 }
 
+// Store v to global memory when pred holds (a predicated store, no branch).
+__device__ __forceinline__ void st_global_if(float *ptr, float v, bool pred)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p st.global.f32 [%0], %1;\n\t}" ::"l"(ptr),
+                 "f"(v), "r"((unsigned)pred)
+                 : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
 // Wait until at most N of this thread's committed copy groups are pending.

@@ -66,7 +66,7 @@ struct WarpScanParams {
     long long ngroups;           // batch * pieces * rgroups
 };
 
-template <typename T, int G>
+template <typename T, int G, bool BIDIR>
 struct WarpLayout {
     static constexpr int RPW = 32 / G;            // channels per warp
     static constexpr int NS = 16 / G;             // states per lane
@@ -76,7 +76,7 @@ struct WarpLayout {
     static constexpr int SLOT = ((16 - ES) + kTC * ES + 15) / 16 * 16;
     // rows are staggered by 16 bytes every 8 rows so that rows r and r+8 fall
     // on different bank groups
-    static constexpr int ROWB = RPW * SLOT + 16 * ((RPW - 1) >> 3) + 16;
+    static constexpr int ROWB = RPW * SLOT + 16 * ((RPW - 1) >> 3);
     // one ring stage (bytes)
     static constexpr int oD = 0;
     static constexpr int oX = oD + ROWB;
@@ -84,16 +84,15 @@ struct WarpLayout {
     static constexpr int oB = oZ + ROWB;
     static constexpr int oC = oB + kTC * 16 * ES;
     static constexpr int oPY = oC + kTC * 16 * ES;
-    static constexpr int kStageBytes = (oPY + kTC * RPW * 4 + 15) / 16 * 16;
+    static constexpr int kStageBytes = (oPY + (BIDIR ? kTC * RPW * 4 : 0) + 15) / 16 * 16;
     // one warp's region (bytes)
     static constexpr int oBC = kStages * kStageBytes;   // fp32 [kTC][32]: B[16], C[16]
     // output tile [RPW][OTP] in the output type; the pitch makes the scan's
     // column writes (one row per lane) land on distinct banks
     static constexpr int OTP = ES == 2 ? kTC + 2 : kTC + 1;
-    static constexpr int oYS = oBC + kTC * 32 * 4;      // fp32 [kTC][RPW] partial y
-    static constexpr int oOT = oYS + kTC * RPW * 4;
+    static constexpr int oOT = oBC + kTC * 32 * 4;
     static constexpr int oBar = (oOT + RPW * OTP * ES + 15) / 16 * 16;
-    static constexpr int kWarpBytes = (oBar + 16 + 127) / 128 * 128;
+    static constexpr int kWarpBytes = oBar + 16;
     static_assert(SLOT % 16 == 0 && ROWB % 16 == 0 && kStageBytes % 16 == 0 && oBar % 16 == 0,
                   "alignment");
 
@@ -152,7 +151,7 @@ __device__ __forceinline__ float silu_f32(float z)
 
 template <typename T, int G, int DIRS, int W>
 struct WarpScan {
-    using Lay = WarpLayout<T, G>;
+    using Lay = WarpLayout<T, G, DIRS == 3>;
     static constexpr int RPW = Lay::RPW, NS = Lay::NS, ES = Lay::ES;
     static constexpr int NDIR = (DIRS == 3) ? 2 : 1;
 
@@ -270,7 +269,7 @@ struct WarpScan {
         const float *bc = reinterpret_cast<const float *>(wsm + Lay::oBC);
         T *ot = reinterpret_cast<T *>(wsm + Lay::oOT) + r * Lay::OTP;
         const float *py = reinterpret_cast<const float *>(st + Lay::oPY);
-        float *ys = reinterpret_cast<float *>(wsm + Lay::oYS);
+        float *yrow = (DIRS == 3 && !FIN) ? p.ybuf + (grp * p.piece_len + (c0 - ta)) * RPW + r : nullptr;
         const uint32_t lead = lead_of(lane_emod, c0);
         const T *rd = reinterpret_cast<const T *>(st + Lay::oD + Lay::row_off(r) + lead);
         const T *rx = reinterpret_cast<const T *>(st + Lay::oX + Lay::row_off(r) + lead);
@@ -310,7 +309,7 @@ struct WarpScan {
                 if (G >= 4) y += __shfl_xor_sync(0xffffffffu, y, 2);
                 // (all G lanes of a channel hold the same y and store it alike)
                 if (!FIN) {
-                    if (DIRS == 3) ys[i * RPW + r] = y;
+                    if (DIRS == 3) st_global_if(yrow + i * RPW, y, i < len);
                 } else {
                     float tot = y + fmaf(Dsum, xv, (DIRS == 3) ? py[i * RPW + r] : 0.f);
                     if (GATE) tot *= silu_f32<T>(ld_as_f32(rz + i));
@@ -337,19 +336,6 @@ struct WarpScan {
             }
         }
         __syncwarp();
-    }
-
-    // Bulk-store the chunk's partial y (rows c0..c1-1 of RPW floats) to the
-    // y-buffer.
-    __device__ void store_partial(int c0, int c1)
-    {
-        float *ys = reinterpret_cast<float *>(wsm + Lay::oYS);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            bulk_s2g(p.ybuf + (grp * p.piece_len + (c0 - ta)) * RPW, ys, (uint32_t)((c1 - c0) * RPW * 4));
-            bulk_commit();
-        }
     }
 
     // Write the chunk's outputs from the output tile with row-contiguous
@@ -452,10 +438,6 @@ struct WarpScan {
                 zero_tail(s, c0, len);
                 widen_bc(s, len);
                 const uint32_t rmask = reset_mask(c0, len);
-                if (DIRS == 3 && !fin) {          // ys is free once the previous bulk store read it
-                    if (lane == 0) bulk_wait_read();
-                    __syncwarp();
-                }
                 if (fin) {
                     if (seg) {
                         if (hasZ) scan_dispatch<true, true, true>(h, Ap, Dsum, s, c0, len, rmask);
@@ -468,7 +450,6 @@ struct WarpScan {
                 } else {
                     if (seg) scan_dispatch<false, true, false>(h, Ap, Dsum, s, c0, len, rmask);
                     else scan_dispatch<false, false, false>(h, Ap, Dsum, s, c0, len, rmask);
-                    if (DIRS == 3) store_partial(c0, c1);
                 }
                 if (k + kStages < nk) {
                     int n0, n1;
@@ -481,7 +462,6 @@ struct WarpScan {
             cp_async_wait<0>();
             if (DIRS == 3 && phase == 0) {
                 // Partial y fully written before the partner reads it.
-                if (lane == 0) bulk_wait_all();
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(pairbar);
@@ -493,27 +473,24 @@ struct WarpScan {
             }
         }
         cp_async_wait<0>();
-        if (lane == 0) bulk_wait_all();
     }
 };
 
 // CTAs per SM that the shared-memory footprint allows; used as the register
 // budget hint so that registers never limit residency below it.
-template <typename T, int G, int W>
+template <typename T, int G, int DIRS, int W>
 constexpr int warp_scan_min_blocks()
 {
-    return (227 * 1024) / (W * WarpLayout<T, G>::kWarpBytes) < 1
-               ? 1
-               : ((227 * 1024) / (W * WarpLayout<T, G>::kWarpBytes) > 8
-                      ? 8
-                      : (227 * 1024) / (W * WarpLayout<T, G>::kWarpBytes));
+    // 228 KB of shared memory per SM, 1 KB of it reserved per CTA
+    constexpr int kb = W * WarpLayout<T, G, DIRS == 3>::kWarpBytes + 1024;
+    return (228 * 1024) / kb < 1 ? 1 : ((228 * 1024) / kb > 8 ? 8 : (228 * 1024) / kb);
 }
 
 template <typename T, int G, int DIRS, int W>
-__global__ void __launch_bounds__(W * 32, (warp_scan_min_blocks<T, G, W>()))
+__global__ void __launch_bounds__(W * 32, (warp_scan_min_blocks<T, G, DIRS, W>()))
 warp_scan_kernel(const WarpScanParams p)
 {
-    using Lay = WarpLayout<T, G>;
+    using Lay = WarpLayout<T, G, DIRS == 3>;
     constexpr int NDIR = (DIRS == 3) ? 2 : 1;
     static_assert(W % NDIR == 0, "whole pairs per CTA");
     extern __shared__ __align__(128) unsigned char smem_raw[];

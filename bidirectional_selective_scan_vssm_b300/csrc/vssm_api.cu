@@ -71,16 +71,6 @@ constexpr int kTargetCtas = 148 * 8;         // enough CTAs to fill 148 SMs
 
 constexpr int kWarpTargetWarps = 148 * 8;      // warps that fill 148 SMs at 8 warps each
 
-template <typename T>
-int warp_bytes(int G)
-{
-    switch (G) {
-    case 1: return vssm::WarpLayout<T, 1>::kWarpBytes;
-    case 2: return vssm::WarpLayout<T, 2>::kWarpBytes;
-    default: return vssm::WarpLayout<T, 4>::kWarpBytes;
-    }
-}
-
 constexpr int warps_per_cta(int G) { return G == 4 ? 8 : (G == 2 ? 4 : 2); }
 
 // Plan for the warp kernel (dstate == 16).
@@ -282,9 +272,12 @@ template <typename T, int G, int DIRS>
 int launch_warp_variant(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t stream)
 {
     constexpr int W = warps_per_cta(G);
-    const size_t smem = (size_t)W * vssm::WarpLayout<T, G>::kWarpBytes;
+    const size_t smem = (size_t)W * vssm::WarpLayout<T, G, DIRS == 3>::kWarpBytes;
     auto kern = vssm::warp_scan_kernel<T, G, DIRS, W>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)   // all of the unified L1/shared array as shared memory: residency is smem-bound
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess)
         return fail(VSSM_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     kern<<<(unsigned)pl.ctas, W * 32, smem, stream>>>(p);
