@@ -289,9 +289,15 @@ def oracle_sample_run(wl, inp, target_s):
     nd = wl.dim if nb > 1 or rows >= wl.dim else min(wl.dim, rows)
     a = slice_inputs(nb, nd)
     secs = run(a)
+    reps = 1
+    # a sample that covers the whole workload in well under the target is
+    # repeated (at most 30 times) so that the time is not dominated by noise
+    while secs < target_s and reps < 30 and nb * nd == wl.batch * wl.dim:
+        secs += run(a)
+        reps += 1
     desc = (f"{nb} of {wl.batch} batch entries x {nd} of {wl.dim} channels x {wl.seqlen} tokens "
-            f"({nb * nd * wl.seqlen} token-channels), fp64, {threads} OpenMP threads")
-    return nb * nd * wl.seqlen, secs, threads, desc
+            f"({nb * nd * wl.seqlen} token-channels), {reps} run(s), fp64, {threads} OpenMP threads")
+    return reps * nb * nd * wl.seqlen, secs, threads, desc
 
 
 def run_reference(args):

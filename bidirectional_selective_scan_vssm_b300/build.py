@@ -50,6 +50,21 @@ def build(force: bool = False, verbose: bool = False, out: str = LIB, defines=()
     return out
 
 
+PROBE_SRC = os.path.join(CSRC, "ceiling_probe.cu")
+PROBE = os.path.join(PKG, "ceiling_probe")
+
+
+def build_probe() -> str:
+    """The MUFU / FMA-pipe ceiling probe (a standalone program)."""
+    cmd = [NVCC, *ARCH, "-O3", "-std=c++17", "-o", PROBE, PROBE_SRC]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stdout + r.stderr)
+    return PROBE
+
+
 if __name__ == "__main__":
     build(force="--force" in sys.argv, verbose="-v" in sys.argv)
     print(LIB)
+    if "--probe" in sys.argv:
+        print(build_probe())

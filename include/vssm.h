@@ -159,9 +159,9 @@ int vssm_scan_folded(const vssm_scan_args *a, int seg_len, void *stream);
 /*
  * Synchronises `stream`, then reads and clears this device's error word.
  * Returns VSSM_ERR_TIMEOUT if a kernel launched by this library since the
- * last check stopped because one of its bounded waits (for a bulk copy or for
- * its partner warp; limit 1 s) expired -- its output is then invalid -- and
- * VSSM_OK otherwise. The kernels never trap and never wait without a limit.
+ * last check stopped because its bounded wait for its partner warp (limit
+ * 1 s) expired -- its output is then invalid -- and VSSM_OK otherwise. The
+ * kernels never trap and never spin without a limit.
  */
 int vssm_device_error(void *stream);
 
