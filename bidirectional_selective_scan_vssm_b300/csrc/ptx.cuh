@@ -3,6 +3,7 @@
 // packed f32x2 arithmetic and the MUFU exp2.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -82,11 +83,18 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t 
 }
 
 // Store v to global memory when pred holds (a predicated store, no branch).
+// No memory clobber: the compiler may move other loads and stores across it;
+// it stays ordered with the other volatile asm, fences included.
 __device__ __forceinline__ void st_global_if(float *ptr, float v, bool pred)
 {
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p st.global.f32 [%0], %1;\n\t}" ::"l"(ptr),
-                 "f"(v), "r"((unsigned)pred)
-                 : "memory");
+                 "f"(v), "r"((unsigned)pred));
+}
+
+__device__ __forceinline__ void st_global_if(__nv_bfloat16 *ptr, __nv_bfloat16 v, bool pred)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p st.global.b16 [%0], %1;\n\t}" ::"l"(ptr),
+                 "h"(*reinterpret_cast<unsigned short *>(&v)), "r"((unsigned)pred));
 }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }

@@ -349,10 +349,9 @@ struct WarpScan {
         const int rows = min(RPW, p.dim - d0);
         T *op = out_row0 + (long long)sub * p.L + c0 + i;
         const long long step = (long long)RPI * p.L;
-        if (i < len) {
+        const bool in = i < len;
 #pragma unroll 4
-            for (int rr = sub; rr < rows; rr += RPI, op += step) *op = ot[rr * Lay::OTP + i];
-        }
+        for (int rr = sub; rr < rows; rr += RPI, op += step) st_global_if(op, ot[rr * Lay::OTP + i], in);
         __syncwarp();
     }
 
