@@ -97,6 +97,16 @@ __device__ __forceinline__ void st_global_if(__nv_bfloat16 *ptr, __nv_bfloat16 v
                  "h"(*reinterpret_cast<unsigned short *>(&v)), "r"((unsigned)pred));
 }
 
+// cp_async16 issued only when pred holds (a predicated instruction; nothing is
+// read or written otherwise).
+__device__ __forceinline__ void cp_async16_if(void *dst, const void *src, bool pred)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t"
+                 "@p cp.async.cg.shared.global [%0], [%1], 16;\n\t}" ::"r"(smem_addr(dst)),
+                 "l"(src), "r"((unsigned)pred)
+                 : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
 // Wait until at most N of this thread's committed copy groups are pending.

@@ -194,9 +194,14 @@ struct WarpScan {
             const long long off = (long long)c0 * ES - lead;
             unsigned char *dst = st + Lay::row_off(r);
             if (avail >= 16 * nblk) {             // every block lies inside the tensor
-                for (int a = 0; a < narr; ++a)
-                    for (int k = 0; k < nblk; ++k)
-                        cp_async16(dst + a * Lay::ROWB + 16 * k, rowp[a] + off + 16 * k, 16u);
+                const char *s0 = rowp[0] + off, *s1 = rowp[1] + off, *s2 = rowp[2] + off;
+#pragma unroll
+                for (int k = 0; k < Lay::SLOT / 16; ++k) {
+                    const bool in = k < nblk;
+                    cp_async16_if(dst + 16 * k, s0 + 16 * k, in);
+                    cp_async16_if(dst + Lay::ROWB + 16 * k, s1 + 16 * k, in);
+                    if (narr == 3) cp_async16_if(dst + 2 * Lay::ROWB + 16 * k, s2 + 16 * k, in);
+                }
             } else {                              // the tensor's final row: clip the last block
                 for (int a = 0; a < narr; ++a)
                     for (int k = 0; k < nblk; ++k) {
@@ -211,15 +216,21 @@ struct WarpScan {
             const long long boff = ((long long)b * p.L + c0) * 16 * ES;
             const char *srcB = static_cast<const char *>(p.B[dir]) + boff;
             const char *srcC = static_cast<const char *>(p.C[dir]) + boff;
-            for (int j = lane; j < nb; j += 32) {
-                cp_async16(st + Lay::oB + 16 * j, srcB + 16 * j, 16u);
-                cp_async16(st + Lay::oC + 16 * j, srcC + 16 * j, 16u);
+#pragma unroll
+            for (int m = 0; m < kTC * ES / 32; ++m) {
+                const int j = lane + 32 * m;
+                cp_async16_if(st + Lay::oB + 16 * j, srcB + 16 * j, j < nb);
+                cp_async16_if(st + Lay::oC + 16 * j, srcC + 16 * j, j < nb);
             }
         }
         if (DIRS == 3 && fin) {   // partner's partial y, len rows of RPW floats
             const int nb = len * RPW / 4;
             const char *src = reinterpret_cast<const char *>(p.ybuf + (grp * p.piece_len + (c0 - ta)) * RPW);
-            for (int j = lane; j < nb; j += 32) cp_async16(st + Lay::oPY + 16 * j, src + 16 * j, 16u);
+#pragma unroll
+            for (int m = 0; m < kTC * RPW / 128; ++m) {
+                const int j = lane + 32 * m;
+                cp_async16_if(st + Lay::oPY + 16 * j, src + 16 * j, j < nb);
+            }
         }
         cp_async_commit();
     }
@@ -522,7 +533,7 @@ warp_scan_kernel(const WarpScanParams p)
     ws.lane_emod = (uint32_t)(ws.lane_erow & 15);
     ws.rowp[0] = static_cast<const char *>(p.delta) + ws.lane_erow * Lay::ES;
     ws.rowp[1] = static_cast<const char *>(p.x) + ws.lane_erow * Lay::ES;
-    ws.rowp[2] = p.z ? static_cast<const char *>(p.z) + ws.lane_erow * Lay::ES : nullptr;
+    ws.rowp[2] = p.z ? static_cast<const char *>(p.z) + ws.lane_erow * Lay::ES : ws.rowp[1];
     ws.out_row0 = static_cast<T *>(p.out) + e0;
     ws.run();
 }
