@@ -69,7 +69,10 @@ constexpr int kOneDirR = 64, kOneDirG = 2;   // 128 threads
 constexpr int kYSmemMaxBytes = 48 * 1024;    // shared y-buffer budget per CTA
 constexpr int kTargetCtas = 148 * 8;         // enough CTAs to fill 148 SMs
 
-constexpr int kWarpTargetWarps = 148 * 8;      // warps that fill 148 SMs at 8 warps each
+// Folded sequences are cut into independent pieces (each starts on a reset):
+// aim for about three waves of 148 SMs x 14 resident warps, so that the last
+// wave is short.
+constexpr int kFoldTargetWarps = 148 * 48;
 
 constexpr int warps_per_cta(int G) { return G == 4 ? 8 : (G == 2 ? 4 : 2); }
 
@@ -81,22 +84,11 @@ void make_warp_plan(const vssm_scan_args *a, int seg_len, Plan *pl)
     pl->warp = true;
     pl->dirs = (int)dirs;
     const long long nseg = seg_len > 0 ? (a->seqlen + seg_len - 1) / seg_len : 1;
-    // Smallest G (most states per lane) that still yields enough warps;
-    // folded sequences are first split into independent pieces.
-    int G = 4;
-    for (int g : {1, 2, 4}) {
-        const long long rg = (a->dim + 32 / g - 1) / (32 / g);
-        long long pieces = 1;
-        if (seg_len > 0) {
-            const long long per_piece_warps = (long long)a->batch * rg * ndir;
-            pieces = std::min<long long>(nseg, std::max<long long>(
-                1, (kWarpTargetWarps + per_piece_warps - 1) / std::max<long long>(1, per_piece_warps)));
-        }
-        if ((long long)a->batch * rg * pieces * ndir >= kWarpTargetWarps * 3 / 4 || g == 4) {
-            G = g;
-            break;
-        }
-    }
+    // One lane per channel, all 16 states in its registers. Measured on
+    // B300, the variants that split a channel's states over 2 or 4 lanes
+    // (more warps, a shuffle per token) were slower on every workload, long
+    // rows with few channels included.
+    const int G = 1;
     pl->G = G;
     pl->W = warps_per_cta(G);
     const int rpw = 32 / G;
@@ -105,7 +97,7 @@ void make_warp_plan(const vssm_scan_args *a, int seg_len, Plan *pl)
     pl->piece_len = a->seqlen;
     if (seg_len > 0 && a->seqlen > 0) {
         const long long per_piece_warps = (long long)a->batch * pl->rgroups * ndir;
-        long long want = (kWarpTargetWarps + per_piece_warps - 1) / std::max<long long>(1, per_piece_warps);
+        long long want = (kFoldTargetWarps + per_piece_warps - 1) / std::max<long long>(1, per_piece_warps);
         want = std::max<long long>(1, std::min<long long>(want, nseg));
         const long long per = (nseg + want - 1) / want;        // segments per piece
         pl->pieces = (int)((nseg + per - 1) / per);
@@ -299,11 +291,7 @@ int launch_warp_dirs(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t
 template <typename T>
 int launch_warp(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t s)
 {
-    switch (pl.G) {
-    case 1: return launch_warp_dirs<T, 1>(p, pl, s);
-    case 2: return launch_warp_dirs<T, 2>(p, pl, s);
-    default: return launch_warp_dirs<T, 4>(p, pl, s);
-    }
+    return launch_warp_dirs<T, 1>(p, pl, s);
 }
 
 template <typename T>
