@@ -280,15 +280,25 @@ def oracle_sample_run(wl, inp, target_s):
                     a["D_bwd"], a["z"], dirs=wl.dirs, seg_len=wl.seg_len)
         return time.perf_counter() - t0
 
-    # calibrate on a few channels of one batch entry
-    nd0 = min(wl.dim, max(threads, 16))
-    t_cal = run(slice_inputs(1, nd0))
-    per_row = t_cal / nd0
-    rows = max(1, int(target_s / max(per_row, 1e-9)))
-    nb = min(wl.batch, max(1, rows // wl.dim))
-    nd = wl.dim if nb > 1 or rows >= wl.dim else min(wl.dim, rows)
+    def shape(rows):
+        nb = min(wl.batch, max(1, rows // wl.dim))
+        nd = wl.dim if nb > 1 or rows >= wl.dim else min(wl.dim, rows)
+        return nb, nd
+
+    # calibrate on a few channels of one batch entry, then grow the sample
+    # while it runs well under the target (a small calibration run is
+    # dominated by thread start-up and overestimates the per-row time)
+    rows = min(wl.dim, max(threads, 16))
+    nb, nd = shape(rows)
     a = slice_inputs(nb, nd)
     secs = run(a)
+    for _ in range(4):
+        if secs >= 0.5 * target_s or nb * nd == wl.batch * wl.dim:
+            break
+        rows = max(rows + 1, int(nb * nd * target_s / max(secs, 1e-4)))
+        nb, nd = shape(rows)
+        a = slice_inputs(nb, nd)
+        secs = run(a)
     reps = 1
     # a sample that covers the whole workload in well under the target is
     # repeated (at most 30 times) so that the time is not dominated by noise

@@ -45,7 +45,10 @@
 namespace vssm {
 
 constexpr int kTC = 16;          // tokens per chunk
-constexpr int kStages = 2;       // depth of the copy ring
+#ifndef VSSM_SCAN_STAGES
+#define VSSM_SCAN_STAGES 2
+#endif
+constexpr int kStages = VSSM_SCAN_STAGES;   // depth of the copy ring
 #ifndef VSSM_SCAN_UNROLL
 #define VSSM_SCAN_UNROLL 2
 #endif
