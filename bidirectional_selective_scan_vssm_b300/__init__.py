@@ -31,8 +31,9 @@ STATUS = {0: "VSSM_OK", -1: "VSSM_ERR_INVALID_ARG", -2: "VSSM_ERR_UNSUPPORTED",
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libvssm.so")
 EXPORTS = ["vssm_scan_bidir", "vssm_scan_bidir_noalloc", "vssm_scan_folded",
-           "vssm_scan_workspace_size", "vssm_device_error", "vssm_status_string",
-           "vssm_last_error", "vssm_version"]
+           "vssm_scan_chunked", "vssm_scan_workspace_size", "vssm_scan_chunked_workspace_size",
+           "vssm_scan_plan_query",
+           "vssm_device_error", "vssm_status_string", "vssm_last_error", "vssm_version"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -70,8 +71,16 @@ def _load():
     lib.vssm_scan_bidir_noalloc.restype = ctypes.c_int
     lib.vssm_scan_folded.argtypes = [P, ctypes.c_int, ctypes.c_void_p]
     lib.vssm_scan_folded.restype = ctypes.c_int
+    lib.vssm_scan_chunked.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    lib.vssm_scan_chunked.restype = ctypes.c_int
     lib.vssm_scan_workspace_size.argtypes = [P, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
     lib.vssm_scan_workspace_size.restype = ctypes.c_int
+    lib.vssm_scan_chunked_workspace_size.argtypes = [P, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.POINTER(ctypes.c_size_t)]
+    lib.vssm_scan_chunked_workspace_size.restype = ctypes.c_int
+    lib.vssm_scan_plan_query.argtypes = [P, ctypes.c_int, ctypes.c_int,
+                                         ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
+    lib.vssm_scan_plan_query.restype = ctypes.c_int
     lib.vssm_status_string.argtypes = [ctypes.c_int]
     lib.vssm_status_string.restype = ctypes.c_char_p
     lib.vssm_last_error.argtypes = []
@@ -140,10 +149,23 @@ def make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, out=
     return a
 
 
-def workspace_size(a: ScanArgs, seg_len: int = 0) -> int:
+def workspace_size(a: ScanArgs, seg_len: int = 0, pieces: Optional[int] = None) -> int:
+    """Workspace bytes for the call (``pieces`` given: for ``vssm_scan_chunked``)."""
     n = ctypes.c_size_t(0)
-    _check(lib.vssm_scan_workspace_size(ctypes.byref(a), seg_len, ctypes.byref(n)))
+    if pieces is None:
+        _check(lib.vssm_scan_workspace_size(ctypes.byref(a), seg_len, ctypes.byref(n)))
+    else:
+        _check(lib.vssm_scan_chunked_workspace_size(ctypes.byref(a), seg_len, pieces,
+                                                    ctypes.byref(n)))
     return int(n.value)
+
+
+def plan(a: ScanArgs, seg_len: int = 0, pieces: int = 0):
+    """(token ranges per row, kernel launches) of the call (``vssm_scan_plan_query``)."""
+    r, n = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib.vssm_scan_plan_query(ctypes.byref(a), seg_len, pieces, ctypes.byref(r),
+                                    ctypes.byref(n)))
+    return int(r.value), int(n.value)
 
 
 _ws_cache = {}
@@ -162,8 +184,9 @@ def _workspace(device: torch.device, stream, nbytes: int) -> Optional[torch.Tens
     return ws
 
 
-def _launch(fn, a: ScanArgs, seg_len: Optional[int], device, workspace, stream):
-    need = workspace_size(a, seg_len or 0)
+def _launch(fn, a: ScanArgs, seg_len: Optional[int], device, workspace, stream,
+            pieces: Optional[int] = None):
+    need = workspace_size(a, seg_len or 0, pieces)
     stream = stream if stream is not None else torch.cuda.current_stream(device)
     if workspace is None:
         workspace = _workspace(device, stream, need)
@@ -171,7 +194,9 @@ def _launch(fn, a: ScanArgs, seg_len: Optional[int], device, workspace, stream):
         a.workspace = workspace.data_ptr()
         a.workspace_bytes = workspace.numel() * workspace.element_size()
     s = stream.cuda_stream
-    if seg_len is None:
+    if pieces is not None:
+        _check(fn(ctypes.byref(a), int(seg_len or 0), int(pieces), ctypes.c_void_p(s)))
+    elif seg_len is None:
         _check(fn(ctypes.byref(a), ctypes.c_void_p(s)))
     else:
         _check(fn(ctypes.byref(a), int(seg_len), ctypes.c_void_p(s)))
@@ -212,6 +237,20 @@ def scan_folded(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *,
         out = torch.empty_like(x)
     a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, out, B_bwd, C_bwd, dirs)
     _launch(lib.vssm_scan_folded, a, seg_len, x.device, workspace, stream)
+    return out
+
+
+def scan_chunked(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *,
+                 pieces: int, seg_len: int = 0, dirs: int = DIR_BOTH, out=None, B_bwd=None,
+                 C_bwd=None, stream: Optional[torch.cuda.Stream] = None,
+                 workspace=None) -> torch.Tensor:
+    """``vssm_scan_chunked``: the scan with each row cut into ``pieces`` token
+    ranges joined by the exact carry (0 = the library's choice). ``seg_len``
+    > 0 makes it the folded scan."""
+    if out is None:
+        out = torch.empty_like(x)
+    a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, out, B_bwd, C_bwd, dirs)
+    _launch(lib.vssm_scan_chunked, a, seg_len, x.device, workspace, stream, pieces)
     return out
 
 

@@ -62,12 +62,21 @@ struct WarpScanParams {
     const float *A[2], *D[2];
     void *out;
     float *ybuf;                 // [ngroups][piece_len][RPW] floats (both directions only)
+    float *summ;                 // carry summaries [slot][srows][pieces][kSummFloats], or null
+                                 // when every piece starts from a zero state
     unsigned *err;               // device error word
     long long total;             // batch * dim * L elements
     int batch, dim, L, seg_len, pieces, piece_len;
     int rgroups;                 // ceil(dim / RPW)
     long long ngroups;           // batch * pieces * rgroups
+    long long srows;             // batch * rgroups
 };
+
+// One piece's summary for 32 channels: the state reached by scanning the
+// piece from zero, h[n][lane] (n < 16), then the piece's delta sum [16][lane],
+// or kCutBits there when a folded reset inside the piece cuts the carry.
+constexpr int kSummFloats = 17 * 32;
+constexpr uint32_t kCutBits = 0xffffffffu;
 
 template <typename T, int G, bool BIDIR>
 struct WarpLayout {
@@ -152,7 +161,7 @@ __device__ __forceinline__ float silu_f32(float z)
     return __fdividef(z, 1.0f + ex2_mufu(-1.4426950408889634f * z));
 }
 
-template <typename T, int G, int DIRS, int W>
+template <typename T, int G, int DIRS, int W, bool CARRY = false>
 struct WarpScan {
     using Lay = WarpLayout<T, G, DIRS == 3>;
     static constexpr int RPW = Lay::RPW, NS = Lay::NS, ES = Lay::ES;
@@ -162,6 +171,8 @@ struct WarpScan {
     unsigned char *wsm;          // this warp's shared region
     uint64_t *pairbar;           // pair rendezvous (both directions)
     int lane, dir, r, g;
+    int slot;                    // direction slot of the carry summaries
+    int piece, rg;               // token range and channel group of this warp
     long long grp;
     int b, d0, ta, tb;
     bool ok;                     // false once the pair rendezvous has timed out
@@ -171,6 +182,21 @@ struct WarpScan {
     T *out_row0;                 // output row (b, d0, 0)
 
     __device__ WarpScan(const WarpScanParams &p_) : p(p_) {}
+
+    // Token range, channel rows and row pointers from (b, rg, piece).
+    __device__ void place()
+    {
+        d0 = rg * RPW;
+        ta = piece * p.piece_len;
+        tb = min(p.L, ta + p.piece_len);
+        const long long e0 = ((long long)b * p.dim + d0) * p.L;
+        lane_erow = e0 + (long long)r * p.L;
+        lane_emod = (uint32_t)(lane_erow & 15);
+        rowp[0] = static_cast<const char *>(p.delta) + lane_erow * ES;
+        rowp[1] = static_cast<const char *>(p.x) + lane_erow * ES;
+        rowp[2] = p.z ? static_cast<const char *>(p.z) + lane_erow * ES : rowp[1];
+        out_row0 = static_cast<T *>(p.out) + e0;
+    }
 
     __device__ __forceinline__ unsigned char *stage(int s) const { return wsm + s * Lay::kStageBytes; }
 
@@ -388,13 +414,12 @@ struct WarpScan {
         else scan_chunk<1, FIN, SEG, GATE>(h, Ap, Dsum, s, c0, len, rmask);
     }
 
-    __device__ void run()
+    // A * log2(e) for this lane's states, and a zero state.
+    __device__ __forceinline__ void init_state(f2 (&Ap)[NS / 2], f2 (&h)[NS / 2]) const
     {
-        // ---- per-lane parameters
         const int d = d0 + r;
         const bool active = d < p.dim;
         constexpr float kLog2e = 1.4426950408889634f;
-        f2 Ap[NS / 2], h[NS / 2];
 #pragma unroll
         for (int j = 0; j < NS / 2; ++j) {
             const int n = g * NS + 2 * j;
@@ -403,6 +428,157 @@ struct WarpScan {
             Ap[j] = pack2(a0, a1);
             h[j] = pack2(0.f, 0.f);
         }
+    }
+
+    __device__ __forceinline__ float *summary_ptr(int j) const
+    {
+        return p.summ + (((long long)slot * p.srows + (long long)b * p.rgroups + rg) * p.pieces + j) * kSummFloats;
+    }
+
+    // State entering this warp's piece, from the summaries of the pieces that
+    // precede it in this warp's direction (Vim page §3.1, parallel scan). A
+    // piece maps a state h to P*h + hp, with P = 2^(A*log2e * its delta sum)
+    // per state (0 when a folded reset lies inside it) and hp its state from
+    // zero. Composing the maps, (P1, h1) then (P2, h2) = (P1*P2, P2*h1 + h2),
+    // is associative, and the exclusive prefix applied to h = 0 reduces to
+    // h <- P*h + hp over the preceding pieces in order.
+    __device__ void carry_in(f2 (&h)[NS / 2], const f2 (&Ap)[NS / 2]) const
+    {
+        static_assert(G == 1, "summaries hold one channel per lane");
+        const int n = dir == 0 ? piece : p.pieces - 1 - piece;
+        constexpr int kBatch = 4;        // summaries loaded together (L2 latency)
+        for (int s0 = 0; s0 < n; s0 += kBatch) {
+            float v[kBatch][17];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                if (s0 + k < n) {
+                    const float *u = summary_ptr(dir == 0 ? s0 + k : p.pieces - 1 - s0 - k);
+#pragma unroll
+                    for (int m = 0; m < 17; ++m) v[k][m] = __ldcg(u + m * 32 + lane);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                if (s0 + k < n) {
+                    const float S = v[k][16];
+                    const bool cut = __float_as_uint(S) == kCutBits;
+                    const f2 SS = pack2(S, S);
+#pragma unroll
+                    for (int q = 0; q < NS / 2; ++q) {
+                        const f2 e = cut ? pack2(0.f, 0.f) : ex2_mul2(SS, Ap[q]);
+                        h[q] = fma2(e, h[q], pack2(v[k][2 * q], v[k][2 * q + 1]));
+                    }
+                }
+            }
+        }
+    }
+
+    // Scan the staged chunk for the piece summary: the state recurrence and
+    // the delta sum only (no C, no output).
+    template <int DIR, bool SEG>
+    __device__ __forceinline__ void summary_chunk(f2 (&h)[NS / 2], const f2 (&Ap)[NS / 2], float &S,
+                                                  int s, int c0, int len, uint32_t rmask)
+    {
+        const unsigned char *st = stage(s);
+        const float *bc = reinterpret_cast<const float *>(wsm + Lay::oBC);
+        const uint32_t lead = lead_of(lane_emod, c0);
+        const T *rd = reinterpret_cast<const T *>(st + Lay::oD + Lay::row_off(r) + lead);
+        const T *rx = reinterpret_cast<const T *>(st + Lay::oX + Lay::row_off(r) + lead);
+        const int n4 = (len + kUnroll - 1) / kUnroll * kUnroll;
+#pragma unroll 1
+        for (int k0 = 0; k0 < n4; k0 += kUnroll) {
+#pragma unroll
+            for (int j = 0; j < kUnroll; ++j) {
+                const int i = (DIR == 0) ? (k0 + j) : (n4 - 1 - k0 - j);
+                const float dtv = ld_as_f32(rd + i);
+                const float xv = ld_as_f32(rx + i);
+                S += dtv;
+                const float dx = dtv * xv;
+                const f2 dd = pack2(dtv, dtv), uu = pack2(dx, dx);
+                const float *bcp = bc + i * 32;
+                f2 ll = pack2(0.f, 0.f);
+                if (SEG) {
+                    const float lam = __uint_as_float(0xff800000u & (0u - ((rmask >> i) & 1u)));
+                    ll = pack2(lam, lam);
+                }
+#pragma unroll
+                for (int q = 0; q < NS / 4; ++q) {
+                    f2 B0, B1;
+                    lds_2xf2(bcp + g * NS + 4 * q, B0, B1);
+                    const f2 e0 = SEG ? ex2_fma2(dd, Ap[2 * q], ll) : ex2_mul2(dd, Ap[2 * q]);
+                    const f2 e1 = SEG ? ex2_fma2(dd, Ap[2 * q + 1], ll) : ex2_mul2(dd, Ap[2 * q + 1]);
+                    h[2 * q] = fma2(e0, h[2 * q], mul2(uu, B0));
+                    h[2 * q + 1] = fma2(e1, h[2 * q + 1], mul2(uu, B1));
+                }
+            }
+        }
+        __syncwarp();
+    }
+
+    // Summary of this warp's piece in its direction (see carry_in).
+    __device__ void run_summary()
+    {
+        static_assert(G == 1, "summaries hold one channel per lane");
+        f2 Ap[NS / 2], h[NS / 2];
+        init_state(Ap, h);
+        float S = 0.f;
+        bool cut = false;
+        const bool seg = p.seg_len > 0;
+        const int nk = (tb - ta + kTC - 1) / kTC;
+        for (int k = 0; k < kStages; ++k) {
+            if (k < nk) {
+                int c0, c1;
+                chunk_range(k, ta, tb, c0, c1);
+                issue(k, c0, c1, false);
+            } else {
+                cp_async_commit();
+            }
+        }
+        for (int k = 0; k < nk; ++k) {
+            const int s = k % kStages;
+            int c0, c1;
+            chunk_range(k, ta, tb, c0, c1);
+            cp_async_wait<kStages - 1>();
+            __syncwarp();
+            const int len = c1 - c0;
+            zero_tail(s, c0, len);
+            widen_bc(s, len);
+            const uint32_t rmask = reset_mask(c0, len);
+            cut = cut || rmask != 0u;
+            if (dir == 0) {
+                if (seg) summary_chunk<0, true>(h, Ap, S, s, c0, len, rmask);
+                else summary_chunk<0, false>(h, Ap, S, s, c0, len, rmask);
+            } else {
+                if (seg) summary_chunk<1, true>(h, Ap, S, s, c0, len, rmask);
+                else summary_chunk<1, false>(h, Ap, S, s, c0, len, rmask);
+            }
+            if (k + kStages < nk) {
+                int n0, n1;
+                chunk_range(k + kStages, ta, tb, n0, n1);
+                issue(s, n0, n1, false);
+            } else {
+                cp_async_commit();
+            }
+        }
+        cp_async_wait<0>();
+        float *u = summary_ptr(piece);
+#pragma unroll
+        for (int q = 0; q < NS / 2; ++q) {
+            const float2 v = unpack2(h[q]);
+            u[(2 * q) * 32 + lane] = v.x;
+            u[(2 * q + 1) * 32 + lane] = v.y;
+        }
+        u[16 * 32 + lane] = cut ? __uint_as_float(kCutBits) : S;
+    }
+
+    __device__ void run()
+    {
+        // ---- per-lane parameters
+        const int d = d0 + r;
+        const bool active = d < p.dim;
+        f2 Ap[NS / 2], h[NS / 2];
+        init_state(Ap, h);
+        if constexpr (CARRY) carry_in(h, Ap);
         float Dsum = 0.f;
         if (active) {
             if (DIRS == 3) {
@@ -499,7 +675,9 @@ constexpr int warp_scan_min_blocks()
     return (228 * 1024) / kb < 1 ? 1 : ((228 * 1024) / kb > 8 ? 8 : (228 * 1024) / kb);
 }
 
-template <typename T, int G, int DIRS, int W>
+// CARRY: the row is cut into ranges that start from the state carried in by
+// warp_carry_kernel's summaries (else every range starts from zero).
+template <typename T, int G, int DIRS, int W, bool CARRY>
 __global__ void __launch_bounds__(W * 32, (warp_scan_min_blocks<T, G, DIRS, W>()))
 warp_scan_kernel(const WarpScanParams p)
 {
@@ -508,7 +686,7 @@ warp_scan_kernel(const WarpScanParams p)
     static_assert(W % NDIR == 0, "whole pairs per CTA");
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int warp = threadIdx.x >> 5;
-    WarpScan<T, G, DIRS, W> ws(p);
+    WarpScan<T, G, DIRS, W, CARRY> ws(p);
     ws.lane = threadIdx.x & 31;
     ws.r = ws.lane / G;
     ws.g = ws.lane % G;
@@ -528,17 +706,45 @@ warp_scan_kernel(const WarpScanParams p)
     t /= p.rgroups;
     const int piece = (int)(t % p.pieces);
     ws.b = (int)(t / p.pieces);
-    ws.d0 = rg * Lay::RPW;
-    ws.ta = piece * p.piece_len;
-    ws.tb = min(p.L, ws.ta + p.piece_len);
-    const long long e0 = ((long long)ws.b * p.dim + ws.d0) * p.L;
-    ws.lane_erow = e0 + (long long)ws.r * p.L;
-    ws.lane_emod = (uint32_t)(ws.lane_erow & 15);
-    ws.rowp[0] = static_cast<const char *>(p.delta) + ws.lane_erow * Lay::ES;
-    ws.rowp[1] = static_cast<const char *>(p.x) + ws.lane_erow * Lay::ES;
-    ws.rowp[2] = p.z ? static_cast<const char *>(p.z) + ws.lane_erow * Lay::ES : ws.rowp[1];
-    ws.out_row0 = static_cast<T *>(p.out) + e0;
+    ws.rg = rg;
+    ws.piece = piece;
+    ws.slot = (DIRS == 3) ? ws.dir : 0;
+    ws.place();
     ws.run();
+}
+
+// Piece summaries for the carry between token ranges of a row: one warp per
+// (direction slot, channel group, piece that has a successor in that
+// direction). Runs before warp_scan_kernel on the same stream.
+template <typename T, int DIRS, int W>
+__global__ void __launch_bounds__(W * 32, (warp_scan_min_blocks<T, 1, 1, W>()))
+warp_carry_kernel(const WarpScanParams p)
+{
+    using Lay = WarpLayout<T, 1, false>;
+    constexpr int NDIR = (DIRS == 3) ? 2 : 1;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const int warp = threadIdx.x >> 5;
+    const long long per_slot = p.srows * (p.pieces - 1);
+    const long long u = (long long)blockIdx.x * W + warp;
+    if (u >= NDIR * per_slot) return;
+    WarpScan<T, 1, 1, W> ws(p);                  // single-direction staging layout
+    ws.slot = (int)(u / per_slot);
+    const long long rem = u % per_slot;
+    const int jj = (int)(rem % (p.pieces - 1));
+    const long long row = rem / (p.pieces - 1);
+    ws.dir = (DIRS == 3) ? ws.slot : (DIRS == 1 ? 0 : 1);
+    ws.lane = threadIdx.x & 31;
+    ws.r = ws.lane;
+    ws.g = 0;
+    ws.wsm = smem_raw + warp * Lay::kWarpBytes;
+    ws.pairbar = nullptr;
+    ws.ok = true;
+    ws.rg = (int)(row % p.rgroups);
+    ws.b = (int)(row / p.rgroups);
+    ws.piece = ws.dir == 0 ? jj : jj + 1;
+    ws.grp = ((long long)ws.b * p.pieces + ws.piece) * p.rgroups + ws.rg;
+    ws.place();
+    ws.run_summary();
 }
 
 }  // namespace vssm

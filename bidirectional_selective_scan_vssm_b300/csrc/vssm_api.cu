@@ -60,8 +60,12 @@ struct Plan {
     int piece_len = 0;     // tokens per range
     bool ysmem = false;    // y-buffer in shared memory
     int ypitch = 0;        // floats per channel of the shared y-buffer
-    size_t workspace = 0;  // bytes of global y-buffer needed
+    size_t workspace = 0;  // bytes of workspace needed (y-buffer, then carry summaries)
     long long ctas = 0;
+    bool carry = false;    // pieces joined by the carry (summary kernel first)
+    size_t summ_off = 0;   // byte offset of the summaries in the workspace
+    long long srows = 0;   // batch x channel groups
+    long long summ_ctas = 0;
 };
 
 constexpr int kBidirR = 32, kBidirG = 2;     // 128 threads: 64 forward, 64 backward
@@ -75,9 +79,71 @@ constexpr int kTargetCtas = 148 * 8;         // enough CTAs to fill 148 SMs
 constexpr int kFoldTargetWarps = 148 * 48;
 
 constexpr int warps_per_cta(int G) { return G == 4 ? 8 : (G == 2 ? 4 : 2); }
+constexpr int kCarryW = 4;                   // warps per CTA of the summary kernel
 
-// Plan for the warp kernel (dstate == 16).
-void make_warp_plan(const vssm_scan_args *a, int seg_len, Plan *pl)
+// Sub-partitions of the GPU (148 SMs x 4 schedulers).
+constexpr int kSubParts = 148 * 4;
+
+// Estimated SM cycles of one call with each row cut into P ranges of lp
+// tokens. The constants are a least-squares fit to B300 timings of both
+// kernels (nine shapes from batch 1 x 384 channels x 197 tokens to batch 8 x
+// 768 x 4097, 1 to 64 ranges of at least 32 tokens; 8 % rms error): a scan
+// warp costs about 247 cycles per token when it has its scheduler to itself,
+// 189 with two warps per scheduler and 210 with three; a summary warp 0.75 of
+// that; a cut call about 4.5 us more plus 0.47 us per range. Up to the
+// residency limit (3 warps per scheduler) the busiest scheduler holds
+// ceil(warps / kSubParts) of them at once; beyond it the warps stream
+// through and the load is their average.
+double carry_cost(long long row_warps, long long lp, int P)
+{
+    auto per_token = [](long long w) {
+        return w <= kSubParts ? 247.0 : (w <= 2 * kSubParts ? 189.0 : 210.0);
+    };
+    auto load = [](long long w) {
+        return w <= 3 * kSubParts ? (double)((w + kSubParts - 1) / kSubParts) : (double)w / kSubParts;
+    };
+    const long long wm = row_warps * P;
+    double c = load(wm) * (double)lp * per_token(wm);
+    if (P > 1) {
+        const long long ws = row_warps * (P - 1);
+        c += 0.75 * load(ws) * (double)lp * per_token(ws);
+        c += (4.5 + 0.47 * (P - 1)) * 2032.0;
+    }
+    return c;
+}
+
+// Ranges per row (cut on the 16-token chunk grid) that minimise carry_cost;
+// 1 when the rows alone fill the GPU. Returns the range length in *lp_out.
+int auto_carry_pieces(long long row_warps, int L, long long *lp_out)
+{
+    *lp_out = L;
+    if (row_warps <= 0 || row_warps >= 3 * kSubParts || L < 64) return 1;
+    const double one = carry_cost(row_warps, L, 1);
+    double best = 0.0;
+    int bestP = 1;
+    long long bestLp = L;
+    for (int P = 2; P <= 64; ++P) {
+        const long long lp = ((long long)L + P - 1) / P;
+        if (lp < 32) break;
+        const long long lp16 = (lp + 15) / 16 * 16;
+        const int pieces = (int)(((long long)L + lp16 - 1) / lp16);
+        if (pieces < 2) continue;
+        const double c = carry_cost(row_warps, lp16, pieces);
+        if (bestP == 1 || c < best) {
+            best = c;
+            bestP = pieces;
+            bestLp = lp16;
+        }
+    }
+    if (bestP == 1 || best >= 0.95 * one) return 1;   // cut only for a clear gain
+    *lp_out = bestLp;
+    return bestP;
+}
+
+// Plan for the warp kernel (dstate == 16). pieces_req: 0 lets the plan
+// choose; otherwise each row is cut into about that many token ranges
+// joined by the carry.
+void make_warp_plan(const vssm_scan_args *a, int seg_len, int pieces_req, Plan *pl)
 {
     const unsigned dirs = a->dir_flags;
     const int ndir = dirs == 3 ? 2 : 1;
@@ -95,7 +161,20 @@ void make_warp_plan(const vssm_scan_args *a, int seg_len, Plan *pl)
     pl->rgroups = (a->dim + rpw - 1) / rpw;
     pl->pieces = 1;
     pl->piece_len = a->seqlen;
-    if (seg_len > 0 && a->seqlen > 0) {
+    pl->srows = (long long)a->batch * pl->rgroups;
+    long long lp = a->seqlen;
+    int carry_p = pieces_req;
+    if (carry_p > 1) {                     // ceil(L / ceil(L / P)) ranges
+        lp = std::max(1LL, ((long long)a->seqlen + carry_p - 1) / carry_p);
+        carry_p = (int)(((long long)a->seqlen + lp - 1) / lp);
+    } else if (carry_p == 0 && seg_len == 0) {
+        carry_p = auto_carry_pieces(pl->srows * ndir, a->seqlen, &lp);
+    }
+    if (carry_p > 1) {
+        pl->piece_len = (int)lp;
+        pl->pieces = carry_p;
+        pl->carry = true;
+    } else if (seg_len > 0 && a->seqlen > 0) {
         const long long per_piece_warps = (long long)a->batch * pl->rgroups * ndir;
         long long want = (kFoldTargetWarps + per_piece_warps - 1) / std::max<long long>(1, per_piece_warps);
         want = std::max<long long>(1, std::min<long long>(want, nseg));
@@ -107,12 +186,20 @@ void make_warp_plan(const vssm_scan_args *a, int seg_len, Plan *pl)
     const int gpc = pl->W / ndir;
     pl->ctas = (pl->ngroups + gpc - 1) / gpc;
     pl->workspace = dirs == 3 ? (size_t)pl->ngroups * pl->piece_len * rpw * sizeof(float) : 0;
+    if (pl->carry) {
+        pl->summ_off = (pl->workspace + 255) / 256 * 256;
+        pl->workspace = pl->summ_off + (size_t)ndir * pl->srows * pl->pieces * vssm::kSummFloats * sizeof(float);
+        const long long units = (long long)ndir * pl->srows * (pl->pieces - 1);
+        pl->summ_ctas = (units + kCarryW - 1) / kCarryW;
+    }
 }
 
-int make_plan(const vssm_scan_args *a, int seg_len, Plan *pl)
+// pieces_req as in make_warp_plan; only the dstate-16 kernel joins pieces by
+// the carry, and the caller rejects pieces_req > 1 for other state sizes.
+int make_plan(const vssm_scan_args *a, int seg_len, int pieces_req, Plan *pl)
 {
     if (a->dstate == vssm::kMaxState) {
-        make_warp_plan(a, seg_len, pl);
+        make_warp_plan(a, seg_len, pieces_req, pl);
         return VSSM_OK;
     }
     const unsigned dirs = a->dir_flags;
@@ -260,12 +347,35 @@ void *noalloc_scratch()
     return addr[dev];
 }
 
+template <typename T, int DIRS>
+int launch_carry(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t stream)
+{
+    constexpr int W = kCarryW;
+    const size_t smem = (size_t)W * vssm::WarpLayout<T, 1, false>::kWarpBytes;
+    auto kern = vssm::warp_carry_kernel<T, DIRS, W>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess)
+        return fail(VSSM_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    kern<<<(unsigned)pl.summ_ctas, W * 32, smem, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    return VSSM_OK;
+}
+
 template <typename T, int G, int DIRS>
 int launch_warp_variant(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t stream)
 {
+    if (pl.carry) {
+        const int st = launch_carry<T, DIRS>(p, pl, stream);
+        if (st != VSSM_OK) return st;
+    }
     constexpr int W = warps_per_cta(G);
     const size_t smem = (size_t)W * vssm::WarpLayout<T, G, DIRS == 3>::kWarpBytes;
-    auto kern = vssm::warp_scan_kernel<T, G, DIRS, W>;
+    auto kern = pl.carry ? vssm::warp_scan_kernel<T, G, DIRS, W, true>
+                         : vssm::warp_scan_kernel<T, G, DIRS, W, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess)   // all of the unified L1/shared array as shared memory: residency is smem-bound
         e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -306,14 +416,19 @@ int launch_typed(const vssm::ScanParams &p, const Plan &pl, cudaStream_t s)
     }
 }
 
-int run(const vssm_scan_args *a, int seg_len, bool folded, void *stream)
+int run(const vssm_scan_args *a, int seg_len, bool folded, int pieces_req, void *stream)
 {
     int st = validate(a, seg_len, folded);
     if (st != VSSM_OK) return st;
+    if (pieces_req < 0) return fail(VSSM_ERR_INVALID_ARG, "pieces=%d must be >= 0", pieces_req);
+    if (pieces_req > 1 && a->dstate != vssm::kMaxState)
+        return fail(VSSM_ERR_UNSUPPORTED, "pieces joined by the carry need dstate %d (got %d)",
+                    vssm::kMaxState, a->dstate);
     if ((long long)a->batch * a->dim * a->seqlen == 0) return VSSM_OK;
     Plan pl;
-    make_plan(a, folded ? seg_len : 0, &pl);
-    if (pl.ctas > 0x7fffffffLL) return fail(VSSM_ERR_UNSUPPORTED, "problem too large for one grid");
+    make_plan(a, folded ? seg_len : 0, pieces_req, &pl);
+    if (pl.ctas > 0x7fffffffLL || pl.summ_ctas > 0x7fffffffLL)
+        return fail(VSSM_ERR_UNSUPPORTED, "problem too large for one grid");
     if (pl.workspace > 0 && (!a->workspace || a->workspace_bytes < pl.workspace))
         return fail(VSSM_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", pl.workspace,
                     a->workspace ? a->workspace_bytes : (size_t)0);
@@ -332,7 +447,9 @@ int run(const vssm_scan_args *a, int seg_len, bool folded, void *stream)
         w.D[0] = a->D_fwd;
         w.D[1] = a->D_bwd;
         w.out = a->out;
-        w.ybuf = pl.workspace ? static_cast<float *>(a->workspace) : nullptr;
+        w.ybuf = pl.dirs == 3 ? static_cast<float *>(a->workspace) : nullptr;
+        w.summ = pl.carry ? reinterpret_cast<float *>(static_cast<char *>(a->workspace) + pl.summ_off)
+                          : nullptr;
         w.err = device_error_word();
         if (!w.err) return fail(VSSM_ERR_CUDA, "cannot locate the device error word");
         w.total = (long long)a->batch * a->dim * a->seqlen;
@@ -344,6 +461,7 @@ int run(const vssm_scan_args *a, int seg_len, bool folded, void *stream)
         w.piece_len = pl.piece_len;
         w.rgroups = pl.rgroups;
         w.ngroups = pl.ngroups;
+        w.srows = pl.srows;
         return a->dtype == VSSM_F32 ? launch_warp<float>(w, pl, s) : launch_warp<__nv_bfloat16>(w, pl, s);
     }
     vssm::ScanParams p{};
@@ -383,12 +501,53 @@ int vssm_scan_workspace_size(const vssm_scan_args *a, int seg_len, size_t *bytes
         seg_len < 0)
         return fail(VSSM_ERR_INVALID_ARG, "invalid sizes or dir_flags");
     Plan pl;
-    make_plan(a, seg_len, &pl);
+    make_plan(a, seg_len, 0, &pl);
     *bytes = pl.workspace;
     return VSSM_OK;
 }
 
-int vssm_scan_bidir(const vssm_scan_args *a, void *stream) { return run(a, 0, false, stream); }
+int vssm_scan_chunked_workspace_size(const vssm_scan_args *a, int seg_len, int pieces, size_t *bytes)
+{
+    if (!a || !bytes) return fail(VSSM_ERR_INVALID_ARG, "args or bytes is NULL");
+    if (a->batch < 0 || a->dim < 0 || a->seqlen < 0 || a->dir_flags < 1 || a->dir_flags > 3 ||
+        seg_len < 0 || pieces < 0)
+        return fail(VSSM_ERR_INVALID_ARG, "invalid sizes, dir_flags or pieces");
+    Plan pl;
+    make_plan(a, seg_len, pieces, &pl);
+    *bytes = pl.workspace;
+    return VSSM_OK;
+}
+
+int vssm_scan_plan_query(const vssm_scan_args *a, int seg_len, int pieces, int *ranges_per_row,
+                         int *launches)
+{
+    if (!a || !ranges_per_row || !launches) return fail(VSSM_ERR_INVALID_ARG, "NULL argument");
+    if (a->batch < 0 || a->dim < 0 || a->seqlen < 0 || a->dir_flags < 1 || a->dir_flags > 3 ||
+        seg_len < 0 || pieces < 0)
+        return fail(VSSM_ERR_INVALID_ARG, "invalid sizes, dir_flags or pieces");
+    if (a->dstate < 1 || a->dstate > vssm::kMaxState)
+        return fail(VSSM_ERR_UNSUPPORTED, "dstate=%d outside 1..%d", a->dstate, vssm::kMaxState);
+    if (pieces > 1 && a->dstate != vssm::kMaxState)
+        return fail(VSSM_ERR_UNSUPPORTED, "pieces joined by the carry need dstate %d (got %d)",
+                    vssm::kMaxState, a->dstate);
+    if ((long long)a->batch * a->dim * a->seqlen == 0) {
+        *ranges_per_row = 0;
+        *launches = 0;
+        return VSSM_OK;
+    }
+    Plan pl;
+    make_plan(a, seg_len, pieces, &pl);
+    *ranges_per_row = pl.pieces;
+    *launches = pl.carry ? 2 : 1;
+    return VSSM_OK;
+}
+
+int vssm_scan_bidir(const vssm_scan_args *a, void *stream) { return run(a, 0, false, 0, stream); }
+
+int vssm_scan_chunked(const vssm_scan_args *a, int seg_len, int pieces, void *stream)
+{
+    return run(a, seg_len, seg_len > 0, pieces, stream);
+}
 
 int vssm_scan_bidir_noalloc(const vssm_scan_args *a, void *stream)
 {
@@ -397,8 +556,14 @@ int vssm_scan_bidir_noalloc(const vssm_scan_args *a, void *stream)
     b.workspace = nullptr;
     b.workspace_bytes = 0;
     size_t need = 0;
-    const int st = vssm_scan_workspace_size(&b, 0, &need);
+    int pieces = 0;
+    int st = vssm_scan_workspace_size(&b, 0, &need);
     if (st != VSSM_OK) return st;
+    if (need > VSSM_NOALLOC_SCRATCH_BYTES) {   // rows not cut for the carry need less
+        pieces = 1;
+        st = vssm_scan_chunked_workspace_size(&b, 0, pieces, &need);
+        if (st != VSSM_OK) return st;
+    }
     if (need > VSSM_NOALLOC_SCRATCH_BYTES)
         return fail(VSSM_ERR_UNSUPPORTED,
                     "vssm_scan_bidir_noalloc: this call needs %zu bytes of scratch but the built-in "
@@ -409,12 +574,12 @@ int vssm_scan_bidir_noalloc(const vssm_scan_args *a, void *stream)
         if (!b.workspace) return VSSM_ERR_CUDA;
         b.workspace_bytes = VSSM_NOALLOC_SCRATCH_BYTES;
     }
-    return run(&b, 0, false, stream);
+    return run(&b, 0, false, pieces, stream);
 }
 
 int vssm_scan_folded(const vssm_scan_args *a, int seg_len, void *stream)
 {
-    return run(a, seg_len, true, stream);
+    return run(a, seg_len, true, 0, stream);
 }
 
 int vssm_device_error(void *stream)

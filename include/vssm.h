@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define VSSM_VERSION 100 /* 1.0.0 */
+#define VSSM_VERSION 110 /* 1.1.0 */
 
 typedef enum {
     VSSM_OK = 0,
@@ -102,16 +102,70 @@ int vssm_scan_workspace_size(const vssm_scan_args *a, int seg_len, size_t *bytes
 /*
  * Bidirectional (or single-direction, by dir_flags) selective scan over
  * independent sequences of seqlen tokens. Vim page §2.2 and §3.1; VSSD page
- * §4.1.2 and §4.2.1.3.
+ * §4.1.2 and §4.2.1.3. When the rows are too few to occupy the GPU (small
+ * batch x dim), each row is cut into token ranges joined by the carry, as in
+ * vssm_scan_chunked; the result is the same up to fp32 rounding order.
  */
 int vssm_scan_bidir(const vssm_scan_args *a, void *stream);
 
 /*
+ * The scan of vssm_scan_bidir (seg_len == 0) or vssm_scan_folded
+ * (seg_len >= 1) with each row cut into a chosen number of contiguous token
+ * ranges that are scanned in parallel and joined exactly (Vim page §3.1,
+ * parallel scan; SF-Mamba page, the warp-scan remark):
+ *
+ *   1. every range except the last one in a direction is scanned from a zero
+ *      state, giving its end state hp[n] and its decay
+ *      P[n] = exp(A[d][n] * sum of delta over the range), or P = 0 when a
+ *      folded reset lies inside it;
+ *   2. the range maps an incoming state h to P*h + hp; these maps compose
+ *      associatively, (P1, h1) then (P2, h2) = (P1*P2, P2*h1 + h2), and the
+ *      exclusive prefix of the ranges before a range, applied to h = 0, is
+ *      that range's incoming state;
+ *   3. every range is scanned from its incoming state and writes its output.
+ *
+ * In exact arithmetic the result equals the unsplit scan; in fp32 it differs
+ * only in rounding order. Step 1 repeats the recurrence's exponentials on the
+ * ranges it summarises, so splitting pays only when the rows alone leave the
+ * GPU idle; vssm_scan_bidir chooses the count itself.
+ *
+ * pieces: 0 = the library's choice (what vssm_scan_bidir / vssm_scan_folded
+ * do); 1 = rows are not cut for the carry (a folded call may still be split
+ * at segment starts, which needs no carry); P > 1 = rows are cut into
+ * ceil(seqlen / ceil(seqlen / P)) ranges of ceil(seqlen / P) tokens (the last
+ * one shorter). P > 1 needs dstate == 16, else VSSM_ERR_UNSUPPORTED. The
+ * workspace must hold vssm_scan_chunked_workspace_size bytes: the partial
+ * outputs of bidirectional calls plus 2176 bytes per 32-channel group, range
+ * and direction for the range summaries. Other arguments and errors as in
+ * vssm_scan_bidir and vssm_scan_folded; seg_len < 0 or pieces < 0 give
+ * VSSM_ERR_INVALID_ARG.
+ */
+int vssm_scan_chunked(const vssm_scan_args *a, int seg_len, int pieces, void *stream);
+
+/* Workspace bytes for vssm_scan_chunked with these seg_len and pieces. */
+int vssm_scan_chunked_workspace_size(const vssm_scan_args *a, int seg_len, int pieces, size_t *bytes);
+
+/*
+ * How the call vssm_scan_chunked(a, seg_len, pieces, ...) would run (pieces
+ * = 0: also vssm_scan_bidir for seg_len == 0 and vssm_scan_folded for
+ * seg_len >= 1): *ranges_per_row receives the number of token ranges each
+ * row is scanned in (independent ranges at folded segment starts, or ranges
+ * joined by the carry), *launches the number of kernel launches (2 when a
+ * summary pass runs first, else 1; 0 for an empty problem). Reads only the
+ * sizes, dstate, dtype and dir_flags of `a`; touches no device. Errors:
+ * VSSM_ERR_INVALID_ARG for NULL pointers or invalid sizes, dir_flags,
+ * seg_len or pieces; VSSM_ERR_UNSUPPORTED as in vssm_scan_chunked.
+ */
+int vssm_scan_plan_query(const vssm_scan_args *a, int seg_len, int pieces, int *ranges_per_row,
+                         int *launches);
+
+/*
  * Bytes of the built-in scratch that vssm_scan_bidir_noalloc uses (16 MiB).
  * A call needs as much scratch as vssm_scan_workspace_size reports for it;
- * for bidirectional calls with dstate 16 that is 4 bytes per token and
- * channel (rounded up to whole 32-channel groups), so up to about 4.19
- * million token-channels fit.
+ * when that is more than the built-in scratch, the call runs without cutting
+ * rows for the carry, which for bidirectional calls with dstate 16 needs 4
+ * bytes per token and channel (rounded up to whole 32-channel groups), so up
+ * to about 4.19 million token-channels fit.
  */
 #define VSSM_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 

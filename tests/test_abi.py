@@ -27,7 +27,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ("vssm_scan_bidir", "vssm_scan_folded", "vssm_scan_workspace_size",
+    for n in ("vssm_scan_bidir", "vssm_scan_folded", "vssm_scan_chunked",
+              "vssm_scan_workspace_size", "vssm_scan_chunked_workspace_size",
               "vssm_status_string", "vssm_last_error", "vssm_version"):
         assert n in names
 
@@ -37,7 +38,7 @@ def test_library_exports_every_declared_symbol(v):
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared in vssm.h but not exported"
     assert set(v.EXPORTS) <= set(declared_functions())
-    assert v.version() == 100
+    assert v.version() == 110
 
 
 def test_args_struct_layout_matches_header(v):
@@ -81,12 +82,14 @@ def test_folded_validation(v):
 
 
 def test_workspace_required_for_long_rows(v):
-    a = _args(v, seqlen=4097, dim=64)
+    far = 1 << 32                                                # fake tensors may not overlap
+    a = _args(v, batch=32, seqlen=1025, dim=768, **{k: far * (i + 1) for i, k in enumerate(
+        ("x", "delta", "z", "B", "C", "A_fwd", "A_bwd", "D_fwd", "D_bwd", "out"))})  # no cuts
     n = ctypes.c_size_t()
     assert v.lib.vssm_scan_workspace_size(ctypes.byref(a), 0, ctypes.byref(n)) == 0
-    assert n.value == 64 * 4097 * 4
+    assert n.value == 32 * 768 * 1025 * 4
     assert _call(v, a) == -6                                     # no workspace given
-    a.workspace, a.workspace_bytes = (1 << 20) * 11, n.value - 16
+    a.workspace, a.workspace_bytes = far * 11, n.value - 16
     assert _call(v, a) == -6                                     # too small
 
 
@@ -109,3 +112,73 @@ def test_workspace_sizes(v):
 def test_empty_problem_launches_nothing(v):
     assert _call(v, _args(v, batch=0)) == 0
     assert _call(v, _args(v, seqlen=0, x=None, out=None)) == 0
+
+
+def _chunked_ws(v, a, seg, pieces):
+    n = ctypes.c_size_t(7)
+    st = v.lib.vssm_scan_chunked_workspace_size(ctypes.byref(a), seg, pieces, ctypes.byref(n))
+    return st, n.value
+
+
+def test_chunked_workspace_sizes(v):
+    a = _args(v, batch=1, dim=384, seqlen=197, dtype=0)        # 12 channel groups
+    # one piece: one fp32 partial output per token and channel
+    assert _chunked_ws(v, a, 0, 1) == (0, 384 * 197 * 4)
+    # 4 pieces of 50 tokens: partial outputs per range (rounded to 32-channel
+    # groups), then 2 directions x 12 groups x 4 summaries of 17 x 32 floats
+    assert _chunked_ws(v, a, 0, 4) == (0, 12 * 4 * 50 * 32 * 4 + 2 * 12 * 4 * 17 * 32 * 4)
+    # 5 requested pieces of 6 tokens on 26 tokens leave 5 pieces; 3 on 5 leave 3
+    a1 = _args(v, batch=1, dim=32, seqlen=26, dir_flags=1)
+    assert _chunked_ws(v, a1, 0, 5) == (0, 1 * 5 * 17 * 32 * 4)
+    a2 = _args(v, batch=1, dim=32, seqlen=5, dir_flags=2)
+    assert _chunked_ws(v, a2, 0, 4) == (0, 1 * 3 * 17 * 32 * 4)  # ceil(5/ceil(5/4)) = 3
+    # more pieces than tokens: one token each
+    a3 = _args(v, batch=1, dim=32, seqlen=3, dir_flags=1)
+    assert _chunked_ws(v, a3, 0, 64) == (0, 3 * 17 * 32 * 4)
+    # the library's choice for few rows includes summaries; for many rows it does not
+    n = ctypes.c_size_t()
+    assert v.lib.vssm_scan_workspace_size(ctypes.byref(a), 0, ctypes.byref(n)) == 0
+    assert n.value > 384 * 197 * 4
+    big = _args(v, batch=128, dim=768, seqlen=197)
+    assert v.lib.vssm_scan_workspace_size(ctypes.byref(big), 0, ctypes.byref(n)) == 0
+    assert n.value == 128 * 768 * 197 * 4
+
+
+def test_chunked_validation(v):
+    a = _args(v)
+    assert v.lib.vssm_scan_chunked(ctypes.byref(a), 0, -1, None) == -1
+    assert _chunked_ws(v, a, 0, -1)[0] == -1
+    assert _chunked_ws(v, a, -2, 2)[0] == -1
+    a8 = _args(v, dstate=8)
+    assert v.lib.vssm_scan_chunked(ctypes.byref(a8), 0, 2, None) == -2   # carry needs dstate 16
+    assert "dstate" in v.lib.vssm_last_error().decode()
+    assert v.lib.vssm_scan_chunked(ctypes.byref(_args(v, seqlen=10)), 4, 2, None) == -1  # L % seg
+
+
+def _plan(v, a, seg=0, pieces=0):
+    r, n = ctypes.c_int(-1), ctypes.c_int(-1)
+    st = v.lib.vssm_scan_plan_query(ctypes.byref(a), seg, pieces, ctypes.byref(r), ctypes.byref(n))
+    return st, r.value, n.value
+
+
+def test_plan_query(v):
+    # rows enough to fill the GPU: one range, one launch
+    assert _plan(v, _args(v, batch=128, dim=768, seqlen=197)) == (0, 1, 1)
+    # the 1024^2 workload (8 x 24 channel groups per direction, one warp per
+    # scheduler at most) is cut into ranges joined by the carry: summary
+    # pass + scan
+    st, r, n = _plan(v, _args(v, batch=8, dim=768, seqlen=4097))
+    assert st == 0 and 2 <= r <= 16 and n == 2
+    # so is a single 197-token row of 384 channels (the 224^2 Vim-Ti case)
+    st, r, n = _plan(v, _args(v, batch=1, dim=384, seqlen=197))
+    assert st == 0 and r > 1 and n == 2
+    # explicit pieces
+    assert _plan(v, _args(v, seqlen=26), 0, 5) == (0, 5, 2)
+    assert _plan(v, _args(v, seqlen=26), 0, 1) == (0, 1, 1)
+    # folded rows with many segments: independent ranges at segment starts
+    st, r, n = _plan(v, _args(v, batch=1, dim=1024, seqlen=52224, dir_flags=1), 51)
+    assert st == 0 and r > 1 and n == 1 and 52224 % r == 0 or (st == 0 and n == 1)
+    # empty problem, bad arguments
+    assert _plan(v, _args(v, batch=0)) == (0, 0, 0)
+    assert _plan(v, _args(v), 0, -1)[0] == -1
+    assert _plan(v, _args(v, dstate=8), 0, 2)[0] == -2
