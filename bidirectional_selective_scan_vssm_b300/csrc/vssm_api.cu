@@ -79,65 +79,106 @@ constexpr int kTargetCtas = 148 * 8;         // enough CTAs to fill 148 SMs
 constexpr int kFoldTargetWarps = 148 * 48;
 
 constexpr int warps_per_cta(int G) { return G == 4 ? 8 : (G == 2 ? 4 : 2); }
-constexpr int kCarryW = 4;                   // warps per CTA of the summary kernel
+#ifndef VSSM_CARRY_WARPS
+#define VSSM_CARRY_WARPS 1
+#endif
+constexpr int kCarryW = VSSM_CARRY_WARPS;    // warps per CTA of the summary kernel
 
 // Sub-partitions of the GPU (148 SMs x 4 schedulers).
 constexpr int kSubParts = 148 * 4;
 
-// Estimated SM cycles of one call with each row cut into P ranges of lp
-// tokens. The constants are a least-squares fit to B300 timings of both
-// kernels (nine shapes from batch 1 x 384 channels x 197 tokens to batch 8 x
-// 768 x 4097, 1 to 64 ranges of at least 32 tokens; 8 % rms error): a scan
-// warp costs about 247 cycles per token when it has its scheduler to itself,
-// 189 with two warps per scheduler and 210 with three; a summary warp 0.75 of
-// that; a cut call about 4.5 us more plus 0.47 us per range. Up to the
-// residency limit (3 warps per scheduler) the busiest scheduler holds
-// ceil(warps / kSubParts) of them at once; beyond it the warps stream
-// through and the load is their average.
-double carry_cost(long long row_warps, long long lp, int P)
+// Cost model of one call with each row cut into P ranges of lp tokens, in
+// microseconds. It is a least-squares fit to B300 timings of each kernel
+// (ncu launch lists over 34 cuts of six shapes, batch 1 x 384 channels x
+// 197 tokens to batch 16 x 768 x 1025 and batch 8 x 768 x 4097; 3.4 % rms
+// error for the scan, 5.9 % for the summary pass). A kernel's warps run in
+// rounds of its residency (warps that fit on the GPU at once); in a round
+// each scheduler holds k of them, and a warp costs c(k) cycles per token plus
+// a start-up cost. The scan also pays for gathering up to P - 1 summaries.
+struct KernelCost {
+    double c1, c2, c3;   // cycles per token per warp with 1, 2, >= 3 warps per scheduler
+    double start;        // cycles per warp outside the token loop
+    double launch_us;    // per launch
+};
+constexpr KernelCost kScanCost{268.8, 189.2, 173.4, 5717.0, 3.7};
+constexpr KernelCost kSummaryCost{170.9, 130.3, 113.4, 620.0, 4.3};
+constexpr double kFoldUsPerRange = 0.2;
+constexpr double kClockMHz = 2032.0;
+
+double kernel_us(const KernelCost &m, long long warps, long long lp, long long resident)
 {
-    auto per_token = [](long long w) {
-        return w <= kSubParts ? 247.0 : (w <= 2 * kSubParts ? 189.0 : 210.0);
-    };
-    auto load = [](long long w) {
-        return w <= 3 * kSubParts ? (double)((w + kSubParts - 1) / kSubParts) : (double)w / kSubParts;
-    };
-    const long long wm = row_warps * P;
-    double c = load(wm) * (double)lp * per_token(wm);
-    if (P > 1) {
-        const long long ws = row_warps * (P - 1);
-        c += 0.75 * load(ws) * (double)lp * per_token(ws);
-        c += (4.5 + 0.47 * (P - 1)) * 2032.0;
+    auto per_token = [&](double k) { return k <= 1.0 ? m.c1 : (k <= 2.0 ? m.c2 : m.c3); };
+    const long long full = warps / resident, rem = warps - full * resident;
+    const double kf = (double)resident / kSubParts;
+    double cyc = (double)full * kf * ((double)lp * per_token(kf) + m.start);
+    if (rem > 0) {
+        const double kr = (double)((rem + kSubParts - 1) / kSubParts);
+        cyc += kr * ((double)lp * per_token(kr) + m.start);
     }
-    return c;
+    return cyc / kClockMHz + m.launch_us;
 }
 
-// Ranges per row (cut on the 16-token chunk grid) that minimise carry_cost;
-// 1 when the rows alone fill the GPU. Returns the range length in *lp_out.
-int auto_carry_pieces(long long row_warps, int L, long long *lp_out)
+// Warps of a kernel resident on the GPU at once: shared memory per SM
+// (228 KB, 1 KB reserved per CTA) over the CTA footprint.
+long long resident_warps(size_t warp_bytes, int warps_per_cta)
+{
+    const long long per_sm = (228 * 1024) / ((long long)warps_per_cta * warp_bytes + 1024);
+    return 148LL * std::max(1LL, std::min(32LL, per_sm)) * warps_per_cta;
+}
+
+struct CarryShape {
+    long long row_warps;         // batch x channel groups x directions
+    long long res_scan, res_summary;
+};
+
+double carry_us(const CarryShape &c, long long lp, int P)
+{
+    double t = kernel_us(kScanCost, c.row_warps * P, lp, c.res_scan);
+    if (P > 1)
+        t += kernel_us(kSummaryCost, c.row_warps * (P - 1), lp, c.res_summary) +
+             kFoldUsPerRange * (P - 1);
+    return t;
+}
+
+// Ranges per row (cut on the 16-token chunk grid, at most 32, at least 32
+// tokens each) that minimise carry_us; 1 unless cutting saves 5 % or more.
+// Returns the range length in *lp_out.
+int auto_carry_pieces(const CarryShape &c, int L, long long *lp_out)
 {
     *lp_out = L;
-    if (row_warps <= 0 || row_warps >= 3 * kSubParts || L < 64) return 1;
-    const double one = carry_cost(row_warps, L, 1);
+    if (c.row_warps <= 0 || c.row_warps >= c.res_scan || L < 64) return 1;
+    const double one = carry_us(c, L, 1);
     double best = 0.0;
     int bestP = 1;
     long long bestLp = L;
-    for (int P = 2; P <= 64; ++P) {
+    for (int P = 2; P <= 32; ++P) {
         const long long lp = ((long long)L + P - 1) / P;
         if (lp < 32) break;
         const long long lp16 = (lp + 15) / 16 * 16;
         const int pieces = (int)(((long long)L + lp16 - 1) / lp16);
         if (pieces < 2) continue;
-        const double c = carry_cost(row_warps, lp16, pieces);
-        if (bestP == 1 || c < best) {
-            best = c;
+        const double t = carry_us(c, lp16, pieces);
+        if (bestP == 1 || t < best) {
+            best = t;
             bestP = pieces;
             bestLp = lp16;
         }
     }
-    if (bestP == 1 || best >= 0.95 * one) return 1;   // cut only for a clear gain
+    if (bestP == 1 || best >= 0.95 * one) return 1;
     *lp_out = bestLp;
     return bestP;
+}
+
+template <typename T>
+CarryShape carry_shape(long long row_warps, unsigned dirs)
+{
+    CarryShape c;
+    c.row_warps = row_warps;
+    const size_t scan_bytes = dirs == 3 ? vssm::WarpLayout<T, 1, true>::kWarpBytes
+                                        : vssm::WarpLayout<T, 1, false>::kWarpBytes;
+    c.res_scan = resident_warps(scan_bytes, warps_per_cta(1));
+    c.res_summary = resident_warps(vssm::WarpLayout<T, 1, false>::kWarpBytes, kCarryW);
+    return c;
 }
 
 // Plan for the warp kernel (dstate == 16). pieces_req: 0 lets the plan
@@ -168,7 +209,9 @@ void make_warp_plan(const vssm_scan_args *a, int seg_len, int pieces_req, Plan *
         lp = std::max(1LL, ((long long)a->seqlen + carry_p - 1) / carry_p);
         carry_p = (int)(((long long)a->seqlen + lp - 1) / lp);
     } else if (carry_p == 0 && seg_len == 0) {
-        carry_p = auto_carry_pieces(pl->srows * ndir, a->seqlen, &lp);
+        const CarryShape cs = a->dtype == VSSM_F32 ? carry_shape<float>(pl->srows * ndir, dirs)
+                                                   : carry_shape<__nv_bfloat16>(pl->srows * ndir, dirs);
+        carry_p = auto_carry_pieces(cs, a->seqlen, &lp);
     }
     if (carry_p > 1) {
         pl->piece_len = (int)lp;
