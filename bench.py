@@ -260,11 +260,12 @@ def cpu_model():
 
 # ------------------------------------------------------------------ CPU oracle leg
 
-def oracle_sample_run(wl, inp, target_s):
+def oracle_sample_run(wl, inp, target_s, nthreads=0):
     """Time the fp64 oracle (as it stands) on a slice of the workload sized to
-    about target_s seconds. Returns (tokch, seconds, threads, description)."""
+    about target_s seconds, on nthreads OpenMP threads (0: all cores).
+    Returns (tokch, seconds, threads, description)."""
     import oracle
-    threads = oracle.max_threads()
+    threads = nthreads if nthreads > 0 else oracle.max_threads()
 
     def slice_inputs(nb, nd):
         s = (slice(0, nb), slice(0, nd))
@@ -277,7 +278,7 @@ def oracle_sample_run(wl, inp, target_s):
     def run(a):
         t0 = time.perf_counter()
         oracle.scan(a["x"], a["delta"], a["A_fwd"], a["A_bwd"], a["B"], a["C"], a["D_fwd"],
-                    a["D_bwd"], a["z"], dirs=wl.dirs, seg_len=wl.seg_len)
+                    a["D_bwd"], a["z"], dirs=wl.dirs, seg_len=wl.seg_len, nthreads=nthreads)
         return time.perf_counter() - t0
 
     def shape(rows):
@@ -512,6 +513,10 @@ def run_ours(args):
         cpu = {"value": round(tok * (set_bytes / wl.tokch) / secs / 1e9, 5), "unit": "GB/s",
                "cores": threads, "kind": "oracle", "sample": desc,
                "gtokch_per_s": round(tok / secs / 1e9, 6), "cpu": cpu_model()}
+        tok1, secs1, _, desc1 = oracle_sample_run(wl, inp, min(5.0, args.cpu_seconds / 2), nthreads=1)
+        cpu["single_thread"] = {"value": round(tok1 * (set_bytes / wl.tokch) / secs1 / 1e9, 5),
+                                "unit": "GB/s", "gtokch_per_s": round(tok1 / secs1 / 1e9, 6),
+                                "sample": desc1}
 
     if rank == 0:
         line = {
