@@ -18,8 +18,10 @@ Pins (in ``tests/test_oracle_pins.py``): the quadratic form, a hand-worked
 two-step example from the SSD page's linear-form section, closed forms for
 A = 0 (prefix sum), vanishing decay, Δ = 0 and C = 0, L = 1, the
 backward-equals-flipped-forward invariant, folded-equals-per-segment, the
-silu gate against scipy's logistic function, linearity in x, and a mutation
-test that plants mistakes in a copy of the C source.
+silu gate against scipy's logistic function, linearity in x, the fused step
+map against the closed-form inverse of softplus (and softplus(0) = ln 2), the
+per-direction step as a sum of single-direction scans, and a mutation test
+that plants mistakes in a copy of the C source.
 """
 from __future__ import annotations
 
@@ -63,6 +65,9 @@ def load_library(path: str):
     lib.oracle_scan.restype = ctypes.c_int
     lib.oracle_scan.argtypes = [dp] * 12 + [ctypes.c_long] * 4 + [
         ctypes.c_int, ctypes.c_long, ctypes.c_int]
+    lib.oracle_scan_ex.restype = ctypes.c_int
+    lib.oracle_scan_ex.argtypes = [dp] * 14 + [ctypes.c_int, dp] + [ctypes.c_long] * 4 + [
+        ctypes.c_int, ctypes.c_long, ctypes.c_int]
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
 
@@ -88,11 +93,21 @@ def _as_f64(a):
 
 def scan(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None,
          B_bwd=None, C_bwd=None, dirs: int = DIR_BOTH, seg_len: int = 0,
-         nthreads: int = 0, lib=None) -> np.ndarray:
+         nthreads: int = 0, lib=None, delta_bwd=None, delta_bias=None,
+         delta_bias_bwd=None, delta_softplus: bool = False) -> np.ndarray:
     """Run the fp64 oracle. Arrays may be any float dtype; they are widened to
     float64 exactly. Shapes: x, delta, z (batch, dim, L); B, C (batch, L, N);
-    A (dim, N); D (dim,). Returns out (batch, dim, L) float64."""
+    A (dim, N); D (dim,). Returns out (batch, dim, L) float64.
+
+    delta_bwd: the backward direction's step (None = delta). With
+    delta_softplus each direction's step is softplus(its delta + its bias[d])
+    (delta_bias, delta_bias_bwd: (dim,); None = 0 / = delta_bias)."""
     lib = lib or _get_lib()
+    if delta_bwd is not None or delta_bias is not None or delta_bias_bwd is not None \
+            or delta_softplus:
+        return _scan_ex(lib, x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, B_bwd, C_bwd,
+                        dirs, seg_len, nthreads, delta_bwd, delta_bias, delta_bias_bwd,
+                        delta_softplus)
     x = np.asarray(x)
     batch, dim, L = x.shape
     N = np.asarray(B).shape[-1]
@@ -110,6 +125,26 @@ def scan(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None,
                          int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_scan rejected its arguments (status {rc})")
+    return out
+
+
+def _scan_ex(lib, x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, B_bwd, C_bwd, dirs, seg_len,
+             nthreads, delta_bwd, delta_bias, delta_bias_bwd, delta_softplus):
+    x = np.asarray(x)
+    batch, dim, L = x.shape
+    N = np.asarray(B).shape[-1]
+    keep, ptrs = [], []
+    for a in (x, delta, z, B, C, B_bwd, C_bwd, A_fwd, A_bwd, D_fwd, D_bwd,
+              delta_bwd, delta_bias, delta_bias_bwd):
+        arr, p = _as_f64(a)
+        keep.append(arr)
+        ptrs.append(p)
+    out = np.empty((batch, dim, L), dtype=np.float64)
+    pout = out.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+    rc = lib.oracle_scan_ex(*ptrs, int(bool(delta_softplus)), pout, batch, dim, L, N,
+                            int(dirs), int(seg_len), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_scan_ex rejected its arguments (status {rc})")
     return out
 
 

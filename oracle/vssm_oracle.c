@@ -26,6 +26,15 @@
  * No hidden state is returned (SF-Mamba page, "实现优化": hidden-state output
  * suppressed at inference).
  *
+ * Per-direction step and fused step transform (oracle_scan_ex): each
+ * direction is its own SSM module (Vim page §2.2, the forward_ssm /
+ * backward_ssm sketch), so the backward direction may take its own delta.
+ * The step may also be given before its positivity map: with `softplus` set,
+ * the step of direction k is softplus(delta_k[t] + bias_k[d]), the bias being
+ * the step projection's bias (Mamba2D page, "Mamba2D Block结构": dt_proj has
+ * bias=True) and softplus(v) = log(1 + exp(v)) the map the Mamba family uses
+ * to keep the step positive (the pages name no map; this is a reading).
+ *
  * Layouts (row-major, last index fastest): x, delta, z, out: [batch][dim][L];
  * B, C (and B_bwd, C_bwd): [batch][L][N]; A: [dim][N]; D: [dim].
  */
@@ -39,7 +48,7 @@
 #define ORACLE_EINVAL (-1)
 #define ORACLE_ENOMEM (-2)
 
-int oracle_version(void) { return 1; }
+int oracle_version(void) { return 2; }
 
 int oracle_max_threads(void) {
 #ifdef _OPENMP
@@ -77,6 +86,23 @@ static void scan_row_direction(const double *xr, const double *dtr,
     }
 }
 
+/* softplus(v) = log(1 + exp(v)), evaluated as max(v, 0) + log(1 + exp(-|v|))
+ * so that exp never overflows (the two forms are equal). */
+static double softplus(double v)
+{
+    return (v > 0.0 ? v : 0.0) + log1p(exp(-fabs(v)));
+}
+
+/* The step of one direction over one row: the raw values, or, with
+ * softplus set, softplus(raw + bias). */
+static const double *direction_step(const double *raw, long L, int use_softplus, double bias,
+                                    double *buf)
+{
+    if (!use_softplus) return raw;
+    for (long t = 0; t < L; ++t) buf[t] = softplus(raw[t] + bias);
+    return buf;
+}
+
 /*
  * dirs: bit 0 = forward, bit 1 = backward (at least one set).
  * seg_len: 0 = plain sequences; > 0 = folded with reset every seg_len tokens
@@ -84,6 +110,17 @@ static void scan_row_direction(const double *xr, const double *dtr,
  * z, D_fwd, D_bwd may be NULL (no gate / zero skip). B_bwd, C_bwd may be NULL
  * (backward shares B, C). nthreads <= 0 uses the OpenMP default.
  */
+int oracle_scan_ex(const double *x, const double *delta, const double *z,
+                   const double *B, const double *C,
+                   const double *B_bwd, const double *C_bwd,
+                   const double *A_fwd, const double *A_bwd,
+                   const double *D_fwd, const double *D_bwd,
+                   const double *delta_bwd, const double *bias_fwd, const double *bias_bwd,
+                   int use_softplus, double *out,
+                   long batch, long dim, long L, long N,
+                   int dirs, long seg_len, int nthreads);
+
+/* The scan with one step tensor for both directions, used as given. */
 int oracle_scan(const double *x, const double *delta, const double *z,
                 const double *B, const double *C,
                 const double *B_bwd, const double *C_bwd,
@@ -92,6 +129,26 @@ int oracle_scan(const double *x, const double *delta, const double *z,
                 double *out,
                 long batch, long dim, long L, long N,
                 int dirs, long seg_len, int nthreads)
+{
+    return oracle_scan_ex(x, delta, z, B, C, B_bwd, C_bwd, A_fwd, A_bwd, D_fwd, D_bwd,
+                          NULL, NULL, NULL, 0, out, batch, dim, L, N, dirs, seg_len, nthreads);
+}
+
+/*
+ * As oracle_scan, plus: delta_bwd ([batch][dim][L]) is the backward step
+ * (NULL = delta); with use_softplus set each direction's step is
+ * softplus(its delta + its bias[d]), bias_fwd / bias_bwd ([dim]; NULL = 0 for
+ * the forward bias, = bias_fwd for the backward one).
+ */
+int oracle_scan_ex(const double *x, const double *delta, const double *z,
+                   const double *B, const double *C,
+                   const double *B_bwd, const double *C_bwd,
+                   const double *A_fwd, const double *A_bwd,
+                   const double *D_fwd, const double *D_bwd,
+                   const double *delta_bwd, const double *bias_fwd, const double *bias_bwd,
+                   int use_softplus, double *out,
+                   long batch, long dim, long L, long N,
+                   int dirs, long seg_len, int nthreads)
 {
     if (!x || !delta || !B || !C || !out) return ORACLE_EINVAL;
     if (batch < 0 || dim < 0 || L < 0 || N <= 0) return ORACLE_EINVAL;
@@ -102,6 +159,8 @@ int oracle_scan(const double *x, const double *delta, const double *z,
     if (seg_len > 0 && (dirs & 2) && L % seg_len != 0) return ORACLE_EINVAL;
     if (!B_bwd) B_bwd = B;
     if (!C_bwd) C_bwd = C;
+    if (!delta_bwd) delta_bwd = delta;
+    if (!bias_bwd) bias_bwd = bias_fwd;
 
     const long rows = batch * dim;
     int err = ORACLE_OK;
@@ -112,7 +171,8 @@ int oracle_scan(const double *x, const double *delta, const double *z,
     {
         double *h = (double *)malloc(sizeof(double) * (size_t)N);
         double *acc = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
-        if (!h || !acc) {
+        double *step = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+        if (!h || !acc || !step) {
 #ifdef _OPENMP
 #pragma omp atomic write
 #endif
@@ -124,16 +184,21 @@ int oracle_scan(const double *x, const double *delta, const double *z,
             for (long r = 0; r < rows; ++r) {
                 const long b = r / dim, d = r % dim;
                 const double *xr = x + r * L;
-                const double *dtr = delta + r * L;
                 for (long t = 0; t < L; ++t) acc[t] = 0.0;
-                if (dirs & 1)
+                if (dirs & 1) {
+                    const double *dtr = direction_step(delta + r * L, L, use_softplus,
+                                                       bias_fwd ? bias_fwd[d] : 0.0, step);
                     scan_row_direction(xr, dtr, B + b * L * N, C + b * L * N,
                                        A_fwd + d * N, D_fwd ? D_fwd[d] : 0.0,
                                        L, N, 0, seg_len, h, acc);
-                if (dirs & 2)
+                }
+                if (dirs & 2) {
+                    const double *dtr = direction_step(delta_bwd + r * L, L, use_softplus,
+                                                       bias_bwd ? bias_bwd[d] : 0.0, step);
                     scan_row_direction(xr, dtr, B_bwd + b * L * N, C_bwd + b * L * N,
                                        A_bwd + d * N, D_bwd ? D_bwd[d] : 0.0,
                                        L, N, 1, seg_len, h, acc);
+                }
                 double *outr = out + r * L;
                 for (long t = 0; t < L; ++t) {
                     double g = 1.0;
@@ -147,6 +212,7 @@ int oracle_scan(const double *x, const double *delta, const double *z,
         }
         free(h);
         free(acc);
+        free(step);
     }
     return err;
 }

@@ -226,10 +226,84 @@ def pin_linearity(lib):
     return _close(y3, a * y1 + b * y2, 1e-12)
 
 
+def _softplus_inverse(step):
+    """The pre-activation whose softplus is `step` (> 0): log(exp(step) - 1),
+    from the closed form of the inverse."""
+    return np.log(np.expm1(step))
+
+
+def pin_softplus_step(lib):
+    """Fused step map: softplus(delta + bias) per direction, checked against
+    targets built with the closed-form inverse of softplus. A direction fed
+    raw = log(expm1(s)) - bias must scan exactly like the plain oracle fed the
+    step s; both directions together (no gate) are the sum of the two
+    single-direction scans, each with its own step and bias."""
+    rng = np.random.default_rng(31)
+    p = _rand_problem(rng, 2, 5, 23, 6, gate=False)
+    s_f = np.exp(rng.normal(-1.5, 0.6, size=p["x"].shape))      # target steps, > 0
+    s_b = np.exp(rng.normal(-1.0, 0.6, size=p["x"].shape))
+    bias_f = rng.normal(0.0, 1.0, size=5)
+    bias_b = rng.normal(0.0, 1.0, size=5)
+    raw_f = _softplus_inverse(s_f) - bias_f[None, :, None]
+    raw_b = _softplus_inverse(s_b) - bias_b[None, :, None]
+    ok = True
+    for dirs in (1, 2, 3):
+        got = oracle.scan(p["x"], raw_f, p["A_fwd"], p["A_bwd"], p["B"], p["C"], p["D_fwd"],
+                          p["D_bwd"], None, dirs=dirs, lib=lib, delta_bwd=raw_b,
+                          delta_bias=bias_f, delta_bias_bwd=bias_b, delta_softplus=True)
+        want = 0.0
+        if dirs & 1:
+            want = want + oracle.scan(p["x"], s_f, p["A_fwd"], p["A_bwd"], p["B"], p["C"],
+                                      p["D_fwd"], p["D_bwd"], None, dirs=1, lib=lib)
+        if dirs & 2:
+            want = want + oracle.scan(p["x"], s_b, p["A_fwd"], p["A_bwd"], p["B"], p["C"],
+                                      p["D_fwd"], p["D_bwd"], None, dirs=2, lib=lib)
+        ok = ok and _close(got, want, 1e-10)
+    # softplus(0) = ln 2: raw = -bias gives the constant step ln 2
+    zero = -np.broadcast_to(bias_f[None, :, None], p["x"].shape)
+    got = oracle.scan(p["x"], zero, p["A_fwd"], p["A_bwd"], p["B"], p["C"], p["D_fwd"],
+                      p["D_bwd"], None, dirs=1, lib=lib, delta_bias=bias_f, delta_softplus=True)
+    want = oracle.scan(p["x"], np.full(p["x"].shape, np.log(2.0)), p["A_fwd"], p["A_bwd"],
+                       p["B"], p["C"], p["D_fwd"], p["D_bwd"], None, dirs=1, lib=lib)
+    ok = ok and _close(got, want, 1e-12)
+    # large pre-activations: softplus(v) = v to within exp(-v); no overflow at 800
+    for v in (40.0, 800.0):
+        big = np.full(p["x"].shape, v)
+        got = oracle.scan(p["x"], big, p["A_fwd"], p["A_bwd"], p["B"], p["C"], p["D_fwd"],
+                          p["D_bwd"], None, dirs=1, lib=lib, delta_softplus=True)
+        want = oracle.scan(p["x"], big, p["A_fwd"], p["A_bwd"], p["B"], p["C"], p["D_fwd"],
+                           p["D_bwd"], None, dirs=1, lib=lib)
+        ok = ok and _close(got, want, 1e-12)
+    return ok
+
+
+def pin_per_direction_step(lib):
+    """The backward direction with its own step: both directions (no gate) are
+    the forward scan with delta plus the backward scan with delta_bwd, and the
+    backward scan with delta_bwd is the forward scan of the flipped sequence
+    (A_bwd, D_bwd, flipped delta_bwd, x, B, C)."""
+    rng = np.random.default_rng(37)
+    p = _rand_problem(rng, 2, 4, 19, 5, gate=False)
+    d_b = np.log1p(np.exp(rng.normal(-0.5, 0.5, size=p["x"].shape)))
+    both = oracle.scan(p["x"], p["delta"], p["A_fwd"], p["A_bwd"], p["B"], p["C"], p["D_fwd"],
+                       p["D_bwd"], None, dirs=3, lib=lib, delta_bwd=d_b)
+    fwd = oracle.scan(p["x"], p["delta"], p["A_fwd"], p["A_bwd"], p["B"], p["C"], p["D_fwd"],
+                      p["D_bwd"], None, dirs=1, lib=lib)
+    bwd = oracle.scan(p["x"], p["delta"], p["A_fwd"], p["A_bwd"], p["B"], p["C"], p["D_fwd"],
+                      p["D_bwd"], None, dirs=2, lib=lib, delta_bwd=d_b)
+    fl = lambda a: np.ascontiguousarray(a[..., ::-1])
+    fB = np.ascontiguousarray(p["B"][:, ::-1, :])
+    fC = np.ascontiguousarray(p["C"][:, ::-1, :])
+    flipped = fl(oracle.scan(fl(p["x"]), fl(d_b), p["A_bwd"], p["A_bwd"], fB, fC, p["D_bwd"],
+                             p["D_bwd"], None, dirs=1, lib=lib))
+    return _close(both, fwd + bwd, 1e-12) and _close(bwd, flipped, 1e-12)
+
+
 PINS = [pin_worked_example, pin_quadratic_form, pin_A_zero_prefix_sum,
         pin_vanishing_decay, pin_zero_input_paths, pin_single_token,
         pin_backward_is_flipped_forward, pin_folded_equals_segments,
-        pin_reset_first_token, pin_gate, pin_linearity]
+        pin_reset_first_token, pin_gate, pin_linearity, pin_softplus_step,
+        pin_per_direction_step]
 
 
 def failing_pins(lib):

@@ -38,6 +38,11 @@ MUTANTS = {
     "gate_sign": ("zt / (1.0 + exp(-zt))", "zt / (1.0 + exp(zt))"),
     "bwd_uses_fwd_A": ("A_bwd + d * N", "A_fwd + d * N"),
     "state_not_reset_between_rows": ("for (long n = 0; n < N; ++n) h[n] = 0.0;", ""),
+    "softplus_drops_log": ("log1p(exp(-fabs(v)))", "exp(-fabs(v))"),
+    "softplus_wrong_branch": ("(v > 0.0 ? v : 0.0)", "(v > 0.0 ? 0.0 : v)"),
+    "step_bias_not_added": ("softplus(raw[t] + bias)", "softplus(raw[t])"),
+    "bwd_step_uses_fwd_bias": ("bias_bwd ? bias_bwd[d] : 0.0", "bias_fwd ? bias_fwd[d] : 0.0"),
+    "bwd_uses_fwd_step": ("direction_step(delta_bwd + r * L", "direction_step(delta + r * L"),
 }
 
 
