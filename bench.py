@@ -60,7 +60,26 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle sample")
+    p.add_argument("--fused-step", action="store_true",
+                   help="pass per-direction steps before softplus, with biases (the kernel "
+                        "applies softplus(delta + bias))")
     return p.parse_args(argv)
+
+
+def selected_workload(args):
+    wl = WORKLOADS[args.workload]
+    return wl.scaled(fused_step=True) if args.fused_step else wl
+
+
+STEP_KEYS = ("delta_bwd", "delta_bias", "delta_bias_bwd")
+
+
+def step_kwargs(t, wl):
+    """Step options of the call: per-direction steps and biases, softplus inside."""
+    if not wl.fused_step:
+        return {}
+    return dict(delta_bwd=t["delta_bwd"], delta_bias=t["delta_bias"],
+                delta_bias_bwd=t["delta_bias_bwd"], delta_softplus=True)
 
 
 # ------------------------------------------------------------------ distributed
@@ -269,16 +288,23 @@ def oracle_sample_run(wl, inp, target_s, nthreads=0):
 
     def slice_inputs(nb, nd):
         s = (slice(0, nb), slice(0, nd))
-        return dict(x=np.asarray(inp.x[s], np.float64), delta=np.asarray(inp.delta[s], np.float64),
-                    z=np.asarray(inp.z[s], np.float64), B=np.asarray(inp.B[:nb], np.float64),
-                    C=np.asarray(inp.C[:nb], np.float64), A_fwd=inp.A_fwd[:nd].astype(np.float64),
-                    A_bwd=inp.A_bwd[:nd].astype(np.float64), D_fwd=inp.D_fwd[:nd].astype(np.float64),
-                    D_bwd=inp.D_bwd[:nd].astype(np.float64))
+        a = dict(x=np.asarray(inp.x[s], np.float64), delta=np.asarray(inp.delta[s], np.float64),
+                 z=np.asarray(inp.z[s], np.float64), B=np.asarray(inp.B[:nb], np.float64),
+                 C=np.asarray(inp.C[:nb], np.float64), A_fwd=inp.A_fwd[:nd].astype(np.float64),
+                 A_bwd=inp.A_bwd[:nd].astype(np.float64), D_fwd=inp.D_fwd[:nd].astype(np.float64),
+                 D_bwd=inp.D_bwd[:nd].astype(np.float64), step={})
+        if wl.fused_step:
+            a["step"] = dict(delta_bwd=np.asarray(inp.delta_bwd[s], np.float64),
+                             delta_bias=inp.delta_bias[:nd].astype(np.float64),
+                             delta_bias_bwd=inp.delta_bias_bwd[:nd].astype(np.float64),
+                             delta_softplus=True)
+        return a
 
     def run(a):
         t0 = time.perf_counter()
         oracle.scan(a["x"], a["delta"], a["A_fwd"], a["A_bwd"], a["B"], a["C"], a["D_fwd"],
-                    a["D_bwd"], a["z"], dirs=wl.dirs, seg_len=wl.seg_len, nthreads=nthreads)
+                    a["D_bwd"], a["z"], dirs=wl.dirs, seg_len=wl.seg_len, nthreads=nthreads,
+                    **a["step"])
         return time.perf_counter() - t0
 
     def shape(rows):
@@ -315,7 +341,7 @@ def run_reference(args):
     rank, world = dist_init("gloo")
     if rank != 0:
         return
-    wl = WORKLOADS[args.workload]
+    wl = selected_workload(args)
     inp = make_inputs(wl, seed=0)
     per_step = min(10.0, max(0.2, 150.0 / max(1, args.steps + args.warmup)))
     bpt = algorithmic_bytes(wl) / wl.tokch
@@ -348,6 +374,8 @@ def workload_config(wl, l2_note):
             "dstate": wl.dstate, "io_dtype": wl.dtype,
             "dirs": {DIR_FWD: "fwd", DIR_BWD: "bwd", DIR_BOTH: "both"}[wl.dirs],
             "seg_len": wl.seg_len or None, "gate": "silu(z)", "l2": l2_note,
+            "step": ("softplus(delta + bias), own delta and bias per direction" if wl.fused_step
+                     else "delta as given (post-softplus), shared by both directions"),
             "description": wl.description}
 
 
@@ -363,7 +391,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dist_init("nccl")
     dev = torch.device("cuda", local)
-    wl = WORKLOADS[args.workload]
+    wl = selected_workload(args)
     inp = make_inputs(wl, seed=rank)
     set_bytes = algorithmic_bytes(wl)
 
@@ -375,6 +403,10 @@ def run_ours(args):
     base = {k: upload(inp.storage(k)) for k in ("x", "delta", "z", "B", "C")}
     for k in ("A_fwd", "A_bwd", "D_fwd", "D_bwd"):
         base[k] = torch.from_numpy(getattr(inp, k)).to(dev)
+    if wl.fused_step:
+        base["delta_bwd"] = upload(inp.storage("delta_bwd"))
+        base["delta_bias"] = torch.from_numpy(inp.delta_bias).to(dev)
+        base["delta_bias_bwd"] = torch.from_numpy(inp.delta_bias_bwd).to(dev)
     nsets = int(min(64, max(2, math.ceil(3 * L2_BYTES / set_bytes))))
     sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(nsets - 1)]
     outs = [torch.empty_like(base["x"]) for _ in range(nsets)]
@@ -390,7 +422,7 @@ def run_ours(args):
     ws = None
     for s, o in zip(sets, outs):
         a = vssm.make_args(s["x"], s["delta"], s["A_fwd"], s["A_bwd"], s["B"], s["C"],
-                           s["D_fwd"], s["D_bwd"], s["z"], o, dirs=wl.dirs)
+                           s["D_fwd"], s["D_bwd"], s["z"], o, dirs=wl.dirs, **step_kwargs(s, wl))
         need = vssm.workspace_size(a, seg)
         if need and ws is None:
             ws = torch.empty(need, dtype=torch.uint8, device=dev)
@@ -452,7 +484,7 @@ def run_ours(args):
     roofline = {
         "bound": "alu", "achieved": round(ach, 2), "peak": round(peak_upd, 2),
         "unit": "Gupdate/s", "frac": round(ach / peak_upd, 4),
-        "traffic": ncu_traffic(wl.name),
+        "traffic": ncu_traffic(wl.name + ("+fused_step" if wl.fused_step else "")),
         "update": "one (token, channel, state, direction) recurrence step: 1 MUFU ex2 + 4 fp32 FMA-pipe ops",
         "peak_basis": f"{EX2_PER_CLK_SM} ex2/clk/SM (and {FMA_PER_CLK_SM}/4 FMA-pipe updates/clk/SM) "
                       f"x {SMS} SMs x {MAX_SM_MHZ:.0f} MHz max SM clock",
@@ -481,7 +513,7 @@ def run_ours(args):
             for k in host:
                 dst[k].copy_(host[k], non_blocking=True)
             kw = dict(D_fwd=dst["D_fwd"], D_bwd=dst["D_bwd"], z=dst["z"], dirs=wl.dirs,
-                      out=out_d, workspace=ws)
+                      out=out_d, workspace=ws, **step_kwargs(dst, wl))
             if seg:
                 vssm.scan_folded(dst["x"], dst["delta"], dst["A_fwd"], dst["A_bwd"], dst["B"],
                                  dst["C"], seg_len=seg, **kw)

@@ -49,6 +49,8 @@ class ScanArgs(ctypes.Structure):
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("batch", ctypes.c_int), ("dim", ctypes.c_int), ("seqlen", ctypes.c_int),
         ("dstate", ctypes.c_int), ("dtype", ctypes.c_int), ("dir_flags", ctypes.c_uint),
+        ("delta_bwd", ctypes.c_void_p), ("delta_bias", ctypes.c_void_p),
+        ("delta_bias_bwd", ctypes.c_void_p), ("delta_softplus", ctypes.c_int),
     ]
 
 
@@ -121,8 +123,13 @@ def _dev_tensor(name, t, dtype=None, shape=None, device=None):
 
 
 def make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, out=None,
-              B_bwd=None, C_bwd=None, dirs: int = DIR_BOTH) -> ScanArgs:
-    """Validate tensors and fill a ``vssm_scan_args`` (no workspace yet)."""
+              B_bwd=None, C_bwd=None, dirs: int = DIR_BOTH, delta_bwd=None, delta_bias=None,
+              delta_bias_bwd=None, delta_softplus: bool = False) -> ScanArgs:
+    """Validate tensors and fill a ``vssm_scan_args`` (no workspace yet).
+
+    delta_bwd: the backward direction's step (None = delta). delta_softplus:
+    each direction's step is softplus(its delta + its bias[d]) (delta_bias,
+    delta_bias_bwd: (dim,) float32; None = 0 / = delta_bias)."""
     x = _dev_tensor("x", x)
     if x.dtype not in (torch.float32, torch.bfloat16) or x.dim() != 3:
         raise TypeError("x must be a 3-D float32 or bfloat16 tensor (batch, dim, L)")
@@ -130,13 +137,15 @@ def make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, out=
     N = B.shape[-1]
     dev, dt = x.device, x.dtype
     _dev_tensor("delta", delta, dt, x.shape, dev)
+    _dev_tensor("delta_bwd", delta_bwd, dt, x.shape, dev)
     _dev_tensor("z", z, dt, x.shape, dev)
     _dev_tensor("out", out, dt, x.shape, dev)
     for n, t in (("B", B), ("C", C), ("B_bwd", B_bwd), ("C_bwd", C_bwd)):
         _dev_tensor(n, t, dt, (batch, L, N), dev)
     for n, t in (("A_fwd", A_fwd), ("A_bwd", A_bwd)):
         _dev_tensor(n, t, torch.float32, (dim, N), dev)
-    for n, t in (("D_fwd", D_fwd), ("D_bwd", D_bwd)):
+    for n, t in (("D_fwd", D_fwd), ("D_bwd", D_bwd), ("delta_bias", delta_bias),
+                 ("delta_bias_bwd", delta_bias_bwd)):
         _dev_tensor(n, t, torch.float32, (dim,), dev)
     a = ScanArgs()
     a.x, a.delta, a.z = _ptr(x), _ptr(delta), _ptr(z)
@@ -146,6 +155,8 @@ def make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, out=
     a.batch, a.dim, a.seqlen, a.dstate = batch, dim, L, N
     a.dtype = VSSM_F32 if dt == torch.float32 else VSSM_BF16
     a.dir_flags = dirs
+    a.delta_bwd, a.delta_bias, a.delta_bias_bwd = _ptr(delta_bwd), _ptr(delta_bias), _ptr(delta_bias_bwd)
+    a.delta_softplus = 1 if delta_softplus else 0
     return a
 
 
@@ -204,25 +215,28 @@ def _launch(fn, a: ScanArgs, seg_len: Optional[int], device, workspace, stream,
 
 def scan_bidir(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None,
                dirs: int = DIR_BOTH, out=None, B_bwd=None, C_bwd=None,
-               stream: Optional[torch.cuda.Stream] = None, workspace=None) -> torch.Tensor:
-    """Selective scan over independent sequences (``vssm_scan_bidir``)."""
+               stream: Optional[torch.cuda.Stream] = None, workspace=None,
+               **step) -> torch.Tensor:
+    """Selective scan over independent sequences (``vssm_scan_bidir``).
+    ``step``: delta_bwd, delta_bias, delta_bias_bwd, delta_softplus (see
+    :func:`make_args`)."""
     if out is None:
         out = torch.empty_like(x)
-    a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, out, B_bwd, C_bwd, dirs)
+    a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, out, B_bwd, C_bwd, dirs, **step)
     _launch(lib.vssm_scan_bidir, a, None, x.device, workspace, stream)
     return out
 
 
 def scan_bidir_noalloc(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None,
                        dirs: int = DIR_BOTH, out=None, B_bwd=None, C_bwd=None,
-                       stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+                       stream: Optional[torch.cuda.Stream] = None, **step) -> torch.Tensor:
     """``vssm_scan_bidir_noalloc``: the same scan as :func:`scan_bidir` with the
     library's built-in scratch instead of a workspace (for callers that cannot
     allocate device memory; calls share the scratch, so keep them on one
     stream). ``out`` is allocated here only when not given."""
     if out is None:
         out = torch.empty_like(x)
-    a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, out, B_bwd, C_bwd, dirs)
+    a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, out, B_bwd, C_bwd, dirs, **step)
     stream = stream if stream is not None else torch.cuda.current_stream(x.device)
     _check(lib.vssm_scan_bidir_noalloc(ctypes.byref(a), ctypes.c_void_p(stream.cuda_stream)))
     return out
@@ -230,12 +244,13 @@ def scan_bidir_noalloc(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=N
 
 def scan_folded(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *,
                 seg_len: int, dirs: int = DIR_FWD, out=None, B_bwd=None, C_bwd=None,
-                stream: Optional[torch.cuda.Stream] = None, workspace=None) -> torch.Tensor:
+                stream: Optional[torch.cuda.Stream] = None, workspace=None,
+                **step) -> torch.Tensor:
     """Batch-folded scan with a state reset every ``seg_len`` tokens
     (``vssm_scan_folded``)."""
     if out is None:
         out = torch.empty_like(x)
-    a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, out, B_bwd, C_bwd, dirs)
+    a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, out, B_bwd, C_bwd, dirs, **step)
     _launch(lib.vssm_scan_folded, a, seg_len, x.device, workspace, stream)
     return out
 
@@ -243,13 +258,13 @@ def scan_folded(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *,
 def scan_chunked(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *,
                  pieces: int, seg_len: int = 0, dirs: int = DIR_BOTH, out=None, B_bwd=None,
                  C_bwd=None, stream: Optional[torch.cuda.Stream] = None,
-                 workspace=None) -> torch.Tensor:
+                 workspace=None, **step) -> torch.Tensor:
     """``vssm_scan_chunked``: the scan with each row cut into ``pieces`` token
     ranges joined by the exact carry (0 = the library's choice). ``seg_len``
     > 0 makes it the folded scan."""
     if out is None:
         out = torch.empty_like(x)
-    a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, out, B_bwd, C_bwd, dirs)
+    a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, out, B_bwd, C_bwd, dirs, **step)
     _launch(lib.vssm_scan_chunked, a, seg_len, x.device, workspace, stream, pieces)
     return out
 

@@ -249,4 +249,21 @@ __device__ __forceinline__ float tanh_mufu(float x)
     return y;
 }
 
+__device__ __forceinline__ float lg2_mufu(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// softplus(v) = log(1 + exp(v)) = ln 2 * log2(1 + 2^(v * log2 e)) on the MUFU
+// unit (absolute error about 1e-7, from lg2.approx). Above 15 it is v (the
+// difference, log(1 + exp(-v)), is below 3.1e-7); below -30 it is 0 (the true
+// value is below 1e-13), so a pre-activation of -inf gives a step of exactly 0.
+__device__ __forceinline__ float softplus_f32(float v)
+{
+    const float s = 0.6931471805599453f * lg2_mufu(1.0f + ex2_mufu(v * 1.4426950408889634f));
+    return v > 15.0f ? v : (v < -30.0f ? 0.0f : s);
+}
+
 }  // namespace vssm

@@ -31,6 +31,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "ptx.cuh"
+
 namespace vssm {
 
 constexpr int kMaxState = 16;       // N <= 16
@@ -38,7 +40,9 @@ constexpr int kChunk = 32;          // tokens per direction per staging step
 constexpr int kPitch = kChunk + 1;  // padded row pitch (floats): rows hit distinct banks
 
 struct ScanParams {
-    const void *x, *delta, *z;
+    const void *x, *delta[2], *z;   // delta: [0] forward, [1] backward step
+    const float *dbias[2];          // step bias per direction (softplus only), or null
+    int softplus;                   // 1: step = softplus(delta + bias)
     const void *B[2], *C[2];        // [0] forward, [1] backward
     const float *A[2], *D[2];
     void *out;
@@ -110,7 +114,6 @@ scan_kernel(const ScanParams p)
     const bool active = d < p.dim;
 
     const T *X = static_cast<const T *>(p.x);
-    const T *DT = static_cast<const T *>(p.delta);
     const T *Z = static_cast<const T *>(p.z);
     T *OUT = static_cast<T *>(p.out);
     const bool hasZ = Z != nullptr;
@@ -168,12 +171,15 @@ scan_kernel(const ScanParams p)
                 const int ds = (DIRS == 2) ? 1 : s;
                 float *blk = smem + s * DB;
                 const int len = c1[s] - c0[s];
+                const T *DT = static_cast<const T *>(p.delta[ds]);
+                const float *dbias = p.dbias[ds];
                 for (int idx = tid; idx < R * kChunk; idx += NT) {
                     const int rr = idx / kChunk, i = idx % kChunk;
                     float dtv = 0.f, xv = 0.f, zv = 0.f, yv = 0.f;
                     if (i < len && d0 + rr < p.dim) {
                         const size_t gi = row0 + (size_t)rr * p.L + c0[s] + i;
                         dtv = to_f32(DT[gi]);
+                        if (p.softplus) dtv = softplus_f32(dtv + (dbias ? dbias[d0 + rr] : 0.f));
                         xv = to_f32(X[gi]);
                         if (fin && hasZ) zv = to_f32(Z[gi]);
                         if (DIRS == 3 && fin)

@@ -57,7 +57,8 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s
 constexpr unsigned kErrTimeout = 1u;
 
 struct WarpScanParams {
-    const void *x, *delta, *z;
+    const void *x, *delta[2], *z;  // delta: [0] forward, [1] backward step
+    const float *dbias[2];         // step bias per direction (SP kernels), or null
     const void *B[2], *C[2];     // [0] forward, [1] backward
     const float *A[2], *D[2];
     void *out;
@@ -161,7 +162,9 @@ __device__ __forceinline__ float silu_f32(float z)
     return __fdividef(z, 1.0f + ex2_mufu(-1.4426950408889634f * z));
 }
 
-template <typename T, int G, int DIRS, int W, bool CARRY = false>
+// CARRY: ranges start from a carried-in state. SP: the step is
+// softplus(delta + bias[d]) of the direction's own delta and bias.
+template <typename T, int G, int DIRS, int W, bool CARRY = false, bool SP = false>
 struct WarpScan {
     using Lay = WarpLayout<T, G, DIRS == 3>;
     static constexpr int RPW = Lay::RPW, NS = Lay::NS, ES = Lay::ES;
@@ -173,6 +176,7 @@ struct WarpScan {
     int lane, dir, r, g;
     int slot;                    // direction slot of the carry summaries
     int piece, rg;               // token range and channel group of this warp
+    float dbias_l;               // this lane's step bias (SP)
     long long grp;
     int b, d0, ta, tb;
     bool ok;                     // false once the pair rendezvous has timed out
@@ -192,7 +196,8 @@ struct WarpScan {
         const long long e0 = ((long long)b * p.dim + d0) * p.L;
         lane_erow = e0 + (long long)r * p.L;
         lane_emod = (uint32_t)(lane_erow & 15);
-        rowp[0] = static_cast<const char *>(p.delta) + lane_erow * ES;
+        rowp[0] = static_cast<const char *>(p.delta[dir]) + lane_erow * ES;
+        dbias_l = (SP && d0 + r < p.dim && p.dbias[dir]) ? p.dbias[dir][d0 + r] : 0.f;
         rowp[1] = static_cast<const char *>(p.x) + lane_erow * ES;
         rowp[2] = p.z ? static_cast<const char *>(p.z) + lane_erow * ES : rowp[1];
         out_row0 = static_cast<T *>(p.out) + e0;
@@ -320,7 +325,8 @@ struct WarpScan {
 #pragma unroll
             for (int j = 0; j < kUnroll; ++j) {
                 const int i = (DIR == 0) ? (k0 + j) : (n4 - 1 - k0 - j);
-                const float dtv = ld_as_f32(rd + i);
+                float dtv = ld_as_f32(rd + i);
+                if (SP) dtv = softplus_f32(dtv + dbias_l);
                 const float xv = ld_as_f32(rx + i);
                 const float dx = dtv * xv;
                 const f2 dd = pack2(dtv, dtv), uu = pack2(dx, dx);
@@ -361,7 +367,8 @@ struct WarpScan {
     }
 
     // Zero delta and x of the tokens between len and the unroll multiple in
-    // this lane's row slot (only for a partial chunk).
+    // this lane's row slot (only for a partial chunk). With SP the padded
+    // delta is -inf, whose softplus is exactly 0.
     __device__ void zero_tail(int s, int c0, int len)
     {
         const int n4 = (len + kUnroll - 1) / kUnroll * kUnroll;
@@ -371,7 +378,7 @@ struct WarpScan {
             T *rd = reinterpret_cast<T *>(st + Lay::oD + Lay::row_off(r) + lead);
             T *rx = reinterpret_cast<T *>(st + Lay::oX + Lay::row_off(r) + lead);
             for (int i = len; i < n4; ++i) {
-                rd[i] = T(0.f);
+                rd[i] = T(SP ? -INFINITY : 0.f);
                 rx[i] = T(0.f);
             }
         }
@@ -490,7 +497,8 @@ struct WarpScan {
 #pragma unroll
             for (int j = 0; j < kUnroll; ++j) {
                 const int i = (DIR == 0) ? (k0 + j) : (n4 - 1 - k0 - j);
-                const float dtv = ld_as_f32(rd + i);
+                float dtv = ld_as_f32(rd + i);
+                if (SP) dtv = softplus_f32(dtv + dbias_l);
                 const float xv = ld_as_f32(rx + i);
                 S += dtv;
                 const float dx = dtv * xv;
@@ -677,7 +685,7 @@ constexpr int warp_scan_min_blocks()
 
 // CARRY: the row is cut into ranges that start from the state carried in by
 // warp_carry_kernel's summaries (else every range starts from zero).
-template <typename T, int G, int DIRS, int W, bool CARRY>
+template <typename T, int G, int DIRS, int W, bool CARRY, bool SP>
 __global__ void __launch_bounds__(W * 32, (warp_scan_min_blocks<T, G, DIRS, W>()))
 warp_scan_kernel(const WarpScanParams p)
 {
@@ -686,7 +694,7 @@ warp_scan_kernel(const WarpScanParams p)
     static_assert(W % NDIR == 0, "whole pairs per CTA");
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int warp = threadIdx.x >> 5;
-    WarpScan<T, G, DIRS, W, CARRY> ws(p);
+    WarpScan<T, G, DIRS, W, CARRY, SP> ws(p);
     ws.lane = threadIdx.x & 31;
     ws.r = ws.lane / G;
     ws.g = ws.lane % G;
@@ -716,7 +724,7 @@ warp_scan_kernel(const WarpScanParams p)
 // Piece summaries for the carry between token ranges of a row: one warp per
 // (direction slot, channel group, piece that has a successor in that
 // direction). Runs before warp_scan_kernel on the same stream.
-template <typename T, int DIRS, int W>
+template <typename T, int DIRS, int W, bool SP>
 __global__ void __launch_bounds__(W * 32, (warp_scan_min_blocks<T, 1, 1, W>()))
 warp_carry_kernel(const WarpScanParams p)
 {
@@ -727,7 +735,7 @@ warp_carry_kernel(const WarpScanParams p)
     const long long per_slot = p.srows * (p.pieces - 1);
     const long long u = (long long)blockIdx.x * W + warp;
     if (u >= NDIR * per_slot) return;
-    WarpScan<T, 1, 1, W> ws(p);                  // single-direction staging layout
+    WarpScan<T, 1, 1, W, false, SP> ws(p);       // single-direction staging layout
     ws.slot = (int)(u / per_slot);
     const long long rem = u % per_slot;
     const int jj = (int)(rem % (p.pieces - 1));

@@ -306,11 +306,15 @@ int validate(const vssm_scan_args *a, int seg_len, bool folded)
         return fail(VSSM_ERR_INVALID_ARG, "A_fwd is required for the forward direction");
     if ((a->dir_flags & VSSM_DIR_BWD) && !a->A_bwd)
         return fail(VSSM_ERR_INVALID_ARG, "A_bwd is required for the backward direction");
+    if (a->delta_softplus != 0 && a->delta_softplus != 1)
+        return fail(VSSM_ERR_INVALID_ARG, "delta_softplus=%d must be 0 or 1", a->delta_softplus);
     const void *ptrs[] = {a->x, a->delta, a->z, a->B, a->C, a->B_bwd, a->C_bwd, a->A_fwd,
-                          a->A_bwd, a->D_fwd, a->D_bwd, a->out, a->workspace};
+                          a->A_bwd, a->D_fwd, a->D_bwd, a->out, a->workspace,
+                          a->delta_bwd, a->delta_bias, a->delta_bias_bwd};
     const char *names[] = {"x", "delta", "z", "B", "C", "B_bwd", "C_bwd", "A_fwd",
-                           "A_bwd", "D_fwd", "D_bwd", "out", "workspace"};
-    for (int i = 0; i < 13; ++i)
+                           "A_bwd", "D_fwd", "D_bwd", "out", "workspace",
+                           "delta_bwd", "delta_bias", "delta_bias_bwd"};
+    for (int i = 0; i < 16; ++i)
         if (ptrs[i] && !aligned16(ptrs[i]))
             return fail(VSSM_ERR_MISALIGNED, "%s=%p is not 16-byte aligned", names[i], ptrs[i]);
     const size_t es = a->dtype == VSSM_F32 ? 4 : 2;
@@ -322,7 +326,9 @@ int validate(const vssm_scan_args *a, int seg_len, bool folded)
         {a->B, nbc, "B"}, {a->C, nbc, "C"}, {a->B_bwd, nbc, "B_bwd"}, {a->C_bwd, nbc, "C_bwd"},
         {a->A_fwd, npar, "A_fwd"}, {a->A_bwd, npar, "A_bwd"},
         {a->D_fwd, (size_t)a->dim * 4, "D_fwd"}, {a->D_bwd, (size_t)a->dim * 4, "D_bwd"},
-        {a->workspace, a->workspace_bytes, "workspace"}};
+        {a->workspace, a->workspace_bytes, "workspace"}, {a->delta_bwd, nact, "delta_bwd"},
+        {a->delta_bias, (size_t)a->dim * 4, "delta_bias"},
+        {a->delta_bias_bwd, (size_t)a->dim * 4, "delta_bias_bwd"}};
     for (const auto &in : ins)
         if (overlaps(a->out, nact, in.p, in.n))
             return fail(VSSM_ERR_INVALID_ARG, "out overlaps %s", in.name);
@@ -390,12 +396,12 @@ void *noalloc_scratch()
     return addr[dev];
 }
 
-template <typename T, int DIRS>
+template <typename T, int DIRS, bool SP>
 int launch_carry(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t stream)
 {
     constexpr int W = kCarryW;
     const size_t smem = (size_t)W * vssm::WarpLayout<T, 1, false>::kWarpBytes;
-    auto kern = vssm::warp_carry_kernel<T, DIRS, W>;
+    auto kern = vssm::warp_carry_kernel<T, DIRS, W, SP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -408,17 +414,17 @@ int launch_carry(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t str
     return VSSM_OK;
 }
 
-template <typename T, int G, int DIRS>
+template <typename T, int G, int DIRS, bool SP>
 int launch_warp_variant(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t stream)
 {
     if (pl.carry) {
-        const int st = launch_carry<T, DIRS>(p, pl, stream);
+        const int st = launch_carry<T, DIRS, SP>(p, pl, stream);
         if (st != VSSM_OK) return st;
     }
     constexpr int W = warps_per_cta(G);
     const size_t smem = (size_t)W * vssm::WarpLayout<T, G, DIRS == 3>::kWarpBytes;
-    auto kern = pl.carry ? vssm::warp_scan_kernel<T, G, DIRS, W, true>
-                         : vssm::warp_scan_kernel<T, G, DIRS, W, false>;
+    auto kern = pl.carry ? vssm::warp_scan_kernel<T, G, DIRS, W, true, SP>
+                         : vssm::warp_scan_kernel<T, G, DIRS, W, false, SP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess)   // all of the unified L1/shared array as shared memory: residency is smem-bound
         e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -431,20 +437,20 @@ int launch_warp_variant(const vssm::WarpScanParams &p, const Plan &pl, cudaStrea
     return VSSM_OK;
 }
 
-template <typename T, int G>
+template <typename T, int G, bool SP>
 int launch_warp_dirs(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t s)
 {
     switch (pl.dirs) {
-    case 1: return launch_warp_variant<T, G, 1>(p, pl, s);
-    case 2: return launch_warp_variant<T, G, 2>(p, pl, s);
-    default: return launch_warp_variant<T, G, 3>(p, pl, s);
+    case 1: return launch_warp_variant<T, G, 1, SP>(p, pl, s);
+    case 2: return launch_warp_variant<T, G, 2, SP>(p, pl, s);
+    default: return launch_warp_variant<T, G, 3, SP>(p, pl, s);
     }
 }
 
 template <typename T>
-int launch_warp(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t s)
+int launch_warp(const vssm::WarpScanParams &p, const Plan &pl, bool softplus, cudaStream_t s)
 {
-    return launch_warp_dirs<T, 1>(p, pl, s);
+    return softplus ? launch_warp_dirs<T, 1, true>(p, pl, s) : launch_warp_dirs<T, 1, false>(p, pl, s);
 }
 
 template <typename T>
@@ -479,7 +485,10 @@ int run(const vssm_scan_args *a, int seg_len, bool folded, int pieces_req, void 
     if (pl.warp) {
         vssm::WarpScanParams w{};
         w.x = a->x;
-        w.delta = a->delta;
+        w.delta[0] = a->delta;
+        w.delta[1] = a->delta_bwd ? a->delta_bwd : a->delta;
+        w.dbias[0] = a->delta_bias;
+        w.dbias[1] = a->delta_bias_bwd ? a->delta_bias_bwd : a->delta_bias;
         w.z = a->z;
         w.B[0] = a->B;
         w.C[0] = a->C;
@@ -505,11 +514,17 @@ int run(const vssm_scan_args *a, int seg_len, bool folded, int pieces_req, void 
         w.rgroups = pl.rgroups;
         w.ngroups = pl.ngroups;
         w.srows = pl.srows;
-        return a->dtype == VSSM_F32 ? launch_warp<float>(w, pl, s) : launch_warp<__nv_bfloat16>(w, pl, s);
+        const bool sp = a->delta_softplus != 0;
+        return a->dtype == VSSM_F32 ? launch_warp<float>(w, pl, sp, s)
+                                    : launch_warp<__nv_bfloat16>(w, pl, sp, s);
     }
     vssm::ScanParams p{};
     p.x = a->x;
-    p.delta = a->delta;
+    p.delta[0] = a->delta;
+    p.delta[1] = a->delta_bwd ? a->delta_bwd : a->delta;
+    p.dbias[0] = a->delta_bias;
+    p.dbias[1] = a->delta_bias_bwd ? a->delta_bias_bwd : a->delta_bias;
+    p.softplus = a->delta_softplus;
     p.z = a->z;
     p.B[0] = a->B;
     p.C[0] = a->C;

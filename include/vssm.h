@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define VSSM_VERSION 110 /* 1.1.0 */
+#define VSSM_VERSION 120 /* 1.2.0 */
 
 typedef enum {
     VSSM_OK = 0,
@@ -84,6 +84,18 @@ typedef struct {
     int dstate;             /* 1..16                                              */
     int dtype;              /* vssm_dtype                                         */
     unsigned dir_flags;     /* VSSM_DIR_FWD | VSSM_DIR_BWD (at least one)         */
+    /* Step options (zero-initialise the struct to leave them off). Each
+     * direction is its own SSM module (Vim page §2.2, forward_ssm /
+     * backward_ssm), so the backward direction may take its own step; and the
+     * step may be passed before its positivity map, as the output of a step
+     * projection with bias (Mamba2D page, "Mamba2D Block结构", dt_proj with
+     * bias=True). With delta_softplus = 1 the step of each direction is
+     * softplus(its delta + its bias[d]), softplus(v) = log(1 + exp(v)),
+     * evaluated in fp32 (absolute error about 1e-7). */
+    const void *delta_bwd;        /* backward step [batch][dim][seqlen]; NULL = delta */
+    const float *delta_bias;      /* [dim] forward step bias; NULL = 0 (softplus only) */
+    const float *delta_bias_bwd;  /* [dim] backward step bias; NULL = delta_bias      */
+    int delta_softplus;           /* 0: steps used as given; 1: softplus(step + bias)  */
 } vssm_scan_args;
 
 /*

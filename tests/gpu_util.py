@@ -17,6 +17,10 @@ def to_device(inp, device="cuda"):
     t = {k: act(k) for k in ("x", "delta", "z", "B", "C")}
     for k in ("A_fwd", "A_bwd", "D_fwd", "D_bwd"):
         t[k] = torch.from_numpy(getattr(inp, k)).to(device)
+    if inp.delta_bwd is not None:          # fused-step inputs
+        t["delta_bwd"] = act("delta_bwd")
+        t["delta_bias"] = torch.from_numpy(inp.delta_bias).to(device)
+        t["delta_bias_bwd"] = torch.from_numpy(inp.delta_bias_bwd).to(device)
     return t
 
 

@@ -2,6 +2,7 @@
 declares, and rejects invalid calls before launching anything. No call here
 reaches the GPU (validation fails first, or the problem is empty)."""
 import ctypes
+import subprocess
 import os
 import re
 
@@ -38,12 +39,31 @@ def test_library_exports_every_declared_symbol(v):
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared in vssm.h but not exported"
     assert set(v.EXPORTS) <= set(declared_functions())
-    assert v.version() == 110
+    assert v.version() == 120
 
 
 def test_args_struct_layout_matches_header(v):
-    # 13 pointers + size_t, then 5 ints and an unsigned -> 8*14 + 4*6 = 136 bytes
-    assert ctypes.sizeof(v.ScanArgs) == 136
+    # 13 pointers + size_t, 5 ints and an unsigned (136 bytes), then 3 pointers
+    # and an int padded to 8 -> 136 + 24 + 8 = 168 bytes
+    assert ctypes.sizeof(v.ScanArgs) == 168
+
+
+def test_args_struct_matches_c_header(v, tmp_path):
+    """Compile a C program against include/vssm.h and compare the struct's
+    size and field offsets with the ctypes mirror."""
+    src = tmp_path / "layout.c"
+    fields = [f[0] for f in v.ScanArgs._fields_]
+    src.write_text("#include <stdio.h>\n#include <stddef.h>\n#include \"vssm.h\"\n"
+                   "int main(void) {\n  printf(\"%zu\\n\", sizeof(vssm_scan_args));\n" +
+                   "".join(f"  printf(\"%zu\\n\", offsetof(vssm_scan_args, {f}));\n"
+                           for f in fields) + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.dirname(HEADER), "-o", str(exe), str(src)],
+                   check=True, capture_output=True)
+    got = [int(t) for t in subprocess.run([str(exe)], check=True, capture_output=True,
+                                          text=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(v.ScanArgs)
+    assert got[1:] == [getattr(v.ScanArgs, f).offset for f in fields]
 
 
 def _args(v, **kw):
@@ -69,6 +89,9 @@ def _call(v, a, seg=None):
     (dict(batch=-1), -1), (dict(dstate=0), -2), (dict(dstate=17), -2), (dict(dtype=7), -2),
     (dict(dir_flags=0), -1), (dict(dir_flags=4), -1), (dict(x=(1 << 20) + 2), -3),
     (dict(out=(1 << 20) * 2), -1),                    # out aliases delta
+    (dict(delta_softplus=2), -1), (dict(delta_bwd=(1 << 20) * 12 + 4), -3),
+    (dict(delta_bwd=(1 << 20) * 10), -1),             # out aliases delta_bwd
+    (dict(delta_bias=(1 << 20) * 12 + 8), -3),
 ])
 def test_invalid_calls_are_rejected(v, kw, status):
     assert _call(v, _args(v, **kw)) == status

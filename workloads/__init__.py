@@ -26,6 +26,13 @@ x, Δ, z, B, C, A_fwd, A_bwd, D_fwd, D_bwd from numpy's PCG64 ``default_rng``.
 
 Layouts: x, delta, z, out are (batch, dim, L) with L fastest; B, C are
 (batch, L, N) with N fastest; A is (dim, N); D is (dim,).
+
+Fused-step variant (``fused_step=True``, any workload): the step is passed
+before its positivity map, per direction. The draw at Δ's position is kept as
+the pre-activation v ~ N(μ, 0.5); after D_bwd come bias_fwd, bias_bwd ~
+U[-0.5, 0.5] per channel and the backward pre-activation v_b ~ N(μ, 0.5).
+The stored steps are delta = v - bias_fwd and delta_bwd = v_b - bias_bwd, so
+softplus(delta + bias) has the plain workloads' distribution in each direction.
 """
 from __future__ import annotations
 
@@ -52,6 +59,7 @@ class Workload:
     delta_mu: float = -2.0
     delta_sigma: float = 0.5
     description: str = ""
+    fused_step: bool = False   # per-direction pre-activation steps + biases (softplus inside)
 
     @property
     def tokch(self) -> int:
@@ -113,6 +121,9 @@ class Inputs:
     D_fwd: np.ndarray
     D_bwd: np.ndarray
     bits: Optional[Dict[str, np.ndarray]] = None
+    delta_bwd: Optional[np.ndarray] = None        # fused-step workloads only
+    delta_bias: Optional[np.ndarray] = None
+    delta_bias_bwd: Optional[np.ndarray] = None
 
     def storage(self, name: str) -> np.ndarray:
         """The array as stored for the device: uint16 bits (bf16) or float32."""
@@ -131,8 +142,9 @@ def make_inputs(wl: Workload, seed: int = 0) -> Inputs:
     rng = np.random.default_rng(seed)
     b, L, D, N = wl.batch, wl.seqlen, wl.dim, wl.dstate
     x = rng.standard_normal((b, D, L), dtype=np.float32)
-    delta = _softplus(rng.standard_normal((b, D, L), dtype=np.float32)
-                      * np.float32(wl.delta_sigma) + np.float32(wl.delta_mu))
+    v = (rng.standard_normal((b, D, L), dtype=np.float32) * np.float32(wl.delta_sigma)
+         + np.float32(wl.delta_mu))
+    delta = v if wl.fused_step else _softplus(v)
     z = rng.standard_normal((b, D, L), dtype=np.float32)
     scale = np.float32(1.0 / np.sqrt(N))
     B = rng.standard_normal((b, L, N), dtype=np.float32) * scale
@@ -142,15 +154,27 @@ def make_inputs(wl: Workload, seed: int = 0) -> Inputs:
     A_bwd = (-np.exp(rng.uniform(lo, hi, size=(D, N)))).astype(np.float32)
     D_fwd = rng.standard_normal(D, dtype=np.float32)
     D_bwd = rng.standard_normal(D, dtype=np.float32)
+    extra = {}
+    if wl.fused_step:
+        bias_f = rng.uniform(-0.5, 0.5, size=D).astype(np.float32)
+        bias_b = rng.uniform(-0.5, 0.5, size=D).astype(np.float32)
+        v_b = (rng.standard_normal((b, D, L), dtype=np.float32) * np.float32(wl.delta_sigma)
+               + np.float32(wl.delta_mu))
+        delta = (v - bias_f[None, :, None]).astype(np.float32)
+        extra = dict(delta_bwd=(v_b - bias_b[None, :, None]).astype(np.float32),
+                     delta_bias=bias_f, delta_bias_bwd=bias_b)
     bits = None
     if wl.dtype == "bf16":
         bits = {}
         for name, arr in (("x", x), ("delta", delta), ("z", z), ("B", B), ("C", C)):
             bits[name] = bf16_round(arr)
         x, delta, z, B, C = (bf16_to_f32(bits[k]) for k in ("x", "delta", "z", "B", "C"))
+        if "delta_bwd" in extra:
+            bits["delta_bwd"] = bf16_round(extra["delta_bwd"])
+            extra["delta_bwd"] = bf16_to_f32(bits["delta_bwd"])
     elif wl.dtype != "f32":
         raise ValueError(f"unknown dtype {wl.dtype}")
-    return Inputs(wl, x, delta, z, B, C, A_fwd, A_bwd, D_fwd, D_bwd, bits)
+    return Inputs(wl, x, delta, z, B, C, A_fwd, A_bwd, D_fwd, D_bwd, bits, **extra)
 
 
 def algorithmic_bytes(wl: Workload) -> int:
@@ -158,8 +182,11 @@ def algorithmic_bytes(wl: Workload) -> int:
     (4 * tokch elements), B and C read once per token, A and D per direction."""
     e = 4 if wl.dtype == "f32" else 2
     ndir = (1 if wl.dirs & DIR_FWD else 0) + (1 if wl.dirs & DIR_BWD else 0)
-    return (4 * wl.tokch * e + 2 * wl.batch * wl.seqlen * wl.dstate * e
-            + ndir * (wl.dim * wl.dstate + wl.dim) * 4)
+    n = (4 * wl.tokch * e + 2 * wl.batch * wl.seqlen * wl.dstate * e
+         + ndir * (wl.dim * wl.dstate + wl.dim) * 4)
+    if wl.fused_step:   # the backward step tensor and the per-direction biases
+        n += (wl.tokch * e if wl.dirs & DIR_BWD else 0) + ndir * wl.dim * 4
+    return n
 
 
 def exp_count(wl: Workload) -> int:
