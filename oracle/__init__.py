@@ -12,7 +12,7 @@ Contents:
     they follow.
   * ``quadform.py`` -- the SSD page's quadratic (matrix) form, NumPy, used only
     to pin the recurrence on tiny inputs.
-  * ``scan()`` below -- ctypes binding of the C oracle.
+  * ``scan()`` and ``conv_silu()`` below -- ctypes bindings of the C oracle.
 
 Pins (in ``tests/test_oracle_pins.py``): the quadratic form, a hand-worked
 two-step example from the SSD page's linear-form section, closed forms for
@@ -20,8 +20,10 @@ A = 0 (prefix sum), vanishing decay, Δ = 0 and C = 0, L = 1, the
 backward-equals-flipped-forward invariant, folded-equals-per-segment, the
 silu gate against scipy's logistic function, linearity in x, the fused step
 map against the closed-form inverse of softplus (and softplus(0) = ln 2), the
-per-direction step as a sum of single-direction scans, and a mutation test
-that plants mistakes in a copy of the C source.
+per-direction step as a sum of single-direction scans, the directional
+convolution's taps against shifted inputs (forward, backward, across folded
+segment edges) and its feed into each direction, and a mutation test that
+plants mistakes in a copy of the C source.
 """
 from __future__ import annotations
 
@@ -66,8 +68,10 @@ def load_library(path: str):
     lib.oracle_scan.argtypes = [dp] * 12 + [ctypes.c_long] * 4 + [
         ctypes.c_int, ctypes.c_long, ctypes.c_int]
     lib.oracle_scan_ex.restype = ctypes.c_int
-    lib.oracle_scan_ex.argtypes = [dp] * 14 + [ctypes.c_int, dp] + [ctypes.c_long] * 4 + [
+    lib.oracle_scan_ex.argtypes = [dp] * 14 + [ctypes.c_int, dp, dp] + [ctypes.c_long] * 4 + [
         ctypes.c_int, ctypes.c_long, ctypes.c_int]
+    lib.oracle_conv_silu.restype = ctypes.c_int
+    lib.oracle_conv_silu.argtypes = [dp] * 4 + [ctypes.c_long] * 4 + [ctypes.c_int, ctypes.c_long]
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
 
@@ -94,20 +98,32 @@ def _as_f64(a):
 def scan(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None,
          B_bwd=None, C_bwd=None, dirs: int = DIR_BOTH, seg_len: int = 0,
          nthreads: int = 0, lib=None, delta_bwd=None, delta_bias=None,
-         delta_bias_bwd=None, delta_softplus: bool = False) -> np.ndarray:
+         delta_bias_bwd=None, delta_softplus: bool = False, conv_w=None, conv_b=None,
+         conv_w_bwd=None, conv_b_bwd=None) -> np.ndarray:
     """Run the fp64 oracle. Arrays may be any float dtype; they are widened to
     float64 exactly. Shapes: x, delta, z (batch, dim, L); B, C (batch, L, N);
     A (dim, N); D (dim,). Returns out (batch, dim, L) float64.
 
     delta_bwd: the backward direction's step (None = delta). With
     delta_softplus each direction's step is softplus(its delta + its bias[d])
-    (delta_bias, delta_bias_bwd: (dim,); None = 0 / = delta_bias)."""
+    (delta_bias, delta_bias_bwd: (dim,); None = 0 / = delta_bias).
+
+    conv_w (dim, K) and conv_b (dim,): the directional depthwise convolution +
+    SiLU in front of the scan (``conv_silu``); each direction reads its own
+    convolution of x (conv_w_bwd, conv_b_bwd: None = the forward one)."""
     lib = lib or _get_lib()
+    x_bwd = None
+    if conv_w is not None:
+        cw_b = conv_w if conv_w_bwd is None else conv_w_bwd
+        cb_b = conv_b if conv_b_bwd is None else conv_b_bwd
+        x_in = x
+        x = conv_silu(x_in, conv_w, conv_b, reverse=False, seg_len=seg_len, lib=lib)
+        x_bwd = conv_silu(x_in, cw_b, cb_b, reverse=True, seg_len=seg_len, lib=lib)
     if delta_bwd is not None or delta_bias is not None or delta_bias_bwd is not None \
-            or delta_softplus:
+            or delta_softplus or x_bwd is not None:
         return _scan_ex(lib, x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, B_bwd, C_bwd,
                         dirs, seg_len, nthreads, delta_bwd, delta_bias, delta_bias_bwd,
-                        delta_softplus)
+                        delta_softplus, x_bwd)
     x = np.asarray(x)
     batch, dim, L = x.shape
     N = np.asarray(B).shape[-1]
@@ -128,8 +144,28 @@ def scan(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None,
     return out
 
 
+def conv_silu(x, w, b=None, reverse: bool = False, seg_len: int = 0, lib=None) -> np.ndarray:
+    """Directional depthwise convolution + SiLU (C oracle ``oracle_conv_silu``):
+    x (batch, dim, L), w (dim, K), b (dim,) or None. reverse=False is the
+    causal (forward) convolution, True the backward one."""
+    lib = lib or _get_lib()
+    x = np.asarray(x)
+    batch, dim, L = x.shape
+    w = np.asarray(w)
+    K = w.shape[-1]
+    xa, px = _as_f64(x)
+    wa, pw = _as_f64(w)
+    ba, pb = _as_f64(b)
+    out = np.empty((batch, dim, L), dtype=np.float64)
+    rc = lib.oracle_conv_silu(px, pw, pb, out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                              batch, dim, L, K, int(bool(reverse)), int(seg_len))
+    if rc != 0:
+        raise ValueError(f"oracle_conv_silu rejected its arguments (status {rc})")
+    return out
+
+
 def _scan_ex(lib, x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, B_bwd, C_bwd, dirs, seg_len,
-             nthreads, delta_bwd, delta_bias, delta_bias_bwd, delta_softplus):
+             nthreads, delta_bwd, delta_bias, delta_bias_bwd, delta_softplus, x_bwd=None):
     x = np.asarray(x)
     batch, dim, L = x.shape
     N = np.asarray(B).shape[-1]
@@ -139,9 +175,10 @@ def _scan_ex(lib, x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, B_bwd, C_bwd, d
         arr, p = _as_f64(a)
         keep.append(arr)
         ptrs.append(p)
+    xb, pxb = _as_f64(x_bwd)
     out = np.empty((batch, dim, L), dtype=np.float64)
     pout = out.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
-    rc = lib.oracle_scan_ex(*ptrs, int(bool(delta_softplus)), pout, batch, dim, L, N,
+    rc = lib.oracle_scan_ex(*ptrs, int(bool(delta_softplus)), pxb, pout, batch, dim, L, N,
                             int(dirs), int(seg_len), int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_scan_ex rejected its arguments (status {rc})")

@@ -35,6 +35,19 @@
  * bias=True) and softplus(v) = log(1 + exp(v)) the map the Mamba family uses
  * to keep the step positive (the pages name no map; this is a reading).
  *
+ * Directional convolution in front of the scan (oracle_conv_silu): "the
+ * forward and backward paths use 1D convolutions of different directions"
+ * (Vim page §2.3), and the SSM branch takes SiLU of a 1D depthwise
+ * convolution (SF-Mamba page, "MambaVision Mixer": X1 = SSM(σ(Conv(...))),
+ * σ = SiLU). Per channel d with K taps w[d][0..K-1] and bias b[d]:
+ *   forward (causal):   u[t] = silu(b + sum_k w[k] * x[t - (K-1) + k])
+ *   backward (reverse): u[t] = silu(b + sum_k w[k] * x[t + (K-1) - k])
+ * i.e. the backward one is the causal convolution of the flipped sequence.
+ * Taps outside the row are zero; on a folded row they are also zero outside
+ * the current segment ("1D深度可分离卷积适配": implicit padding at every
+ * segment boundary, the convolution never crosses sequences). The scan then
+ * reads each direction's u in place of x (input term and skip alike).
+ *
  * Layouts (row-major, last index fastest): x, delta, z, out: [batch][dim][L];
  * B, C (and B_bwd, C_bwd): [batch][L][N]; A: [dim][N]; D: [dim].
  */
@@ -86,6 +99,37 @@ static void scan_row_direction(const double *xr, const double *dtr,
     }
 }
 
+/* silu(v) = v / (1 + exp(-v)). */
+static double silu(double v) { return v / (1.0 + exp(-v)); }
+
+/*
+ * Directional depthwise convolution + SiLU over [batch][dim][L] rows (see the
+ * header): reverse = 0 is the causal (forward) one, 1 the backward one. w is
+ * [dim][K], b is [dim] (NULL = 0). seg_len > 0 zeroes the taps that fall in
+ * another segment. out has x's shape.
+ */
+int oracle_conv_silu(const double *x, const double *w, const double *b, double *out,
+                     long batch, long dim, long L, long K, int reverse, long seg_len)
+{
+    if (!x || !w || !out || batch < 0 || dim < 0 || L < 0 || K < 1 || seg_len < 0)
+        return -1;
+    for (long r = 0; r < batch * dim; ++r) {
+        const long d = r % dim;
+        const double *xr = x + r * L;
+        for (long t = 0; t < L; ++t) {
+            double acc = b ? b[d] : 0.0;
+            for (long k = 0; k < K; ++k) {
+                const long s = reverse ? t + (K - 1) - k : t - (K - 1) + k;
+                if (s < 0 || s >= L) continue;
+                if (seg_len > 0 && s / seg_len != t / seg_len) continue;
+                acc += w[d * K + k] * xr[s];
+            }
+            out[r * L + t] = silu(acc);
+        }
+    }
+    return 0;
+}
+
 /* softplus(v) = log(1 + exp(v)), evaluated as max(v, 0) + log(1 + exp(-|v|))
  * so that exp never overflows (the two forms are equal). */
 static double softplus(double v)
@@ -116,7 +160,7 @@ int oracle_scan_ex(const double *x, const double *delta, const double *z,
                    const double *A_fwd, const double *A_bwd,
                    const double *D_fwd, const double *D_bwd,
                    const double *delta_bwd, const double *bias_fwd, const double *bias_bwd,
-                   int use_softplus, double *out,
+                   int use_softplus, const double *x_bwd, double *out,
                    long batch, long dim, long L, long N,
                    int dirs, long seg_len, int nthreads);
 
@@ -131,14 +175,16 @@ int oracle_scan(const double *x, const double *delta, const double *z,
                 int dirs, long seg_len, int nthreads)
 {
     return oracle_scan_ex(x, delta, z, B, C, B_bwd, C_bwd, A_fwd, A_bwd, D_fwd, D_bwd,
-                          NULL, NULL, NULL, 0, out, batch, dim, L, N, dirs, seg_len, nthreads);
+                          NULL, NULL, NULL, 0, NULL, out, batch, dim, L, N, dirs, seg_len,
+                          nthreads);
 }
 
 /*
  * As oracle_scan, plus: delta_bwd ([batch][dim][L]) is the backward step
  * (NULL = delta); with use_softplus set each direction's step is
  * softplus(its delta + its bias[d]), bias_fwd / bias_bwd ([dim]; NULL = 0 for
- * the forward bias, = bias_fwd for the backward one).
+ * the forward bias, = bias_fwd for the backward one); x_bwd is the backward
+ * direction's input (NULL = x), e.g. its own convolution output.
  */
 int oracle_scan_ex(const double *x, const double *delta, const double *z,
                    const double *B, const double *C,
@@ -146,7 +192,7 @@ int oracle_scan_ex(const double *x, const double *delta, const double *z,
                    const double *A_fwd, const double *A_bwd,
                    const double *D_fwd, const double *D_bwd,
                    const double *delta_bwd, const double *bias_fwd, const double *bias_bwd,
-                   int use_softplus, double *out,
+                   int use_softplus, const double *x_bwd, double *out,
                    long batch, long dim, long L, long N,
                    int dirs, long seg_len, int nthreads)
 {
@@ -160,6 +206,7 @@ int oracle_scan_ex(const double *x, const double *delta, const double *z,
     if (!B_bwd) B_bwd = B;
     if (!C_bwd) C_bwd = C;
     if (!delta_bwd) delta_bwd = delta;
+    if (!x_bwd) x_bwd = x;
     if (!bias_bwd) bias_bwd = bias_fwd;
 
     const long rows = batch * dim;
@@ -195,7 +242,7 @@ int oracle_scan_ex(const double *x, const double *delta, const double *z,
                 if (dirs & 2) {
                     const double *dtr = direction_step(delta_bwd + r * L, L, use_softplus,
                                                        bias_bwd ? bias_bwd[d] : 0.0, step);
-                    scan_row_direction(xr, dtr, B_bwd + b * L * N, C_bwd + b * L * N,
+                    scan_row_direction(x_bwd + r * L, dtr, B_bwd + b * L * N, C_bwd + b * L * N,
                                        A_bwd + d * N, D_bwd ? D_bwd[d] : 0.0,
                                        L, N, 1, seg_len, h, acc);
                 }

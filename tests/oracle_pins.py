@@ -299,11 +299,82 @@ def pin_per_direction_step(lib):
     return _close(both, fwd + bwd, 1e-12) and _close(bwd, flipped, 1e-12)
 
 
+def _shift(a, s):
+    """a[..., t - s] along the last axis, zero where t - s falls outside."""
+    out = np.zeros_like(a)
+    L = a.shape[-1]
+    if s >= 0:
+        out[..., s:] = a[..., :L - s] if s < L else 0.0
+    else:
+        out[..., :L + s] = a[..., -s:] if -s < L else 0.0
+    return out
+
+
+def _silu(v):
+    return v * expit(v)
+
+
+def pin_conv_taps(lib):
+    """Directional convolution + SiLU against shifted inputs: a one-hot tap k
+    of K = 4 reads x[t - 3 + k] going forward and x[t + 3 - k] going
+    backward (zero outside the row, and outside the segment on a folded
+    row); two taps add; a bias alone gives silu(bias)."""
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((2, 3, 17))
+    ok = True
+    for k in range(4):
+        w = np.zeros((3, 4))
+        w[:, k] = 1.0
+        ok = ok and _close(oracle.conv_silu(x, w, lib=lib), _silu(_shift(x, 3 - k)), 1e-14)
+        ok = ok and _close(oracle.conv_silu(x, w, reverse=True, lib=lib),
+                           _silu(_shift(x, k - 3)), 1e-14)
+    w = np.zeros((3, 4))
+    w[:, 0], w[:, 3] = 0.5, -2.0
+    ok = ok and _close(oracle.conv_silu(x, w, lib=lib),
+                       _silu(0.5 * _shift(x, 3) - 2.0 * x), 1e-14)
+    bias = rng.standard_normal(3)
+    ok = ok and _close(oracle.conv_silu(x, np.zeros((3, 4)), bias, lib=lib),
+                       np.broadcast_to(_silu(bias)[None, :, None], x.shape), 1e-14)
+    # folded rows: segments of 5, the taps stop at segment edges
+    w = np.zeros((3, 4))
+    w[:, 1] = 1.0                     # x[t - 2] forward, x[t + 2] backward
+    seg = 5
+    t = np.arange(17)
+    keep_f = (t % seg) >= 2
+    keep_b = (t % seg) <= seg - 3
+    keep_b &= t + 2 < 17
+    ok = ok and _close(oracle.conv_silu(x, w, seg_len=seg, lib=lib),
+                       _silu(_shift(x, 2) * keep_f), 1e-14)
+    ok = ok and _close(oracle.conv_silu(x, w, reverse=True, seg_len=seg, lib=lib),
+                       _silu(_shift(x, -2) * keep_b), 1e-14)
+    return ok
+
+
+def pin_conv_feeds_each_direction(lib):
+    """With the convolution on, both directions (no gate) are the forward
+    scan of the forward convolution plus the backward scan of the backward
+    convolution, each with its own weights."""
+    rng = np.random.default_rng(43)
+    p = _rand_problem(rng, 2, 4, 21, 5, gate=False)
+    w_f, w_b = rng.standard_normal((4, 4)) * 0.5, rng.standard_normal((4, 4)) * 0.5
+    b_f, b_b = rng.standard_normal(4) * 0.3, rng.standard_normal(4) * 0.3
+    both = oracle.scan(p["x"], p["delta"], p["A_fwd"], p["A_bwd"], p["B"], p["C"], p["D_fwd"],
+                       p["D_bwd"], None, dirs=3, lib=lib, conv_w=w_f, conv_b=b_f,
+                       conv_w_bwd=w_b, conv_b_bwd=b_b)
+    u_f = oracle.conv_silu(p["x"], w_f, b_f, lib=lib)
+    u_b = oracle.conv_silu(p["x"], w_b, b_b, reverse=True, lib=lib)
+    fwd = oracle.scan(u_f, p["delta"], p["A_fwd"], p["A_bwd"], p["B"], p["C"], p["D_fwd"],
+                      p["D_bwd"], None, dirs=1, lib=lib)
+    bwd = oracle.scan(u_b, p["delta"], p["A_fwd"], p["A_bwd"], p["B"], p["C"], p["D_fwd"],
+                      p["D_bwd"], None, dirs=2, lib=lib)
+    return _close(both, fwd + bwd, 1e-12)
+
+
 PINS = [pin_worked_example, pin_quadratic_form, pin_A_zero_prefix_sum,
         pin_vanishing_decay, pin_zero_input_paths, pin_single_token,
         pin_backward_is_flipped_forward, pin_folded_equals_segments,
         pin_reset_first_token, pin_gate, pin_linearity, pin_softplus_step,
-        pin_per_direction_step]
+        pin_per_direction_step, pin_conv_taps, pin_conv_feeds_each_direction]
 
 
 def failing_pins(lib):

@@ -43,6 +43,12 @@ MUTANTS = {
     "step_bias_not_added": ("softplus(raw[t] + bias)", "softplus(raw[t])"),
     "bwd_step_uses_fwd_bias": ("bias_bwd ? bias_bwd[d] : 0.0", "bias_fwd ? bias_fwd[d] : 0.0"),
     "bwd_uses_fwd_step": ("direction_step(delta_bwd + r * L", "direction_step(delta + r * L"),
+    "conv_taps_reversed": ("t - (K - 1) + k;", "t - k;"),
+    "conv_backward_is_causal": ("reverse ? t + (K - 1) - k", "reverse ? t - (K - 1) + k"),
+    "conv_crosses_segments": ("if (seg_len > 0 && s / seg_len != t / seg_len) continue;", ""),
+    "conv_without_silu": ("out[r * L + t] = silu(acc);", "out[r * L + t] = acc;"),
+    "conv_bias_dropped": ("double acc = b ? b[d] : 0.0;", "double acc = 0.0;"),
+    "bwd_reads_shared_input": ("scan_row_direction(x_bwd + r * L", "scan_row_direction(xr"),
 }
 
 
