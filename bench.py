@@ -63,23 +63,40 @@ def parse_args(argv=None):
     p.add_argument("--fused-step", action="store_true",
                    help="pass per-direction steps before softplus, with biases (the kernel "
                         "applies softplus(delta + bias))")
+    p.add_argument("--conv", type=int, default=0, choices=[0, 1, 2, 3, 4],
+                   help="taps of the directional depthwise convolution + SiLU in front of "
+                        "the scan (0: none)")
     return p.parse_args(argv)
 
 
 def selected_workload(args):
     wl = WORKLOADS[args.workload]
-    return wl.scaled(fused_step=True) if args.fused_step else wl
+    if args.fused_step:
+        wl = wl.scaled(fused_step=True)
+    if args.conv:
+        wl = wl.scaled(conv=args.conv)
+    return wl
+
+
+def variant_key(wl):
+    """Workload name plus its options, the key of the committed traffic record."""
+    return wl.name + ("+fused_step" if wl.fused_step else "") + (f"+conv{wl.conv}" if wl.conv else "")
 
 
 STEP_KEYS = ("delta_bwd", "delta_bias", "delta_bias_bwd")
 
 
 def step_kwargs(t, wl):
-    """Step options of the call: per-direction steps and biases, softplus inside."""
-    if not wl.fused_step:
-        return {}
-    return dict(delta_bwd=t["delta_bwd"], delta_bias=t["delta_bias"],
-                delta_bias_bwd=t["delta_bias_bwd"], delta_softplus=True)
+    """Options of the call: per-direction steps and biases with softplus
+    inside, and the directional convolution."""
+    kw = {}
+    if wl.fused_step:
+        kw.update(delta_bwd=t["delta_bwd"], delta_bias=t["delta_bias"],
+                  delta_bias_bwd=t["delta_bias_bwd"], delta_softplus=True)
+    if wl.conv:
+        kw.update(conv_w=t["conv_w"], conv_b=t["conv_b"], conv_w_bwd=t["conv_w_bwd"],
+                  conv_b_bwd=t["conv_b_bwd"])
+    return kw
 
 
 # ------------------------------------------------------------------ distributed
@@ -298,6 +315,9 @@ def oracle_sample_run(wl, inp, target_s, nthreads=0):
                              delta_bias=inp.delta_bias[:nd].astype(np.float64),
                              delta_bias_bwd=inp.delta_bias_bwd[:nd].astype(np.float64),
                              delta_softplus=True)
+        if wl.conv:
+            a["step"].update({k: getattr(inp, k)[:nd].astype(np.float64)
+                              for k in ("conv_w", "conv_b", "conv_w_bwd", "conv_b_bwd")})
         return a
 
     def run(a):
@@ -376,6 +396,8 @@ def workload_config(wl, l2_note):
             "seg_len": wl.seg_len or None, "gate": "silu(z)", "l2": l2_note,
             "step": ("softplus(delta + bias), own delta and bias per direction" if wl.fused_step
                      else "delta as given (post-softplus), shared by both directions"),
+            "conv": (f"silu(depthwise conv, {wl.conv} taps), causal forward, reversed backward"
+                     if wl.conv else None),
             "description": wl.description}
 
 
@@ -407,6 +429,9 @@ def run_ours(args):
         base["delta_bwd"] = upload(inp.storage("delta_bwd"))
         base["delta_bias"] = torch.from_numpy(inp.delta_bias).to(dev)
         base["delta_bias_bwd"] = torch.from_numpy(inp.delta_bias_bwd).to(dev)
+    if wl.conv:
+        for k in ("conv_w", "conv_b", "conv_w_bwd", "conv_b_bwd"):
+            base[k] = torch.from_numpy(getattr(inp, k)).to(dev)
     nsets = int(min(64, max(2, math.ceil(3 * L2_BYTES / set_bytes))))
     sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(nsets - 1)]
     outs = [torch.empty_like(base["x"]) for _ in range(nsets)]
@@ -484,7 +509,7 @@ def run_ours(args):
     roofline = {
         "bound": "alu", "achieved": round(ach, 2), "peak": round(peak_upd, 2),
         "unit": "Gupdate/s", "frac": round(ach / peak_upd, 4),
-        "traffic": ncu_traffic(wl.name + ("+fused_step" if wl.fused_step else "")),
+        "traffic": ncu_traffic(variant_key(wl)),
         "update": "one (token, channel, state, direction) recurrence step: 1 MUFU ex2 + 4 fp32 FMA-pipe ops",
         "peak_basis": f"{EX2_PER_CLK_SM} ex2/clk/SM (and {FMA_PER_CLK_SM}/4 FMA-pipe updates/clk/SM) "
                       f"x {SMS} SMs x {MAX_SM_MHZ:.0f} MHz max SM clock",

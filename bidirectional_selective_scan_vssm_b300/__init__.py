@@ -51,6 +51,8 @@ class ScanArgs(ctypes.Structure):
         ("dstate", ctypes.c_int), ("dtype", ctypes.c_int), ("dir_flags", ctypes.c_uint),
         ("delta_bwd", ctypes.c_void_p), ("delta_bias", ctypes.c_void_p),
         ("delta_bias_bwd", ctypes.c_void_p), ("delta_softplus", ctypes.c_int),
+        ("conv_w", ctypes.c_void_p), ("conv_b", ctypes.c_void_p),
+        ("conv_w_bwd", ctypes.c_void_p), ("conv_b_bwd", ctypes.c_void_p), ("conv_k", ctypes.c_int),
     ]
 
 
@@ -124,12 +126,18 @@ def _dev_tensor(name, t, dtype=None, shape=None, device=None):
 
 def make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, out=None,
               B_bwd=None, C_bwd=None, dirs: int = DIR_BOTH, delta_bwd=None, delta_bias=None,
-              delta_bias_bwd=None, delta_softplus: bool = False) -> ScanArgs:
+              delta_bias_bwd=None, delta_softplus: bool = False, conv_w=None, conv_b=None,
+              conv_w_bwd=None, conv_b_bwd=None) -> ScanArgs:
     """Validate tensors and fill a ``vssm_scan_args`` (no workspace yet).
 
     delta_bwd: the backward direction's step (None = delta). delta_softplus:
     each direction's step is softplus(its delta + its bias[d]) (delta_bias,
-    delta_bias_bwd: (dim,) float32; None = 0 / = delta_bias)."""
+    delta_bias_bwd: (dim,) float32; None = 0 / = delta_bias).
+
+    conv_w (dim, K) float32, K <= 4, conv_b (dim,): the directional depthwise
+    convolution + SiLU in front of the scan (causal forward, reversed
+    backward); conv_w_bwd, conv_b_bwd: the backward direction's (None = the
+    forward ones)."""
     x = _dev_tensor("x", x)
     if x.dtype not in (torch.float32, torch.bfloat16) or x.dim() != 3:
         raise TypeError("x must be a 3-D float32 or bfloat16 tensor (batch, dim, L)")
@@ -145,8 +153,18 @@ def make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, out=
     for n, t in (("A_fwd", A_fwd), ("A_bwd", A_bwd)):
         _dev_tensor(n, t, torch.float32, (dim, N), dev)
     for n, t in (("D_fwd", D_fwd), ("D_bwd", D_bwd), ("delta_bias", delta_bias),
-                 ("delta_bias_bwd", delta_bias_bwd)):
+                 ("delta_bias_bwd", delta_bias_bwd), ("conv_b", conv_b),
+                 ("conv_b_bwd", conv_b_bwd)):
         _dev_tensor(n, t, torch.float32, (dim,), dev)
+    K = 0
+    if conv_w is not None:
+        if conv_w.dim() != 2 or conv_w.shape[0] != dim:
+            raise ValueError(f"conv_w must be (dim, K), got {tuple(conv_w.shape)}")
+        K = int(conv_w.shape[1])
+        _dev_tensor("conv_w", conv_w, torch.float32, (dim, K), dev)
+        _dev_tensor("conv_w_bwd", conv_w_bwd, torch.float32, (dim, K), dev)
+    elif conv_w_bwd is not None or conv_b is not None or conv_b_bwd is not None:
+        raise ValueError("conv_w is required with the other convolution arguments")
     a = ScanArgs()
     a.x, a.delta, a.z = _ptr(x), _ptr(delta), _ptr(z)
     a.B, a.C, a.B_bwd, a.C_bwd = _ptr(B), _ptr(C), _ptr(B_bwd), _ptr(C_bwd)
@@ -157,6 +175,9 @@ def make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, out=
     a.dir_flags = dirs
     a.delta_bwd, a.delta_bias, a.delta_bias_bwd = _ptr(delta_bwd), _ptr(delta_bias), _ptr(delta_bias_bwd)
     a.delta_softplus = 1 if delta_softplus else 0
+    a.conv_w, a.conv_b, a.conv_w_bwd, a.conv_b_bwd = (_ptr(conv_w), _ptr(conv_b), _ptr(conv_w_bwd),
+                                                      _ptr(conv_b_bwd))
+    a.conv_k = K
     return a
 
 

@@ -36,6 +36,7 @@
 namespace vssm {
 
 constexpr int kMaxState = 16;       // N <= 16
+constexpr int kMaxConv = 4;         // taps of the directional convolution
 constexpr int kChunk = 32;          // tokens per direction per staging step
 constexpr int kPitch = kChunk + 1;  // padded row pitch (floats): rows hit distinct banks
 
@@ -43,6 +44,8 @@ struct ScanParams {
     const void *x, *delta[2], *z;   // delta: [0] forward, [1] backward step
     const float *dbias[2];          // step bias per direction (softplus only), or null
     int softplus;                   // 1: step = softplus(delta + bias)
+    const float *conv_w[2], *conv_b[2];   // directional convolution per direction
+    int conv_k;                     // 0: none; else taps (input = silu(conv(x)))
     const void *B[2], *C[2];        // [0] forward, [1] backward
     const float *A[2], *D[2];
     void *out;
@@ -180,7 +183,23 @@ scan_kernel(const ScanParams p)
                         const size_t gi = row0 + (size_t)rr * p.L + c0[s] + i;
                         dtv = to_f32(DT[gi]);
                         if (p.softplus) dtv = softplus_f32(dtv + (dbias ? dbias[d0 + rr] : 0.f));
-                        xv = to_f32(X[gi]);
+                        if (p.conv_k > 0) {
+                            // silu of the direction's convolution at token t: taps
+                            // t-(K-1)+k forward, t+(K-1)-k backward; zero outside the
+                            // row and, folded, outside t's segment
+                            const int K = p.conv_k, t = c0[s] + i;
+                            const float *w = p.conv_w[ds] + (size_t)(d0 + rr) * K;
+                            float acc = p.conv_b[ds] ? p.conv_b[ds][d0 + rr] : 0.f;
+                            for (int k = 0; k < K; ++k) {
+                                const int ts = ds == 0 ? t - (K - 1) + k : t + (K - 1) - k;
+                                if (ts < 0 || ts >= p.L) continue;
+                                if (p.seg_len > 0 && ts / p.seg_len != t / p.seg_len) continue;
+                                acc = fmaf(w[k], to_f32(X[gi - t + ts]), acc);
+                            }
+                            xv = silu(acc);
+                        } else {
+                            xv = to_f32(X[gi]);
+                        }
                         if (fin && hasZ) zv = to_f32(Z[gi]);
                         if (DIRS == 3 && fin)
                             yv = YSMEM ? ybig[rr * p.ypitch + (c0[s] - ta) + i] : p.ybuf[gi];

@@ -59,6 +59,8 @@ constexpr unsigned kErrTimeout = 1u;
 struct WarpScanParams {
     const void *x, *delta[2], *z;  // delta: [0] forward, [1] backward step
     const float *dbias[2];         // step bias per direction (SP kernels), or null
+    const float *conv_w[2], *conv_b[2];   // directional convolution (CONV kernels)
+    int conv_k;                    // its taps, 1..4
     const void *B[2], *C[2];     // [0] forward, [1] backward
     const float *A[2], *D[2];
     void *out;
@@ -163,8 +165,11 @@ __device__ __forceinline__ float silu_f32(float z)
 }
 
 // CARRY: ranges start from a carried-in state. SP: the step is
-// softplus(delta + bias[d]) of the direction's own delta and bias.
-template <typename T, int G, int DIRS, int W, bool CARRY = false, bool SP = false>
+// softplus(delta + bias[d]) of the direction's own delta and bias. CONV: the
+// input is silu of the direction's depthwise convolution of x, computed from
+// a three-token history of x that each lane carries in registers.
+template <typename T, int G, int DIRS, int W, bool CARRY = false, bool SP = false,
+          bool CONV = false>
 struct WarpScan {
     using Lay = WarpLayout<T, G, DIRS == 3>;
     static constexpr int RPW = Lay::RPW, NS = Lay::NS, ES = Lay::ES;
@@ -177,6 +182,7 @@ struct WarpScan {
     int slot;                    // direction slot of the carry summaries
     int piece, rg;               // token range and channel group of this warp
     float dbias_l;               // this lane's step bias (SP)
+    float cw[4], cb;             // this lane's convolution taps, right-aligned, and bias (CONV)
     long long grp;
     int b, d0, ta, tb;
     bool ok;                     // false once the pair rendezvous has timed out
@@ -198,6 +204,19 @@ struct WarpScan {
         lane_emod = (uint32_t)(lane_erow & 15);
         rowp[0] = static_cast<const char *>(p.delta[dir]) + lane_erow * ES;
         dbias_l = (SP && d0 + r < p.dim && p.dbias[dir]) ? p.dbias[dir][d0 + r] : 0.f;
+        if (CONV) {
+            // taps right-aligned: cw[3] multiplies x_t, cw[3-j] the token j
+            // steps back along this direction
+            const bool act = d0 + r < p.dim;
+            const int K = p.conv_k;
+            const float *w = p.conv_w[dir] + (long long)(d0 + r) * K;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int k = j - (4 - K);
+                cw[j] = (act && k >= 0) ? w[k] : 0.f;
+            }
+            cb = (act && p.conv_b[dir]) ? p.conv_b[dir][d0 + r] : 0.f;
+        }
         rowp[1] = static_cast<const char *>(p.x) + lane_erow * ES;
         rowp[2] = p.z ? static_cast<const char *>(p.z) + lane_erow * ES : rowp[1];
         out_row0 = static_cast<T *>(p.out) + e0;
@@ -308,7 +327,8 @@ struct WarpScan {
     // h unchanged.
     template <int DIR, bool FIN, bool SEG, bool GATE>
     __device__ __forceinline__ void scan_chunk(f2 (&h)[NS / 2], const f2 (&Ap)[NS / 2], float Dsum,
-                                               int s, int c0, int len, uint32_t rmask)
+                                               float (&xh)[3], int s, int c0, int len,
+                                               uint32_t rmask)
     {
         const unsigned char *st = stage(s);
         const float *bc = reinterpret_cast<const float *>(wsm + Lay::oBC);
@@ -327,7 +347,7 @@ struct WarpScan {
                 const int i = (DIR == 0) ? (k0 + j) : (n4 - 1 - k0 - j);
                 float dtv = ld_as_f32(rd + i);
                 if (SP) dtv = softplus_f32(dtv + dbias_l);
-                const float xv = ld_as_f32(rx + i);
+                const float xv = conv_input<SEG>(ld_as_f32(rx + i), xh, i, len, rmask);
                 const float dx = dtv * xv;
                 const f2 dd = pack2(dtv, dtv), uu = pack2(dx, dx);
                 const float *bcp = bc + i * 32;
@@ -355,6 +375,8 @@ struct WarpScan {
                 if (G >= 4) y += __shfl_xor_sync(0xffffffffu, y, 2);
                 // (all G lanes of a channel hold the same y and store it alike)
                 if (!FIN) {
+                    // with CONV each direction adds its own skip D * u here
+                    if (CONV) y = fmaf(Dsum, xv, y);
                     if (DIRS == 3) st_global_if(yrow + i * RPW, y, i < len);
                 } else {
                     float tot = y + fmaf(Dsum, xv, (DIRS == 3) ? py[i * RPW + r] : 0.f);
@@ -415,10 +437,52 @@ struct WarpScan {
 
     template <bool FIN, bool SEG, bool GATE>
     __device__ __forceinline__ void scan_dispatch(f2 (&h)[NS / 2], const f2 (&Ap)[NS / 2], float Dsum,
-                                                  int s, int c0, int len, uint32_t rmask)
+                                                  float (&xh)[3], int s, int c0, int len,
+                                                  uint32_t rmask)
     {
-        if (dir == 0) scan_chunk<0, FIN, SEG, GATE>(h, Ap, Dsum, s, c0, len, rmask);
-        else scan_chunk<1, FIN, SEG, GATE>(h, Ap, Dsum, s, c0, len, rmask);
+        if (dir == 0) scan_chunk<0, FIN, SEG, GATE>(h, Ap, Dsum, xh, s, c0, len, rmask);
+        else scan_chunk<1, FIN, SEG, GATE>(h, Ap, Dsum, xh, s, c0, len, rmask);
+    }
+
+    // History of the convolution at the first token t0 this warp visits in
+    // its direction: x at t0 -/+ 1, 2, 3, zero outside the row and, folded,
+    // outside t0's segment.
+    __device__ __forceinline__ void conv_history(float (&xh)[3], int t0) const
+    {
+        const T *xr = reinterpret_cast<const T *>(rowp[1]);
+        const bool act = d0 + r < p.dim;
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            const int ts = dir == 0 ? t0 - 1 - j : t0 + 1 + j;
+            const bool in = act && ts >= 0 && ts < p.L &&
+                            (p.seg_len <= 0 || ts / p.seg_len == t0 / p.seg_len);
+            xh[j] = in ? ld_as_f32(xr + ts) : 0.f;
+        }
+    }
+
+    // Input of token i of the chunk: x itself, or silu of the convolution
+    // (CONV), which then shifts x into the history (not for the padding past
+    // len, which must leave it as it is). A segment start clears the history.
+    template <bool SEG>
+    __device__ __forceinline__ float conv_input(float xraw, float (&xh)[3], int i, int len,
+                                                uint32_t rmask) const
+    {
+        if (!CONV) return xraw;
+        if (SEG) {
+            const float keep = ((rmask >> i) & 1u) ? 0.f : 1.f;
+            xh[0] *= keep;
+            xh[1] *= keep;
+            xh[2] *= keep;
+        }
+        float pre = fmaf(cw[3], xraw, cb);
+        pre = fmaf(cw[2], xh[0], pre);
+        pre = fmaf(cw[1], xh[1], pre);
+        pre = fmaf(cw[0], xh[2], pre);
+        const bool in = i < len;
+        xh[2] = in ? xh[1] : xh[2];
+        xh[1] = in ? xh[0] : xh[1];
+        xh[0] = in ? xraw : xh[0];
+        return silu_f32<T>(pre);
     }
 
     // A * log2(e) for this lane's states, and a zero state.
@@ -484,7 +548,8 @@ struct WarpScan {
     // the delta sum only (no C, no output).
     template <int DIR, bool SEG>
     __device__ __forceinline__ void summary_chunk(f2 (&h)[NS / 2], const f2 (&Ap)[NS / 2], float &S,
-                                                  int s, int c0, int len, uint32_t rmask)
+                                                  float (&xh)[3], int s, int c0, int len,
+                                                  uint32_t rmask)
     {
         const unsigned char *st = stage(s);
         const float *bc = reinterpret_cast<const float *>(wsm + Lay::oBC);
@@ -499,7 +564,7 @@ struct WarpScan {
                 const int i = (DIR == 0) ? (k0 + j) : (n4 - 1 - k0 - j);
                 float dtv = ld_as_f32(rd + i);
                 if (SP) dtv = softplus_f32(dtv + dbias_l);
-                const float xv = ld_as_f32(rx + i);
+                const float xv = conv_input<SEG>(ld_as_f32(rx + i), xh, i, len, rmask);
                 S += dtv;
                 const float dx = dtv * xv;
                 const f2 dd = pack2(dtv, dtv), uu = pack2(dx, dx);
@@ -529,6 +594,8 @@ struct WarpScan {
         static_assert(G == 1, "summaries hold one channel per lane");
         f2 Ap[NS / 2], h[NS / 2];
         init_state(Ap, h);
+        float xh[3] = {0.f, 0.f, 0.f};
+        if (CONV) conv_history(xh, dir == 0 ? ta : tb - 1);
         float S = 0.f;
         bool cut = false;
         const bool seg = p.seg_len > 0;
@@ -554,11 +621,11 @@ struct WarpScan {
             const uint32_t rmask = reset_mask(c0, len);
             cut = cut || rmask != 0u;
             if (dir == 0) {
-                if (seg) summary_chunk<0, true>(h, Ap, S, s, c0, len, rmask);
-                else summary_chunk<0, false>(h, Ap, S, s, c0, len, rmask);
+                if (seg) summary_chunk<0, true>(h, Ap, S, xh, s, c0, len, rmask);
+                else summary_chunk<0, false>(h, Ap, S, xh, s, c0, len, rmask);
             } else {
-                if (seg) summary_chunk<1, true>(h, Ap, S, s, c0, len, rmask);
-                else summary_chunk<1, false>(h, Ap, S, s, c0, len, rmask);
+                if (seg) summary_chunk<1, true>(h, Ap, S, xh, s, c0, len, rmask);
+                else summary_chunk<1, false>(h, Ap, S, xh, s, c0, len, rmask);
             }
             if (k + kStages < nk) {
                 int n0, n1;
@@ -587,9 +654,12 @@ struct WarpScan {
         f2 Ap[NS / 2], h[NS / 2];
         init_state(Ap, h);
         if constexpr (CARRY) carry_in(h, Ap);
-        float Dsum = 0.f;
+        float xh[3] = {0.f, 0.f, 0.f};
+        if (CONV) conv_history(xh, dir == 0 ? ta : tb - 1);
+        float Dsum = 0.f;   // skip weight applied to the input: both directions' (x
+                            // shared) or this direction's own (CONV: inputs differ)
         if (active) {
-            if (DIRS == 3) {
+            if (DIRS == 3 && !CONV) {
                 Dsum = (p.D[0] ? p.D[0][d] : 0.f) + (p.D[1] ? p.D[1][d] : 0.f);
             } else {
                 Dsum = p.D[dir] ? p.D[dir][d] : 0.f;
@@ -637,16 +707,16 @@ struct WarpScan {
                 const uint32_t rmask = reset_mask(c0, len);
                 if (fin) {
                     if (seg) {
-                        if (hasZ) scan_dispatch<true, true, true>(h, Ap, Dsum, s, c0, len, rmask);
-                        else scan_dispatch<true, true, false>(h, Ap, Dsum, s, c0, len, rmask);
+                        if (hasZ) scan_dispatch<true, true, true>(h, Ap, Dsum, xh, s, c0, len, rmask);
+                        else scan_dispatch<true, true, false>(h, Ap, Dsum, xh, s, c0, len, rmask);
                     } else {
-                        if (hasZ) scan_dispatch<true, false, true>(h, Ap, Dsum, s, c0, len, rmask);
-                        else scan_dispatch<true, false, false>(h, Ap, Dsum, s, c0, len, rmask);
+                        if (hasZ) scan_dispatch<true, false, true>(h, Ap, Dsum, xh, s, c0, len, rmask);
+                        else scan_dispatch<true, false, false>(h, Ap, Dsum, xh, s, c0, len, rmask);
                     }
                     store_out(c0, c1);
                 } else {
-                    if (seg) scan_dispatch<false, true, false>(h, Ap, Dsum, s, c0, len, rmask);
-                    else scan_dispatch<false, false, false>(h, Ap, Dsum, s, c0, len, rmask);
+                    if (seg) scan_dispatch<false, true, false>(h, Ap, Dsum, xh, s, c0, len, rmask);
+                    else scan_dispatch<false, false, false>(h, Ap, Dsum, xh, s, c0, len, rmask);
                 }
                 if (k + kStages < nk) {
                     int n0, n1;
@@ -685,7 +755,7 @@ constexpr int warp_scan_min_blocks()
 
 // CARRY: the row is cut into ranges that start from the state carried in by
 // warp_carry_kernel's summaries (else every range starts from zero).
-template <typename T, int G, int DIRS, int W, bool CARRY, bool SP>
+template <typename T, int G, int DIRS, int W, bool CARRY, bool SP, bool CONV>
 __global__ void __launch_bounds__(W * 32, (warp_scan_min_blocks<T, G, DIRS, W>()))
 warp_scan_kernel(const WarpScanParams p)
 {
@@ -694,7 +764,7 @@ warp_scan_kernel(const WarpScanParams p)
     static_assert(W % NDIR == 0, "whole pairs per CTA");
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int warp = threadIdx.x >> 5;
-    WarpScan<T, G, DIRS, W, CARRY, SP> ws(p);
+    WarpScan<T, G, DIRS, W, CARRY, SP, CONV> ws(p);
     ws.lane = threadIdx.x & 31;
     ws.r = ws.lane / G;
     ws.g = ws.lane % G;
@@ -724,7 +794,7 @@ warp_scan_kernel(const WarpScanParams p)
 // Piece summaries for the carry between token ranges of a row: one warp per
 // (direction slot, channel group, piece that has a successor in that
 // direction). Runs before warp_scan_kernel on the same stream.
-template <typename T, int DIRS, int W, bool SP>
+template <typename T, int DIRS, int W, bool SP, bool CONV>
 __global__ void __launch_bounds__(W * 32, (warp_scan_min_blocks<T, 1, 1, W>()))
 warp_carry_kernel(const WarpScanParams p)
 {
@@ -735,7 +805,7 @@ warp_carry_kernel(const WarpScanParams p)
     const long long per_slot = p.srows * (p.pieces - 1);
     const long long u = (long long)blockIdx.x * W + warp;
     if (u >= NDIR * per_slot) return;
-    WarpScan<T, 1, 1, W, false, SP> ws(p);       // single-direction staging layout
+    WarpScan<T, 1, 1, W, false, SP, CONV> ws(p);  // single-direction staging layout
     ws.slot = (int)(u / per_slot);
     const long long rem = u % per_slot;
     const int jj = (int)(rem % (p.pieces - 1));

@@ -308,13 +308,19 @@ int validate(const vssm_scan_args *a, int seg_len, bool folded)
         return fail(VSSM_ERR_INVALID_ARG, "A_bwd is required for the backward direction");
     if (a->delta_softplus != 0 && a->delta_softplus != 1)
         return fail(VSSM_ERR_INVALID_ARG, "delta_softplus=%d must be 0 or 1", a->delta_softplus);
+    if (a->conv_k < 0 || a->conv_k > vssm::kMaxConv)
+        return fail(VSSM_ERR_UNSUPPORTED, "conv_k=%d outside 0..%d", a->conv_k, vssm::kMaxConv);
+    if (a->conv_k > 0 && !a->conv_w)
+        return fail(VSSM_ERR_INVALID_ARG, "conv_w is required when conv_k > 0");
     const void *ptrs[] = {a->x, a->delta, a->z, a->B, a->C, a->B_bwd, a->C_bwd, a->A_fwd,
                           a->A_bwd, a->D_fwd, a->D_bwd, a->out, a->workspace,
-                          a->delta_bwd, a->delta_bias, a->delta_bias_bwd};
+                          a->delta_bwd, a->delta_bias, a->delta_bias_bwd,
+                          a->conv_w, a->conv_b, a->conv_w_bwd, a->conv_b_bwd};
     const char *names[] = {"x", "delta", "z", "B", "C", "B_bwd", "C_bwd", "A_fwd",
                            "A_bwd", "D_fwd", "D_bwd", "out", "workspace",
-                           "delta_bwd", "delta_bias", "delta_bias_bwd"};
-    for (int i = 0; i < 16; ++i)
+                           "delta_bwd", "delta_bias", "delta_bias_bwd",
+                           "conv_w", "conv_b", "conv_w_bwd", "conv_b_bwd"};
+    for (int i = 0; i < 20; ++i)
         if (ptrs[i] && !aligned16(ptrs[i]))
             return fail(VSSM_ERR_MISALIGNED, "%s=%p is not 16-byte aligned", names[i], ptrs[i]);
     const size_t es = a->dtype == VSSM_F32 ? 4 : 2;
@@ -328,7 +334,11 @@ int validate(const vssm_scan_args *a, int seg_len, bool folded)
         {a->D_fwd, (size_t)a->dim * 4, "D_fwd"}, {a->D_bwd, (size_t)a->dim * 4, "D_bwd"},
         {a->workspace, a->workspace_bytes, "workspace"}, {a->delta_bwd, nact, "delta_bwd"},
         {a->delta_bias, (size_t)a->dim * 4, "delta_bias"},
-        {a->delta_bias_bwd, (size_t)a->dim * 4, "delta_bias_bwd"}};
+        {a->delta_bias_bwd, (size_t)a->dim * 4, "delta_bias_bwd"},
+        {a->conv_w, (size_t)a->dim * a->conv_k * 4, "conv_w"},
+        {a->conv_b, (size_t)a->dim * 4, "conv_b"},
+        {a->conv_w_bwd, (size_t)a->dim * a->conv_k * 4, "conv_w_bwd"},
+        {a->conv_b_bwd, (size_t)a->dim * 4, "conv_b_bwd"}};
     for (const auto &in : ins)
         if (overlaps(a->out, nact, in.p, in.n))
             return fail(VSSM_ERR_INVALID_ARG, "out overlaps %s", in.name);
@@ -396,12 +406,12 @@ void *noalloc_scratch()
     return addr[dev];
 }
 
-template <typename T, int DIRS, bool SP>
+template <typename T, int DIRS, bool SP, bool CONV>
 int launch_carry(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t stream)
 {
     constexpr int W = kCarryW;
     const size_t smem = (size_t)W * vssm::WarpLayout<T, 1, false>::kWarpBytes;
-    auto kern = vssm::warp_carry_kernel<T, DIRS, W, SP>;
+    auto kern = vssm::warp_carry_kernel<T, DIRS, W, SP, CONV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -414,17 +424,17 @@ int launch_carry(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t str
     return VSSM_OK;
 }
 
-template <typename T, int G, int DIRS, bool SP>
+template <typename T, int G, int DIRS, bool SP, bool CONV>
 int launch_warp_variant(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t stream)
 {
     if (pl.carry) {
-        const int st = launch_carry<T, DIRS, SP>(p, pl, stream);
+        const int st = launch_carry<T, DIRS, SP, CONV>(p, pl, stream);
         if (st != VSSM_OK) return st;
     }
     constexpr int W = warps_per_cta(G);
     const size_t smem = (size_t)W * vssm::WarpLayout<T, G, DIRS == 3>::kWarpBytes;
-    auto kern = pl.carry ? vssm::warp_scan_kernel<T, G, DIRS, W, true, SP>
-                         : vssm::warp_scan_kernel<T, G, DIRS, W, false, SP>;
+    auto kern = pl.carry ? vssm::warp_scan_kernel<T, G, DIRS, W, true, SP, CONV>
+                         : vssm::warp_scan_kernel<T, G, DIRS, W, false, SP, CONV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess)   // all of the unified L1/shared array as shared memory: residency is smem-bound
         e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -437,20 +447,25 @@ int launch_warp_variant(const vssm::WarpScanParams &p, const Plan &pl, cudaStrea
     return VSSM_OK;
 }
 
-template <typename T, int G, bool SP>
+template <typename T, int G, bool SP, bool CONV>
 int launch_warp_dirs(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t s)
 {
     switch (pl.dirs) {
-    case 1: return launch_warp_variant<T, G, 1, SP>(p, pl, s);
-    case 2: return launch_warp_variant<T, G, 2, SP>(p, pl, s);
-    default: return launch_warp_variant<T, G, 3, SP>(p, pl, s);
+    case 1: return launch_warp_variant<T, G, 1, SP, CONV>(p, pl, s);
+    case 2: return launch_warp_variant<T, G, 2, SP, CONV>(p, pl, s);
+    default: return launch_warp_variant<T, G, 3, SP, CONV>(p, pl, s);
     }
 }
 
 template <typename T>
-int launch_warp(const vssm::WarpScanParams &p, const Plan &pl, bool softplus, cudaStream_t s)
+int launch_warp(const vssm::WarpScanParams &p, const Plan &pl, bool softplus, bool conv,
+                cudaStream_t s)
 {
-    return softplus ? launch_warp_dirs<T, 1, true>(p, pl, s) : launch_warp_dirs<T, 1, false>(p, pl, s);
+    if (conv)
+        return softplus ? launch_warp_dirs<T, 1, true, true>(p, pl, s)
+                        : launch_warp_dirs<T, 1, false, true>(p, pl, s);
+    return softplus ? launch_warp_dirs<T, 1, true, false>(p, pl, s)
+                    : launch_warp_dirs<T, 1, false, false>(p, pl, s);
 }
 
 template <typename T>
@@ -489,6 +504,11 @@ int run(const vssm_scan_args *a, int seg_len, bool folded, int pieces_req, void 
         w.delta[1] = a->delta_bwd ? a->delta_bwd : a->delta;
         w.dbias[0] = a->delta_bias;
         w.dbias[1] = a->delta_bias_bwd ? a->delta_bias_bwd : a->delta_bias;
+        w.conv_w[0] = a->conv_w;
+        w.conv_w[1] = a->conv_w_bwd ? a->conv_w_bwd : a->conv_w;
+        w.conv_b[0] = a->conv_b;
+        w.conv_b[1] = a->conv_b_bwd ? a->conv_b_bwd : a->conv_b;
+        w.conv_k = a->conv_k;
         w.z = a->z;
         w.B[0] = a->B;
         w.C[0] = a->C;
@@ -514,9 +534,9 @@ int run(const vssm_scan_args *a, int seg_len, bool folded, int pieces_req, void 
         w.rgroups = pl.rgroups;
         w.ngroups = pl.ngroups;
         w.srows = pl.srows;
-        const bool sp = a->delta_softplus != 0;
-        return a->dtype == VSSM_F32 ? launch_warp<float>(w, pl, sp, s)
-                                    : launch_warp<__nv_bfloat16>(w, pl, sp, s);
+        const bool sp = a->delta_softplus != 0, cv = a->conv_k > 0;
+        return a->dtype == VSSM_F32 ? launch_warp<float>(w, pl, sp, cv, s)
+                                    : launch_warp<__nv_bfloat16>(w, pl, sp, cv, s);
     }
     vssm::ScanParams p{};
     p.x = a->x;
@@ -525,6 +545,11 @@ int run(const vssm_scan_args *a, int seg_len, bool folded, int pieces_req, void 
     p.dbias[0] = a->delta_bias;
     p.dbias[1] = a->delta_bias_bwd ? a->delta_bias_bwd : a->delta_bias;
     p.softplus = a->delta_softplus;
+    p.conv_w[0] = a->conv_w;
+    p.conv_w[1] = a->conv_w_bwd ? a->conv_w_bwd : a->conv_w;
+    p.conv_b[0] = a->conv_b;
+    p.conv_b[1] = a->conv_b_bwd ? a->conv_b_bwd : a->conv_b;
+    p.conv_k = a->conv_k;
     p.z = a->z;
     p.B[0] = a->B;
     p.C[0] = a->C;

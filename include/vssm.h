@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define VSSM_VERSION 120 /* 1.2.0 */
+#define VSSM_VERSION 130 /* 1.3.0 */
 
 typedef enum {
     VSSM_OK = 0,
@@ -96,6 +96,22 @@ typedef struct {
     const float *delta_bias;      /* [dim] forward step bias; NULL = 0 (softplus only) */
     const float *delta_bias_bwd;  /* [dim] backward step bias; NULL = delta_bias      */
     int delta_softplus;           /* 0: steps used as given; 1: softplus(step + bias)  */
+    /* Directional depthwise convolution + SiLU in front of the scan (off when
+     * conv_k = 0). The forward and backward paths use 1D convolutions of
+     * opposite directions (Vim page §2.3), and the SSM reads SiLU of the
+     * convolution (SF-Mamba page, "MambaVision Mixer", X1 = SSM(σ(Conv(...)))).
+     * Per channel d, K = conv_k taps w[d][0..K-1] and bias b[d]:
+     *   forward:  u[t] = silu(b + sum_k w[k] * x[t - (K-1) + k])   (causal)
+     *   backward: u[t] = silu(b + sum_k w[k] * x[t + (K-1) - k])   (reversed)
+     * Taps outside the row read 0; on a folded row (vssm_scan_folded) also
+     * outside the current segment (SF-Mamba page, "1D深度可分离卷积适配": the
+     * convolution never crosses sequences). Each direction then reads its own
+     * u in place of x, for the input term and its skip D*u alike. */
+    const float *conv_w;          /* [dim][conv_k] forward taps; required if conv_k > 0 */
+    const float *conv_b;          /* [dim] forward bias; NULL = 0                     */
+    const float *conv_w_bwd;      /* [dim][conv_k] backward taps; NULL = conv_w       */
+    const float *conv_b_bwd;      /* [dim] backward bias; NULL = conv_b               */
+    int conv_k;                   /* 0 = no convolution; 1..4 taps                    */
 } vssm_scan_args;
 
 /*

@@ -21,6 +21,9 @@ def to_device(inp, device="cuda"):
         t["delta_bwd"] = act("delta_bwd")
         t["delta_bias"] = torch.from_numpy(inp.delta_bias).to(device)
         t["delta_bias_bwd"] = torch.from_numpy(inp.delta_bias_bwd).to(device)
+    if inp.conv_w is not None:             # convolution inputs
+        for k in ("conv_w", "conv_b", "conv_w_bwd", "conv_b_bwd"):
+            t[k] = torch.from_numpy(getattr(inp, k)).to(device)
     return t
 
 

@@ -39,13 +39,13 @@ def test_library_exports_every_declared_symbol(v):
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared in vssm.h but not exported"
     assert set(v.EXPORTS) <= set(declared_functions())
-    assert v.version() == 120
+    assert v.version() == 130
 
 
 def test_args_struct_layout_matches_header(v):
-    # 13 pointers + size_t, 5 ints and an unsigned (136 bytes), then 3 pointers
-    # and an int padded to 8 -> 136 + 24 + 8 = 168 bytes
-    assert ctypes.sizeof(v.ScanArgs) == 168
+    # 13 pointers + size_t, 5 ints and an unsigned (136 bytes); 3 pointers and
+    # an int padded to 8 (32); 4 pointers and an int padded to 8 (40) -> 208
+    assert ctypes.sizeof(v.ScanArgs) == 208
 
 
 def test_args_struct_matches_c_header(v, tmp_path):
@@ -92,6 +92,9 @@ def _call(v, a, seg=None):
     (dict(delta_softplus=2), -1), (dict(delta_bwd=(1 << 20) * 12 + 4), -3),
     (dict(delta_bwd=(1 << 20) * 10), -1),             # out aliases delta_bwd
     (dict(delta_bias=(1 << 20) * 12 + 8), -3),
+    (dict(conv_k=5, conv_w=(1 << 20) * 13), -2), (dict(conv_k=-1), -2),
+    (dict(conv_k=4), -1),                             # conv_w missing
+    (dict(conv_k=4, conv_w=(1 << 20) * 13 + 4), -3),
 ])
 def test_invalid_calls_are_rejected(v, kw, status):
     assert _call(v, _args(v, **kw)) == status

@@ -33,6 +33,11 @@ the pre-activation v ~ N(μ, 0.5); after D_bwd come bias_fwd, bias_bwd ~
 U[-0.5, 0.5] per channel and the backward pre-activation v_b ~ N(μ, 0.5).
 The stored steps are delta = v - bias_fwd and delta_bwd = v_b - bias_bwd, so
 softplus(delta + bias) has the plain workloads' distribution in each direction.
+
+Convolution variant (``conv=K``, any workload): after everything above come
+the forward taps and bias, then the backward taps and bias, each ~
+U[-1/sqrt(K), 1/sqrt(K)] (the usual fan-in initialisation of a depthwise
+convolution with K taps); shapes (dim, K) and (dim,).
 """
 from __future__ import annotations
 
@@ -60,6 +65,7 @@ class Workload:
     delta_sigma: float = 0.5
     description: str = ""
     fused_step: bool = False   # per-direction pre-activation steps + biases (softplus inside)
+    conv: int = 0              # taps of the directional convolution + SiLU in front (0: none)
 
     @property
     def tokch(self) -> int:
@@ -124,6 +130,10 @@ class Inputs:
     delta_bwd: Optional[np.ndarray] = None        # fused-step workloads only
     delta_bias: Optional[np.ndarray] = None
     delta_bias_bwd: Optional[np.ndarray] = None
+    conv_w: Optional[np.ndarray] = None           # convolution workloads only
+    conv_b: Optional[np.ndarray] = None
+    conv_w_bwd: Optional[np.ndarray] = None
+    conv_b_bwd: Optional[np.ndarray] = None
 
     def storage(self, name: str) -> np.ndarray:
         """The array as stored for the device: uint16 bits (bf16) or float32."""
@@ -163,6 +173,11 @@ def make_inputs(wl: Workload, seed: int = 0) -> Inputs:
         delta = (v - bias_f[None, :, None]).astype(np.float32)
         extra = dict(delta_bwd=(v_b - bias_b[None, :, None]).astype(np.float32),
                      delta_bias=bias_f, delta_bias_bwd=bias_b)
+    if wl.conv:
+        lim = 1.0 / np.sqrt(wl.conv)
+        for sfx in ("", "_bwd"):
+            extra["conv_w" + sfx] = rng.uniform(-lim, lim, size=(D, wl.conv)).astype(np.float32)
+            extra["conv_b" + sfx] = rng.uniform(-lim, lim, size=D).astype(np.float32)
     bits = None
     if wl.dtype == "bf16":
         bits = {}
@@ -186,6 +201,8 @@ def algorithmic_bytes(wl: Workload) -> int:
          + ndir * (wl.dim * wl.dstate + wl.dim) * 4)
     if wl.fused_step:   # the backward step tensor and the per-direction biases
         n += (wl.tokch * e if wl.dirs & DIR_BWD else 0) + ndir * wl.dim * 4
+    if wl.conv:         # taps and bias per direction
+        n += ndir * wl.dim * (wl.conv + 1) * 4
     return n
 
 
