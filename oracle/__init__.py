@@ -70,6 +70,8 @@ def load_library(path: str):
     lib.oracle_scan_ex.restype = ctypes.c_int
     lib.oracle_scan_ex.argtypes = [dp] * 14 + [ctypes.c_int, dp, dp] + [ctypes.c_long] * 4 + [
         ctypes.c_int, ctypes.c_long, ctypes.c_int]
+    lib.oracle_scan_grad.restype = ctypes.c_int
+    lib.oracle_scan_grad.argtypes = [dp] * 23 + [ctypes.c_long] * 4 + [ctypes.c_int, ctypes.c_long]
     lib.oracle_conv_silu.restype = ctypes.c_int
     lib.oracle_conv_silu.argtypes = [dp] * 4 + [ctypes.c_long] * 4 + [ctypes.c_int, ctypes.c_long]
     lib.oracle_max_threads.restype = ctypes.c_int
@@ -183,6 +185,40 @@ def _scan_ex(lib, x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, B_bwd, C_bwd, d
     if rc != 0:
         raise ValueError(f"oracle_scan_ex rejected its arguments (status {rc})")
     return out
+
+
+def scan_grad(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, dout=None,
+              B_bwd=None, C_bwd=None, dirs: int = DIR_BOTH, seg_len: int = 0, lib=None) -> dict:
+    """Gradients of L = sum(dout * scan(...)) (C oracle ``oracle_scan_grad``):
+    dict with dx, ddelta, dz (None without z), dB, dC, dB_bwd / dC_bwd (None
+    when the backward direction shares B / C), dA_fwd, dA_bwd, dD_fwd, dD_bwd
+    (None for a direction that is not run). float64."""
+    lib = lib or _get_lib()
+    x = np.asarray(x)
+    batch, dim, L = x.shape
+    N = np.asarray(B).shape[-1]
+    keep, ptrs = [], []
+    for a in (x, delta, z, B, C, B_bwd, C_bwd, A_fwd, A_bwd, D_fwd, D_bwd, dout):
+        arr, p = _as_f64(a)
+        keep.append(arr)
+        ptrs.append(p)
+    act = lambda: np.zeros((batch, dim, L))
+    bc = lambda: np.zeros((batch, L, N))
+    g = dict(dx=act(), ddelta=act(), dz=act() if z is not None else None, dB=bc(), dC=bc(),
+             dB_bwd=bc() if B_bwd is not None else None, dC_bwd=bc() if C_bwd is not None else None,
+             dA_fwd=np.zeros((dim, N)) if dirs & DIR_FWD else None,
+             dA_bwd=np.zeros((dim, N)) if dirs & DIR_BWD else None,
+             dD_fwd=np.zeros(dim) if dirs & DIR_FWD else None,
+             dD_bwd=np.zeros(dim) if dirs & DIR_BWD else None)
+    outp = [_as_f64(g[k])[1] if g[k] is not None else None
+            for k in ("dx", "ddelta", "dz", "dB", "dC", "dB_bwd", "dC_bwd", "dA_fwd", "dA_bwd",
+                      "dD_fwd", "dD_bwd")]
+    # _as_f64 returns the same array for float64 C-contiguous input, so the
+    # pointers above write into g's arrays
+    rc = lib.oracle_scan_grad(*ptrs, *outp, batch, dim, L, N, int(dirs), int(seg_len))
+    if rc != 0:
+        raise ValueError(f"oracle_scan_grad rejected its arguments (status {rc})")
+    return g
 
 
 def scan_inputs(inp, dirs: Optional[int] = None, seg_len: Optional[int] = None,

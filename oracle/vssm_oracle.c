@@ -71,6 +71,15 @@ int oracle_max_threads(void) {
 #endif
 }
 
+/* Folded segment start in a direction's scan order: t mod seg_len == 0
+ * going forward, t mod seg_len == seg_len - 1 going backward (never when
+ * seg_len == 0). */
+static int reset_at(long t, long seg_len, int rev)
+{
+    if (seg_len <= 0) return 0;
+    return rev ? (t % seg_len == seg_len - 1) : (t % seg_len == 0);
+}
+
 /* One direction over one row. `rev` = 0 walks t upward, 1 walks downward.
  * Adds y_t into acc[t]. */
 static void scan_row_direction(const double *xr, const double *dtr,
@@ -86,9 +95,7 @@ static void scan_row_direction(const double *xr, const double *dtr,
         const double xt = xr[t];
         const double *Bt = Bb + t * N;
         const double *Ct = Cb + t * N;
-        int reset = 0;
-        if (seg_len > 0)
-            reset = rev ? (t % seg_len == seg_len - 1) : (t % seg_len == 0);
+        const int reset = reset_at(t, seg_len, rev);
         double y = 0.0;
         for (long n = 0; n < N; ++n) {
             const double abar = reset ? 0.0 : exp(dt * Ad[n]);
@@ -249,10 +256,7 @@ int oracle_scan_ex(const double *x, const double *delta, const double *z,
                 double *outr = out + r * L;
                 for (long t = 0; t < L; ++t) {
                     double g = 1.0;
-                    if (z) {
-                        const double zt = z[r * L + t];
-                        g = zt / (1.0 + exp(-zt));
-                    }
+                    if (z) g = silu(z[r * L + t]);
                     outr[t] = acc[t] * g;
                 }
             }
@@ -262,4 +266,156 @@ int oracle_scan_ex(const double *x, const double *delta, const double *z,
         free(step);
     }
     return err;
+}
+
+/*
+ * Gradient of the scan (reverse-mode, the plain adjoint of the recurrence
+ * above). Given dout = dL/d out, every output gradient below is the exact
+ * derivative of L = sum(dout * out) with respect to that input:
+ *
+ *   s_t = y_fwd_t + y_bwd_t, out_t = s_t * g(z_t), g = silu,
+ *   g'(z) = sigma(z) * (1 + z * (1 - sigma(z)));
+ *   ds_t = dout_t * g(z_t);   dz_t = dout_t * s_t * g'(z_t);
+ *   per direction, walking the tokens against its scan order with the
+ *   adjoint lambda_t = dL/dh_t (an N-vector):
+ *     lambda_t = ds_t * C_t + abar_next * lambda_next      (0 past the end)
+ *     dC_t    += ds_t * h_t;           dB_t += lambda_t * delta_t * x_t
+ *     dx_t    += ds_t * D + sum_n lambda_t[n] * delta_t * B_t[n]
+ *     ddelta_t += sum_n lambda_t[n] * (x_t * B_t[n] + A[n] * abar_t[n] * h_prev[n])
+ *     dA[n]   += lambda_t[n] * abar_t[n] * h_prev[n] * delta_t
+ *     dD      += ds_t * x_t
+ *   where h_prev is the state before token t in scan order and abar_t =
+ *   exp(delta_t * A); at a folded reset abar_t is the constant 0, so neither
+ *   ddelta nor dA gets a decay term there and lambda is not carried past it.
+ *
+ * Inputs as oracle_scan (steps used as given, shared x). z, D_fwd, D_bwd may
+ * be NULL. Gradients are written (not accumulated): dx, ddelta, dz
+ * [batch][dim][L] (dz ignored if z is NULL); dB, dC [batch][L][N]; when
+ * B_bwd / C_bwd are given, the backward direction's go to dB_bwd / dC_bwd
+ * (else into dB / dC); dA_fwd, dA_bwd [dim][N]; dD_fwd, dD_bwd [dim]
+ * (NULL for a direction that is not run).
+ */
+int oracle_scan_grad(const double *x, const double *delta, const double *z,
+                     const double *B, const double *C,
+                     const double *B_bwd, const double *C_bwd,
+                     const double *A_fwd, const double *A_bwd,
+                     const double *D_fwd, const double *D_bwd,
+                     const double *dout,
+                     double *dx, double *ddelta, double *dz,
+                     double *dB, double *dC, double *dB_bwd, double *dC_bwd,
+                     double *dA_fwd, double *dA_bwd, double *dD_fwd, double *dD_bwd,
+                     long batch, long dim, long L, long N, int dirs, long seg_len)
+{
+    if (!x || !delta || !B || !C || !dout || !dx || !ddelta || !dB || !dC) return ORACLE_EINVAL;
+    if (batch < 0 || dim < 0 || L < 0 || N <= 0 || dirs < 1 || dirs > 3 || seg_len < 0)
+        return ORACLE_EINVAL;
+    if ((dirs & 1) && (!A_fwd || !dA_fwd || !dD_fwd)) return ORACLE_EINVAL;
+    if ((dirs & 2) && (!A_bwd || !dA_bwd || !dD_bwd)) return ORACLE_EINVAL;
+    if (seg_len > 0 && (dirs & 2) && L % seg_len != 0) return ORACLE_EINVAL;
+    if ((B_bwd && !dB_bwd) || (C_bwd && !dC_bwd)) return ORACLE_EINVAL;
+    const long rows = batch * dim;
+    for (long i = 0; i < rows * L; ++i) {
+        dx[i] = 0.0;
+        ddelta[i] = 0.0;
+        if (z && dz) dz[i] = 0.0;
+    }
+    for (long i = 0; i < batch * L * N; ++i) {
+        dB[i] = 0.0;
+        dC[i] = 0.0;
+        if (B_bwd) dB_bwd[i] = 0.0;
+        if (C_bwd) dC_bwd[i] = 0.0;
+    }
+    for (long i = 0; i < dim * N; ++i) {
+        if (dirs & 1) dA_fwd[i] = 0.0;
+        if (dirs & 2) dA_bwd[i] = 0.0;
+    }
+    for (long i = 0; i < dim; ++i) {
+        if (dirs & 1) dD_fwd[i] = 0.0;
+        if (dirs & 2) dD_bwd[i] = 0.0;
+    }
+    double *H = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * (size_t)N * 2);
+    double *Ab = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * (size_t)N * 2);
+    double *y = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * 2);
+    double *lam = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!H || !Ab || !y || !lam) {
+        free(H); free(Ab); free(y); free(lam);
+        return ORACLE_ENOMEM;
+    }
+    for (long r = 0; r < rows; ++r) {
+        const long b = r / dim, d = r % dim;
+        const double *xr = x + r * L, *dtr = delta + r * L;
+        /* forward states and outputs of each direction (k = 0 fwd, 1 bwd) */
+        for (int k = 0; k < 2; ++k) {
+            if (!(dirs & (1 << k))) continue;
+            const double *Bk = (k && B_bwd ? B_bwd : B) + b * L * N;
+            const double *Ck = (k && C_bwd ? C_bwd : C) + b * L * N;
+            const double *Ak = (k ? A_bwd : A_fwd) + d * N;
+            const double Dk = k ? (D_bwd ? D_bwd[d] : 0.0) : (D_fwd ? D_fwd[d] : 0.0);
+            double *Hk = H + (size_t)k * L * N, *Abk = Ab + (size_t)k * L * N;
+            for (long s = 0; s < L; ++s) {
+                const long t = k ? L - 1 - s : s;
+                const int reset = reset_at(t, seg_len, k);
+                const long tp = k ? t + 1 : t - 1;           /* previous token in scan order */
+                double yy = 0.0;
+                for (long n = 0; n < N; ++n) {
+                    const double a = reset ? 0.0 : exp(dtr[t] * Ak[n]);
+                    const double hp = (s == 0) ? 0.0 : Hk[tp * N + n];
+                    Abk[t * N + n] = a;
+                    Hk[t * N + n] = a * hp + dtr[t] * Bk[t * N + n] * xr[t];
+                    yy += Ck[t * N + n] * Hk[t * N + n];
+                }
+                y[k * L + t] = yy + Dk * xr[t];
+            }
+        }
+        for (int k = 0; k < 2; ++k) {
+            if (!(dirs & (1 << k))) continue;
+            const double *Bk = (k && B_bwd ? B_bwd : B) + b * L * N;
+            const double *Ck = (k && C_bwd ? C_bwd : C) + b * L * N;
+            double *dBk = (k && B_bwd ? dB_bwd : dB) + b * L * N;
+            double *dCk = (k && C_bwd ? dC_bwd : dC) + b * L * N;
+            const double *Ak = (k ? A_bwd : A_fwd) + d * N;
+            double *dAk = (k ? dA_bwd : dA_fwd) + d * N;
+            const double Dk = k ? (D_bwd ? D_bwd[d] : 0.0) : (D_fwd ? D_fwd[d] : 0.0);
+            double *dDk = (k ? dD_bwd : dD_fwd) + d;
+            const double *Hk = H + (size_t)k * L * N, *Abk = Ab + (size_t)k * L * N;
+            for (long n = 0; n < N; ++n) lam[n] = 0.0;
+            /* against the scan order: forward walks down, backward walks up */
+            for (long s = L - 1; s >= 0; --s) {
+                const long t = k ? L - 1 - s : s;
+                const long tp = k ? t + 1 : t - 1;
+                const double g = z ? silu(z[r * L + t]) : 1.0;
+                const double ds = dout[r * L + t] * g;
+                *dDk += ds * xr[t];
+                double dxx = ds * Dk, ddt = 0.0;
+                for (long n = 0; n < N; ++n) {
+                    lam[n] = ds * Ck[t * N + n] + lam[n];
+                    dCk[t * N + n] += ds * Hk[t * N + n];
+                    dBk[t * N + n] += lam[n] * dtr[t] * xr[t];
+                    dxx += lam[n] * dtr[t] * Bk[t * N + n];
+                    const double hp = (s == 0) ? 0.0 : Hk[tp * N + n];
+                    const double a = Abk[t * N + n];
+                    ddt += lam[n] * (xr[t] * Bk[t * N + n] + Ak[n] * a * hp);
+                    dAk[n] += lam[n] * a * hp * dtr[t];
+                    lam[n] = a * lam[n];
+                }
+                dx[r * L + t] += dxx;
+                ddelta[r * L + t] += ddt;
+            }
+        }
+        if (z && dz) {
+            for (long t = 0; t < L; ++t) {
+                const double zt = z[r * L + t];
+                const double sg = 1.0 / (1.0 + exp(-zt));
+                double s = 0.0;
+                if (dirs & 1) s += y[t];
+                if (dirs & 2) s += y[L + t];
+                dz[r * L + t] = dout[r * L + t] * s * sg * (1.0 + zt * (1.0 - sg));
+            }
+        }
+    }
+    free(H);
+    free(Ab);
+    free(y);
+    free(lam);
+    return ORACLE_OK;
 }

@@ -370,11 +370,67 @@ def pin_conv_feeds_each_direction(lib):
     return _close(both, fwd + bwd, 1e-12)
 
 
+def _grad_fd_ok(lib, rng, dirs, gate, seg_len, own_bc, L=6):
+    """Every entry of every gradient of L = sum(dout * out) against a central
+    finite difference of the (pinned) forward oracle."""
+    b, d, N = 1, 2, 3
+    p = _rand_problem(rng, b, d, L, N, gate=gate)
+    if own_bc:
+        p["B_bwd"] = rng.standard_normal((b, L, N)) / np.sqrt(N)
+        p["C_bwd"] = rng.standard_normal((b, L, N)) / np.sqrt(N)
+    dout = rng.standard_normal((b, d, L))
+    keys = ("x", "delta", "A_fwd", "A_bwd", "B", "C", "D_fwd", "D_bwd", "z", "B_bwd", "C_bwd")
+
+    def loss(q):
+        out = oracle.scan(q["x"], q["delta"], q["A_fwd"], q["A_bwd"], q["B"], q["C"], q["D_fwd"],
+                          q["D_bwd"], q.get("z"), B_bwd=q.get("B_bwd"), C_bwd=q.get("C_bwd"),
+                          dirs=dirs, seg_len=seg_len, lib=lib)
+        return float(np.sum(dout * out))
+
+    g = oracle.scan_grad(p["x"], p["delta"], p["A_fwd"], p["A_bwd"], p["B"], p["C"], p["D_fwd"],
+                         p["D_bwd"], p.get("z"), dout, B_bwd=p.get("B_bwd"),
+                         C_bwd=p.get("C_bwd"), dirs=dirs, seg_len=seg_len, lib=lib)
+    names = {"x": "dx", "delta": "ddelta", "z": "dz", "B": "dB", "C": "dC", "B_bwd": "dB_bwd",
+             "C_bwd": "dC_bwd", "A_fwd": "dA_fwd", "A_bwd": "dA_bwd", "D_fwd": "dD_fwd",
+             "D_bwd": "dD_bwd"}
+    eps = 1e-6
+    for k in keys:
+        if p.get(k) is None:
+            continue
+        if k.endswith("_fwd") and not dirs & 1 or k.endswith("_bwd") and not dirs & 2:
+            continue
+        fd = np.zeros_like(p[k])
+        for idx in np.ndindex(p[k].shape):
+            q = {kk: (vv.copy() if isinstance(vv, np.ndarray) else vv) for kk, vv in p.items()}
+            q[k][idx] += eps
+            lp = loss(q)
+            q[k][idx] -= 2 * eps
+            fd[idx] = (lp - loss(q)) / (2 * eps)
+        if not _close(g[names[k]], fd, 1e-6):
+            return False
+    return True
+
+
+def pin_gradient_finite_differences(lib):
+    """The adjoint gradients (dx, ddelta, dz, dB, dC, per-direction dB/dC,
+    dA, dD) equal central finite differences of the forward oracle, for each
+    direction alone and both, with and without the gate, on folded rows, and
+    with the backward direction's own B and C."""
+    rng = np.random.default_rng(47)
+    ok = True
+    for dirs, gate, seg, own in ((1, True, 0, False), (2, True, 0, False), (3, True, 0, False),
+                                 (3, False, 0, False), (3, True, 3, False), (3, True, 0, True),
+                                 (1, True, 2, False)):
+        ok = ok and _grad_fd_ok(lib, rng, dirs, gate, seg, own)
+    return ok
+
+
 PINS = [pin_worked_example, pin_quadratic_form, pin_A_zero_prefix_sum,
         pin_vanishing_decay, pin_zero_input_paths, pin_single_token,
         pin_backward_is_flipped_forward, pin_folded_equals_segments,
         pin_reset_first_token, pin_gate, pin_linearity, pin_softplus_step,
-        pin_per_direction_step, pin_conv_taps, pin_conv_feeds_each_direction]
+        pin_per_direction_step, pin_conv_taps, pin_conv_feeds_each_direction,
+        pin_gradient_finite_differences]
 
 
 def failing_pins(lib):

@@ -35,7 +35,7 @@ MUTANTS = {
     "backward_not_reversed": ("rev ? (L - 1 - k) : k", "k"),
     "fwd_reset_off_by_one": ("(t % seg_len == 0)", "(t % seg_len == 1)"),
     "bwd_reset_at_fwd_start": ("(t % seg_len == seg_len - 1)", "(t % seg_len == 0)"),
-    "gate_sign": ("zt / (1.0 + exp(-zt))", "zt / (1.0 + exp(zt))"),
+    "gate_sign": ("return v / (1.0 + exp(-v));", "return v / (1.0 + exp(v));"),
     "bwd_uses_fwd_A": ("A_bwd + d * N", "A_fwd + d * N"),
     "state_not_reset_between_rows": ("for (long n = 0; n < N; ++n) h[n] = 0.0;", ""),
     "softplus_drops_log": ("log1p(exp(-fabs(v)))", "exp(-fabs(v))"),
@@ -49,6 +49,13 @@ MUTANTS = {
     "conv_without_silu": ("out[r * L + t] = silu(acc);", "out[r * L + t] = acc;"),
     "conv_bias_dropped": ("double acc = b ? b[d] : 0.0;", "double acc = 0.0;"),
     "bwd_reads_shared_input": ("scan_row_direction(x_bwd + r * L", "scan_row_direction(xr"),
+    "grad_adjoint_not_carried": ("lam[n] = a * lam[n];", "lam[n] = 0.0;"),
+    "grad_dB_without_step": ("dBk[t * N + n] += lam[n] * dtr[t] * xr[t];",
+                             "dBk[t * N + n] += lam[n] * xr[t];"),
+    "grad_ddelta_without_decay_term": ("+ Ak[n] * a * hp);", ");"),
+    "grad_gate_derivative_sign": ("(1.0 + zt * (1.0 - sg))", "(1.0 - zt * (1.0 - sg))"),
+    "grad_skip_dropped": ("double dxx = ds * Dk, ddt = 0.0;", "double dxx = 0.0, ddt = 0.0;"),
+    "grad_dA_without_step": ("dAk[n] += lam[n] * a * hp * dtr[t];", "dAk[n] += lam[n] * a * hp;"),
 }
 
 
