@@ -12,7 +12,8 @@ Contents:
     they follow.
   * ``quadform.py`` -- the SSD page's quadratic (matrix) form, NumPy, used only
     to pin the recurrence on tiny inputs.
-  * ``scan()`` and ``conv_silu()`` below -- ctypes bindings of the C oracle.
+  * ``scan()``, ``scan_grad()`` and ``conv_silu()`` below -- ctypes bindings
+    of the C oracle.
 
 Pins (in ``tests/test_oracle_pins.py``): the quadratic form, a hand-worked
 two-step example from the SSD page's linear-form section, closed forms for
@@ -22,8 +23,9 @@ silu gate against scipy's logistic function, linearity in x, the fused step
 map against the closed-form inverse of softplus (and softplus(0) = ln 2), the
 per-direction step as a sum of single-direction scans, the directional
 convolution's taps against shifted inputs (forward, backward, across folded
-segment edges) and its feed into each direction, and a mutation test that
-plants mistakes in a copy of the C source.
+segment edges) and its feed into each direction, the adjoint gradients
+against central finite differences of the forward oracle, and a mutation test
+that plants mistakes in a copy of the C source.
 """
 from __future__ import annotations
 
