@@ -32,7 +32,7 @@ STATUS = {0: "VSSM_OK", -1: "VSSM_ERR_INVALID_ARG", -2: "VSSM_ERR_UNSUPPORTED",
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libvssm.so")
 EXPORTS = ["vssm_scan_bidir", "vssm_scan_bidir_noalloc", "vssm_scan_folded",
            "vssm_scan_chunked", "vssm_scan_workspace_size", "vssm_scan_chunked_workspace_size",
-           "vssm_scan_plan_query",
+           "vssm_scan_plan_query", "vssm_scan_grad", "vssm_scan_grad_workspace_size",
            "vssm_device_error", "vssm_status_string", "vssm_last_error", "vssm_version"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -54,6 +54,13 @@ class ScanArgs(ctypes.Structure):
         ("conv_w", ctypes.c_void_p), ("conv_b", ctypes.c_void_p),
         ("conv_w_bwd", ctypes.c_void_p), ("conv_b_bwd", ctypes.c_void_p), ("conv_k", ctypes.c_int),
     ]
+
+
+class GradArgs(ctypes.Structure):
+    """Mirror of ``vssm_grad_args`` (include/vssm.h)."""
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "dout", "dx", "ddelta", "dz", "dB", "dC", "dB_bwd", "dC_bwd", "dA_fwd", "dA_bwd",
+        "dD_fwd", "dD_bwd")]
 
 
 class VssmError(RuntimeError):
@@ -85,6 +92,10 @@ def _load():
     lib.vssm_scan_plan_query.argtypes = [P, ctypes.c_int, ctypes.c_int,
                                          ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
     lib.vssm_scan_plan_query.restype = ctypes.c_int
+    lib.vssm_scan_grad.argtypes = [P, ctypes.POINTER(GradArgs), ctypes.c_int, ctypes.c_void_p]
+    lib.vssm_scan_grad.restype = ctypes.c_int
+    lib.vssm_scan_grad_workspace_size.argtypes = [P, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
+    lib.vssm_scan_grad_workspace_size.restype = ctypes.c_int
     lib.vssm_status_string.argtypes = [ctypes.c_int]
     lib.vssm_status_string.restype = ctypes.c_char_p
     lib.vssm_last_error.argtypes = []
@@ -287,6 +298,50 @@ def scan_chunked(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *
         out = torch.empty_like(x)
     a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, out, B_bwd, C_bwd, dirs, **step)
     _launch(lib.vssm_scan_chunked, a, seg_len, x.device, workspace, stream, pieces)
+    return out
+
+
+def grad_workspace_size(a: ScanArgs, seg_len: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib.vssm_scan_grad_workspace_size(ctypes.byref(a), seg_len, ctypes.byref(n)))
+    return int(n.value)
+
+
+def scan_grad(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *, dout,
+              dirs: int = DIR_BOTH, seg_len: int = 0, B_bwd=None, C_bwd=None,
+              stream: Optional[torch.cuda.Stream] = None, workspace=None) -> dict:
+    """``vssm_scan_grad``: gradients of sum(dout * out) for the forward call
+    with these arguments (``seg_len`` > 0: the folded scan). Returns a dict
+    with dx, ddelta, dz (None without z) in x's dtype and float32 dB, dC,
+    dB_bwd, dC_bwd (None when shared), dA_fwd, dA_bwd, dD_fwd, dD_bwd (None
+    for a direction that is not run). Output tensors are allocated here."""
+    a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, None, B_bwd, C_bwd, dirs)
+    _dev_tensor("dout", dout, x.dtype, x.shape, x.device)
+    batch, dim, L = x.shape
+    N = B.shape[-1]
+    f32 = dict(dtype=torch.float32, device=x.device)
+    out = dict(dx=torch.empty_like(x), ddelta=torch.empty_like(x),
+               dz=torch.empty_like(x) if z is not None else None,
+               dB=torch.empty(batch, L, N, **f32), dC=torch.empty(batch, L, N, **f32),
+               dB_bwd=torch.empty(batch, L, N, **f32) if B_bwd is not None else None,
+               dC_bwd=torch.empty(batch, L, N, **f32) if C_bwd is not None else None,
+               dA_fwd=torch.empty(dim, N, **f32) if dirs & DIR_FWD else None,
+               dA_bwd=torch.empty(dim, N, **f32) if dirs & DIR_BWD else None,
+               dD_fwd=torch.empty(dim, **f32) if dirs & DIR_FWD else None,
+               dD_bwd=torch.empty(dim, **f32) if dirs & DIR_BWD else None)
+    g = GradArgs()
+    g.dout = dout.data_ptr()
+    for k, v in out.items():
+        setattr(g, k, _ptr(v))
+    stream = stream if stream is not None else torch.cuda.current_stream(x.device)
+    need = grad_workspace_size(a, seg_len)
+    if workspace is None:
+        workspace = _workspace(x.device, stream, need)
+    if workspace is not None:
+        a.workspace = workspace.data_ptr()
+        a.workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.vssm_scan_grad(ctypes.byref(a), ctypes.byref(g), int(seg_len),
+                              ctypes.c_void_p(stream.cuda_stream)))
     return out
 
 

@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "scan_kernel.cuh"
+#include "scan_grad.cuh"
 #include "scan_warp.cuh"
 #include "vssm.h"
 
@@ -278,7 +279,8 @@ int make_plan(const vssm_scan_args *a, int seg_len, int pieces_req, Plan *pl)
     return VSSM_OK;
 }
 
-int validate(const vssm_scan_args *a, int seg_len, bool folded)
+// need_out: the call writes a->out (the gradient does not read it).
+int validate(const vssm_scan_args *a, int seg_len, bool folded, bool need_out = true)
 {
     if (!a) return fail(VSSM_ERR_INVALID_ARG, "args is NULL");
     if (a->batch < 0 || a->dim < 0 || a->seqlen < 0)
@@ -300,7 +302,7 @@ int validate(const vssm_scan_args *a, int seg_len, bool folded)
     }
     const long long tok = (long long)a->batch * a->dim * a->seqlen;
     if (tok == 0) return VSSM_OK;
-    if (!a->x || !a->delta || !a->B || !a->C || !a->out)
+    if (!a->x || !a->delta || !a->B || !a->C || (need_out && !a->out))
         return fail(VSSM_ERR_INVALID_ARG, "x, delta, B, C and out are required");
     if ((a->dir_flags & VSSM_DIR_FWD) && !a->A_fwd)
         return fail(VSSM_ERR_INVALID_ARG, "A_fwd is required for the forward direction");
@@ -573,6 +575,64 @@ int run(const vssm_scan_args *a, int seg_len, bool folded, int pieces_req, void 
                                 : launch_typed<__nv_bfloat16>(p, pl, s);
 }
 
+
+struct GradPlan {
+    int ndir = 1, rgroups = 0, nch = 0;
+    long long ngroups = 0;
+    size_t ckpt_bytes = 0, part_off = 0, workspace = 0;
+};
+
+GradPlan make_grad_plan(const vssm_scan_args *a)
+{
+    GradPlan g;
+    g.ndir = a->dir_flags == 3 ? 2 : 1;
+    g.rgroups = (a->dim + 31) / 32;
+    g.ngroups = (long long)a->batch * g.rgroups;
+    g.nch = (a->seqlen + vssm::kTG - 1) / vssm::kTG;
+    g.ckpt_bytes = (size_t)g.ndir * g.ngroups * g.nch * 512 * sizeof(float);
+    g.part_off = (g.ckpt_bytes + 255) / 256 * 256;
+    g.workspace = a->dir_flags == 3 ? g.part_off + (size_t)g.ngroups * a->seqlen * 96 * sizeof(float)
+                                    : g.ckpt_bytes;
+    return g;
+}
+
+int zero_f32(float *p, size_t n, cudaStream_t s)
+{
+    if (!p || n == 0) return VSSM_OK;
+    const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, 148 * 8);
+    vssm::zero_f32_kernel<<<blocks, 256, 0, s>>>(p, (long long)n);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? VSSM_OK : fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+}
+
+template <typename T, int DIRS>
+int launch_grad(const vssm::GradParams &p, const GradPlan &g, cudaStream_t s)
+{
+    constexpr int NDIR = DIRS == 3 ? 2 : 1;
+    const long long units = (long long)NDIR * g.ngroups;
+    vssm::grad_ckpt_kernel<T, DIRS><<<(unsigned)((units + 3) / 4), 128, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    const size_t smem = (size_t)NDIR * vssm::GradLayout<T, DIRS>::kWarpBytes;
+    auto kern = vssm::grad_adjoint_kernel<T, DIRS>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    kern<<<(unsigned)g.ngroups, NDIR * 32, smem, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    return VSSM_OK;
+}
+
+template <typename T>
+int launch_grad_dirs(const vssm::GradParams &p, const GradPlan &g, int dirs, cudaStream_t s)
+{
+    switch (dirs) {
+    case 1: return launch_grad<T, 1>(p, g, s);
+    case 2: return launch_grad<T, 2>(p, g, s);
+    default: return launch_grad<T, 3>(p, g, s);
+    }
+}
+
 }  // namespace
 
 extern "C" {
@@ -626,6 +686,124 @@ int vssm_scan_plan_query(const vssm_scan_args *a, int seg_len, int pieces, int *
 }
 
 int vssm_scan_bidir(const vssm_scan_args *a, void *stream) { return run(a, 0, false, 0, stream); }
+
+int vssm_scan_grad_workspace_size(const vssm_scan_args *a, int seg_len, size_t *bytes)
+{
+    if (!a || !bytes) return fail(VSSM_ERR_INVALID_ARG, "args or bytes is NULL");
+    if (a->batch < 0 || a->dim < 0 || a->seqlen < 0 || a->dir_flags < 1 || a->dir_flags > 3 ||
+        seg_len < 0)
+        return fail(VSSM_ERR_INVALID_ARG, "invalid sizes or dir_flags");
+    *bytes = (long long)a->batch * a->dim * a->seqlen == 0 ? 0 : make_grad_plan(a).workspace;
+    return VSSM_OK;
+}
+
+int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len, void *stream)
+{
+    const bool folded = seg_len > 0;
+    if (seg_len < 0) return fail(VSSM_ERR_INVALID_ARG, "seg_len=%d must be >= 0", seg_len);
+    if (!g) return fail(VSSM_ERR_INVALID_ARG, "grad args is NULL");
+    int st = validate(a, seg_len, folded, false);
+    if (st != VSSM_OK) return st;
+    if (a->dstate != vssm::kMaxState)
+        return fail(VSSM_ERR_UNSUPPORTED, "the gradient needs dstate %d (got %d)", vssm::kMaxState,
+                    a->dstate);
+    if (a->delta_softplus || a->delta_bwd || a->conv_k)
+        return fail(VSSM_ERR_UNSUPPORTED,
+                    "the gradient supports steps used as given, shared, without convolution");
+    if ((long long)a->batch * a->dim * a->seqlen == 0) return VSSM_OK;
+    const unsigned dirs = a->dir_flags;
+    if (!g->dout || !g->dx || !g->ddelta || !g->dB || !g->dC)
+        return fail(VSSM_ERR_INVALID_ARG, "dout, dx, ddelta, dB and dC are required");
+    if (a->z && !g->dz) return fail(VSSM_ERR_INVALID_ARG, "dz is required when z is given");
+    if ((a->B_bwd != nullptr) != (g->dB_bwd != nullptr) || (a->C_bwd != nullptr) != (g->dC_bwd != nullptr))
+        return fail(VSSM_ERR_INVALID_ARG, "dB_bwd / dC_bwd go with B_bwd / C_bwd");
+    if ((dirs & 1) && (!g->dA_fwd || !g->dD_fwd))
+        return fail(VSSM_ERR_INVALID_ARG, "dA_fwd and dD_fwd are required for the forward direction");
+    if ((dirs & 2) && (!g->dA_bwd || !g->dD_bwd))
+        return fail(VSSM_ERR_INVALID_ARG, "dA_bwd and dD_bwd are required for the backward direction");
+    const void *gp[] = {g->dout, g->dx, g->ddelta, g->dz, g->dB, g->dC, g->dB_bwd, g->dC_bwd,
+                        g->dA_fwd, g->dA_bwd, g->dD_fwd, g->dD_bwd};
+    for (const void *q : gp)
+        if (q && !aligned16(q)) return fail(VSSM_ERR_MISALIGNED, "gradient pointer %p is not 16-byte aligned", q);
+    const GradPlan gl = make_grad_plan(a);
+    if (!a->workspace || a->workspace_bytes < gl.workspace)
+        return fail(VSSM_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", gl.workspace,
+                    a->workspace ? a->workspace_bytes : (size_t)0);
+    if (gl.ngroups > 0x7fffffffLL) return fail(VSSM_ERR_UNSUPPORTED, "problem too large for one grid");
+    const size_t es = a->dtype == VSSM_F32 ? 4 : 2;
+    const size_t nact = (size_t)a->batch * a->dim * a->seqlen * es;
+    const size_t nbc = (size_t)a->batch * a->seqlen * a->dstate * 4;
+    const size_t npar = (size_t)a->dim * a->dstate * 4, nd = (size_t)a->dim * 4;
+    const struct { const void *p; size_t n; } outs[] = {
+        {g->dx, nact}, {g->ddelta, nact}, {g->dz, nact}, {g->dB, nbc}, {g->dC, nbc},
+        {g->dB_bwd, nbc}, {g->dC_bwd, nbc}, {g->dA_fwd, npar}, {g->dA_bwd, npar},
+        {g->dD_fwd, nd}, {g->dD_bwd, nd}};
+    const void *ins[] = {a->x, a->delta, a->z, a->B, a->C, a->B_bwd, a->C_bwd, a->A_fwd, a->A_bwd,
+                         a->D_fwd, a->D_bwd, g->dout};
+    const size_t insz[] = {nact, nact, nact, nbc / 4 * es, nbc / 4 * es, nbc / 4 * es, nbc / 4 * es,
+                           npar, npar, nd, nd, nact};
+    for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
+        if (!outs[i].p) continue;
+        if (overlaps(outs[i].p, outs[i].n, a->workspace, a->workspace_bytes))
+            return fail(VSSM_ERR_INVALID_ARG, "a gradient output overlaps the workspace");
+        for (size_t k = 0; k < sizeof(ins) / sizeof(ins[0]); ++k)
+            if (overlaps(outs[i].p, outs[i].n, ins[k], insz[k]))
+                return fail(VSSM_ERR_INVALID_ARG, "a gradient output overlaps an input");
+        for (size_t k = i + 1; k < sizeof(outs) / sizeof(outs[0]); ++k)
+            if (overlaps(outs[i].p, outs[i].n, outs[k].p, outs[k].n))
+                return fail(VSSM_ERR_INVALID_ARG, "two gradient outputs overlap");
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    vssm::GradParams p{};
+    p.x = a->x;
+    p.delta = a->delta;
+    p.z = a->z;
+    p.dout = g->dout;
+    p.B[0] = a->B;
+    p.C[0] = a->C;
+    p.B[1] = a->B_bwd ? a->B_bwd : a->B;
+    p.C[1] = a->C_bwd ? a->C_bwd : a->C;
+    p.A[0] = a->A_fwd;
+    p.A[1] = a->A_bwd;
+    p.D[0] = a->D_fwd;
+    p.D[1] = a->D_bwd;
+    p.dx = g->dx;
+    p.ddelta = g->ddelta;
+    p.dz = g->dz;
+    p.dB[0] = g->dB;
+    p.dC[0] = g->dC;
+    p.dB[1] = g->dB_bwd ? g->dB_bwd : g->dB;
+    p.dC[1] = g->dC_bwd ? g->dC_bwd : g->dC;
+    p.dA[0] = g->dA_fwd;
+    p.dA[1] = g->dA_bwd;
+    p.dD[0] = g->dD_fwd;
+    p.dD[1] = g->dD_bwd;
+    p.ckpt = static_cast<float *>(a->workspace);
+    p.part = dirs == 3 ? reinterpret_cast<float *>(static_cast<char *>(a->workspace) + gl.part_off)
+                       : nullptr;
+    p.err = device_error_word();
+    if (!p.err) return fail(VSSM_ERR_CUDA, "cannot locate the device error word");
+    p.batch = a->batch;
+    p.dim = a->dim;
+    p.L = a->seqlen;
+    p.seg_len = seg_len;
+    p.rgroups = gl.rgroups;
+    p.nch = gl.nch;
+    p.ngroups = gl.ngroups;
+    // the reductions accumulate atomically: start them at zero
+    const size_t nbcf = (size_t)a->batch * a->seqlen * a->dstate;
+    float *zs[] = {g->dB, g->dC, g->dB_bwd, g->dC_bwd};
+    for (float *q : zs)
+        if ((st = zero_f32(q, nbcf, s)) != VSSM_OK) return st;
+    if ((dirs & 1) && ((st = zero_f32(g->dA_fwd, (size_t)a->dim * 16, s)) != VSSM_OK ||
+                       (st = zero_f32(g->dD_fwd, (size_t)a->dim, s)) != VSSM_OK))
+        return st;
+    if ((dirs & 2) && ((st = zero_f32(g->dA_bwd, (size_t)a->dim * 16, s)) != VSSM_OK ||
+                       (st = zero_f32(g->dD_bwd, (size_t)a->dim, s)) != VSSM_OK))
+        return st;
+    return a->dtype == VSSM_F32 ? launch_grad_dirs<float>(p, gl, (int)dirs, s)
+                                : launch_grad_dirs<__nv_bfloat16>(p, gl, (int)dirs, s);
+}
 
 int vssm_scan_chunked(const vssm_scan_args *a, int seg_len, int pieces, void *stream)
 {

@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define VSSM_VERSION 130 /* 1.3.0 */
+#define VSSM_VERSION 140 /* 1.4.0 */
 
 typedef enum {
     VSSM_OK = 0,
@@ -237,6 +237,50 @@ int vssm_scan_bidir_noalloc(const vssm_scan_args *a, void *stream);
  * VSSM_ERR_INVALID_ARG).
  */
 int vssm_scan_folded(const vssm_scan_args *a, int seg_len, void *stream);
+
+/*
+ * Gradient of the scan (training). Arguments of the forward call plus the
+ * gradient of a loss with respect to its output; all device pointers,
+ * caller-owned.
+ */
+typedef struct {
+    const void *dout;        /* [batch][dim][seqlen] dL/d out, dtype of x      required */
+    void *dx, *ddelta, *dz;  /* [batch][dim][seqlen], dtype of x, written; dz
+                                required iff the forward call has z           */
+    float *dB, *dC;          /* [batch][seqlen][dstate] fp32, written         required */
+    float *dB_bwd, *dC_bwd;  /* required iff B_bwd / C_bwd are given (the
+                                backward direction's own); else NULL          */
+    float *dA_fwd, *dA_bwd;  /* [dim][dstate] fp32, written; required for each
+                                direction the call runs                       */
+    float *dD_fwd, *dD_bwd;  /* [dim] fp32, written; as dA                     */
+} vssm_grad_args;
+
+/*
+ * Reverse-mode gradient of L = sum(dout * out) for the forward call
+ * vssm_scan_bidir(a) (seg_len == 0) or vssm_scan_folded(a, seg_len): the
+ * exact derivative with respect to x, delta, z, B, C (and B_bwd, C_bwd), A
+ * and D of each direction (the adjoint recurrence of the scan: each
+ * direction's adjoint walks against its own scan order; VSSD page §4.2.1.3
+ * for the recurrence, Vim page §2.2 for the two directions). a->out is not
+ * read. dx, ddelta, dz are rounded once to the I/O dtype; dB, dC, dA, dD are
+ * fp32 sums over batch, channels and tokens, computed with atomic additions
+ * (their summation order, and so their last bits, can vary from run to run).
+ *
+ * Supported: dstate == 16, steps used as given and shared by both
+ * directions, no convolution (delta_softplus == 0, delta_bwd == NULL,
+ * conv_k == 0); anything else is VSSM_ERR_UNSUPPORTED. a->workspace must hold
+ * vssm_scan_grad_workspace_size bytes and must not overlap any input or
+ * output. Asynchronous on `stream`; the
+ * pair rendezvous of the two directions is bounded as in the forward kernel
+ * (vssm_device_error).
+ */
+int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len, void *stream);
+
+/* Workspace bytes of vssm_scan_grad: 8 bytes per token, channel and
+ * direction for the state checkpoints (16 fp32 every 8 tokens), plus 12 bytes
+ * per token and channel for the partial gradients exchanged between the two
+ * directions (both directions only), channels rounded up to groups of 32. */
+int vssm_scan_grad_workspace_size(const vssm_scan_args *a, int seg_len, size_t *bytes);
 
 /*
  * Synchronises `stream`, then reads and clears this device's error word.

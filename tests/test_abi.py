@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(v):
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared in vssm.h but not exported"
     assert set(v.EXPORTS) <= set(declared_functions())
-    assert v.version() == 130
+    assert v.version() == 140
 
 
 def test_args_struct_layout_matches_header(v):
@@ -208,3 +208,45 @@ def test_plan_query(v):
     assert _plan(v, _args(v, batch=0)) == (0, 0, 0)
     assert _plan(v, _args(v), 0, -1)[0] == -1
     assert _plan(v, _args(v, dstate=8), 0, 2)[0] == -2
+
+
+def _grad_args(v, **kw):
+    g = v.GradArgs()
+    base = 1 << 30                      # fake, aligned, far from the inputs of _args
+    for i, name in enumerate(("dout", "dx", "ddelta", "dz", "dB", "dC", "dA_fwd", "dA_bwd",
+                              "dD_fwd", "dD_bwd")):
+        setattr(g, name, base * (i + 1))
+    for k, val in kw.items():
+        setattr(g, k, val)
+    return g
+
+
+def test_grad_workspace_size(v):
+    a = _args(v, batch=1, dim=384, seqlen=197, dtype=0)
+    n = ctypes.c_size_t()
+    assert v.lib.vssm_scan_grad_workspace_size(ctypes.byref(a), 0, ctypes.byref(n)) == 0
+    # checkpoints: 2 directions x 12 groups x 25 chunks of 8 tokens x 16 x 32 floats,
+    # then partial dx, ddelta, dz: 12 groups x 197 tokens x 3 x 32 floats
+    assert n.value == 2 * 12 * 25 * 512 * 4 + 12 * 197 * 96 * 4
+    a1 = _args(v, batch=1, dim=384, seqlen=197, dtype=0, dir_flags=1)
+    assert v.lib.vssm_scan_grad_workspace_size(ctypes.byref(a1), 0, ctypes.byref(n)) == 0
+    assert n.value == 12 * 25 * 512 * 4
+
+
+def test_grad_validation(v):
+    def call(a, g, seg=0):
+        return v.lib.vssm_scan_grad(ctypes.byref(a), ctypes.byref(g), seg, None)
+    assert call(_args(v, dstate=8), _grad_args(v)) == -2
+    assert call(_args(v, delta_softplus=1), _grad_args(v)) == -2
+    assert call(_args(v, conv_k=4, conv_w=(1 << 20) * 13), _grad_args(v)) == -2
+    assert call(_args(v), _grad_args(v, dout=None)) == -1
+    assert call(_args(v), _grad_args(v, dz=None)) == -1          # the call has z
+    assert call(_args(v, B_bwd=(1 << 20) * 14), _grad_args(v)) == -1  # dB_bwd missing
+    assert call(_args(v), _grad_args(v, dA_bwd=None)) == -1
+    assert call(_args(v), _grad_args(v, dx=(1 << 30) + 4)) == -3
+    ws = dict(workspace=(1 << 20) * 15, workspace_bytes=1 << 20)
+    assert call(_args(v, **ws), _grad_args(v, dx=(1 << 20) * 2)) == -1  # dx overlaps delta
+    assert call(_args(v, **ws), _grad_args(v, dB=(1 << 20) * 15)) == -1  # dB overlaps workspace
+    assert call(_args(v), _grad_args(v), seg=-1) == -1
+    assert call(_args(v), _grad_args(v)) == -6                    # no workspace
+    assert call(_args(v, batch=0), _grad_args(v)) == 0            # empty: nothing to do
