@@ -63,6 +63,9 @@ def parse_args(argv=None):
     p.add_argument("--fused-step", action="store_true",
                    help="pass per-direction steps before softplus, with biases (the kernel "
                         "applies softplus(delta + bias))")
+    p.add_argument("--grad", action="store_true",
+                   help="time a training step: the forward scan plus its gradient "
+                        "(vssm_scan_grad) for a seeded upstream gradient")
     p.add_argument("--conv", type=int, default=0, choices=[0, 1, 2, 3, 4],
                    help="taps of the directional depthwise convolution + SiLU in front of "
                         "the scan (0: none)")
@@ -459,9 +462,44 @@ def run_ours(args):
     # the library cut them and join the ranges by the carry)
     ranges, launches = vssm.plan(argsets[0], seg)
 
+    grad_calls = []
+    if args.grad:
+        # the training step adds the gradient of sum(dout * out): seeded dout,
+        # outputs and workspace allocated once
+        if wl.fused_step or wl.conv:
+            raise SystemExit("--grad covers the scan with steps as given and no convolution")
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(1234 + rank)
+        dout = torch.randn(base["x"].shape, device=dev, generator=gen).to(base["x"].dtype)
+        gws = None
+        for s_, a in zip(sets, argsets):
+            batch, dim, L = s_["x"].shape
+            f32 = dict(dtype=torch.float32, device=dev)
+            outs_g = dict(dx=torch.empty_like(s_["x"]), ddelta=torch.empty_like(s_["x"]),
+                          dz=torch.empty_like(s_["x"]), dB=torch.empty(batch, L, 16, **f32),
+                          dC=torch.empty(batch, L, 16, **f32),
+                          dA_fwd=torch.empty(dim, 16, **f32) if wl.dirs & 1 else None,
+                          dA_bwd=torch.empty(dim, 16, **f32) if wl.dirs & 2 else None,
+                          dD_fwd=torch.empty(dim, **f32) if wl.dirs & 1 else None,
+                          dD_bwd=torch.empty(dim, **f32) if wl.dirs & 2 else None)
+            g = vssm.GradArgs()
+            g.dout = dout.data_ptr()
+            for k, v in outs_g.items():
+                setattr(g, k, v.data_ptr() if v is not None else None)
+            ga = vssm.ScanArgs.from_buffer_copy(a)
+            need = vssm.grad_workspace_size(ga, seg)
+            if gws is None:
+                gws = torch.empty(need, dtype=torch.uint8, device=dev)
+            ga.workspace, ga.workspace_bytes = gws.data_ptr(), need
+            grad_calls.append((ga, g, outs_g))
+        launches += 8   # six zero-fills, the checkpoint pass and the adjoint
+
     def launch(i):
         a = ctypes.byref(argsets[i % nsets])
         st = fn(a, seg, sptr) if seg else fn(a, sptr)
+        if st == 0 and grad_calls:
+            ga, g, _ = grad_calls[i % nsets]
+            st = vssm.lib.vssm_scan_grad(ctypes.byref(ga), ctypes.byref(g), seg, sptr)
         if st != 0:
             raise RuntimeError(vssm.lib.vssm_last_error().decode())
 
@@ -490,7 +528,16 @@ def run_ours(args):
     kern_ms = [b.elapsed_time(e) for b, e in zip(ev_b, ev_e)]
     kern_avg_s = statistics.fmean(kern_ms) / 1e3
 
-    gbs = aggregate(set_bytes * args.steps, world, region_s) / 1e9
+    # bytes a step must move: the forward's, plus with --grad the gradient's
+    # (x, delta, z, dout read and dx, ddelta, dz written in the I/O dtype; B, C
+    # read and dB, dC written in fp32; A, D read and dA, dD written)
+    step_bytes = set_bytes
+    if args.grad:
+        e = 4 if wl.dtype == "f32" else 2
+        ndir = 2 if wl.dirs == 3 else 1
+        step_bytes += (7 * wl.tokch * e + 2 * wl.batch * wl.seqlen * wl.dstate * (e + 4)
+                       + 2 * ndir * (wl.dim * wl.dstate + wl.dim) * 4)
+    gbs = aggregate(step_bytes * args.steps, world, region_s) / 1e9
     gtok = aggregate(wl.tokch * args.steps, world, region_s) / 1e9
     peaks, peaks_kind = measured_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
@@ -501,15 +548,15 @@ def run_ours(args):
     # the plan cuts rows (launches == 2) the events bracket the summary pass
     # and the scan together, and only the algorithmic updates are counted
     # (the summary pass's repeated ones are not credited).
-    upd = exp_count(wl)
+    upd = exp_count(wl) * (2 if args.grad else 1)
     ach = upd / kern_avg_s / 1e9
     peak_upd = EX2_PER_CLK_SM * SMS * MAX_SM_MHZ * 1e6 / 1e9
-    kern_gbs = set_bytes / kern_avg_s / 1e9
+    kern_gbs = step_bytes / kern_avg_s / 1e9
     med = clocks.get("sm_mhz")
     roofline = {
         "bound": "alu", "achieved": round(ach, 2), "peak": round(peak_upd, 2),
         "unit": "Gupdate/s", "frac": round(ach / peak_upd, 4),
-        "traffic": ncu_traffic(variant_key(wl)),
+        "traffic": ncu_traffic(variant_key(wl) + ("+grad" if args.grad else "")),
         "update": "one (token, channel, state, direction) recurrence step: 1 MUFU ex2 + 4 fp32 FMA-pipe ops",
         "peak_basis": f"{EX2_PER_CLK_SM} ex2/clk/SM (and {FMA_PER_CLK_SM}/4 FMA-pipe updates/clk/SM) "
                       f"x {SMS} SMs x {MAX_SM_MHZ:.0f} MHz max SM clock",
@@ -521,12 +568,12 @@ def run_ours(args):
         "hbm_frac": round(kern_gbs / hbm_peak, 4),
         "hbm_peak_gbs": hbm_peak, "hbm_peak_kind": peaks_kind,
         "hbm_frac_spec_8tbs": round(kern_gbs / SPEC_HBM_GBS, 4),
-        "algorithmic_bytes_per_launch": set_bytes,
+        "algorithmic_bytes_per_launch": step_bytes,
     }
 
     # ---- end to end through the public API: pinned host -> device, scan, -> host
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and not args.grad:
         host = {k: v.cpu().pin_memory() for k, v in base.items()}
         dst = {k: torch.empty_like(v) for k, v in base.items()}
         out_h = torch.empty(base["x"].shape, dtype=base["x"].dtype).pin_memory()
@@ -581,7 +628,8 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(region_s / args.steps * 1e3, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": workload_config(wl, l2_note),
+            "config": dict(workload_config(wl, l2_note),
+                           step="forward + gradient (training)" if args.grad else "forward"),
             "gtokch_per_s": round(gtok, 4),
             "hbm_frac_of_measured": round(gbs / world / hbm_peak, 4),
             "hbm_frac_of_spec_8tbs": round(gbs / world / SPEC_HBM_GBS, 4),

@@ -17,7 +17,8 @@
 //
 //  * grad_ckpt_kernel: one warp per (direction, channel group) runs the
 //    forward recurrence over the row and stores the state entering every
-//    8-token chunk (in that direction's scan order) to a checkpoint buffer.
+//    chunk of kTG tokens (in that direction's scan order) to a checkpoint
+//    buffer.
 //  * grad_adjoint_kernel: the two directions of a channel group are a warp
 //    pair that meets in the middle, as in the forward kernel but walking
 //    against the scan orders: the forward direction's adjoint walks the
@@ -27,9 +28,11 @@
 //    In phase 0 each warp leaves its fp32 partial dx, ddelta, dz for its half
 //    in the workspace; after a bounded rendezvous, phase 1 adds the
 //    partner's partials and writes the gradients. dB and dC are reduced
-//    over the warp's 32 channels by a butterfly reduce-scatter (each lane
-//    ends with one of the 32 sums) and added to global memory atomically;
-//    dA and dD accumulate in registers over the row and are added at the end.
+//    over the warp's 32 channels through shared memory (each lane writes its
+//    32 contributions as a row, then sums one column) and added to global
+//    memory atomically, one value per lane and token; dA and dD accumulate
+//    in registers over the row and are added at the end. The state and B/C
+//    arithmetic runs on packed f32x2 instructions.
 //
 // The only wait on another warp is the pair rendezvous (bounded, as in the
 // forward kernel).
@@ -44,7 +47,10 @@
 
 namespace vssm {
 
-constexpr int kTG = 8;                  // tokens per gradient chunk
+#ifndef VSSM_GRAD_CHUNK
+#define VSSM_GRAD_CHUNK 4
+#endif
+constexpr int kTG = VSSM_GRAD_CHUNK;     // tokens per gradient chunk
 
 struct GradParams {
     const void *x, *delta, *z, *dout;
@@ -103,69 +109,112 @@ __global__ void __launch_bounds__(128) grad_ckpt_kernel(const GradParams p)
         float *cj = ck + (long long)j * 512;
 #pragma unroll
         for (int n = 0; n < 16; ++n) cj[n * 32 + lane] = h[n];
-        const int t0 = j * kTG, t1 = min(p.L, t0 + kTG);
-        for (int k = 0; k < t1 - t0; ++k) {
-            const int t = dir == 0 ? t0 + k : t1 - 1 - k;
-            const float dt = act ? gload<T>(p.delta, row + t) : 0.f;
-            const float xv = act ? gload<T>(p.x, row + t) : 0.f;
-            const bool rs = reset_at(t, p.seg_len, dir);
-            const T *Bt = reinterpret_cast<const T *>(Bb) + (long long)t * 16;
+        const int t0 = j * kTG, t1 = min(p.L, t0 + kTG), len = t1 - t0;
+        // the chunk's steps and inputs first (independent loads in flight together)
+        float dtv[kTG], xv[kTG];
 #pragma unroll
-            for (int n = 0; n < 16; ++n) {
-                const float a = rs ? 0.f : ex2_mufu(dt * Al2[n]);
-                h[n] = fmaf(a, h[n], dt * xv * ld_as_f32(Bt + n));
+        for (int k = 0; k < kTG; ++k) {
+            const bool in = act && k < len;
+            const long long e = row + (dir == 0 ? t0 + k : t1 - 1 - k);
+            dtv[k] = in ? gload<T>(p.delta, e) : 0.f;
+            xv[k] = in ? gload<T>(p.x, e) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kTG; ++k) {
+            if (k < len) {
+                const int t = dir == 0 ? t0 + k : t1 - 1 - k;
+                const bool rs = reset_at(t, p.seg_len, dir);
+                float Bv[16];                                   // B_t: 32 or 64 aligned bytes
+                load16_f32(reinterpret_cast<const T *>(Bb) + (long long)t * 16, Bv);
+                const float ux = dtv[k] * xv[k];
+#pragma unroll
+                for (int n = 0; n < 16; ++n) {
+                    const float a = rs ? 0.f : ex2_mufu(dtv[k] * Al2[n]);
+                    h[n] = fmaf(a, h[n], ux * Bv[n]);
+                }
             }
         }
     }
 }
 
-// One butterfly stage over the 2W live values v[0..2W): the lane keeps the
-// half selected by its bit W, sends the other half to lane ^ W and adds what
-// comes back.
-template <int W>
-__device__ __forceinline__ void reduce_scatter_stage(float (&v)[32], bool upper)
+// 16 bytes of shared memory as two fp32 pairs, and back (ordered against the
+// warp's other shared-memory accesses by the memory clobber).
+__device__ __forceinline__ void lds2(const float *p, f2 &a, f2 &b)
 {
-#pragma unroll
-    for (int i = 0; i < W; ++i) {
-        const float send = upper ? v[i] : v[i + W];
-        const float keep = upper ? v[i + W] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, W);
-    }
+    asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a.v), "=l"(b.v) : "r"(smem_addr(p)) : "memory");
 }
-
-// Butterfly reduce-scatter of 32 values over the warp: on return lane l holds
-// the warp's sum of v[l] in v[0] (31 shuffles and 31 adds per lane).
-__device__ __forceinline__ void reduce_scatter32(float (&v)[32], int lane)
+__device__ __forceinline__ void sts2(float *p, f2 a, f2 b)
 {
-    reduce_scatter_stage<16>(v, (lane & 16) != 0);
-    reduce_scatter_stage<8>(v, (lane & 8) != 0);
-    reduce_scatter_stage<4>(v, (lane & 4) != 0);
-    reduce_scatter_stage<2>(v, (lane & 2) != 0);
-    reduce_scatter_stage<1>(v, (lane & 1) != 0);
+    asm volatile("st.shared.v2.b64 [%0], {%1, %2};" :: "r"(smem_addr(p)), "l"(a.v), "l"(b.v) : "memory");
 }
 
 template <typename T, int DIRS>
 struct GradLayout {
-    // per warp: states [kTG + 1][16][32] fp32, then B and C of the chunk [kTG][32] fp32
-    static constexpr int kH = (kTG + 1) * 16 * 32 * 4;
-    static constexpr int kBC = kTG * 32 * 4;
-    static constexpr int kWarpBytes = kH + kBC + 16;      // + pair barrier
+    static constexpr int ES = (int)sizeof(T);
+    static constexpr bool BIDIR = DIRS == 3;
+    // one ring stage: this lane's 16-byte blocks of delta, x, z, dout over the
+    // chunk (row slots of SLOT bytes), B and C of the chunk (raw), the
+    // chunk's checkpoint [16][32] fp32 and, both directions, the partner's
+    // partial gradients [kTG][3][32] fp32
+    static constexpr int SLOT = ((16 - ES) + kTG * ES + 15) / 16 * 16;
+    // rows staggered by 16 bytes every 8 rows so that lanes r and r + 8 read
+    // different banks
+    static constexpr int ROWS = 32 * SLOT + 16 * 3;           // one array's 32 rows
+    __device__ static constexpr int row_off(int a, int r) { return a * ROWS + r * SLOT + 16 * (r >> 3); }
+    static constexpr int sROW = 0;
+    static constexpr int sB = sROW + 4 * ROWS;
+    static constexpr int sC = sB + kTG * 16 * ES;
+    static constexpr int sCK = sC + kTG * 16 * ES;
+    static constexpr int sPT = sCK + 512 * 4;
+    static constexpr int kStage = sPT + (BIDIR ? kTG * 96 * 4 : 0);
+    // per warp: 2 stages, then
+    //   hb  [kTG + 1][4][32 lanes][4] states (quarter q of a lane's 16 states;
+    //                                 a warp's access to one quarter is 512
+    //                                 contiguous bytes)
+    //   bc  [kTG][32]                 B[16], C[16] of each token, fp32
+    //   tr  [2][32 lanes][kTP]        per-token dB, dC contributions, transposed
+    //                                 (double-buffered: a token's column sums
+    //                                 run while the next token is computed)
+    static constexpr int kTP = 36;
+    static constexpr int oHB = 2 * kStage;
+    static constexpr int oBC = oHB + (kTG + 1) * 4 * 32 * 16;
+    static constexpr int oTR = oBC + kTG * 32 * 4;              // two buffers
+    static constexpr int kWarpBytes = oTR + 2 * 32 * kTP * 4 + 16;   // + pair barrier
+    static_assert(kStage % 16 == 0 && oHB % 16 == 0 && oTR % 16 == 0, "alignment");
+    // CTAs per SM that shared memory allows (228 KB, 1 KB reserved per CTA)
+    static constexpr int kPerSm = (228 * 1024) / ((BIDIR ? 2 : 1) * kWarpBytes + 1024);
+    static constexpr int kMinBlocks = kPerSm < 1 ? 1 : (kPerSm > 8 ? 8 : kPerSm);
 };
 
+// Column `lane` of a [32][TP] buffer summed over its 32 rows (four partial
+// sums), added to dB (lanes 0-15) or dC (lanes 16-31) of token t.
+template <int TP>
+__device__ __forceinline__ void column_sum_add(const float *buf, int lane, float *dB, float *dC,
+                                               long long bcrow, int t)
+{
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int l = 0; l < 32; ++l) c[l & 3] += buf[l * TP + lane];
+    float *dst = lane < 16 ? dB + bcrow + (long long)t * 16 + lane
+                           : dC + bcrow + (long long)t * 16 + (lane - 16);
+    atomicAdd(dst, (c[0] + c[1]) + (c[2] + c[3]));
+}
+
 template <typename T, int DIRS>
-__global__ void __launch_bounds__((DIRS == 3 ? 2 : 1) * 32, 1)
+__global__ void __launch_bounds__((DIRS == 3 ? 2 : 1) * 32, (GradLayout<T, DIRS>::kMinBlocks))
 grad_adjoint_kernel(const GradParams p)
 {
-    constexpr int NDIR = (DIRS == 3) ? 2 : 1;
     using Lay = GradLayout<T, DIRS>;
+    constexpr int TP = Lay::kTP, ES = Lay::ES;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long grp = blockIdx.x;
     const int slot = warp;
     const int dir = (DIRS == 3) ? warp : (DIRS == 1 ? 0 : 1);
     unsigned char *wsm = smem_raw + warp * Lay::kWarpBytes;
-    float *hb = reinterpret_cast<float *>(wsm);                 // [kTG + 1][16][32]
-    float *bc = reinterpret_cast<float *>(wsm + Lay::kH);       // [kTG][32]: B[16], C[16]
+    float *hb = reinterpret_cast<float *>(wsm + Lay::oHB);
+    float *bc = reinterpret_cast<float *>(wsm + Lay::oBC);
+    float *tr = reinterpret_cast<float *>(wsm + Lay::oTR);
     uint64_t *pairbar = reinterpret_cast<uint64_t *>(smem_raw + Lay::kWarpBytes - 16);
     if (DIRS == 3 && threadIdx.x == 0) {
         mbar_init(pairbar, 2);
@@ -178,29 +227,32 @@ grad_adjoint_kernel(const GradParams p)
     const int d = d0 + lane;
     const bool act = d < p.dim;
     constexpr float kLog2e = 1.4426950408889634f;
-    float Al2[16], Aa[16], lam[16], dA[16];
+    f2 Ap[8], Aa[8], lam[8], dA[8];
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
-        Aa[n] = act ? p.A[dir][(long long)d * 16 + n] : 0.f;
-        Al2[n] = Aa[n] * kLog2e;
-        lam[n] = 0.f;
-        dA[n] = 0.f;
+    for (int q = 0; q < 8; ++q) {
+        const float a0 = act ? p.A[dir][(long long)d * 16 + 2 * q] : 0.f;
+        const float a1 = act ? p.A[dir][(long long)d * 16 + 2 * q + 1] : 0.f;
+        Aa[q] = pack2(a0, a1);
+        Ap[q] = pack2(a0 * kLog2e, a1 * kLog2e);
+        lam[q] = pack2(0.f, 0.f);
+        dA[q] = pack2(0.f, 0.f);
     }
     const float Dk = (act && p.D[dir]) ? p.D[dir][d] : 0.f;
     float dD = 0.f;
-    const long long row = ((long long)b * p.dim + (act ? d : d0)) * p.L;
+    const long long total = (long long)p.batch * p.dim * p.L;
+    const long long erow = ((long long)b * p.dim + (act ? d : d0)) * p.L;   // element of (b, d, 0)
     const long long bcrow = (long long)b * p.L * 16;
     const float *ck = p.ckpt + ((long long)slot * p.ngroups + grp) * p.nch * 512;
     const bool hasZ = p.z != nullptr;
     float *dBk = p.dB[dir], *dCk = p.dC[dir];
+    float *my_h = hb + lane * 4;              // quarter q of slot s: my_h + (s * 4 + q) * 128
+    const void *arr[4] = {p.delta, p.x, hasZ ? p.z : p.x, p.dout};
 
-    // chunks of each phase, walked against the scan order
     const int Hc = (p.nch + 1) / 2;
     const int nphase = (DIRS == 3) ? 2 : 1;
-    bool ok = true;
-    for (int phase = 0; phase < nphase && ok; ++phase) {
-        const bool fin = phase == nphase - 1;
-        int clo, chi;                                  // chunk range [clo, chi)
+    // chunk list: phase 0 then phase 1, each against the scan order
+    auto chunk_of = [&](int phase, int s, int &j) -> bool {
+        int clo, chi;
         if (DIRS == 3) {
             const bool upper = (dir == 0) == (phase == 0);
             clo = upper ? Hc : 0;
@@ -209,126 +261,222 @@ grad_adjoint_kernel(const GradParams p)
             clo = 0;
             chi = p.nch;
         }
-        for (int s = 0; s < chi - clo; ++s) {
-            const int j = dir == 0 ? chi - 1 - s : clo + s;
+        if (s >= chi - clo) return false;
+        j = dir == 0 ? chi - 1 - s : clo + s;
+        return true;
+    };
+    auto nchunks = [&](int phase) {
+        if (DIRS != 3) return p.nch;
+        const bool upper = (dir == 0) == (phase == 0);
+        return upper ? p.nch - Hc : Hc;
+    };
+    // copy chunk j (phase ph) into ring stage st and commit it as one group
+    auto issue = [&](int st, int j, bool fin) {
+        unsigned char *sg = wsm + st * Lay::kStage;
+        const int t0 = j * kTG, len = min(p.L, t0 + kTG) - t0;
+        if (act) {
+            const uint32_t lead = (uint32_t)(((erow + t0) * ES) & 15);
+            const int nblk = (int)((lead + (uint32_t)(len * ES) + 15u) >> 4);
+            const long long avail = (total - erow - t0) * ES + lead;
+            const long long off = (long long)t0 * ES - lead;
+            for (int a = 0; a < 4; ++a) {
+                if (a == 2 && !hasZ) continue;
+                const char *src = static_cast<const char *>(arr[a]) + erow * ES + off;
+                unsigned char *dst = sg + Lay::sROW + Lay::row_off(a, lane);
+                for (int k = 0; k < nblk; ++k) {
+                    const long long rem = avail - 16 * k;
+                    cp_async16(dst + 16 * k, src + 16 * k, rem >= 16 ? 16u : (uint32_t)rem);
+                }
+            }
+        }
+        {   // B and C: len * 16 * ES bytes each, contiguous
+            const int nb = len * ES;                  // 16-byte blocks per tensor
+            const char *srcB = static_cast<const char *>(p.B[dir]) + (bcrow + (long long)t0 * 16) * ES;
+            const char *srcC = static_cast<const char *>(p.C[dir]) + (bcrow + (long long)t0 * 16) * ES;
+#pragma unroll
+            for (int m = 0; m < (kTG * ES + 31) / 32; ++m) {
+                const int jj = lane + 32 * m;
+                cp_async16_if(sg + Lay::sB + 16 * jj, srcB + 16 * jj, jj < nb);
+                cp_async16_if(sg + Lay::sC + 16 * jj, srcC + 16 * jj, jj < nb);
+            }
+        }
+        {   // the checkpoint entering the chunk: 512 floats
+            const char *src = reinterpret_cast<const char *>(ck + (long long)j * 512);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) cp_async16(sg + Lay::sCK + 16 * (lane + 32 * m), src + 16 * (lane + 32 * m), 16u);
+        }
+        if (DIRS == 3 && fin) {   // the partner's partial gradients of these tokens
+            const char *src = reinterpret_cast<const char *>(p.part + (grp * p.L + t0) * 96);
+            const int nb = len * 24;                  // 384 bytes per token
+#pragma unroll
+            for (int m = 0; m < kTG * 24 / 32; ++m) {
+                const int jj = lane + 32 * m;
+                cp_async16_if(sg + Lay::sPT + 16 * jj, src + 16 * jj, jj < nb);
+            }
+        }
+        cp_async_commit();
+    };
+
+    bool ok = true;
+    int ring = 0;
+    int tb = 0, tprev = -1;                   // tr buffer count, token of the pending column sum
+    for (int phase = 0; phase < nphase && ok; ++phase) {
+        const bool fin = phase == nphase - 1;
+        const int nk = nchunks(phase);
+        for (int s = 0; s < 2; ++s) {
+            int j;
+            if (chunk_of(phase, s, j)) issue((ring + s) & 1, j, fin);
+            else cp_async_commit();
+        }
+        for (int s = 0; s < nk; ++s, ++ring) {
+            const int st = ring & 1;
+            unsigned char *sg = wsm + st * Lay::kStage;
+            int j;
+            chunk_of(phase, s, j);
             const int t0 = j * kTG, t1 = min(p.L, t0 + kTG), len = t1 - t0;
-            // B and C of the chunk (lane = (token, part))
+            cp_async_wait<1>();
+            __syncwarp();
+            const uint32_t lead = (uint32_t)(((erow + t0) * ES) & 15);
+            const T *rowv[4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+                rowv[a] = reinterpret_cast<const T *>(sg + Lay::sROW + Lay::row_off(a, lane) + lead);
+            // B and C to fp32 (lane = (token, quarter of 8 values))
             {
-                const int tk = lane >> 2, q = lane & 3;   // 8 tokens x 4 quarters of 8 values
+                const int tk = lane >> 2, q = lane & 3;
                 if (tk < len) {
-                    const void *src = q < 2 ? p.B[dir] : p.C[dir];
-                    const long long o = bcrow + (long long)(t0 + tk) * 16 + (q & 1) * 8;
+                    const T *src = reinterpret_cast<const T *>(sg + (q < 2 ? Lay::sB : Lay::sC)) + tk * 16 + (q & 1) * 8;
+                    float *dst = bc + tk * 32 + (q >> 1) * 16 + (q & 1) * 8;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) bc[tk * 32 + (q >> 1) * 16 + (q & 1) * 8 + i] = gload<T>(src, o + i);
+                    for (int i = 0; i < 8; ++i) dst[i] = ld_as_f32(src + i);
                 }
             }
-            // this lane's inputs of the chunk, indexed by scan position k
-            // (token t0 + k going forward, t1 - 1 - k going backward)
-            float dtv[kTG], xv[kTG], zv[kTG], go[kTG];
-#pragma unroll
-            for (int k = 0; k < kTG; ++k) {
-                const bool in = act && k < len;
-                const long long e = row + (dir == 0 ? t0 + k : t1 - 1 - k);
-                dtv[k] = in ? gload<T>(p.delta, e) : 0.f;
-                xv[k] = in ? gload<T>(p.x, e) : 0.f;
-                zv[k] = (in && hasZ) ? gload<T>(p.z, e) : 0.f;
-                go[k] = in ? gload<T>(p.dout, e) : 0.f;
-            }
-            // recompute the chunk's states in scan order: slot 0 = entering
-            // state, slot k + 1 = state after the k-th token in scan order
+            // recompute the chunk's states: slot 0 = entering state, slot
+            // k + 1 = state after the token at scan position k
+            f2 h[8];
             {
-                const float *cj = ck + (long long)j * 512;
-                float h[16];
+                const float *cj = reinterpret_cast<const float *>(sg + Lay::sCK);
 #pragma unroll
-                for (int n = 0; n < 16; ++n) {
-                    h[n] = cj[n * 32 + lane];
-                    hb[n * 32 + lane] = h[n];
-                }
-                __syncwarp();
+                for (int q = 0; q < 8; ++q) h[q] = pack2(cj[(2 * q) * 32 + lane], cj[(2 * q + 1) * 32 + lane]);
 #pragma unroll
-                for (int k = 0; k < kTG; ++k) {
-                    if (k < len) {
-                        const int i = dir == 0 ? k : len - 1 - k;
-                        const bool rs = reset_at(t0 + i, p.seg_len, dir);
-                        const float ux = dtv[k] * xv[k];
+                for (int q = 0; q < 4; ++q) sts2(my_h + q * 128, h[2 * q], h[2 * q + 1]);
+            }
+            __syncwarp();
+#pragma unroll 1
+            for (int k = 0; k < len; ++k) {
+                const int i = dir == 0 ? k : len - 1 - k;
+                const float dt = act ? ld_as_f32(rowv[0] + i) : 0.f;
+                const float ux = act ? dt * ld_as_f32(rowv[1] + i) : 0.f;
+                const bool rs = reset_at(t0 + i, p.seg_len, dir);
+                const f2 dd = pack2(dt, dt), uu = pack2(ux, ux);
+                const f2 lmd = rs ? pack2(-INFINITY, -INFINITY) : pack2(0.f, 0.f);
+                const float *Bt = bc + i * 32;
 #pragma unroll
-                        for (int n = 0; n < 16; ++n) {
-                            const float a = rs ? 0.f : ex2_mufu(dtv[k] * Al2[n]);
-                            h[n] = fmaf(a, h[n], ux * bc[i * 32 + n]);
-                            hb[((k + 1) * 16 + n) * 32 + lane] = h[n];
-                        }
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    f2 B0, B1;
+                    lds2(Bt + 4 * q, B0, B1);
+                    h[2 * q] = fma2(ex2_fma2(dd, Ap[2 * q], lmd), h[2 * q], mul2(uu, B0));
+                    h[2 * q + 1] = fma2(ex2_fma2(dd, Ap[2 * q + 1], lmd), h[2 * q + 1], mul2(uu, B1));
+                    sts2(my_h + ((k + 1) * 4 + q) * 128, h[2 * q], h[2 * q + 1]);
                 }
             }
             __syncwarp();
-            // adjoint, against the scan order
-            float hn[16];                               // state after the current token
+            // adjoint, against the scan order; hn = state after the current token
+            f2 hn[8];
 #pragma unroll
-            for (int n = 0; n < 16; ++n) hn[n] = hb[(len * 16 + n) * 32 + lane];
-#pragma unroll
-            for (int k = kTG - 1; k >= 0; --k) {
-                if (k >= len) continue;
+            for (int q = 0; q < 4; ++q) lds2(my_h + (len * 4 + q) * 128, hn[2 * q], hn[2 * q + 1]);
+            const float *pt = reinterpret_cast<const float *>(sg + Lay::sPT);
+#pragma unroll 1
+            for (int k = len - 1; k >= 0; --k) {
                 const int i = dir == 0 ? k : len - 1 - k;
                 const int t = t0 + i;
                 const bool rs = reset_at(t, p.seg_len, dir);
+                const float dt = act ? ld_as_f32(rowv[0] + i) : 0.f;
+                const float xv = act ? ld_as_f32(rowv[1] + i) : 0.f;
+                const float zv = (act && hasZ) ? ld_as_f32(rowv[2] + i) : 0.f;
+                const float go = act ? ld_as_f32(rowv[3] + i) : 0.f;
                 float g = 1.f, gp = 0.f;
                 if (hasZ) {
-                    const float sg = __frcp_rn(1.f + ex2_mufu(-kLog2e * zv[k]));
-                    g = zv[k] * sg;
-                    gp = sg * fmaf(zv[k], 1.f - sg, 1.f);
+                    const float sgm = __frcp_rn(1.f + ex2_mufu(-kLog2e * zv));
+                    g = zv * sgm;
+                    gp = sgm * fmaf(zv, 1.f - sgm, 1.f);
                 }
-                const float ds = go[k] * g;
-                const float *Bt = bc + i * 32, *Ct = Bt + 16;
-                float v[32];                            // dB[16], dC[16] contributions
-                float yk = Dk * xv[k], sB = 0.f, sw = 0.f;
-                const float ux = dtv[k] * xv[k];
+                const float ds = go * g;
+                const float ux = dt * xv;
+                const f2 dsv = pack2(ds, ds), uxv = pack2(ux, ux), dd = pack2(dt, dt);
+                const f2 lmd = rs ? pack2(-INFINITY, -INFINITY) : pack2(0.f, 0.f);
+                const float *Bt = bc + i * 32;
+                f2 yk2 = pack2(0.f, 0.f), sB2 = pack2(0.f, 0.f), sw2 = pack2(0.f, 0.f);
+                float *trow = tr + (tb & 1) * 32 * TP + lane * TP;
 #pragma unroll
-                for (int n = 0; n < 16; ++n) {
-                    const float hp = hb[(k * 16 + n) * 32 + lane];
-                    const float a = rs ? 0.f : ex2_mufu(dtv[k] * Al2[n]);
-                    yk = fmaf(Ct[n], hn[n], yk);
-                    const float l = fmaf(ds, Ct[n], lam[n]);
-                    v[16 + n] = ds * hn[n];
-                    v[n] = l * ux;
-                    sB = fmaf(l, Bt[n], sB);
-                    const float w = l * a * hp;
-                    sw = fmaf(w, Aa[n], sw);
-                    dA[n] = fmaf(w, dtv[k], dA[n]);
-                    lam[n] = a * l;
-                    hn[n] = hp;
+                for (int q = 0; q < 4; ++q) {
+                    f2 B0, B1, C0, C1, hp0, hp1;
+                    lds2(Bt + 4 * q, B0, B1);
+                    lds2(Bt + 16 + 4 * q, C0, C1);
+                    lds2(my_h + (k * 4 + q) * 128, hp0, hp1);
+                    const f2 e0 = ex2_fma2(dd, Ap[2 * q], lmd), e1 = ex2_fma2(dd, Ap[2 * q + 1], lmd);
+                    const f2 l0 = fma2(dsv, C0, lam[2 * q]), l1 = fma2(dsv, C1, lam[2 * q + 1]);
+                    yk2 = fma2(C0, hn[2 * q], yk2);
+                    yk2 = fma2(C1, hn[2 * q + 1], yk2);
+                    sts2(trow + 16 + 4 * q, mul2(dsv, hn[2 * q]), mul2(dsv, hn[2 * q + 1]));   // dC
+                    sts2(trow + 4 * q, mul2(l0, uxv), mul2(l1, uxv));                         // dB
+                    sB2 = fma2(l0, B0, sB2);
+                    sB2 = fma2(l1, B1, sB2);
+                    const f2 w0 = mul2(mul2(l0, e0), hp0), w1 = mul2(mul2(l1, e1), hp1);
+                    sw2 = fma2(w0, Aa[2 * q], sw2);
+                    sw2 = fma2(w1, Aa[2 * q + 1], sw2);
+                    dA[2 * q] = fma2(w0, dd, dA[2 * q]);
+                    dA[2 * q + 1] = fma2(w1, dd, dA[2 * q + 1]);
+                    lam[2 * q] = mul2(e0, l0);
+                    lam[2 * q + 1] = mul2(e1, l1);
+                    hn[2 * q] = hp0;
+                    hn[2 * q + 1] = hp1;
                 }
-                dD = fmaf(ds, xv[k], dD);
-                float gx = fmaf(ds, Dk, dtv[k] * sB);
-                float gdt = fmaf(xv[k], sB, sw);
-                float gz = go[k] * gp * yk;
-                // dB, dC: sum over the warp's channels, then one atomic per lane
-                if (!act) {
-#pragma unroll
-                    for (int n = 0; n < 32; ++n) v[n] = 0.f;
-                }
-                reduce_scatter32(v, lane);
-                float *dst = lane < 16 ? dBk + bcrow + (long long)t * 16 + lane
-                                       : dCk + bcrow + (long long)t * 16 + (lane - 16);
-                atomicAdd(dst, v[0]);
+                const float2 yv = unpack2(yk2), sBv = unpack2(sB2), swv = unpack2(sw2);
+                const float yk = fmaf(Dk, xv, yv.x + yv.y), sB = sBv.x + sBv.y, sw = swv.x + swv.y;
+                dD = fmaf(ds, xv, dD);
+                float gx = fmaf(ds, Dk, dt * sB);
+                float gdt = fmaf(xv, sB, sw);
+                float gz = go * gp * yk;
+                // dB, dC of the previous token: sum of column `lane` of its
+                // buffer over the warp's channels (rows of idle lanes hold
+                // zeros); this token's buffer is summed at the next one
+                __syncwarp();
+                if (tprev >= 0) column_sum_add<TP>(tr + ((tb - 1) & 1) * 32 * TP, lane, dBk, dCk, bcrow, tprev);
+                __syncwarp();                     // that buffer is written again at the next token
+                tprev = t;
+                ++tb;
                 // per-token gradients of x, delta, z
-                float *pp = (DIRS == 3) ? p.part + ((grp * p.L + t) * 3) * 32 + lane : nullptr;
                 if (!fin) {
+                    float *pp = p.part + ((grp * p.L + t) * 3) * 32 + lane;
                     pp[0] = gx;
                     pp[32] = gdt;
                     pp[64] = gz;
                 } else if (act) {
                     if (DIRS == 3) {
-                        gx += __ldcg(pp);
-                        gdt += __ldcg(pp + 32);
-                        gz += __ldcg(pp + 64);
+                        gx += pt[(i * 3 + 0) * 32 + lane];
+                        gdt += pt[(i * 3 + 1) * 32 + lane];
+                        gz += pt[(i * 3 + 2) * 32 + lane];
                     }
-                    st_from_f32(static_cast<T *>(p.dx) + row + t, gx);
-                    st_from_f32(static_cast<T *>(p.ddelta) + row + t, gdt);
-                    if (hasZ) st_from_f32(static_cast<T *>(p.dz) + row + t, gz);
+                    const long long e = erow + t;
+                    st_from_f32(static_cast<T *>(p.dx) + e, gx);
+                    st_from_f32(static_cast<T *>(p.ddelta) + e, gdt);
+                    if (hasZ) st_from_f32(static_cast<T *>(p.dz) + e, gz);
                 }
             }
             __syncwarp();
+            {
+                int jn;
+                if (chunk_of(phase, s + 2, jn)) issue(st, jn, fin);
+                else cp_async_commit();
+            }
+            if (s == nk - 1 && tprev >= 0) {  // the phase's last token
+                column_sum_add<TP>(tr + ((tb - 1) & 1) * 32 * TP, lane, dBk, dCk, bcrow, tprev);
+                tprev = -1;
+                __syncwarp();
+            }
         }
+        cp_async_wait<0>();
         if (DIRS == 3 && phase == 0) {
             __threadfence();
             __syncwarp();
@@ -340,9 +488,14 @@ grad_adjoint_kernel(const GradParams p)
             }
         }
     }
+    cp_async_wait<0>();
     if (act && ok) {
 #pragma unroll
-        for (int n = 0; n < 16; ++n) atomicAdd(p.dA[dir] + (long long)d * 16 + n, dA[n]);
+        for (int q = 0; q < 8; ++q) {
+            const float2 v = unpack2(dA[q]);
+            atomicAdd(p.dA[dir] + (long long)d * 16 + 2 * q, v.x);
+            atomicAdd(p.dA[dir] + (long long)d * 16 + 2 * q + 1, v.y);
+        }
         atomicAdd(p.dD[dir] + d, dD);
     }
 }

@@ -276,8 +276,8 @@ typedef struct {
  */
 int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len, void *stream);
 
-/* Workspace bytes of vssm_scan_grad: 8 bytes per token, channel and
- * direction for the state checkpoints (16 fp32 every 8 tokens), plus 12 bytes
+/* Workspace bytes of vssm_scan_grad: 16 bytes per token, channel and
+ * direction for the state checkpoints (16 fp32 every 4 tokens), plus 12 bytes
  * per token and channel for the partial gradients exchanged between the two
  * directions (both directions only), channels rounded up to groups of 32. */
 int vssm_scan_grad_workspace_size(const vssm_scan_args *a, int seg_len, size_t *bytes);

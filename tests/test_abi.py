@@ -225,12 +225,12 @@ def test_grad_workspace_size(v):
     a = _args(v, batch=1, dim=384, seqlen=197, dtype=0)
     n = ctypes.c_size_t()
     assert v.lib.vssm_scan_grad_workspace_size(ctypes.byref(a), 0, ctypes.byref(n)) == 0
-    # checkpoints: 2 directions x 12 groups x 25 chunks of 8 tokens x 16 x 32 floats,
+    # checkpoints: 2 directions x 12 groups x 50 chunks of 4 tokens x 16 x 32 floats,
     # then partial dx, ddelta, dz: 12 groups x 197 tokens x 3 x 32 floats
-    assert n.value == 2 * 12 * 25 * 512 * 4 + 12 * 197 * 96 * 4
+    assert n.value == 2 * 12 * 50 * 512 * 4 + 12 * 197 * 96 * 4
     a1 = _args(v, batch=1, dim=384, seqlen=197, dtype=0, dir_flags=1)
     assert v.lib.vssm_scan_grad_workspace_size(ctypes.byref(a1), 0, ctypes.byref(n)) == 0
-    assert n.value == 12 * 25 * 512 * 4
+    assert n.value == 12 * 50 * 512 * 4
 
 
 def test_grad_validation(v):
