@@ -33,6 +33,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libvssm.so"
 EXPORTS = ["vssm_scan_bidir", "vssm_scan_bidir_noalloc", "vssm_scan_folded",
            "vssm_scan_chunked", "vssm_scan_workspace_size", "vssm_scan_chunked_workspace_size",
            "vssm_scan_plan_query", "vssm_scan_grad", "vssm_scan_grad_workspace_size",
+           "vssm_selftest_wait_timeout",
            "vssm_device_error", "vssm_status_string", "vssm_last_error", "vssm_version"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -94,6 +95,8 @@ def _load():
     lib.vssm_scan_plan_query.restype = ctypes.c_int
     lib.vssm_scan_grad.argtypes = [P, ctypes.POINTER(GradArgs), ctypes.c_int, ctypes.c_void_p]
     lib.vssm_scan_grad.restype = ctypes.c_int
+    lib.vssm_selftest_wait_timeout.argtypes = [ctypes.c_uint, ctypes.c_void_p]
+    lib.vssm_selftest_wait_timeout.restype = ctypes.c_int
     lib.vssm_scan_grad_workspace_size.argtypes = [P, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
     lib.vssm_scan_grad_workspace_size.restype = ctypes.c_int
     lib.vssm_status_string.argtypes = [ctypes.c_int]

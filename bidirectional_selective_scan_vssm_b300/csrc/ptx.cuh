@@ -62,13 +62,14 @@ __device__ __forceinline__ uint64_t global_timer_ns()
 }
 
 // Bounded wait on an mbarrier phase. Returns false if the phase has not
-// completed within limit_ns (the caller then reports a timeout and stops).
+// completed within limit_ns, or after 2^28 polls whatever the timer says (the
+// caller then reports a timeout and stops).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > limit_ns) return false;
+    for (uint32_t polls = 0; !mbar_try_wait(bar, parity); ++polls) {
+        if (global_timer_ns() - t0 > limit_ns || polls >= (1u << 28)) return false;
     }
     return true;
 }

@@ -687,6 +687,18 @@ int vssm_scan_plan_query(const vssm_scan_args *a, int seg_len, int pieces, int *
 
 int vssm_scan_bidir(const vssm_scan_args *a, void *stream) { return run(a, 0, false, 0, stream); }
 
+int vssm_selftest_wait_timeout(unsigned limit_us, void *stream)
+{
+    if (limit_us < 1 || limit_us > 1000000)
+        return fail(VSSM_ERR_INVALID_ARG, "limit_us=%u outside 1..1000000", limit_us);
+    unsigned *err = device_error_word();
+    if (!err) return fail(VSSM_ERR_CUDA, "cannot locate the device error word");
+    vssm::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        err, (uint64_t)limit_us * 1000ull);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? VSSM_OK : fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+}
+
 int vssm_scan_grad_workspace_size(const vssm_scan_args *a, int seg_len, size_t *bytes)
 {
     if (!a || !bytes) return fail(VSSM_ERR_INVALID_ARG, "args or bytes is NULL");

@@ -291,6 +291,17 @@ int vssm_scan_grad_workspace_size(const vssm_scan_args *a, int seg_len, size_t *
  */
 int vssm_device_error(void *stream);
 
+/*
+ * Test of the timeout path, for callers' own failure-handling tests: runs one
+ * warp that waits on a pair barrier whose second arrival never comes. The
+ * wait gives up after limit_us microseconds (1..1000000, else
+ * VSSM_ERR_INVALID_ARG) and records a timeout in the device error word
+ * exactly as the scan kernels do, so that the next vssm_device_error on that
+ * stream returns VSSM_ERR_TIMEOUT. Nothing traps, faults or hangs; the device
+ * stays usable. Asynchronous on `stream`.
+ */
+int vssm_selftest_wait_timeout(unsigned limit_us, void *stream);
+
 /* Static text for a vssm_status value. */
 const char *vssm_status_string(int status);
 
