@@ -33,7 +33,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libvssm.so"
 EXPORTS = ["vssm_scan_bidir", "vssm_scan_bidir_noalloc", "vssm_scan_folded",
            "vssm_scan_chunked", "vssm_scan_workspace_size", "vssm_scan_chunked_workspace_size",
            "vssm_scan_plan_query", "vssm_scan_grad", "vssm_scan_grad_workspace_size",
-           "vssm_selftest_wait_timeout",
+           "vssm_selftest_wait_timeout", "vssm_scan_host", "vssm_scan_host_workspace_size",
            "vssm_device_error", "vssm_status_string", "vssm_last_error", "vssm_version"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -95,6 +95,11 @@ def _load():
     lib.vssm_scan_plan_query.restype = ctypes.c_int
     lib.vssm_scan_grad.argtypes = [P, ctypes.POINTER(GradArgs), ctypes.c_int, ctypes.c_void_p]
     lib.vssm_scan_grad.restype = ctypes.c_int
+    lib.vssm_scan_host.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    lib.vssm_scan_host.restype = ctypes.c_int
+    lib.vssm_scan_host_workspace_size.argtypes = [P, ctypes.c_int, ctypes.c_int,
+                                                  ctypes.POINTER(ctypes.c_size_t)]
+    lib.vssm_scan_host_workspace_size.restype = ctypes.c_int
     lib.vssm_selftest_wait_timeout.argtypes = [ctypes.c_uint, ctypes.c_void_p]
     lib.vssm_selftest_wait_timeout.restype = ctypes.c_int
     lib.vssm_scan_grad_workspace_size.argtypes = [P, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
@@ -345,6 +350,70 @@ def scan_grad(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *, d
         a.workspace_bytes = workspace.numel() * workspace.element_size()
     _check(lib.vssm_scan_grad(ctypes.byref(a), ctypes.byref(g), int(seg_len),
                               ctypes.c_void_p(stream.cuda_stream)))
+    return out
+
+
+def _host_tensor(name, t, dtype=None, shape=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError(f"{name} must be a host (CPU) tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def scan_host(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *, out=None,
+              dirs: int = DIR_BOTH, seg_len: int = 0, slices: int = 0, B_bwd=None, C_bwd=None,
+              device=None, stream: Optional[torch.cuda.Stream] = None, workspace=None,
+              sync: bool = True) -> torch.Tensor:
+    """``vssm_scan_host``: the scan with every tensor in host memory (use
+    page-locked tensors, ``pin_memory()``, for overlapped copies); the output
+    is written to the host tensor ``out`` (allocated here, pinned, when not
+    given). The device workspace comes from ``workspace`` or the per-stream
+    cache. With ``sync`` the call waits for the stream before returning."""
+    batch, dim, L = x.shape
+    N = B.shape[-1]
+    dt = x.dtype
+    if dt not in (torch.float32, torch.bfloat16):
+        raise TypeError("x must be float32 or bfloat16")
+    for n, t in (("x", x), ("delta", delta), ("z", z)):
+        _host_tensor(n, t, dt, (batch, dim, L))
+    for n, t in (("B", B), ("C", C), ("B_bwd", B_bwd), ("C_bwd", C_bwd)):
+        _host_tensor(n, t, dt, (batch, L, N))
+    for n, t in (("A_fwd", A_fwd), ("A_bwd", A_bwd)):
+        _host_tensor(n, t, torch.float32, (dim, N))
+    for n, t in (("D_fwd", D_fwd), ("D_bwd", D_bwd)):
+        _host_tensor(n, t, torch.float32, (dim,))
+    if out is None:
+        out = torch.empty_like(x).pin_memory()
+    _host_tensor("out", out, dt, (batch, dim, L))
+    a = ScanArgs()
+    a.x, a.delta, a.z = _ptr(x), _ptr(delta), _ptr(z)
+    a.B, a.C, a.B_bwd, a.C_bwd = _ptr(B), _ptr(C), _ptr(B_bwd), _ptr(C_bwd)
+    a.A_fwd, a.A_bwd, a.D_fwd, a.D_bwd = _ptr(A_fwd), _ptr(A_bwd), _ptr(D_fwd), _ptr(D_bwd)
+    a.out = _ptr(out)
+    a.batch, a.dim, a.seqlen, a.dstate = batch, dim, L, N
+    a.dtype = VSSM_F32 if dt == torch.float32 else VSSM_BF16
+    a.dir_flags = dirs
+    device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    stream = stream if stream is not None else torch.cuda.current_stream(device)
+    n = ctypes.c_size_t(0)
+    _check(lib.vssm_scan_host_workspace_size(ctypes.byref(a), int(seg_len), int(slices), ctypes.byref(n)))
+    if workspace is None:
+        workspace = _workspace(device, stream, int(n.value))
+    if workspace is not None:
+        a.workspace = workspace.data_ptr()
+        a.workspace_bytes = workspace.numel() * workspace.element_size()
+    with torch.cuda.device(device):
+        _check(lib.vssm_scan_host(ctypes.byref(a), int(seg_len), int(slices),
+                                  ctypes.c_void_p(stream.cuda_stream)))
+    if sync:
+        stream.synchronize()
     return out
 
 

@@ -633,6 +633,239 @@ int launch_grad_dirs(const vssm::GradParams &p, const GradPlan &g, int dirs, cud
     }
 }
 
+
+// ---- host-buffer pipeline (vssm_scan_host)
+
+// Streams and events of the pipeline, created once per device and kept for
+// the life of the process; calls on one device take the mutex while they
+// enqueue, so that two calls never interleave their use of the events.
+constexpr int kHostRing = 3;           // device slots in flight
+struct HostPipe {
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t copy = nullptr, comp = nullptr, back = nullptr;
+    cudaEvent_t fork = nullptr, params = nullptr, join = nullptr;
+    cudaEvent_t in[kHostRing] = {}, done[kHostRing] = {}, out[kHostRing] = {};
+};
+
+HostPipe *host_pipe(int *status)
+{
+    static std::mutex mu;
+    static HostPipe *pipes[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        *status = fail(VSSM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!pipes[dev]) {
+        HostPipe *hp = new HostPipe;
+        const unsigned sf = cudaStreamNonBlocking, ef = cudaEventDisableTiming;
+        e = cudaStreamCreateWithFlags(&hp->copy, sf);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp->comp, sf);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp->back, sf);
+        cudaEvent_t *evs[] = {&hp->fork, &hp->params, &hp->join};
+        for (cudaEvent_t *ev : evs)
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, ef);
+        for (int i = 0; i < kHostRing && e == cudaSuccess; ++i) {
+            e = cudaEventCreateWithFlags(&hp->in[i], ef);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp->done[i], ef);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp->out[i], ef);
+        }
+        if (e != cudaSuccess) {
+            *status = fail(VSSM_ERR_CUDA, "creating the pipeline's streams: %s", cudaGetErrorString(e));
+            return nullptr;      // (the partial objects are kept; nothing else uses them)
+        }
+        hp->ready = true;
+        pipes[dev] = hp;
+    }
+    return pipes[dev];
+}
+
+// How a host-pipeline call is cut: whole batch entries per slice when there
+// are at least as many entries as slices, else channel ranges (multiples of
+// 32) of one batch entry each.
+struct HostCut {
+    bool by_batch = true;
+    int per_b = 1;           // batch entries per slice (by_batch)
+    int per_d = 0;           // channels per slice (!by_batch)
+    int nslices = 0;
+    size_t slot_bytes = 0;   // one ring slot
+    size_t ws_off = 0;       // scan workspace within a slot
+    size_t up_bytes = 0;     // B, C and per-channel parameters
+    size_t total = 0;
+};
+
+size_t al256(size_t n) { return (n + 255) / 256 * 256; }
+
+int host_cut(const vssm_scan_args *a, int seg_len, int slices, HostCut *c)
+{
+    if (slices < 0) return fail(VSSM_ERR_INVALID_ARG, "slices=%d must be >= 0", slices);
+    const int S = slices == 0 ? 8 : slices;
+    const size_t es = a->dtype == VSSM_F32 ? 4 : 2;
+    const size_t L = (size_t)a->seqlen, N = (size_t)a->dstate, D = (size_t)a->dim;
+    c->by_batch = a->batch >= S;
+    int rows_b = 1, rows_d = a->dim;
+    if (c->by_batch) {
+        c->per_b = (a->batch + S - 1) / S;
+        c->nslices = (a->batch + c->per_b - 1) / c->per_b;
+        rows_b = c->per_b;
+    } else {
+        const int per_entry = std::max(1, (S + a->batch - 1) / std::max(1, a->batch));
+        c->per_d = std::max(32, ((a->dim + per_entry - 1) / per_entry + 31) / 32 * 32);
+        const int nd = (a->dim + c->per_d - 1) / c->per_d;
+        c->nslices = a->batch * nd;
+        rows_d = c->per_d;
+    }
+    // a slot: x, delta, z, delta_bwd, out of one slice, then its scan workspace
+    const size_t act = al256((size_t)rows_b * rows_d * L * es);
+    // the scan workspace of the largest slice and of the last (smaller) one:
+    // a smaller slice may be planned differently
+    vssm_scan_args sub = *a;
+    sub.batch = rows_b;
+    sub.dim = std::min(rows_d, a->dim);
+    Plan pl;
+    make_plan(&sub, seg_len, 0, &pl);
+    size_t ws = pl.workspace;
+    if (c->by_batch) {
+        sub.batch = a->batch - (c->nslices - 1) * c->per_b;
+    } else {
+        const int last = a->dim % c->per_d;
+        sub.dim = last ? last : c->per_d;
+    }
+    Plan pl2;
+    make_plan(&sub, seg_len, 0, &pl2);
+    ws = std::max(ws, pl2.workspace);
+    c->ws_off = 5 * act;
+    c->slot_bytes = al256(c->ws_off + ws);
+    // up front: B, C (and the backward ones), A, D, biases, convolution
+    const size_t bc = al256((size_t)a->batch * L * N * es);
+    const size_t par = al256(D * N * 4), vec = al256(D * 4), cw = al256(D * (size_t)std::max(1, a->conv_k) * 4);
+    c->up_bytes = 4 * bc + 2 * par + 4 * vec + 2 * vec + 2 * cw;
+    c->total = c->up_bytes + (size_t)kHostRing * c->slot_bytes;
+    return VSSM_OK;
+}
+
+int host_scan(const vssm_scan_args *a, int seg_len, int slices, void *stream)
+{
+    const bool folded = seg_len > 0;
+    int st = validate(a, seg_len, folded);
+    if (st != VSSM_OK) return st;
+    if ((long long)a->batch * a->dim * a->seqlen == 0) return VSSM_OK;
+    HostCut c;
+    if ((st = host_cut(a, seg_len, slices, &c)) != VSSM_OK) return st;
+    if (!a->workspace || a->workspace_bytes < c.total)
+        return fail(VSSM_ERR_WORKSPACE, "device workspace of %zu bytes required, %zu given", c.total,
+                    a->workspace ? a->workspace_bytes : (size_t)0);
+    HostPipe *hp = host_pipe(&st);
+    if (!hp) return st;
+    std::lock_guard<std::mutex> lock(hp->mu);
+    cudaStream_t user = static_cast<cudaStream_t>(stream);
+    const size_t es = a->dtype == VSSM_F32 ? 4 : 2;
+    const size_t L = (size_t)a->seqlen, N = (size_t)a->dstate, D = (size_t)a->dim;
+    char *w = static_cast<char *>(a->workspace);
+    cudaError_t e = cudaSuccess;
+    auto h2d = [&](void *dst, const void *src, size_t n) {
+        if (e == cudaSuccess && src && n) e = cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, hp->copy);
+    };
+    // up-front copies
+    const size_t bc = al256((size_t)a->batch * L * N * es);
+    const size_t par = al256(D * N * 4), vec = al256(D * 4), cw = al256(D * (size_t)std::max(1, a->conv_k) * 4);
+    char *up = w;
+    char *dB = up, *dC = up + bc, *dBb = up + 2 * bc, *dCb = up + 3 * bc;
+    char *dAf = up + 4 * bc, *dAb = dAf + par, *dDf = dAb + par, *dDb = dDf + vec;
+    char *dbf = dDb + vec, *dbb = dbf + vec, *dcwf = dbb + vec, *dcwb = dcwf + cw, *dcbf = dcwb + cw,
+         *dcbb = dcbf + vec;
+    e = cudaEventRecord(hp->fork, user);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->copy, hp->fork, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->comp, hp->fork, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->back, hp->fork, 0);
+    const size_t nbc = (size_t)a->batch * L * N * es;
+    h2d(dB, a->B, nbc);
+    h2d(dC, a->C, nbc);
+    h2d(dBb, a->B_bwd, nbc);
+    h2d(dCb, a->C_bwd, nbc);
+    h2d(dAf, a->A_fwd, D * N * 4);
+    h2d(dAb, a->A_bwd, D * N * 4);
+    h2d(dDf, a->D_fwd, D * 4);
+    h2d(dDb, a->D_bwd, D * 4);
+    h2d(dbf, a->delta_bias, D * 4);
+    h2d(dbb, a->delta_bias_bwd, D * 4);
+    h2d(dcwf, a->conv_w, D * a->conv_k * 4);
+    h2d(dcwb, a->conv_w_bwd, D * a->conv_k * 4);
+    h2d(dcbf, a->conv_b, D * 4);
+    h2d(dcbb, a->conv_b_bwd, D * 4);
+    if (e == cudaSuccess) e = cudaEventRecord(hp->params, hp->copy);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->comp, hp->params, 0);
+    if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "pipeline set-up: %s", cudaGetErrorString(e));
+    const size_t act = c.ws_off / 5;
+    const int nd_per_b = c.by_batch ? 1 : (a->dim + c.per_d - 1) / c.per_d;
+    for (int k = 0; k < c.nslices; ++k) {
+        const int sl = k % kHostRing;
+        char *slot = w + c.up_bytes + (size_t)sl * c.slot_bytes;
+        int b0, nb, d0, nd;
+        if (c.by_batch) {
+            b0 = k * c.per_b;
+            nb = std::min(c.per_b, a->batch - b0);
+            d0 = 0;
+            nd = a->dim;
+        } else {
+            b0 = k / nd_per_b;
+            nb = 1;
+            d0 = (k % nd_per_b) * c.per_d;
+            nd = std::min(c.per_d, a->dim - d0);
+        }
+        const size_t off = ((size_t)b0 * D + d0) * L * es;           // first element of the slice
+        const size_t n = (size_t)nb * nd * L * es;                     // contiguous bytes
+        char *sx = slot, *sdt = slot + act, *sz = slot + 2 * act, *sdb = slot + 3 * act, *so = slot + 4 * act;
+        if (k >= kHostRing && e == cudaSuccess) e = cudaStreamWaitEvent(hp->copy, hp->out[sl], 0);
+        h2d(sx, static_cast<const char *>(a->x) + off, n);
+        h2d(sdt, static_cast<const char *>(a->delta) + off, n);
+        if (a->z) h2d(sz, static_cast<const char *>(a->z) + off, n);
+        if (a->delta_bwd) h2d(sdb, static_cast<const char *>(a->delta_bwd) + off, n);
+        if (e == cudaSuccess) e = cudaEventRecord(hp->in[sl], hp->copy);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->comp, hp->in[sl], 0);
+        if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "pipeline copy: %s", cudaGetErrorString(e));
+        vssm_scan_args sub = *a;
+        const size_t bo = (size_t)b0 * L * N * es;
+        sub.x = sx;
+        sub.delta = sdt;
+        sub.z = a->z ? sz : nullptr;
+        sub.delta_bwd = a->delta_bwd ? sdb : nullptr;
+        sub.B = dB + bo;
+        sub.C = dC + bo;
+        sub.B_bwd = a->B_bwd ? dBb + bo : nullptr;
+        sub.C_bwd = a->C_bwd ? dCb + bo : nullptr;
+        sub.A_fwd = a->A_fwd ? reinterpret_cast<const float *>(dAf) + (size_t)d0 * N : nullptr;
+        sub.A_bwd = a->A_bwd ? reinterpret_cast<const float *>(dAb) + (size_t)d0 * N : nullptr;
+        sub.D_fwd = a->D_fwd ? reinterpret_cast<const float *>(dDf) + d0 : nullptr;
+        sub.D_bwd = a->D_bwd ? reinterpret_cast<const float *>(dDb) + d0 : nullptr;
+        sub.delta_bias = a->delta_bias ? reinterpret_cast<const float *>(dbf) + d0 : nullptr;
+        sub.delta_bias_bwd = a->delta_bias_bwd ? reinterpret_cast<const float *>(dbb) + d0 : nullptr;
+        sub.conv_w = a->conv_w ? reinterpret_cast<const float *>(dcwf) + (size_t)d0 * a->conv_k : nullptr;
+        sub.conv_w_bwd = a->conv_w_bwd ? reinterpret_cast<const float *>(dcwb) + (size_t)d0 * a->conv_k : nullptr;
+        sub.conv_b = a->conv_b ? reinterpret_cast<const float *>(dcbf) + d0 : nullptr;
+        sub.conv_b_bwd = a->conv_b_bwd ? reinterpret_cast<const float *>(dcbb) + d0 : nullptr;
+        sub.out = so;
+        sub.workspace = slot + c.ws_off;
+        sub.workspace_bytes = c.slot_bytes - c.ws_off;
+        sub.batch = nb;
+        sub.dim = nd;
+        st = run(&sub, seg_len, folded, 0, hp->comp);
+        if (st != VSSM_OK) return st;
+        e = cudaEventRecord(hp->done[sl], hp->comp);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->back, hp->done[sl], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<char *>(a->out) + off, so, n, cudaMemcpyDeviceToHost, hp->back);
+        if (e == cudaSuccess) e = cudaEventRecord(hp->out[sl], hp->back);
+        if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "pipeline step: %s", cudaGetErrorString(e));
+    }
+    e = cudaEventRecord(hp->join, hp->back);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(user, hp->join, 0);
+    if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "pipeline join: %s", cudaGetErrorString(e));
+    return VSSM_OK;
+}
 }  // namespace
 
 extern "C" {
@@ -686,6 +919,28 @@ int vssm_scan_plan_query(const vssm_scan_args *a, int seg_len, int pieces, int *
 }
 
 int vssm_scan_bidir(const vssm_scan_args *a, void *stream) { return run(a, 0, false, 0, stream); }
+
+int vssm_scan_host_workspace_size(const vssm_scan_args *a, int seg_len, int slices, size_t *bytes)
+{
+    if (!a || !bytes) return fail(VSSM_ERR_INVALID_ARG, "args or bytes is NULL");
+    if (a->batch < 0 || a->dim < 0 || a->seqlen < 0 || a->dir_flags < 1 || a->dir_flags > 3 ||
+        seg_len < 0 || a->conv_k < 0 || a->conv_k > vssm::kMaxConv)
+        return fail(VSSM_ERR_INVALID_ARG, "invalid sizes, dir_flags or conv_k");
+    if ((long long)a->batch * a->dim * a->seqlen == 0) {
+        *bytes = 0;
+        return VSSM_OK;
+    }
+    HostCut c;
+    const int st = host_cut(a, seg_len, slices, &c);
+    if (st != VSSM_OK) return st;
+    *bytes = c.total;
+    return VSSM_OK;
+}
+
+int vssm_scan_host(const vssm_scan_args *a, int seg_len, int slices, void *stream)
+{
+    return host_scan(a, seg_len, slices, stream);
+}
 
 int vssm_selftest_wait_timeout(unsigned limit_us, void *stream)
 {

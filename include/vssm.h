@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define VSSM_VERSION 140 /* 1.4.0 */
+#define VSSM_VERSION 150 /* 1.5.0 */
 
 typedef enum {
     VSSM_OK = 0,
@@ -290,6 +290,32 @@ int vssm_scan_grad_workspace_size(const vssm_scan_args *a, int seg_len, size_t *
  * kernels never trap and never spin without a limit.
  */
 int vssm_device_error(void *stream);
+
+/*
+ * The scan of vssm_scan_bidir (seg_len == 0) or vssm_scan_folded (seg_len >=
+ * 1) with every tensor of `a` in HOST memory (page-locked host memory lets
+ * the copies overlap; pageable memory works but serialises them) and the
+ * output written back to host memory. The library has no counterpart on the
+ * pages: it moves the data for callers whose inputs live on the host.
+ *
+ * The call is cut into `slices` parts (0 = 8): whole batch entries per slice
+ * when batch >= slices, else channel ranges (multiples of 32) of one batch
+ * entry. B, C and the per-channel parameters are copied first; then, through
+ * a ring of three device slots, each slice's x, delta (z, delta_bwd) are
+ * copied in on one stream, scanned on a second and its output copied back on
+ * a third, so that the copies in both directions overlap the scans of other
+ * slices. a->workspace is DEVICE memory of vssm_scan_host_workspace_size
+ * bytes (it holds the slots and the scans' own workspaces); the other
+ * pointers of `a` are host pointers, 16-byte aligned. Asynchronous on
+ * `stream` (the internal streams fork from it and join back); the output is
+ * complete when `stream` reaches the point after the call. Calls on one
+ * device serialise their enqueueing. Errors as vssm_scan_bidir; slices < 0
+ * gives VSSM_ERR_INVALID_ARG.
+ */
+int vssm_scan_host(const vssm_scan_args *a, int seg_len, int slices, void *stream);
+
+/* Device workspace bytes of vssm_scan_host with these seg_len and slices. */
+int vssm_scan_host_workspace_size(const vssm_scan_args *a, int seg_len, int slices, size_t *bytes);
 
 /*
  * Test of the timeout path, for callers' own failure-handling tests: runs one
