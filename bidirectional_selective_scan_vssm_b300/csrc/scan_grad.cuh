@@ -165,21 +165,18 @@ struct GradLayout {
     static constexpr int sB = sROW + 4 * ROWS;
     static constexpr int sC = sB + kTG * 16 * ES;
     static constexpr int sCK = sC + kTG * 16 * ES;
-    static constexpr int sPT = sCK + 512 * 4;
-    static constexpr int kStage = sPT + (BIDIR ? kTG * 96 * 4 : 0);
+    static constexpr int kStage = sCK + 512 * 4;
     // per warp: 2 stages, then
     //   hb  [kTG + 1][4][32 lanes][4] states (quarter q of a lane's 16 states;
     //                                 a warp's access to one quarter is 512
     //                                 contiguous bytes)
     //   bc  [kTG][32]                 B[16], C[16] of each token, fp32
-    //   tr  [2][32 lanes][kTP]        per-token dB, dC contributions, transposed
-    //                                 (double-buffered: a token's column sums
-    //                                 run while the next token is computed)
+    //   tr  [32 lanes][kTP]           per-token dB, dC contributions, transposed
     static constexpr int kTP = 36;
     static constexpr int oHB = 2 * kStage;
     static constexpr int oBC = oHB + (kTG + 1) * 4 * 32 * 16;
     static constexpr int oTR = oBC + kTG * 32 * 4;              // two buffers
-    static constexpr int kWarpBytes = oTR + 2 * 32 * kTP * 4 + 16;   // + pair barrier
+    static constexpr int kWarpBytes = oTR + 32 * kTP * 4 + 16;   // + pair barrier
     static_assert(kStage % 16 == 0 && oHB % 16 == 0 && oTR % 16 == 0, "alignment");
     // CTAs per SM that shared memory allows (228 KB, 1 KB reserved per CTA)
     static constexpr int kPerSm = (228 * 1024) / ((BIDIR ? 2 : 1) * kWarpBytes + 1024);
@@ -305,21 +302,11 @@ grad_adjoint_kernel(const GradParams p)
 #pragma unroll
             for (int m = 0; m < 4; ++m) cp_async16(sg + Lay::sCK + 16 * (lane + 32 * m), src + 16 * (lane + 32 * m), 16u);
         }
-        if (DIRS == 3 && fin) {   // the partner's partial gradients of these tokens
-            const char *src = reinterpret_cast<const char *>(p.part + (grp * p.L + t0) * 96);
-            const int nb = len * 24;                  // 384 bytes per token
-#pragma unroll
-            for (int m = 0; m < kTG * 24 / 32; ++m) {
-                const int jj = lane + 32 * m;
-                cp_async16_if(sg + Lay::sPT + 16 * jj, src + 16 * jj, jj < nb);
-            }
-        }
         cp_async_commit();
     };
 
     bool ok = true;
     int ring = 0;
-    int tb = 0, tprev = -1;                   // tr buffer count, token of the pending column sum
     for (int phase = 0; phase < nphase && ok; ++phase) {
         const bool fin = phase == nphase - 1;
         const int nk = nchunks(phase);
@@ -385,7 +372,6 @@ grad_adjoint_kernel(const GradParams p)
             f2 hn[8];
 #pragma unroll
             for (int q = 0; q < 4; ++q) lds2(my_h + (len * 4 + q) * 128, hn[2 * q], hn[2 * q + 1]);
-            const float *pt = reinterpret_cast<const float *>(sg + Lay::sPT);
 #pragma unroll 1
             for (int k = len - 1; k >= 0; --k) {
                 const int i = dir == 0 ? k : len - 1 - k;
@@ -395,6 +381,14 @@ grad_adjoint_kernel(const GradParams p)
                 const float xv = act ? ld_as_f32(rowv[1] + i) : 0.f;
                 const float zv = (act && hasZ) ? ld_as_f32(rowv[2] + i) : 0.f;
                 const float go = act ? ld_as_f32(rowv[3] + i) : 0.f;
+                // the partner's partials of this token (phase 1), loaded early
+                float px = 0.f, pdt = 0.f, pz = 0.f;
+                if (DIRS == 3 && fin && act) {
+                    const float *pp = p.part + ((grp * p.L + t) * 3) * 32 + lane;
+                    px = __ldcg(pp);
+                    pdt = __ldcg(pp + 32);
+                    pz = __ldcg(pp + 64);
+                }
                 float g = 1.f, gp = 0.f;
                 if (hasZ) {
                     const float sgm = __frcp_rn(1.f + ex2_mufu(-kLog2e * zv));
@@ -407,7 +401,7 @@ grad_adjoint_kernel(const GradParams p)
                 const f2 lmd = rs ? pack2(-INFINITY, -INFINITY) : pack2(0.f, 0.f);
                 const float *Bt = bc + i * 32;
                 f2 yk2 = pack2(0.f, 0.f), sB2 = pack2(0.f, 0.f), sw2 = pack2(0.f, 0.f);
-                float *trow = tr + (tb & 1) * 32 * TP + lane * TP;
+                float *trow = tr + lane * TP;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     f2 B0, B1, C0, C1, hp0, hp1;
@@ -438,14 +432,11 @@ grad_adjoint_kernel(const GradParams p)
                 float gx = fmaf(ds, Dk, dt * sB);
                 float gdt = fmaf(xv, sB, sw);
                 float gz = go * gp * yk;
-                // dB, dC of the previous token: sum of column `lane` of its
-                // buffer over the warp's channels (rows of idle lanes hold
-                // zeros); this token's buffer is summed at the next one
+                // dB, dC of the token: sum of column `lane` over the warp's
+                // channels (rows of idle lanes hold zeros)
                 __syncwarp();
-                if (tprev >= 0) column_sum_add<TP>(tr + ((tb - 1) & 1) * 32 * TP, lane, dBk, dCk, bcrow, tprev);
-                __syncwarp();                     // that buffer is written again at the next token
-                tprev = t;
-                ++tb;
+                column_sum_add<TP>(tr, lane, dBk, dCk, bcrow, t);
+                __syncwarp();                     // the buffer is written again at the next token
                 // per-token gradients of x, delta, z
                 if (!fin) {
                     float *pp = p.part + ((grp * p.L + t) * 3) * 32 + lane;
@@ -453,11 +444,9 @@ grad_adjoint_kernel(const GradParams p)
                     pp[32] = gdt;
                     pp[64] = gz;
                 } else if (act) {
-                    if (DIRS == 3) {
-                        gx += pt[(i * 3 + 0) * 32 + lane];
-                        gdt += pt[(i * 3 + 1) * 32 + lane];
-                        gz += pt[(i * 3 + 2) * 32 + lane];
-                    }
+                    gx += px;
+                    gdt += pdt;
+                    gz += pz;
                     const long long e = erow + t;
                     st_from_f32(static_cast<T *>(p.dx) + e, gx);
                     st_from_f32(static_cast<T *>(p.ddelta) + e, gdt);
@@ -470,11 +459,7 @@ grad_adjoint_kernel(const GradParams p)
                 if (chunk_of(phase, s + 2, jn)) issue(st, jn, fin);
                 else cp_async_commit();
             }
-            if (s == nk - 1 && tprev >= 0) {  // the phase's last token
-                column_sum_add<TP>(tr + ((tb - 1) & 1) * 32 * TP, lane, dBk, dCk, bcrow, tprev);
-                tprev = -1;
-                __syncwarp();
-            }
+
         }
         cp_async_wait<0>();
         if (DIRS == 3 && phase == 0) {
