@@ -12,8 +12,8 @@ Contents:
     they follow.
   * ``quadform.py`` -- the SSD page's quadratic (matrix) form, NumPy, used only
     to pin the recurrence on tiny inputs.
-  * ``scan()``, ``scan_grad()`` and ``conv_silu()`` below -- ctypes bindings
-    of the C oracle.
+  * ``scan()``, ``scan_grad()``, ``conv_silu()`` and ``ncssd()`` below --
+    ctypes bindings of the C oracle.
 
 Pins (in ``tests/test_oracle_pins.py``): the quadratic form, a hand-worked
 two-step example from the SSD page's linear-form section, closed forms for
@@ -24,7 +24,8 @@ map against the closed-form inverse of softplus (and softplus(0) = ln 2), the
 per-direction step as a sum of single-direction scans, the directional
 convolution's taps against shifted inputs (forward, backward, across folded
 segment edges) and its feed into each direction, the adjoint gradients
-against central finite differences of the forward oracle, and a mutation test
+against central finite differences of the forward oracle, NC-SSD against the
+VSSD page's matrix form and its token-order independence, and a mutation test
 that plants mistakes in a copy of the C source.
 """
 from __future__ import annotations
@@ -74,6 +75,8 @@ def load_library(path: str):
         ctypes.c_int, ctypes.c_long, ctypes.c_int]
     lib.oracle_scan_grad.restype = ctypes.c_int
     lib.oracle_scan_grad.argtypes = [dp] * 23 + [ctypes.c_long] * 4 + [ctypes.c_int, ctypes.c_long]
+    lib.oracle_ncssd.restype = ctypes.c_int
+    lib.oracle_ncssd.argtypes = [dp] * 7 + [ctypes.c_long] * 4
     lib.oracle_conv_silu.restype = ctypes.c_int
     lib.oracle_conv_silu.argtypes = [dp] * 4 + [ctypes.c_long] * 4 + [ctypes.c_int, ctypes.c_long]
     lib.oracle_max_threads.restype = ctypes.c_int
@@ -145,6 +148,26 @@ def scan(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None,
                          int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_scan rejected its arguments (status {rc})")
+    return out
+
+
+def ncssd(x, B, C, m, D=None, z=None, lib=None) -> np.ndarray:
+    """NC-SSD (C oracle ``oracle_ncssd``): x, z (batch, dim, L); B, C
+    (batch, L, N); m (batch, L) token weights; D (dim,) or None. float64."""
+    lib = lib or _get_lib()
+    x = np.asarray(x)
+    batch, dim, L = x.shape
+    N = np.asarray(B).shape[-1]
+    keep, ptrs = [], []
+    for a in (x, z, B, C, m, D):
+        arr, p = _as_f64(a)
+        keep.append(arr)
+        ptrs.append(p)
+    out = np.empty((batch, dim, L), dtype=np.float64)
+    rc = lib.oracle_ncssd(*ptrs, out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                          batch, dim, L, N)
+    if rc != 0:
+        raise ValueError(f"oracle_ncssd rejected its arguments (status {rc})")
     return out
 
 

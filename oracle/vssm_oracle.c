@@ -419,3 +419,44 @@ int oracle_scan_grad(const double *x, const double *delta, const double *z,
     free(lam);
     return ORACLE_OK;
 }
+
+/*
+ * NC-SSD, the non-causal global-state variant (VSSD page, §4.2.4 and
+ * §4.2.5): every token contributes m_j * B_j x_j^T to one hidden state per
+ * batch entry, shared by all tokens, and each token reads it through C:
+ *
+ *   H[n][d]  = sum_j m[j] * B_j[n] * x[d][j]                (§4.2.4, H = sum_j (1/A_j) Z_j)
+ *   out[d][t] = (sum_n C_t[n] * H[n][d] + D[d] * x[d][t]) * g(z[d][t])
+ *
+ * with m the per-token weights (the page's m_j = 1/A_j, passed in), D the
+ * optional skip (NULL = 0) and g = silu of the optional gate (NULL = 1), as
+ * in the scan. Layouts as oracle_scan; m is [batch][L].
+ */
+int oracle_ncssd(const double *x, const double *z, const double *B, const double *C,
+                 const double *m, const double *D, double *out,
+                 long batch, long dim, long L, long N)
+{
+    if (!x || !B || !C || !m || !out || batch < 0 || dim < 0 || L < 0 || N <= 0)
+        return ORACLE_EINVAL;
+    double *H = (double *)malloc(sizeof(double) * (size_t)N * (size_t)(dim > 0 ? dim : 1));
+    if (!H) return ORACLE_ENOMEM;
+    for (long b = 0; b < batch; ++b) {
+        const double *xb = x + b * dim * L, *Bb = B + b * L * N, *Cb = C + b * L * N;
+        const double *mb = m + b * L;
+        for (long n = 0; n < N; ++n)
+            for (long d = 0; d < dim; ++d) {
+                double h = 0.0;
+                for (long j = 0; j < L; ++j) h += mb[j] * Bb[j * N + n] * xb[d * L + j];
+                H[n * dim + d] = h;
+            }
+        for (long d = 0; d < dim; ++d)
+            for (long t = 0; t < L; ++t) {
+                double y = D ? D[d] * xb[d * L + t] : 0.0;
+                for (long n = 0; n < N; ++n) y += Cb[t * N + n] * H[n * dim + d];
+                const double g = z ? silu(z[(b * dim + d) * L + t]) : 1.0;
+                out[(b * dim + d) * L + t] = y * g;
+            }
+    }
+    free(H);
+    return ORACLE_OK;
+}

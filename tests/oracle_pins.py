@@ -425,12 +425,57 @@ def pin_gradient_finite_differences(lib):
     return ok
 
 
+def _ncssd_problem(rng, b=2, d=5, L=9, N=4):
+    return dict(x=rng.standard_normal((b, d, L)), B=rng.standard_normal((b, L, N)),
+                C=rng.standard_normal((b, L, N)), m=rng.uniform(0.2, 3.0, (b, L)),
+                D=rng.standard_normal(d), z=rng.standard_normal((b, d, L)))
+
+
+def pin_ncssd_matrix_form(lib):
+    """NC-SSD against the VSSD page's simplified form Y = C (B^T (X m))
+    (§4.2.5.2), evaluated with numpy matrix products, plus the skip and the
+    gate: out = (Y + D x) silu(z). With C = 0 only the gated skip remains."""
+    rng = np.random.default_rng(53)
+    p = _ncssd_problem(rng)
+    got = oracle.ncssd(p["x"], p["B"], p["C"], p["m"], p["D"], p["z"], lib=lib)
+    ok = True
+    for bb in range(p["x"].shape[0]):
+        X = p["x"][bb].T                               # (L, dim)
+        H = p["B"][bb].T @ (X * p["m"][bb][:, None])   # (N, dim)
+        Y = p["C"][bb] @ H                             # (L, dim)
+        want = (Y + X * p["D"][None, :]) * (p["z"][bb].T * expit(p["z"][bb].T))
+        ok = ok and _close(got[bb], want.T, 1e-12)
+    zero = oracle.ncssd(p["x"], p["B"], np.zeros_like(p["C"]), p["m"], p["D"], p["z"], lib=lib)
+    ok = ok and _close(zero, p["D"][None, :, None] * p["x"] * p["z"] * expit(p["z"]), 1e-13)
+    return ok
+
+
+def pin_ncssd_token_order(lib):
+    """The global state does not depend on where the tokens sit (VSSD page
+    §4.2.4): permuting the tokens (x, B, C, m, z together) permutes the
+    output's token axis the same way; the output is linear in m."""
+    rng = np.random.default_rng(59)
+    p = _ncssd_problem(rng, L=11)
+    perm = rng.permutation(11)
+    base = oracle.ncssd(p["x"], p["B"], p["C"], p["m"], p["D"], p["z"], lib=lib)
+    q = dict(x=p["x"][..., perm], B=p["B"][:, perm], C=p["C"][:, perm], m=p["m"][:, perm],
+             z=p["z"][..., perm])
+    moved = oracle.ncssd(np.ascontiguousarray(q["x"]), np.ascontiguousarray(q["B"]),
+                         np.ascontiguousarray(q["C"]), np.ascontiguousarray(q["m"]), p["D"],
+                         np.ascontiguousarray(q["z"]), lib=lib)
+    ok = _close(moved, base[..., perm], 1e-12)
+    m2 = rng.uniform(0.2, 3.0, p["m"].shape)
+    f = lambda m: oracle.ncssd(p["x"], p["B"], p["C"], m, None, None, lib=lib)
+    ok = ok and _close(f(p["m"] + 2.0 * m2), f(p["m"]) + 2.0 * f(m2), 1e-12)
+    return ok
+
+
 PINS = [pin_worked_example, pin_quadratic_form, pin_A_zero_prefix_sum,
         pin_vanishing_decay, pin_zero_input_paths, pin_single_token,
         pin_backward_is_flipped_forward, pin_folded_equals_segments,
         pin_reset_first_token, pin_gate, pin_linearity, pin_softplus_step,
         pin_per_direction_step, pin_conv_taps, pin_conv_feeds_each_direction,
-        pin_gradient_finite_differences]
+        pin_gradient_finite_differences, pin_ncssd_matrix_form, pin_ncssd_token_order]
 
 
 def failing_pins(lib):

@@ -56,6 +56,15 @@ MUTANTS = {
     "grad_gate_derivative_sign": ("(1.0 + zt * (1.0 - sg))", "(1.0 - zt * (1.0 - sg))"),
     "grad_skip_dropped": ("double dxx = ds * Dk, ddt = 0.0;", "double dxx = 0.0, ddt = 0.0;"),
     "grad_dA_without_step": ("dAk[n] += lam[n] * a * hp * dtr[t];", "dAk[n] += lam[n] * a * hp;"),
+    "ncssd_weight_dropped": ("h += mb[j] * Bb[j * N + n] * xb[d * L + j];",
+                             "h += Bb[j * N + n] * xb[d * L + j];"),
+    "ncssd_reads_C_for_B": ("h += mb[j] * Bb[j * N + n] * xb[d * L + j];",
+                            "h += mb[j] * Cb[j * N + n] * xb[d * L + j];"),
+    "ncssd_last_token_missed": ("for (long j = 0; j < L; ++j) h += mb[j]",
+                                "for (long j = 0; j < L - 1; ++j) h += mb[j]"),
+    "ncssd_skip_dropped": ("double y = D ? D[d] * xb[d * L + t] : 0.0;", "double y = 0.0;"),
+    "ncssd_reads_state_of_next_channel": ("y += Cb[t * N + n] * H[n * dim + d];",
+                                          "y += Cb[t * N + n] * H[n * dim + (d + 1) % dim];"),
 }
 
 
