@@ -66,6 +66,9 @@ def parse_args(argv=None):
     p.add_argument("--grad", action="store_true",
                    help="time a training step: the forward scan plus its gradient "
                         "(vssm_scan_grad) for a seeded upstream gradient")
+    p.add_argument("--ncssd", action="store_true",
+                   help="time the NC-SSD global-state variant (vssm_ncssd) on the workload's "
+                        "shapes instead of the scan")
     p.add_argument("--conv", type=int, default=0, choices=[0, 1, 2, 3, 4],
                    help="taps of the directional depthwise convolution + SiLU in front of "
                         "the scan (0: none)")
@@ -406,6 +409,105 @@ def workload_config(wl, l2_note):
 
 # ------------------------------------------------------------------ GPU leg
 
+def run_ncssd(args):
+    """The NC-SSD variant on the workload's shapes (x, z, B, C, D of the
+    workload plus per-token weights m): HBM-bound, so its roofline is the
+    measured copy bandwidth."""
+    import torch
+    import bidirectional_selective_scan_vssm_b300 as vssm
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU path)")
+    torch.cuda.set_device(local)
+    dist_init("nccl")
+    dev = torch.device("cuda", local)
+    wl = WORKLOADS[args.workload].scaled(ncssd=True)
+    inp = make_inputs(wl, seed=rank)
+    e = 4 if wl.dtype == "f32" else 2
+    # bytes the variant must move: x, z read and out written once; B, C, m, D read
+    step_bytes = (3 * wl.tokch * e + 2 * wl.batch * wl.seqlen * wl.dstate * e
+                  + wl.batch * wl.seqlen * 4 + wl.dim * 4)
+
+    def upload(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    base = {k: upload(inp.storage(k)) for k in ("x", "z", "B", "C")}
+    base["m"] = torch.from_numpy(inp.m).to(dev)
+    base["D"] = torch.from_numpy(inp.D_fwd).to(dev)
+    nsets = int(min(64, max(2, math.ceil(3 * L2_BYTES / step_bytes))))
+    sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(nsets - 1)]
+    outs = [torch.empty_like(base["x"]) for _ in range(nsets)]
+    l2_note = (f"{nsets} rotating input/output sets, {nsets * step_bytes / 2**20:.0f} MiB "
+               f"{'>' if nsets * step_bytes > L2_BYTES else '<='} 126 MiB L2")
+    stream = torch.cuda.current_stream(dev)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    argsets, ws = [], None
+    for s_, o in zip(sets, outs):
+        a = vssm.NcssdArgs()
+        a.x, a.z, a.B, a.C = (s_[k].data_ptr() for k in ("x", "z", "B", "C"))
+        a.m, a.D, a.out = s_["m"].data_ptr(), s_["D"].data_ptr(), o.data_ptr()
+        a.batch, a.dim, a.seqlen, a.dstate = wl.batch, wl.dim, wl.seqlen, wl.dstate
+        a.dtype = vssm.VSSM_F32 if wl.dtype == "f32" else vssm.VSSM_BF16
+        n = ctypes.c_size_t(0)
+        vssm.lib.vssm_ncssd_workspace_size(ctypes.byref(a), ctypes.byref(n))
+        if ws is None:
+            ws = torch.empty(max(1, n.value), dtype=torch.uint8, device=dev)
+        a.workspace, a.workspace_bytes = ws.data_ptr(), n.value
+        argsets.append(a)
+
+    def launch(i):
+        st = vssm.lib.vssm_ncssd(ctypes.byref(argsets[i % nsets]), sptr)
+        if st != 0:
+            raise RuntimeError(vssm.lib.vssm_last_error().decode())
+
+    for i in range(args.warmup):
+        launch(i)
+    torch.cuda.synchronize()
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(str(torch.cuda.get_device_properties(dev).uuid))
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize()
+    first_sample = len(sampler.samples)
+    start.record(stream)
+    for i in range(args.steps):
+        ev_b[i].record(stream)
+        launch(i)
+        ev_e[i].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    sampler.stop()
+    region_s = reduce_max(start.elapsed_time(end) / 1e3)
+    kern_avg_s = statistics.fmean(b.elapsed_time(e_) for b, e_ in zip(ev_b, ev_e)) / 1e3
+    peaks, peaks_kind = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    gbs = aggregate(step_bytes * args.steps, world, region_s) / 1e9
+    ach = step_bytes / kern_avg_s / 1e9
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(region_s / args.steps * 1e3, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": dict(workload_config(wl, l2_note), step="NC-SSD (vssm_ncssd)"),
+            "gtokch_per_s": round(aggregate(wl.tokch * args.steps, world, region_s) / 1e9, 4),
+            "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak,
+                         "unit": "GB/s", "frac": round(ach / hbm_peak, 4), "traffic": None,
+                         "peak_kind": peaks_kind, "kernel_avg_us": round(kern_avg_s * 1e6, 3),
+                         "launches_per_call": 3,
+                         "algorithmic_bytes_per_launch": step_bytes},
+            "cpu_baseline": None, "e2e": None, "clocks": sampler.summary(first_sample),
+            "gpu_launches": args.steps * 3, "kernel_source_sha": source_sha(),
+        }
+        print(json.dumps(line), flush=True)
+
+
 def run_ours(args):
     import torch
     import bidirectional_selective_scan_vssm_b300 as vssm
@@ -643,6 +745,8 @@ def main(argv=None):
         raise SystemExit("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.ncssd:
+        run_ncssd(args)
     else:
         run_ours(args)
     import torch.distributed as dist

@@ -34,6 +34,7 @@ EXPORTS = ["vssm_scan_bidir", "vssm_scan_bidir_noalloc", "vssm_scan_folded",
            "vssm_scan_chunked", "vssm_scan_workspace_size", "vssm_scan_chunked_workspace_size",
            "vssm_scan_plan_query", "vssm_scan_grad", "vssm_scan_grad_workspace_size",
            "vssm_selftest_wait_timeout", "vssm_scan_host", "vssm_scan_host_workspace_size",
+           "vssm_ncssd", "vssm_ncssd_workspace_size",
            "vssm_device_error", "vssm_status_string", "vssm_last_error", "vssm_version"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -62,6 +63,18 @@ class GradArgs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "dout", "dx", "ddelta", "dz", "dB", "dC", "dB_bwd", "dC_bwd", "dA_fwd", "dA_bwd",
         "dD_fwd", "dD_bwd")]
+
+
+class NcssdArgs(ctypes.Structure):
+    """Mirror of ``vssm_ncssd_args`` (include/vssm.h)."""
+    _fields_ = [
+        ("x", ctypes.c_void_p), ("z", ctypes.c_void_p), ("B", ctypes.c_void_p),
+        ("C", ctypes.c_void_p), ("m", ctypes.c_void_p), ("D", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("batch", ctypes.c_int), ("dim", ctypes.c_int), ("seqlen", ctypes.c_int),
+        ("dstate", ctypes.c_int), ("dtype", ctypes.c_int),
+    ]
 
 
 class VssmError(RuntimeError):
@@ -100,6 +113,11 @@ def _load():
     lib.vssm_scan_host_workspace_size.argtypes = [P, ctypes.c_int, ctypes.c_int,
                                                   ctypes.POINTER(ctypes.c_size_t)]
     lib.vssm_scan_host_workspace_size.restype = ctypes.c_int
+    NP = ctypes.POINTER(NcssdArgs)
+    lib.vssm_ncssd.argtypes = [NP, ctypes.c_void_p]
+    lib.vssm_ncssd.restype = ctypes.c_int
+    lib.vssm_ncssd_workspace_size.argtypes = [NP, ctypes.POINTER(ctypes.c_size_t)]
+    lib.vssm_ncssd_workspace_size.restype = ctypes.c_int
     lib.vssm_selftest_wait_timeout.argtypes = [ctypes.c_uint, ctypes.c_void_p]
     lib.vssm_selftest_wait_timeout.restype = ctypes.c_int
     lib.vssm_scan_grad_workspace_size.argtypes = [P, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
@@ -350,6 +368,41 @@ def scan_grad(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *, d
         a.workspace_bytes = workspace.numel() * workspace.element_size()
     _check(lib.vssm_scan_grad(ctypes.byref(a), ctypes.byref(g), int(seg_len),
                               ctypes.c_void_p(stream.cuda_stream)))
+    return out
+
+
+def ncssd(x, B, C, m, D=None, z=None, *, out=None, stream: Optional[torch.cuda.Stream] = None,
+          workspace=None) -> torch.Tensor:
+    """``vssm_ncssd``: the VSSD page's non-causal global-state form,
+    out = (C (B^T (x m)) + D x) silu(z); m is (batch, L) float32."""
+    x = _dev_tensor("x", x)
+    if x.dtype not in (torch.float32, torch.bfloat16) or x.dim() != 3:
+        raise TypeError("x must be a 3-D float32 or bfloat16 tensor (batch, dim, L)")
+    batch, dim, L = x.shape
+    N = B.shape[-1]
+    dev, dt = x.device, x.dtype
+    _dev_tensor("z", z, dt, x.shape, dev)
+    _dev_tensor("B", B, dt, (batch, L, N), dev)
+    _dev_tensor("C", C, dt, (batch, L, N), dev)
+    _dev_tensor("m", m, torch.float32, (batch, L), dev)
+    _dev_tensor("D", D, torch.float32, (dim,), dev)
+    if out is None:
+        out = torch.empty_like(x)
+    _dev_tensor("out", out, dt, x.shape, dev)
+    a = NcssdArgs()
+    a.x, a.z, a.B, a.C, a.m, a.D, a.out = (_ptr(x), _ptr(z), _ptr(B), _ptr(C), _ptr(m), _ptr(D),
+                                           _ptr(out))
+    a.batch, a.dim, a.seqlen, a.dstate = batch, dim, L, N
+    a.dtype = VSSM_F32 if dt == torch.float32 else VSSM_BF16
+    stream = stream if stream is not None else torch.cuda.current_stream(dev)
+    n = ctypes.c_size_t(0)
+    _check(lib.vssm_ncssd_workspace_size(ctypes.byref(a), ctypes.byref(n)))
+    if workspace is None:
+        workspace = _workspace(dev, stream, int(n.value))
+    if workspace is not None:
+        a.workspace = workspace.data_ptr()
+        a.workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.vssm_ncssd(ctypes.byref(a), ctypes.c_void_p(stream.cuda_stream)))
     return out
 
 

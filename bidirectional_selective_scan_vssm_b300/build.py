@@ -19,7 +19,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libvssm.so")
 SOURCES = [os.path.join(CSRC, "vssm_api.cu")]
-HEADERS = [os.path.join(CSRC, f) for f in ("scan_kernel.cuh", "scan_warp.cuh", "scan_grad.cuh", "ptx.cuh")] + [
+HEADERS = [os.path.join(CSRC, f) for f in ("scan_kernel.cuh", "scan_warp.cuh", "scan_grad.cuh", "ncssd.cuh", "ptx.cuh")] + [
     os.path.join(ROOT, "include", "vssm.h")]
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "scan_kernel.cuh"
+#include "ncssd.cuh"
 #include "scan_grad.cuh"
 #include "scan_warp.cuh"
 #include "vssm.h"
@@ -940,6 +941,82 @@ int vssm_scan_host_workspace_size(const vssm_scan_args *a, int seg_len, int slic
 int vssm_scan_host(const vssm_scan_args *a, int seg_len, int slices, void *stream)
 {
     return host_scan(a, seg_len, slices, stream);
+}
+
+int vssm_ncssd_workspace_size(const vssm_ncssd_args *a, size_t *bytes)
+{
+    if (!a || !bytes) return fail(VSSM_ERR_INVALID_ARG, "args or bytes is NULL");
+    if (a->batch < 0 || a->dim < 0 || a->seqlen < 0)
+        return fail(VSSM_ERR_INVALID_ARG, "negative size");
+    *bytes = (size_t)a->batch * a->dim * 16 * sizeof(float);
+    return VSSM_OK;
+}
+
+int vssm_ncssd(const vssm_ncssd_args *a, void *stream)
+{
+    if (!a) return fail(VSSM_ERR_INVALID_ARG, "args is NULL");
+    if (a->batch < 0 || a->dim < 0 || a->seqlen < 0)
+        return fail(VSSM_ERR_INVALID_ARG, "negative size (batch=%d dim=%d seqlen=%d)", a->batch,
+                    a->dim, a->seqlen);
+    if (a->dstate != 16) return fail(VSSM_ERR_UNSUPPORTED, "NC-SSD needs dstate 16 (got %d)", a->dstate);
+    if (a->dtype != VSSM_F32 && a->dtype != VSSM_BF16)
+        return fail(VSSM_ERR_UNSUPPORTED, "unknown dtype %d", a->dtype);
+    if (a->batch > 65535) return fail(VSSM_ERR_UNSUPPORTED, "batch=%d above 65535", a->batch);
+    const long long tok = (long long)a->batch * a->dim * a->seqlen;
+    if (tok == 0) return VSSM_OK;
+    if (!a->x || !a->B || !a->C || !a->m || !a->out)
+        return fail(VSSM_ERR_INVALID_ARG, "x, B, C, m and out are required");
+    const void *ptrs[] = {a->x, a->z, a->B, a->C, a->m, a->D, a->out, a->workspace};
+    for (const void *q : ptrs)
+        if (q && !aligned16(q)) return fail(VSSM_ERR_MISALIGNED, "pointer %p is not 16-byte aligned", q);
+    const size_t es = a->dtype == VSSM_F32 ? 4 : 2;
+    const size_t nact = (size_t)tok * es, nbc = (size_t)a->batch * a->seqlen * 16 * es;
+    const size_t need = (size_t)a->batch * a->dim * 16 * sizeof(float);
+    if (!a->workspace || a->workspace_bytes < need)
+        return fail(VSSM_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", need,
+                    a->workspace ? a->workspace_bytes : (size_t)0);
+    const struct { const void *p; size_t n; } ins[] = {
+        {a->x, nact}, {a->z, nact}, {a->B, nbc}, {a->C, nbc},
+        {a->m, (size_t)a->batch * a->seqlen * 4}, {a->D, (size_t)a->dim * 4},
+        {a->workspace, a->workspace_bytes}};
+    for (const auto &in : ins)
+        if (overlaps(a->out, nact, in.p, in.n)) return fail(VSSM_ERR_INVALID_ARG, "out overlaps an input");
+    if (overlaps(a->workspace, a->workspace_bytes, a->x, nact))
+        return fail(VSSM_ERR_INVALID_ARG, "workspace overlaps x");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    vssm::NcssdParams p{};
+    p.x = a->x;
+    p.z = a->z;
+    p.B = a->B;
+    p.C = a->C;
+    p.m = a->m;
+    p.D = a->D;
+    p.out = a->out;
+    p.H = static_cast<float *>(a->workspace);
+    p.batch = a->batch;
+    p.dim = a->dim;
+    p.L = a->seqlen;
+    // tokens per state CTA: enough CTAs for 148 SMs x 8, at least one 32-token tile each
+    const int dtiles = (a->dim + vssm::kNcChS - 1) / vssm::kNcChS;
+    const long long base = (long long)a->batch * dtiles;
+    const int maxsplit = (a->seqlen + vssm::kNcTile - 1) / vssm::kNcTile;
+    const int split = (int)std::max<long long>(1, std::min<long long>(maxsplit, (148 * 8 + base - 1) / base));
+    p.tok_per_cta = ((a->seqlen + split - 1) / split + vssm::kNcTile - 1) / vssm::kNcTile * vssm::kNcTile;
+    const int nsplit = (a->seqlen + p.tok_per_cta - 1) / p.tok_per_cta;
+    int st = zero_f32(p.H, need / sizeof(float), s);
+    if (st != VSSM_OK) return st;
+    const dim3 g1((unsigned)nsplit, (unsigned)dtiles, (unsigned)a->batch);
+    const dim3 g2((unsigned)((a->seqlen + vssm::kNcTok - 1) / vssm::kNcTok),
+                  (unsigned)((a->dim + vssm::kNcCh - 1) / vssm::kNcCh), (unsigned)a->batch);
+    if (a->dtype == VSSM_F32) {
+        vssm::ncssd_state_kernel<float><<<g1, 256, 0, s>>>(p);
+        vssm::ncssd_out_kernel<float><<<g2, 256, 0, s>>>(p);
+    } else {
+        vssm::ncssd_state_kernel<__nv_bfloat16><<<g1, 256, 0, s>>>(p);
+        vssm::ncssd_out_kernel<__nv_bfloat16><<<g2, 256, 0, s>>>(p);
+    }
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? VSSM_OK : fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
 }
 
 int vssm_selftest_wait_timeout(unsigned limit_us, void *stream)

@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define VSSM_VERSION 150 /* 1.5.0 */
+#define VSSM_VERSION 160 /* 1.6.0 */
 
 typedef enum {
     VSSM_OK = 0,
@@ -316,6 +316,36 @@ int vssm_scan_host(const vssm_scan_args *a, int seg_len, int slices, void *strea
 
 /* Device workspace bytes of vssm_scan_host with these seg_len and slices. */
 int vssm_scan_host_workspace_size(const vssm_scan_args *a, int seg_len, int slices, size_t *bytes);
+
+/*
+ * NC-SSD, the non-causal global-state variant (VSSD page, §4.2.4 and §4.2.5:
+ * Y = C (B^T (X m))): one hidden state per batch entry, shared by all tokens,
+ *
+ *   H[n][d]   = sum_j m[j] * B_j[n] * x[d][j]
+ *   out[d][t] = (sum_n C_t[n] * H[n][d] + D[d] * x[d][t]) * silu(z[d][t])
+ *
+ * with per-token weights m (the page's m_j = 1/A_j, computed by the caller),
+ * D optional (NULL = 0) and z optional (NULL = no gate). Accumulation in
+ * fp32; out is rounded once to the I/O dtype. Tensors as in vssm_scan_args:
+ * x, z, out [batch][dim][seqlen], B, C [batch][seqlen][dstate] in `dtype`;
+ * m [batch][seqlen] and D [dim] fp32. dstate must be 16 (else
+ * VSSM_ERR_UNSUPPORTED); batch <= 65535. The workspace holds H (fp32):
+ * vssm_ncssd_workspace_size bytes. The sums over tokens are split over
+ * several CTAs and added atomically, so the last bits of H can vary from run
+ * to run. Device pointers, 16-byte aligned, caller-owned; asynchronous on
+ * `stream`.
+ */
+typedef struct {
+    const void *x, *z, *B, *C;
+    const float *m, *D;
+    void *out;
+    void *workspace;
+    size_t workspace_bytes;
+    int batch, dim, seqlen, dstate, dtype;
+} vssm_ncssd_args;
+
+int vssm_ncssd(const vssm_ncssd_args *a, void *stream);
+int vssm_ncssd_workspace_size(const vssm_ncssd_args *a, size_t *bytes);
 
 /*
  * Test of the timeout path, for callers' own failure-handling tests: runs one

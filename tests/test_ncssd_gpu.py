@@ -1,0 +1,59 @@
+"""NC-SSD (vssm_ncssd), the VSSD page's non-causal global-state form, vs the
+fp64 oracle (itself pinned against the page's matrix form and its
+token-order independence). Covers ragged channel tiles, one-token rows, rows
+split over several CTAs for the state sums, optional skip and gate, and the
+Vim-S 224² size on sampled rows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import TOL, normwise_rel, to_device
+from workloads import WORKLOADS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import bidirectional_selective_scan_vssm_b300 as vssm  # noqa: E402  (fails loudly if unbuilt)
+
+
+def _run(inp, skip=True, gate=True):
+    t = to_device(inp)
+    m = torch.from_numpy(inp.m).cuda()
+    got = vssm.ncssd(t["x"], t["B"], t["C"], m, t["D_fwd"] if skip else None,
+                     t["z"] if gate else None)
+    ref = oracle.ncssd(inp.x, inp.B, inp.C, inp.m, inp.D_fwd if skip else None,
+                       inp.z if gate else None)
+    return got.float().cpu().numpy(), ref
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(2, 40, 9), (1, 130, 1), (1, 130, 33), (3, 64, 197),
+                                   (2, 200, 300), (1, 64, 5000)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_ncssd(dtype, shape):
+    b, d, L = shape
+    wl = WORKLOADS["vim_ti_224"].scaled(batch=b, dim=d, seqlen=L, dtype=dtype, ncssd=True)
+    got, ref = _run(make_inputs(wl, seed=1000 + L))
+    err = normwise_rel(got, ref)
+    assert err <= TOL[dtype], f"{shape}: {err:.3e}"
+
+
+@pytest.mark.parametrize("skip,gate", [(False, False), (True, False), (False, True)])
+def test_ncssd_optional_skip_gate(skip, gate):
+    wl = WORKLOADS["vim_ti_224"].scaled(batch=2, dim=70, seqlen=50, ncssd=True)
+    got, ref = _run(make_inputs(wl, seed=1100), skip=skip, gate=gate)
+    assert normwise_rel(got, ref) <= TOL["f32"]
+
+
+def test_ncssd_vim_s_224_sampled():
+    wl = WORKLOADS["vim_s_224"].scaled(ncssd=True)
+    inp = make_inputs(wl, seed=0)
+    t = to_device(inp)
+    got = vssm.ncssd(t["x"], t["B"], t["C"], torch.from_numpy(inp.m).cuda(), t["D_fwd"], t["z"])
+    bs = [0, 77, 127]
+    ref = oracle.ncssd(inp.x[bs], inp.B[bs], inp.C[bs], inp.m[bs], inp.D_fwd, inp.z[bs])
+    err = normwise_rel(got[bs].float().cpu().numpy(), ref)
+    assert err <= TOL["bf16"], f"{err:.3e}"

@@ -38,6 +38,10 @@ Convolution variant (``conv=K``, any workload): after everything above come
 the forward taps and bias, then the backward taps and bias, each ~
 U[-1/sqrt(K), 1/sqrt(K)] (the usual fan-in initialisation of a depthwise
 convolution with K taps); shapes (dim, K) and (dim,).
+
+NC-SSD variant (``ncssd=True``): after everything above come the per-token
+weights m ~ U[0.5, 1.5], shape (batch, L) (the VSSD page's m_j = 1/A_j, here
+drawn directly).
 """
 from __future__ import annotations
 
@@ -66,6 +70,7 @@ class Workload:
     description: str = ""
     fused_step: bool = False   # per-direction pre-activation steps + biases (softplus inside)
     conv: int = 0              # taps of the directional convolution + SiLU in front (0: none)
+    ncssd: bool = False        # also draw the NC-SSD per-token weights m
 
     @property
     def tokch(self) -> int:
@@ -134,6 +139,7 @@ class Inputs:
     conv_b: Optional[np.ndarray] = None
     conv_w_bwd: Optional[np.ndarray] = None
     conv_b_bwd: Optional[np.ndarray] = None
+    m: Optional[np.ndarray] = None                # NC-SSD workloads only
 
     def storage(self, name: str) -> np.ndarray:
         """The array as stored for the device: uint16 bits (bf16) or float32."""
@@ -178,6 +184,8 @@ def make_inputs(wl: Workload, seed: int = 0) -> Inputs:
         for sfx in ("", "_bwd"):
             extra["conv_w" + sfx] = rng.uniform(-lim, lim, size=(D, wl.conv)).astype(np.float32)
             extra["conv_b" + sfx] = rng.uniform(-lim, lim, size=D).astype(np.float32)
+    if wl.ncssd:
+        extra["m"] = rng.uniform(0.5, 1.5, size=(b, L)).astype(np.float32)
     bits = None
     if wl.dtype == "bf16":
         bits = {}
