@@ -500,10 +500,10 @@ def run_ncssd(args):
             "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak,
                          "unit": "GB/s", "frac": round(ach / hbm_peak, 4), "traffic": None,
                          "peak_kind": peaks_kind, "kernel_avg_us": round(kern_avg_s * 1e6, 3),
-                         "launches_per_call": 3,
+                         "launches_per_call": 1,
                          "algorithmic_bytes_per_launch": step_bytes},
             "cpu_baseline": None, "e2e": None, "clocks": sampler.summary(first_sample),
-            "gpu_launches": args.steps * 3, "kernel_source_sha": source_sha(),
+            "gpu_launches": args.steps, "kernel_source_sha": source_sha(),
         }
         print(json.dumps(line), flush=True)
 

@@ -867,6 +867,29 @@ int host_scan(const vssm_scan_args *a, int seg_len, int slices, void *stream)
     if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "pipeline join: %s", cudaGetErrorString(e));
     return VSSM_OK;
 }
+template <typename T, int Q>
+void ncssd_launch_q(const vssm::NcssdParams &p, bool gate, bool skip, dim3 grid, cudaStream_t s)
+{
+    const dim3 block(vssm::kNcW * 32);
+    if (gate && skip) vssm::ncssd_kernel<T, Q, true, true><<<grid, block, 0, s>>>(p);
+    else if (gate) vssm::ncssd_kernel<T, Q, true, false><<<grid, block, 0, s>>>(p);
+    else if (skip) vssm::ncssd_kernel<T, Q, false, true><<<grid, block, 0, s>>>(p);
+    else vssm::ncssd_kernel<T, Q, false, false><<<grid, block, 0, s>>>(p);
+}
+
+// The NC-SSD kernel with Q CTAs per cluster (1, 2, 4 or 8) and the z / D
+// options fixed at compile time.
+template <typename T>
+void ncssd_launch(const vssm::NcssdParams &p, int q, bool gate, bool skip, dim3 grid, cudaStream_t s)
+{
+    switch (q) {
+    case 1: ncssd_launch_q<T, 1>(p, gate, skip, grid, s); break;
+    case 2: ncssd_launch_q<T, 2>(p, gate, skip, grid, s); break;
+    case 4: ncssd_launch_q<T, 4>(p, gate, skip, grid, s); break;
+    default: ncssd_launch_q<T, 8>(p, gate, skip, grid, s); break;
+    }
+}
+
 }  // namespace
 
 extern "C" {
@@ -948,7 +971,7 @@ int vssm_ncssd_workspace_size(const vssm_ncssd_args *a, size_t *bytes)
     if (!a || !bytes) return fail(VSSM_ERR_INVALID_ARG, "args or bytes is NULL");
     if (a->batch < 0 || a->dim < 0 || a->seqlen < 0)
         return fail(VSSM_ERR_INVALID_ARG, "negative size");
-    *bytes = (size_t)a->batch * a->dim * 16 * sizeof(float);
+    *bytes = 0;
     return VSSM_OK;
 }
 
@@ -966,23 +989,16 @@ int vssm_ncssd(const vssm_ncssd_args *a, void *stream)
     if (tok == 0) return VSSM_OK;
     if (!a->x || !a->B || !a->C || !a->m || !a->out)
         return fail(VSSM_ERR_INVALID_ARG, "x, B, C, m and out are required");
-    const void *ptrs[] = {a->x, a->z, a->B, a->C, a->m, a->D, a->out, a->workspace};
+    const void *ptrs[] = {a->x, a->z, a->B, a->C, a->m, a->D, a->out};
     for (const void *q : ptrs)
         if (q && !aligned16(q)) return fail(VSSM_ERR_MISALIGNED, "pointer %p is not 16-byte aligned", q);
     const size_t es = a->dtype == VSSM_F32 ? 4 : 2;
     const size_t nact = (size_t)tok * es, nbc = (size_t)a->batch * a->seqlen * 16 * es;
-    const size_t need = (size_t)a->batch * a->dim * 16 * sizeof(float);
-    if (!a->workspace || a->workspace_bytes < need)
-        return fail(VSSM_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", need,
-                    a->workspace ? a->workspace_bytes : (size_t)0);
     const struct { const void *p; size_t n; } ins[] = {
         {a->x, nact}, {a->z, nact}, {a->B, nbc}, {a->C, nbc},
-        {a->m, (size_t)a->batch * a->seqlen * 4}, {a->D, (size_t)a->dim * 4},
-        {a->workspace, a->workspace_bytes}};
+        {a->m, (size_t)a->batch * a->seqlen * 4}, {a->D, (size_t)a->dim * 4}};
     for (const auto &in : ins)
         if (overlaps(a->out, nact, in.p, in.n)) return fail(VSSM_ERR_INVALID_ARG, "out overlaps an input");
-    if (overlaps(a->workspace, a->workspace_bytes, a->x, nact))
-        return fail(VSSM_ERR_INVALID_ARG, "workspace overlaps x");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     vssm::NcssdParams p{};
     p.x = a->x;
@@ -992,29 +1008,20 @@ int vssm_ncssd(const vssm_ncssd_args *a, void *stream)
     p.m = a->m;
     p.D = a->D;
     p.out = a->out;
-    p.H = static_cast<float *>(a->workspace);
     p.batch = a->batch;
     p.dim = a->dim;
     p.L = a->seqlen;
-    // tokens per state CTA: enough CTAs for 148 SMs x 8, at least one 32-token tile each
-    const int dtiles = (a->dim + vssm::kNcChS - 1) / vssm::kNcChS;
+    // CTAs per cluster: split the rows until about seven CTAs per SM are
+    // busy, keeping at least 64 tokens per CTA
+    const int dtiles = (a->dim + 31) / 32;
+    if (dtiles > 65535) return fail(VSSM_ERR_UNSUPPORTED, "dim=%d above 65535 x 32", a->dim);
     const long long base = (long long)a->batch * dtiles;
-    const int maxsplit = (a->seqlen + vssm::kNcTile - 1) / vssm::kNcTile;
-    const int split = (int)std::max<long long>(1, std::min<long long>(maxsplit, (148 * 8 + base - 1) / base));
-    p.tok_per_cta = ((a->seqlen + split - 1) / split + vssm::kNcTile - 1) / vssm::kNcTile * vssm::kNcTile;
-    const int nsplit = (a->seqlen + p.tok_per_cta - 1) / p.tok_per_cta;
-    int st = zero_f32(p.H, need / sizeof(float), s);
-    if (st != VSSM_OK) return st;
-    const dim3 g1((unsigned)nsplit, (unsigned)dtiles, (unsigned)a->batch);
-    const dim3 g2((unsigned)((a->seqlen + vssm::kNcTok - 1) / vssm::kNcTok),
-                  (unsigned)((a->dim + vssm::kNcCh - 1) / vssm::kNcCh), (unsigned)a->batch);
-    if (a->dtype == VSSM_F32) {
-        vssm::ncssd_state_kernel<float><<<g1, 256, 0, s>>>(p);
-        vssm::ncssd_out_kernel<float><<<g2, 256, 0, s>>>(p);
-    } else {
-        vssm::ncssd_state_kernel<__nv_bfloat16><<<g1, 256, 0, s>>>(p);
-        vssm::ncssd_out_kernel<__nv_bfloat16><<<g2, 256, 0, s>>>(p);
-    }
+    int q = 1;
+    while (q < vssm::kNcMaxQ && base * q < 148LL * 7 && a->seqlen >= 2 * q * 64) q *= 2;
+    p.rng = (a->seqlen + q - 1) / q;
+    const dim3 grid((unsigned)q, (unsigned)dtiles, (unsigned)a->batch);
+    if (a->dtype == VSSM_F32) ncssd_launch<float>(p, q, a->z != nullptr, a->D != nullptr, grid, s);
+    else ncssd_launch<__nv_bfloat16>(p, q, a->z != nullptr, a->D != nullptr, grid, s);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? VSSM_OK : fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
 }

@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define VSSM_VERSION 160 /* 1.6.0 */
+#define VSSM_VERSION 161 /* 1.6.1 */
 
 typedef enum {
     VSSM_OK = 0,
@@ -329,11 +329,13 @@ int vssm_scan_host_workspace_size(const vssm_scan_args *a, int seg_len, int slic
  * fp32; out is rounded once to the I/O dtype. Tensors as in vssm_scan_args:
  * x, z, out [batch][dim][seqlen], B, C [batch][seqlen][dstate] in `dtype`;
  * m [batch][seqlen] and D [dim] fp32. dstate must be 16 (else
- * VSSM_ERR_UNSUPPORTED); batch <= 65535. The workspace holds H (fp32):
- * vssm_ncssd_workspace_size bytes. The sums over tokens are split over
- * several CTAs and added atomically, so the last bits of H can vary from run
- * to run. Device pointers, 16-byte aligned, caller-owned; asynchronous on
- * `stream`.
+ * VSSM_ERR_UNSUPPORTED); batch <= 65535. H stays on chip: no workspace is
+ * needed (vssm_ncssd_workspace_size reports 0 and `workspace` is ignored).
+ * The sums over tokens are added in a fixed order, so the result is the same
+ * on every run. Device pointers, 16-byte aligned, caller-owned; asynchronous
+ * on `stream`. Errors: VSSM_ERR_INVALID_ARG (NULL x, B, C, m or out;
+ * negative sizes; out overlapping an input), VSSM_ERR_MISALIGNED,
+ * VSSM_ERR_UNSUPPORTED, VSSM_ERR_CUDA (launch failure).
  */
 typedef struct {
     const void *x, *z, *B, *C;

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(v):
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared in vssm.h but not exported"
     assert set(v.EXPORTS) <= set(declared_functions())
-    assert v.version() == 160
+    assert v.version() == 161
 
 
 def test_args_struct_layout_matches_header(v):

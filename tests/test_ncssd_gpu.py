@@ -1,8 +1,9 @@
 """NC-SSD (vssm_ncssd), the VSSD page's non-causal global-state form, vs the
 fp64 oracle (itself pinned against the page's matrix form and its
 token-order independence). Covers ragged channel tiles, one-token rows, rows
-split over several CTAs for the state sums, optional skip and gate, and the
-Vim-S 224² size on sampled rows."""
+split over clusters of 2, 4 and 8 CTAs (joined through distributed shared
+memory), optional skip and gate, run-to-run determinism, and the Vim-S 224²
+size on sampled rows."""
 import numpy as np
 import pytest
 import torch
@@ -30,8 +31,9 @@ def _run(inp, skip=True, gate=True):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+# CTAs per cluster: 1, 1, 1, 2, 4, 8, 8
 @pytest.mark.parametrize("shape", [(2, 40, 9), (1, 130, 1), (1, 130, 33), (3, 64, 197),
-                                   (2, 200, 300), (1, 64, 5000)],
+                                   (2, 200, 300), (1, 64, 5000), (1, 33, 1100)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_ncssd(dtype, shape):
     b, d, L = shape
@@ -46,6 +48,17 @@ def test_ncssd_optional_skip_gate(skip, gate):
     wl = WORKLOADS["vim_ti_224"].scaled(batch=2, dim=70, seqlen=50, ncssd=True)
     got, ref = _run(make_inputs(wl, seed=1100), skip=skip, gate=gate)
     assert normwise_rel(got, ref) <= TOL["f32"]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_ncssd_deterministic(dtype):
+    wl = WORKLOADS["vim_ti_224"].scaled(batch=1, dim=96, seqlen=3000, dtype=dtype, ncssd=True)
+    inp = make_inputs(wl, seed=1200)
+    t = to_device(inp)
+    m = torch.from_numpy(inp.m).cuda()
+    a = vssm.ncssd(t["x"], t["B"], t["C"], m, t["D_fwd"], t["z"])
+    b = vssm.ncssd(t["x"], t["B"], t["C"], m, t["D_fwd"], t["z"])
+    assert torch.equal(a, b)
 
 
 def test_ncssd_vim_s_224_sampled():
