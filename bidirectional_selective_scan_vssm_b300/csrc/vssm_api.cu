@@ -867,18 +867,40 @@ int host_scan(const vssm_scan_args *a, int seg_len, int slices, void *stream)
     if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "pipeline join: %s", cudaGetErrorString(e));
     return VSSM_OK;
 }
+template <typename T, int Q, bool GATE, bool SKIP>
+void ncssd_launch_k(const vssm::NcssdParams &p, dim3 grid, cudaStream_t s)
+{
+    const dim3 block(vssm::kNcW * 32);
+    if (sizeof(T) == 2) vssm::ncssd_mma_kernel<Q, GATE, SKIP><<<grid, block, 0, s>>>(p);
+    else vssm::ncssd_kernel<float, Q, GATE, SKIP><<<grid, block, 0, s>>>(p);
+}
+
 template <typename T, int Q>
 void ncssd_launch_q(const vssm::NcssdParams &p, bool gate, bool skip, dim3 grid, cudaStream_t s)
 {
-    const dim3 block(vssm::kNcW * 32);
-    if (gate && skip) vssm::ncssd_kernel<T, Q, true, true><<<grid, block, 0, s>>>(p);
-    else if (gate) vssm::ncssd_kernel<T, Q, true, false><<<grid, block, 0, s>>>(p);
-    else if (skip) vssm::ncssd_kernel<T, Q, false, true><<<grid, block, 0, s>>>(p);
-    else vssm::ncssd_kernel<T, Q, false, false><<<grid, block, 0, s>>>(p);
+    if (gate && skip) ncssd_launch_k<T, Q, true, true>(p, grid, s);
+    else if (gate) ncssd_launch_k<T, Q, true, false>(p, grid, s);
+    else if (skip) ncssd_launch_k<T, Q, false, true>(p, grid, s);
+    else ncssd_launch_k<T, Q, false, false>(p, grid, s);
+}
+
+template <bool GATE, bool SKIP>
+int ncssd_rows_launch(const vssm::NcssdParams &p, dim3 grid, cudaStream_t s)
+{
+    const vssm::NcRowsLayout lay(p.L, GATE);
+    auto kern = vssm::ncssd_rows_kernel<GATE, SKIP>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    kern<<<grid, vssm::kNcW * 32, lay.total, s>>>(p);
+    return VSSM_OK;
 }
 
 // The NC-SSD kernel with Q CTAs per cluster (1, 2, 4 or 8) and the z / D
-// options fixed at compile time.
+// options fixed at compile time: bf16 I/O on the tensor cores, fp32 I/O on
+// the FMA pipe.
 template <typename T>
 void ncssd_launch(const vssm::NcssdParams &p, int q, bool gate, bool skip, dim3 grid, cudaStream_t s)
 {
@@ -1020,8 +1042,21 @@ int vssm_ncssd(const vssm_ncssd_args *a, void *stream)
     while (q < vssm::kNcMaxQ && base * q < 148LL * 7 && a->seqlen >= 2 * q * 64) q *= 2;
     p.rng = (a->seqlen + q - 1) / q;
     const dim3 grid((unsigned)q, (unsigned)dtiles, (unsigned)a->batch);
-    if (a->dtype == VSSM_F32) ncssd_launch<float>(p, q, a->z != nullptr, a->D != nullptr, grid, s);
-    else ncssd_launch<__nv_bfloat16>(p, q, a->z != nullptr, a->D != nullptr, grid, s);
+    const bool gate = a->z != nullptr, skip = a->D != nullptr;
+    if (a->dtype == VSSM_BF16 && q == 1 && a->dim % 8 == 0 && a->seqlen <= vssm::kNcRowsMaxL) {
+        // whole rows resident in shared memory, spans moved by bulk copies
+        p.err = device_error_word();
+        if (!p.err) return fail(VSSM_ERR_CUDA, "device error word unavailable");
+        const int st = gate ? (skip ? ncssd_rows_launch<true, true>(p, grid, s)
+                                    : ncssd_rows_launch<true, false>(p, grid, s))
+                            : (skip ? ncssd_rows_launch<false, true>(p, grid, s)
+                                    : ncssd_rows_launch<false, false>(p, grid, s));
+        if (st != VSSM_OK) return st;
+    } else if (a->dtype == VSSM_F32) {
+        ncssd_launch<float>(p, q, gate, skip, grid, s);
+    } else {
+        ncssd_launch<__nv_bfloat16>(p, q, gate, skip, grid, s);
+    }
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? VSSM_OK : fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
 }

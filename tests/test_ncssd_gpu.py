@@ -31,9 +31,12 @@ def _run(inp, skip=True, gate=True):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-# CTAs per cluster: 1, 1, 1, 2, 4, 8, 8
-@pytest.mark.parametrize("shape", [(2, 40, 9), (1, 130, 1), (1, 130, 33), (3, 64, 197),
-                                   (2, 200, 300), (1, 64, 5000), (1, 33, 1100)],
+# bf16 kernels: rows resident in shared memory for (2, 40, 9), (8, 48, 100) and
+# (44, 768, 197) (one CTA per row, dim a multiple of 8, L <= 400); otherwise
+# tiles, with 1, 1, 2, 4, 8, 8 CTAs per cluster. fp32: the FMA-pipe kernel.
+@pytest.mark.parametrize("shape", [(2, 40, 9), (8, 48, 100), (44, 768, 197), (1, 130, 1),
+                                   (1, 130, 33), (3, 64, 197), (2, 200, 300), (1, 64, 5000),
+                                   (1, 33, 1100)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_ncssd(dtype, shape):
     b, d, L = shape
@@ -44,10 +47,11 @@ def test_ncssd(dtype, shape):
 
 
 @pytest.mark.parametrize("skip,gate", [(False, False), (True, False), (False, True)])
-def test_ncssd_optional_skip_gate(skip, gate):
-    wl = WORKLOADS["vim_ti_224"].scaled(batch=2, dim=70, seqlen=50, ncssd=True)
+@pytest.mark.parametrize("dtype,dim", [("f32", 70), ("bf16", 70), ("bf16", 64)])
+def test_ncssd_optional_skip_gate(skip, gate, dtype, dim):
+    wl = WORKLOADS["vim_ti_224"].scaled(batch=2, dim=dim, seqlen=50, dtype=dtype, ncssd=True)
     got, ref = _run(make_inputs(wl, seed=1100), skip=skip, gate=gate)
-    assert normwise_rel(got, ref) <= TOL["f32"]
+    assert normwise_rel(got, ref) <= TOL[dtype]
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
