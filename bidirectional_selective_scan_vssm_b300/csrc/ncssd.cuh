@@ -538,7 +538,7 @@ struct NcRowsLayout {
         sx = ((32 * L + kNcPad) * 2 + 15) / 16 * 16;      // one span buffer
         oZ = sx;
         oM = oZ + (gate ? sx : 0);
-        oHB = oM + kNcW * 2 * 32 * kNcMP * 2;
+        oHB = oM + kNcW * 2 * 16 * kNcMP * 2;            // m B rows of one 16-token step per warp
         oD = oHB + 2 * 32 * kNcMP * 2;
         oBar = oD + 32 * 4;
         total = oBar + 16;                                 // two mbarriers: x, z
@@ -552,7 +552,7 @@ __device__ __forceinline__ uint32_t lds_pair(const unsigned short *s, int i)
 }
 
 template <bool GATE, bool SKIP>
-__global__ void __launch_bounds__(kNcW * 32, 4) ncssd_rows_kernel(const NcssdParams p)
+__global__ void __launch_bounds__(kNcW * 32, 6) ncssd_rows_kernel(const NcssdParams p)
 {
     extern __shared__ __align__(128) unsigned char nsm[];
     const int L = p.L;
@@ -562,7 +562,9 @@ __global__ void __launch_bounds__(kNcW * 32, 4) ncssd_rows_kernel(const NcssdPar
     unsigned short (*hb)[32][kNcMP] = reinterpret_cast<unsigned short (*)[32][kNcMP]>(nsm + lay.oHB);
     float *ds = reinterpret_cast<float *>(nsm + lay.oD);
     uint64_t *bar = reinterpret_cast<uint64_t *>(nsm + lay.oBar);
-    float *part = reinterpret_cast<float *>(nsm + lay.oM);               // [kNcW][32][16], over mw
+    // the warps' partial sums, [kNcW][32][16] fp32, over the m B rows and hb
+    float *part = reinterpret_cast<float *>(nsm + lay.oM);
+    static_assert(kNcW * 2 * 16 * kNcMP * 2 + 2 * 32 * kNcMP * 2 >= kNcW * 32 * 16 * 4, "part fits");
     __shared__ int s_ok;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t4 = lane & 3;
@@ -571,7 +573,7 @@ __global__ void __launch_bounds__(kNcW * 32, 4) ncssd_rows_kernel(const NcssdPar
     const long long row0 = ((long long)b * p.dim + d0) * L;
     const uint32_t span = (uint32_t)nch * L * 2;                 // bytes, a multiple of 16
     unsigned short (*mw)[kNcMP] =
-        reinterpret_cast<unsigned short (*)[kNcMP]>(nsm + lay.oM + warp * 2 * 32 * kNcMP * 2);
+        reinterpret_cast<unsigned short (*)[kNcMP]>(nsm + lay.oM + warp * 2 * 16 * kNcMP * 2);
 
     if (threadIdx.x == 0) {
         mbar_init(&bar[0], 1);
@@ -643,30 +645,31 @@ __global__ void __launch_bounds__(kNcW * 32, 4) ncssd_rows_kernel(const NcssdPar
         const int t0 = warp * kNcT + k * kNcW * kNcT;
         if (t0 >= L) break;
         const int len = min(kNcT, L - t0);
-        {   // this lane's token: m_t B_t as hi / lo rows (zeros past the row)
-            const uint32_t w[8] = {braw[k][0].x, braw[k][0].y, braw[k][0].z, braw[k][0].w,
-                                   braw[k][1].x, braw[k][1].y, braw[k][1].z, braw[k][1].w};
-            uint32_t hw[8], lw[8];
+        // this lane's token: m_t B_t as hi / lo rows (zeros past the row)
+        const uint32_t w[8] = {braw[k][0].x, braw[k][0].y, braw[k][0].z, braw[k][0].w,
+                               braw[k][1].x, braw[k][1].y, braw[k][1].z, braw[k][1].w};
+        uint32_t hw[8], lw[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float2 a = bf16x2_to_f2(w[q]);
-                unsigned short h0, l0, h1, l1;
-                split_bf16(mj[k] * a.x, h0, l0);
-                split_bf16(mj[k] * a.y, h1, l1);
-                hw[q] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-                lw[q] = (uint32_t)l0 | ((uint32_t)l1 << 16);
-            }
-            uint4 *dh = reinterpret_cast<uint4 *>(&mw[lane][0]);
-            uint4 *dl = reinterpret_cast<uint4 *>(&mw[32 + lane][0]);
-            dh[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            dh[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-            dl[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            dl[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+        for (int q = 0; q < 8; ++q) {
+            const float2 a = bf16x2_to_f2(w[q]);
+            unsigned short h0, l0, h1, l1;
+            split_bf16(mj[k] * a.x, h0, l0);
+            split_bf16(mj[k] * a.y, h1, l1);
+            hw[q] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+            lw[q] = (uint32_t)l0 | ((uint32_t)l1 << 16);
         }
-        __syncwarp();
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
             if (ks * 16 >= len) break;
+            if ((lane >> 4) == ks) {                   // the step's 16 tokens: rows hi 0..15, lo 16..31
+                uint4 *dh = reinterpret_cast<uint4 *>(&mw[lane & 15][0]);
+                uint4 *dl = reinterpret_cast<uint4 *>(&mw[16 + (lane & 15)][0]);
+                dh[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                dh[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+                dl[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                dl[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+            }
+            __syncwarp();
             uint32_t a[2][4], bh[4], bl[4];
             const int c0 = t0 + ks * 16 + 2 * t4;
             // a token pair at or past the row's end reads the next row: keep
@@ -682,9 +685,9 @@ __global__ void __launch_bounds__(kNcW * 32, 4) ncssd_rows_kernel(const NcssdPar
                 a[mt][2] = lds_pair(xr, e + 8) & m8;
                 a[mt][3] = lds_pair(xr, e + 8 * L + 8) & m8;
             }
-            const int kr = ks * 16 + ((lane >> 3) & 1) * 8 + (lane & 7), nc = (lane >> 4) * 8;
+            const int kr = ((lane >> 3) & 1) * 8 + (lane & 7), nc = (lane >> 4) * 8;
             ldsm_x4_t(&mw[kr][nc], bh);
-            ldsm_x4_t(&mw[32 + kr][nc], bl);
+            ldsm_x4_t(&mw[16 + kr][nc], bl);
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -692,8 +695,8 @@ __global__ void __launch_bounds__(kNcW * 32, 4) ncssd_rows_kernel(const NcssdPar
                     mma_bf16(acc[mt][nt], a[mt], bh[2 * nt], bh[2 * nt + 1]);
                     mma_bf16(acc[mt][nt], a[mt], bl[2 * nt], bl[2 * nt + 1]);
                 }
+            __syncwarp();                              // the rows are read before the next step's
         }
-        __syncwarp();
     }
 
     // ---- 2. join: the warps' sums in warp order, as bf16 hi / lo
@@ -707,12 +710,21 @@ __global__ void __launch_bounds__(kNcW * 32, 4) ncssd_rows_kernel(const NcssdPar
             *reinterpret_cast<float2 *>(q + 8 * 16) = make_float2(acc[mt][nt][2], acc[mt][nt][3]);
         }
     __syncthreads();
-    for (int e = threadIdx.x; e < 32 * 16; e += kNcW * 32) {
-        float s = 0.f;
+    constexpr int kPer = 32 * 16 / (kNcW * 32);
+    float hs[kPer];
 #pragma unroll
-        for (int w = 0; w < kNcW; ++w) s += part[w * 32 * 16 + e];
+    for (int i = 0; i < kPer; ++i) {
+        const int e = threadIdx.x + i * kNcW * 32;
+        hs[i] = 0.f;
+#pragma unroll
+        for (int w = 0; w < kNcW; ++w) hs[i] += part[w * 32 * 16 + e];
+    }
+    __syncthreads();                                   // hb overlaps part
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int e = threadIdx.x + i * kNcW * 32;
         unsigned short hi, lo;
-        split_bf16(s, hi, lo);
+        split_bf16(hs[i], hi, lo);
         hb[0][e >> 4][e & 15] = hi;
         hb[1][e >> 4][e & 15] = lo;
     }
