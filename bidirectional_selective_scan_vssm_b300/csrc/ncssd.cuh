@@ -738,12 +738,14 @@ __global__ void __launch_bounds__(kNcW * 32, 6) ncssd_rows_kernel(const NcssdPar
         ldsm_x4(&hb[0][mt * 16 + (lane & 15)][(lane >> 4) * 8], ah[mt]);
         ldsm_x4(&hb[1][mt * 16 + (lane & 15)][(lane >> 4) * 8], al[mt]);
     }
-    float dv[2][2];
+    f2 dv[2][2];                                       // (D, D) of rows g, g + 8 of each m tile
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
-        dv[mt][0] = ds[mt * 16 + g];
-        dv[mt][1] = ds[mt * 16 + g + 8];
+        dv[mt][0] = pack2(ds[mt * 16 + g], ds[mt * 16 + g]);
+        dv[mt][1] = pack2(ds[mt * 16 + g + 8], ds[mt * 16 + g + 8]);
     }
+    const f2 half2 = pack2(0.5f, 0.5f);
+    auto f32_of = [](unsigned short v) { return __uint_as_float((uint32_t)v << 16); };
 #pragma unroll
     for (int k = 0; k < kNcRowsTiles; ++k) {
         const int t0 = warp * kNcT + k * kNcW * kNcT;
@@ -763,18 +765,17 @@ __global__ void __launch_bounds__(kNcW * 32, 6) ncssd_rows_kernel(const NcssdPar
                 for (int hr = 0; hr < 2; ++hr) {
                     const int r = mt * 16 + g + 8 * hr;
                     const int e = r * L + col;
-                    float y0 = d[2 * hr], y1 = d[2 * hr + 1];
-                    if (SKIP) {
-                        const float2 xv = bf16x2_to_f2(lds_pair(xr, e));
-                        y0 = fmaf(dv[mt][hr], xv.x, y0);
-                        y1 = fmaf(dv[mt][hr], xv.y, y1);
-                    }
+                    // the pair in packed f32x2: y + D x, then y silu(z) with
+                    // silu(z) = h + h tanh(h), h = z / 2 (as silu_f32 for bf16)
+                    f2 y = pack2(d[2 * hr], d[2 * hr + 1]);
+                    if (SKIP) y = fma2(dv[mt][hr], pack2(f32_of(xr[e]), f32_of(xr[e + 1])), y);
                     if (GATE) {
-                        const float2 zv = bf16x2_to_f2(lds_pair(zr, e));
-                        y0 *= silu_f32<__nv_bfloat16>(zv.x);
-                        y1 *= silu_f32<__nv_bfloat16>(zv.y);
+                        const f2 h = mul2(pack2(f32_of(zr[e]), f32_of(zr[e + 1])), half2);
+                        const float2 hv = unpack2(h);
+                        y = mul2(y, fma2(h, pack2(tanh_mufu(hv.x), tanh_mufu(hv.y)), h));
                     }
-                    const uint32_t o = bf16x2_bits(y0, y1);
+                    const float2 yv = unpack2(y);
+                    const uint32_t o = bf16x2_bits(yv.x, yv.y);
                     if (w0) xr[e] = (unsigned short)(o & 0xffffu);
                     if (w1) xr[e + 1] = (unsigned short)(o >> 16);
                 }
