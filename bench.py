@@ -494,11 +494,15 @@ def run_ncssd(args):
             "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(region_s / args.steps * 1e3, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+            "arithmetic": ("contractions as bf16 tensor-core MMAs on hi/lo operand splits, fp32 "
+                           "accumulation and epilogue" if wl.dtype == "bf16" else "fp32 FMA pipe"),
+            "data": "synthetic",
             "config": dict(workload_config(wl, l2_note), step="NC-SSD (vssm_ncssd)"),
             "gtokch_per_s": round(aggregate(wl.tokch * args.steps, world, region_s) / 1e9, 4),
             "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak,
-                         "unit": "GB/s", "frac": round(ach / hbm_peak, 4), "traffic": None,
+                         "unit": "GB/s", "frac": round(ach / hbm_peak, 4),
+                         "traffic": ncu_traffic(wl.name + "+ncssd"),
                          "peak_kind": peaks_kind, "kernel_avg_us": round(kern_avg_s * 1e6, 3),
                          "launches_per_call": 1,
                          "algorithmic_bytes_per_launch": step_bytes},
