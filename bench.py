@@ -259,11 +259,18 @@ class ClockSampler:
 # ------------------------------------------------------------------ helpers
 
 def source_sha() -> str:
+    """Hash of the CUDA sources' code (comments and blank lines removed, so
+    that a comment edit does not orphan the committed ncu records)."""
+    import re
     csrc = os.path.join(ROOT, "bidirectional_selective_scan_vssm_b300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+            text = open(os.path.join(csrc, f), encoding="utf-8").read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", "", text)
+            code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+            h.update(f.encode() + b"\0" + code.encode())
     return h.hexdigest()[:16]
 
 

@@ -5,26 +5,31 @@
 // one hidden state H[n][d] = sum_j m_j B_j[n] x[d][j] shared by all tokens,
 // then out[d][t] = (sum_n C_t[n] H[n][d] + D[d] x[d][t]) silu(z[d][t]).
 // There is no recurrence: two contractions of depth 16 per element, bound by
-// the bytes of x, z and out and by the FMA pipe about equally.
+// the bytes of x, z and out (6 bytes per element at bf16) once the
+// contractions are off the FMA pipe.
 //
-// One kernel, ncssd_kernel. A CTA of four warps owns 32 channels of one batch
-// entry over a token range; a thread-block cluster of Q CTAs (Q = 1, 2, 4 or
-// 8) covers the whole row, so that rows that are few and long still fill the
-// GPU.
+// Every kernel here is one launch per call: a CTA owns 32 channels of one
+// batch entry, sums their part of H, joins the partial sums on chip (warps
+// in order, then, with a cluster, its CTAs in rank order through distributed
+// shared memory) and writes the outputs. No workspace, no atomics; the sums
+// are added in a fixed order, so the result is the same on every run.
 //
-//  1. State. Warps take 32-token tiles in turn. A tile of x is read along
-//     tokens (lane = token, coalesced), scaled by m_j and written transposed
-//     to shared memory; B_j goes to shared memory as fp32. Then lane = channel:
-//     for each token the lane adds x m_j B_j[0..15] (B broadcast) to its 16
-//     fp32 sums in packed f32x2 FMAs.
-//  2. Join. The four warps' sums are added in shared memory in warp order;
-//     with Q > 1 every CTA then adds the Q CTA sums of its cluster in rank
-//     order through distributed shared memory. The order is fixed, so H is
-//     the same on every run.
-//  3. Output. Lane = token again: the lane holds C_t (16 fp32) and walks the
-//     32 channels, H[:, d] and D[d] broadcast from shared memory, reading x,
-//     z and writing out along tokens. x was read moments before by the same
-//     CTA, so its second read comes from L2.
+//  * ncssd_rows_kernel (bf16, 32 whole rows per CTA, L <= 256, dim a
+//    multiple of 8): the rows' x, z and out are contiguous spans moved by
+//    single bulk copies; both contractions on bf16 tensor-core MMAs.
+//  * ncssd_mma_kernel (bf16, any shape): 32 x 32 tiles staged by lanes
+//    along tokens; a cluster of Q = 1, 2, 4 or 8 CTAs covers a long row.
+//  * ncssd_kernel (fp32 I/O): the same structure on the FMA pipe:
+//     1. State. Warps take 32-token tiles in turn. A tile of x is read along
+//        tokens (lane = token, coalesced), scaled by m_j and written
+//        transposed to shared memory; B_j goes to shared memory as fp32. Then
+//        lane = channel: for each token the lane adds x m_j B_j[0..15] (B
+//        broadcast) to its 16 fp32 sums in packed f32x2 FMAs.
+//     2. Join, as above.
+//     3. Output. Lane = token again: the lane holds C_t (16 fp32) and walks
+//        the 32 channels, H[:, d] and D[d] broadcast from shared memory,
+//        reading x, z and writing out along tokens. x was read moments
+//        before by the same CTA, so its second read comes from L2.
 #pragma once
 
 #include <cuda_bf16.h>
