@@ -31,12 +31,14 @@ def _run(inp, skip=True, gate=True):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-# bf16 kernels: rows resident in shared memory for (2, 40, 9), (8, 48, 100) and
-# (44, 768, 197) (one CTA per row, dim a multiple of 8, L <= 400); otherwise
-# tiles, with 1, 1, 2, 4, 8, 8 CTAs per cluster. fp32: the FMA-pipe kernel.
-@pytest.mark.parametrize("shape", [(2, 40, 9), (8, 48, 100), (44, 768, 197), (1, 130, 1),
-                                   (1, 130, 33), (3, 64, 197), (2, 200, 300), (1, 64, 5000),
-                                   (1, 33, 1100)],
+# bf16 kernels: rows resident in shared memory for (2, 40, 9), (3, 64, 1),
+# (8, 48, 100), (44, 768, 197) and (44, 768, 256) (one CTA per 32 rows, dim a
+# multiple of 8, L <= 256); otherwise tiles, with 1 CTA per cluster for
+# (44, 768, 257), (1, 130, 1), (1, 130, 33) and 2, 4, 8, 8 for the rest.
+# fp32: the FMA-pipe kernel.
+@pytest.mark.parametrize("shape", [(2, 40, 9), (3, 64, 1), (8, 48, 100), (44, 768, 197),
+                                   (44, 768, 256), (44, 768, 257), (1, 130, 1), (1, 130, 33),
+                                   (3, 64, 197), (2, 200, 300), (1, 64, 5000), (1, 33, 1100)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_ncssd(dtype, shape):
     b, d, L = shape
