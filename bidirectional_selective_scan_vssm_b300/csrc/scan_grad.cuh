@@ -104,21 +104,34 @@ __global__ void __launch_bounds__(128) grad_ckpt_kernel(const GradParams p)
     const long long row = ((long long)b * p.dim + (act ? d : d0)) * p.L;
     const char *Bb = static_cast<const char *>(p.B[dir]) + (long long)b * p.L * 16 * sizeof(T);
     float *ck = p.ckpt + ((long long)slot * p.ngroups + grp) * p.nch * 512;
+    // steps and inputs of chunk s in scan order (independent loads, issued one
+    // chunk ahead so that their latency overlaps the current chunk's work)
+    auto fetch = [&](int s, float (&dtv)[kTG], float (&xv)[kTG]) {
+        const int j = dir == 0 ? s : p.nch - 1 - s;
+        const int t0 = j * kTG, t1 = min(p.L, t0 + kTG), len = t1 - t0;
+#pragma unroll
+        for (int k = 0; k < kTG; ++k) {
+            const bool in = act && s < p.nch && k < len;
+            const long long e = row + (dir == 0 ? t0 + k : t1 - 1 - k);
+            dtv[k] = in ? gload<T>(p.delta, e) : 0.f;
+            xv[k] = in ? gload<T>(p.x, e) : 0.f;
+        }
+    };
+    float ndt[kTG], nxv[kTG];
+    fetch(0, ndt, nxv);
     for (int s = 0; s < p.nch; ++s) {
         const int j = dir == 0 ? s : p.nch - 1 - s;          // chunk in scan order
         float *cj = ck + (long long)j * 512;
 #pragma unroll
         for (int n = 0; n < 16; ++n) cj[n * 32 + lane] = h[n];
         const int t0 = j * kTG, t1 = min(p.L, t0 + kTG), len = t1 - t0;
-        // the chunk's steps and inputs first (independent loads in flight together)
         float dtv[kTG], xv[kTG];
 #pragma unroll
         for (int k = 0; k < kTG; ++k) {
-            const bool in = act && k < len;
-            const long long e = row + (dir == 0 ? t0 + k : t1 - 1 - k);
-            dtv[k] = in ? gload<T>(p.delta, e) : 0.f;
-            xv[k] = in ? gload<T>(p.x, e) : 0.f;
+            dtv[k] = ndt[k];
+            xv[k] = nxv[k];
         }
+        fetch(s + 1, ndt, nxv);
 #pragma unroll
         for (int k = 0; k < kTG; ++k) {
             if (k < len) {
