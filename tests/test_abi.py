@@ -250,3 +250,39 @@ def test_grad_validation(v):
     assert call(_args(v), _grad_args(v), seg=-1) == -1
     assert call(_args(v), _grad_args(v)) == -6                    # no workspace
     assert call(_args(v, batch=0), _grad_args(v)) == 0            # empty: nothing to do
+
+
+def _nc_args(v, **kw):
+    a = v.NcssdArgs()
+    base = dict(x=(1 << 20) * 1, z=(1 << 20) * 2, B=(1 << 20) * 3, C=(1 << 20) * 4,
+                m=(1 << 20) * 5, D=(1 << 20) * 6, out=(1 << 20) * 7,
+                batch=2, dim=64, seqlen=50, dstate=16, dtype=1)
+    base.update(kw)
+    for k, val in base.items():
+        setattr(a, k, val)
+    return a
+
+
+def test_ncssd_needs_no_workspace(v):
+    n = ctypes.c_size_t(123)
+    assert v.lib.vssm_ncssd_workspace_size(ctypes.byref(_nc_args(v)), ctypes.byref(n)) == 0
+    assert n.value == 0
+    assert v.lib.vssm_ncssd_workspace_size(ctypes.byref(_nc_args(v, batch=-1)), ctypes.byref(n)) == -1
+
+
+def test_ncssd_validation(v):
+    def call(**kw):
+        return v.lib.vssm_ncssd(ctypes.byref(_nc_args(v, **kw)), None)
+    assert v.lib.vssm_ncssd(None, None) == -1
+    assert call(batch=-1) == -1
+    assert call(dstate=8) == -2
+    assert call(dtype=7) == -2
+    assert call(batch=70000) == -2
+    far = {k: (1 << 36) * (i + 1) for i, k in enumerate(("x", "z", "B", "C", "m", "D", "out"))}
+    assert call(dim=65536 * 32, **far) == -2             # more channel blocks than a grid row
+    for k in ("x", "B", "C", "m", "out"):
+        assert call(**{k: None}) == -1, k
+    assert call(z=(1 << 20) * 2 + 4) == -3               # misaligned
+    assert call(out=(1 << 20) * 2) == -1                 # out overlaps z
+    assert call(batch=0) == 0                            # empty: nothing to do
+    assert call(seqlen=0) == 0
