@@ -286,3 +286,53 @@ def test_ncssd_validation(v):
     assert call(out=(1 << 20) * 2) == -1                 # out overlaps z
     assert call(batch=0) == 0                            # empty: nothing to do
     assert call(seqlen=0) == 0
+
+
+def _al256(n):
+    return (n + 255) // 256 * 256
+
+
+def _host_ws(v, a, slices=0, seg=0):
+    n = ctypes.c_size_t(0)
+    st = v.lib.vssm_scan_host_workspace_size(ctypes.byref(a), seg, slices, ctypes.byref(n))
+    return st, n.value
+
+
+def _scan_ws(v, a, seg=0):
+    n = ctypes.c_size_t(0)
+    assert v.lib.vssm_scan_workspace_size(ctypes.byref(a), seg, ctypes.byref(n)) == 0
+    return n.value
+
+
+@pytest.mark.parametrize("batch,dim,slices", [(128, 768, 0), (128, 768, 16), (3, 768, 0), (1, 100, 4)])
+def test_host_pipeline_workspace(v, batch, dim, slices):
+    """vssm_scan_host's device workspace: the up-front parameters, then three
+    ring slots, each holding one slice's five activation arrays and that
+    slice's own scan workspace. Slices are whole batch entries when there are
+    at least as many entries as slices, else 32-channel-aligned ranges."""
+    L, es = 197, 2
+    a = _args(v, batch=batch, dim=dim, seqlen=L)
+    st, total = _host_ws(v, a, slices)
+    assert st == 0
+    S = slices or 8
+    if batch >= S:
+        per_b = -(-batch // S)
+        rows_b, rows_d = per_b, dim
+        nsl = -(-batch // per_b)
+        last = (batch - (nsl - 1) * per_b, dim)
+    else:
+        per_entry = max(1, -(-S // batch))
+        per_d = max(32, (-(-dim // per_entry) + 31) // 32 * 32)
+        rows_b, rows_d = 1, per_d
+        last = (1, dim % per_d or per_d)
+    ws = max(_scan_ws(v, _args(v, batch=rows_b, dim=min(rows_d, dim), seqlen=L)),
+             _scan_ws(v, _args(v, batch=last[0], dim=last[1], seqlen=L)))
+    slot = _al256(5 * _al256(rows_b * rows_d * L * es) + ws)
+    up = 4 * _al256(batch * L * 16 * es) + 2 * _al256(dim * 16 * 4) + 6 * _al256(dim * 4) + 2 * _al256(dim * 4)
+    assert total == up + 3 * slot
+
+
+def test_host_pipeline_validation(v):
+    assert _host_ws(v, _args(v), slices=-1)[0] == -1
+    assert _host_ws(v, _args(v, batch=0))[1] == 0
+    assert v.lib.vssm_scan_host(ctypes.byref(_args(v)), 0, 0, None) == -6      # no workspace
