@@ -59,7 +59,8 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
-                   help="target CPU time of the oracle sample")
+                   help="target CPU time of the oracle sample (the reference arm: at most this "
+                        "per step)")
     p.add_argument("--fused-step", action="store_true",
                    help="pass per-direction steps before softplus, with biases (the kernel "
                         "applies softplus(delta + bias))")
@@ -376,7 +377,9 @@ def run_reference(args):
         return
     wl = selected_workload(args)
     inp = make_inputs(wl, seed=0)
-    per_step = min(10.0, max(0.2, 150.0 / max(1, args.steps + args.warmup)))
+    # each step: a bounded oracle sample, so that the whole run stays within a
+    # few minutes (at most --cpu-seconds per step)
+    per_step = min(args.cpu_seconds, max(0.2, 150.0 / max(1, args.steps + args.warmup)))
     bpt = algorithmic_bytes(wl) / wl.tokch
     for _ in range(args.warmup):
         oracle_sample_run(wl, inp, per_step)

@@ -56,3 +56,25 @@ def test_single_process_defaults():
     assert bench.dist_env()[1] >= 1
     assert bench.reduce_max(3.5) == 3.5
     assert bench.aggregate(10.0, 1, 2.0) == 5.0
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """`bench.py --impl reference` launched the way the multi-GPU run is: two
+    ranks over torch.distributed.run; rank 0 times the oracle and prints the
+    one JSON line, the other rank exits 0 without work."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr=127.0.0.1", f"--master-port={_free_port()}", "bench.py",
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3",
+           "--workload", "vim_ti_224", "--cpu-seconds", "0.3"]
+    r = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
