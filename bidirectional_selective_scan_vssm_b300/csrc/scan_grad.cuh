@@ -61,8 +61,10 @@ struct GradParams {
     float *dA[2], *dD[2];
     float *ckpt;                        // [slot][ngroups][nch][16][32]
     float *part;                        // [ngroups][L][3][32] (both directions only)
+    float *summ;                        // [slot][ngroups][nrange][P 16 | q 16][32] (nrange > 1)
     unsigned *err;
     int batch, dim, L, seg_len, rgroups, nch;
+    int nrange, rch;                    // token ranges per row, chunks per range
     long long ngroups;                  // batch * rgroups
 };
 
@@ -150,6 +152,71 @@ __global__ void __launch_bounds__(128) grad_ckpt_kernel(const GradParams p)
     }
 }
 
+// Adjoint range summaries, for rows cut into nrange ranges of rch chunks. The
+// adjoint of a direction runs against its scan order, l_t = ds_t C_t + lam
+// and then lam = a_t l_t (a_t = exp(delta_t A), 0 at a folded reset), so a
+// range walked from an incoming lam hands lam_out = P lam + q to the next
+// range in walk order, with P = prod(a_t) over the range (exp(A sum(delta)),
+// or 0 across a reset) and q the hand-over of the walk from lam = 0. These
+// maps compose associatively, exactly as the forward range summaries; one
+// warp per (direction, group, range) stores (P, q) for the adjoint kernel's
+// start-up fold.
+template <typename T, int DIRS>
+__global__ void __launch_bounds__(128) grad_adj_summary_kernel(const GradParams p)
+{
+    constexpr int NDIR = (DIRS == 3) ? 2 : 1;
+    constexpr float kLog2e = 1.4426950408889634f;
+    const int lane = threadIdx.x & 31;
+    const long long u = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (u >= (long long)NDIR * p.ngroups * p.nrange) return;
+    const int rr = (int)(u % p.nrange);
+    const long long gu = u / p.nrange;
+    const int slot = (int)(gu / p.ngroups);
+    const long long grp = gu % p.ngroups;
+    const int dir = (DIRS == 3) ? slot : (DIRS == 1 ? 0 : 1);
+    const int b = (int)(grp / p.rgroups), d0 = (int)(grp % p.rgroups) * 32;
+    const int d = d0 + lane;
+    const bool act = d < p.dim;
+    const int ta = min(p.L, rr * p.rch * kTG), tb = min(p.L, (rr + 1) * p.rch * kTG);
+    float Al2[16], lam[16];
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+        Al2[n] = act ? p.A[dir][(long long)d * 16 + n] * kLog2e : 0.f;
+        lam[n] = 0.f;
+    }
+    const long long row = ((long long)b * p.dim + (act ? d : d0)) * p.L;
+    const T *Cb = static_cast<const T *>(p.C[dir]) + (long long)b * p.L * 16;
+    const bool hasZ = p.z != nullptr;
+    float sdt = 0.f;
+    bool cut = false;
+    for (int k = 0; k < tb - ta; ++k) {
+        const int t = dir == 0 ? tb - 1 - k : ta + k;            // against the scan order
+        const float dt = act ? gload<T>(p.delta, row + t) : 0.f;
+        const float go = act ? gload<T>(p.dout, row + t) : 0.f;
+        float ds = go;
+        if (hasZ) {
+            const float zv = act ? gload<T>(p.z, row + t) : 0.f;
+            ds = go * (zv * __frcp_rn(1.f + ex2_mufu(-kLog2e * zv)));
+        }
+        float Cv[16];
+        load16_f32(Cb + (long long)t * 16, Cv);
+        const bool rs = reset_at(t, p.seg_len, dir);
+        cut = cut || rs;
+        sdt += dt;
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+            const float l = fmaf(ds, Cv[n], lam[n]);
+            lam[n] = (rs ? 0.f : ex2_mufu(dt * Al2[n])) * l;
+        }
+    }
+    float *sm = p.summ + (((long long)slot * p.ngroups + grp) * p.nrange + rr) * 1024;
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+        sm[n * 32 + lane] = cut ? 0.f : ex2_mufu(sdt * Al2[n]);
+        sm[(16 + n) * 32 + lane] = lam[n];
+    }
+}
+
 // 16 bytes of shared memory as two fp32 pairs, and back (ordered against the
 // warp's other shared-memory accesses by the memory clobber).
 __device__ __forceinline__ void lds2(const float *p, f2 &a, f2 &b)
@@ -218,7 +285,8 @@ grad_adjoint_kernel(const GradParams p)
     constexpr int TP = Lay::kTP, ES = Lay::ES;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long long grp = blockIdx.x;
+    const long long grp = blockIdx.x / p.nrange;          // CTA = (group, token range)
+    const int rr = (int)(blockIdx.x % p.nrange);
     const int slot = warp;
     const int dir = (DIRS == 3) ? warp : (DIRS == 1 ? 0 : 1);
     unsigned char *wsm = smem_raw + warp * Lay::kWarpBytes;
@@ -258,28 +326,47 @@ grad_adjoint_kernel(const GradParams p)
     float *my_h = hb + lane * 4;              // quarter q of slot s: my_h + (s * 4 + q) * 128
     const void *arr[4] = {p.delta, p.x, hasZ ? p.z : p.x, p.dout};
 
-    const int Hc = (p.nch + 1) / 2;
+    // this CTA's chunks [rlo, rhi); the two directions meet in its middle
+    const int rlo = rr * p.rch, rhi = min(p.nch, rlo + p.rch);
+    const int Hc = rlo + (rhi - rlo + 1) / 2;
     const int nphase = (DIRS == 3) ? 2 : 1;
     // chunk list: phase 0 then phase 1, each against the scan order
     auto chunk_of = [&](int phase, int s, int &j) -> bool {
         int clo, chi;
         if (DIRS == 3) {
             const bool upper = (dir == 0) == (phase == 0);
-            clo = upper ? Hc : 0;
-            chi = upper ? p.nch : Hc;
+            clo = upper ? Hc : rlo;
+            chi = upper ? rhi : Hc;
         } else {
-            clo = 0;
-            chi = p.nch;
+            clo = rlo;
+            chi = rhi;
         }
         if (s >= chi - clo) return false;
         j = dir == 0 ? chi - 1 - s : clo + s;
         return true;
     };
     auto nchunks = [&](int phase) {
-        if (DIRS != 3) return p.nch;
+        if (DIRS != 3) return rhi - rlo;
         const bool upper = (dir == 0) == (phase == 0);
-        return upper ? p.nch - Hc : Hc;
+        return upper ? rhi - Hc : Hc - rlo;
     };
+    // the lam entering this range, from the summaries of the ranges before it
+    // in walk order (the forward direction walks right to left, the backward
+    // one left to right), nearest last
+    if (p.nrange > 1 && act) {
+        const float *sg = p.summ + ((long long)slot * p.ngroups + grp) * p.nrange * 1024 + lane;
+        const int n_before = dir == 0 ? p.nrange - 1 - rr : rr;
+        for (int k = 0; k < n_before; ++k) {
+            const int r2 = dir == 0 ? p.nrange - 1 - k : k;
+            const float *sm = sg + (long long)r2 * 1024;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const f2 P = pack2(__ldcg(sm + (2 * q) * 32), __ldcg(sm + (2 * q + 1) * 32));
+                const f2 Q = pack2(__ldcg(sm + (16 + 2 * q) * 32), __ldcg(sm + (17 + 2 * q) * 32));
+                lam[q] = fma2(P, lam[q], Q);
+            }
+        }
+    }
     // copy chunk j (phase ph) into ring stage st and commit it as one group
     auto issue = [&](int st, int j, bool fin) {
         unsigned char *sg = wsm + st * Lay::kStage;

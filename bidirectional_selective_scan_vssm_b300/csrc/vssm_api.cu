@@ -579,9 +579,17 @@ int run(const vssm_scan_args *a, int seg_len, bool folded, int pieces_req, void 
 
 struct GradPlan {
     int ndir = 1, rgroups = 0, nch = 0;
+    int nrange = 1, rch = 0;          // token ranges per row for the adjoint, chunks per range
     long long ngroups = 0;
-    size_t ckpt_bytes = 0, part_off = 0, workspace = 0;
+    size_t ckpt_bytes = 0, part_off = 0, summ_off = 0, workspace = 0;
 };
+
+// Rows are cut into ranges for the adjoint when there are too few of them
+// to fill the GPU (about two waves of the adjoint's two-warp CTAs at four
+// per SM), keeping at least 16 chunks (64 tokens) per range; the ranges are
+// joined by the adjoint summaries (grad_adj_summary_kernel).
+constexpr long long kGradTargetCtas = 148LL * 8;
+constexpr int kGradMaxRanges = 16, kGradMinRangeChunks = 16;
 
 GradPlan make_grad_plan(const vssm_scan_args *a)
 {
@@ -590,10 +598,22 @@ GradPlan make_grad_plan(const vssm_scan_args *a)
     g.rgroups = (a->dim + 31) / 32;
     g.ngroups = (long long)a->batch * g.rgroups;
     g.nch = (a->seqlen + vssm::kTG - 1) / vssm::kTG;
+    g.rch = g.nch;
+    if (g.ngroups > 0 && g.ngroups < kGradTargetCtas) {
+        const long long want = std::min<long long>(kGradMaxRanges, (kGradTargetCtas + g.ngroups - 1) / g.ngroups);
+        const int r = (int)std::min<long long>(want, g.nch / kGradMinRangeChunks);
+        if (r > 1) {
+            g.rch = (g.nch + r - 1) / r;
+            g.nrange = (g.nch + g.rch - 1) / g.rch;
+        }
+    }
     g.ckpt_bytes = (size_t)g.ndir * g.ngroups * g.nch * 512 * sizeof(float);
     g.part_off = (g.ckpt_bytes + 255) / 256 * 256;
-    g.workspace = a->dir_flags == 3 ? g.part_off + (size_t)g.ngroups * a->seqlen * 96 * sizeof(float)
-                                    : g.ckpt_bytes;
+    const size_t part_end = a->dir_flags == 3 ? g.part_off + (size_t)g.ngroups * a->seqlen * 96 * sizeof(float)
+                                              : g.ckpt_bytes;
+    g.summ_off = (part_end + 255) / 256 * 256;
+    g.workspace = g.nrange > 1 ? g.summ_off + (size_t)g.ndir * g.ngroups * g.nrange * 1024 * sizeof(float)
+                               : part_end;
     return g;
 }
 
@@ -614,11 +634,17 @@ int launch_grad(const vssm::GradParams &p, const GradPlan &g, cudaStream_t s)
     vssm::grad_ckpt_kernel<T, DIRS><<<(unsigned)((units + 3) / 4), 128, 0, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    if (g.nrange > 1) {
+        const long long su = units * g.nrange;
+        vssm::grad_adj_summary_kernel<T, DIRS><<<(unsigned)((su + 3) / 4), 128, 0, s>>>(p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    }
     const size_t smem = (size_t)NDIR * vssm::GradLayout<T, DIRS>::kWarpBytes;
     auto kern = vssm::grad_adjoint_kernel<T, DIRS>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    kern<<<(unsigned)g.ngroups, NDIR * 32, smem, s>>>(p);
+    kern<<<(unsigned)(g.ngroups * g.nrange), NDIR * 32, smem, s>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
     return VSSM_OK;
@@ -1115,7 +1141,7 @@ int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len
     if (!a->workspace || a->workspace_bytes < gl.workspace)
         return fail(VSSM_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", gl.workspace,
                     a->workspace ? a->workspace_bytes : (size_t)0);
-    if (gl.ngroups > 0x7fffffffLL) return fail(VSSM_ERR_UNSUPPORTED, "problem too large for one grid");
+    if (gl.ngroups * gl.nrange > 0x7fffffffLL) return fail(VSSM_ERR_UNSUPPORTED, "problem too large for one grid");
     const size_t es = a->dtype == VSSM_F32 ? 4 : 2;
     const size_t nact = (size_t)a->batch * a->dim * a->seqlen * es;
     const size_t nbc = (size_t)a->batch * a->seqlen * a->dstate * 4;
@@ -1167,6 +1193,8 @@ int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len
     p.ckpt = static_cast<float *>(a->workspace);
     p.part = dirs == 3 ? reinterpret_cast<float *>(static_cast<char *>(a->workspace) + gl.part_off)
                        : nullptr;
+    p.summ = gl.nrange > 1 ? reinterpret_cast<float *>(static_cast<char *>(a->workspace) + gl.summ_off)
+                           : nullptr;
     p.err = device_error_word();
     if (!p.err) return fail(VSSM_ERR_CUDA, "cannot locate the device error word");
     p.batch = a->batch;
@@ -1175,6 +1203,8 @@ int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len
     p.seg_len = seg_len;
     p.rgroups = gl.rgroups;
     p.nch = gl.nch;
+    p.nrange = gl.nrange;
+    p.rch = gl.rch;
     p.ngroups = gl.ngroups;
     // the reductions accumulate atomically: start them at zero
     const size_t nbcf = (size_t)a->batch * a->seqlen * a->dstate;

@@ -226,11 +226,21 @@ def test_grad_workspace_size(v):
     n = ctypes.c_size_t()
     assert v.lib.vssm_scan_grad_workspace_size(ctypes.byref(a), 0, ctypes.byref(n)) == 0
     # checkpoints: 2 directions x 12 groups x 50 chunks of 4 tokens x 16 x 32 floats,
-    # then partial dx, ddelta, dz: 12 groups x 197 tokens x 3 x 32 floats
-    assert n.value == 2 * 12 * 50 * 512 * 4 + 12 * 197 * 96 * 4
+    # then partial dx, ddelta, dz: 12 groups x 197 tokens x 3 x 32 floats; 12 groups
+    # are too few to fill the GPU, so each row is cut into 3 ranges of 17 chunks for the
+    # adjoint, with a (P, q) summary of 2 x 16 x 32 floats per direction, group and range
+    assert n.value == 2 * 12 * 50 * 512 * 4 + 12 * 197 * 96 * 4 + 2 * 12 * 3 * 1024 * 4
     a1 = _args(v, batch=1, dim=384, seqlen=197, dtype=0, dir_flags=1)
     assert v.lib.vssm_scan_grad_workspace_size(ctypes.byref(a1), 0, ctypes.byref(n)) == 0
-    assert n.value == 12 * 50 * 512 * 4
+    assert n.value == 12 * 50 * 512 * 4 + 12 * 3 * 1024 * 4
+    # enough groups (128 x 24 = 3072): whole rows, no summaries
+    a2 = _args(v, batch=128, dim=768, seqlen=197)
+    assert v.lib.vssm_scan_grad_workspace_size(ctypes.byref(a2), 0, ctypes.byref(n)) == 0
+    assert n.value == 2 * 3072 * 50 * 512 * 4 + 3072 * 197 * 96 * 4
+    # short rows (fewer than 32 chunks) are never cut
+    a3 = _args(v, batch=1, dim=384, seqlen=100)
+    assert v.lib.vssm_scan_grad_workspace_size(ctypes.byref(a3), 0, ctypes.byref(n)) == 0
+    assert n.value == 2 * 12 * 25 * 512 * 4 + 12 * 100 * 96 * 4
 
 
 def test_grad_validation(v):

@@ -98,6 +98,51 @@ def test_grad_folded(dtype, dirs, seg, nseg):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dirs", [DIR_FWD, DIR_BWD, DIR_BOTH])
+def test_grad_long_rows_cut_into_ranges(dtype, dirs):
+    """Two 32-channel groups of 1001-token rows: too few groups to fill the
+    GPU, so the adjoint runs each row as 15 ranges of 17 chunks (the last one
+    ragged), joined by the adjoint summaries."""
+    wl = WORKLOADS["vim_ti_224"].scaled(batch=1, dim=40, seqlen=1001, dtype=dtype, dirs=dirs)
+    inp = make_inputs(wl, seed=840)
+    got, ref = _run(inp, dirs)
+    _compare(got, ref, dtype, "ranges")
+
+
+@pytest.mark.parametrize("dirs", [DIR_FWD, DIR_BWD, DIR_BOTH])
+def test_grad_long_folded_rows_cut_into_ranges(dirs):
+    """Folded rows of 20 segments of 51 tokens, cut into ranges that start and
+    end inside segments: the resets must cut the adjoint carry between ranges."""
+    wl = WORKLOADS["sf_folded"].scaled(batch=1, dim=40, seqlen=51 * 20, seg_len=51, dtype="f32",
+                                       dirs=dirs)
+    inp = make_inputs(wl, seed=850)
+    got, ref = _run(inp, dirs, seg_len=51)
+    _compare(got, ref, "f32", "folded ranges")
+
+
+def test_grad_long_workload_sampled():
+    """The 1024² workload (8 x 4097 tokens x 768 channels, 192 groups, rows run as
+    ranges): dB, dC of one batch entry and dx of sampled rows against the oracle."""
+    wl = WORKLOADS["vim_s_1024"]
+    inp = make_inputs(wl, seed=0)
+    t = to_device(inp)
+    dout_t, dout = _dout(inp, 3)
+    got = vssm.scan_grad(t["x"], t["delta"], t["A_fwd"], t["A_bwd"], t["B"], t["C"], t["D_fwd"],
+                         t["D_bwd"], t["z"], dout=dout_t)
+    b = 5
+    sl = slice(b, b + 1)
+    ref = oracle.scan_grad(inp.x[sl], inp.delta[sl], inp.A_fwd, inp.A_bwd, inp.B[sl], inp.C[sl],
+                           inp.D_fwd, inp.D_bwd, inp.z[sl], dout[sl])
+    for k in ("dB", "dC"):
+        err = normwise_rel(got[k][b].cpu().numpy(), ref[k][0])
+        assert err <= SUM_TOL["bf16"], f"{k}: {err:.3e}"
+    for d in (0, 31, 32, 400, 767):
+        for k in ("dx", "ddelta", "dz"):
+            err = normwise_rel(got[k][b, d].float().cpu().numpy(), ref[k][0, d])
+            assert err <= TOL["bf16"], f"{k} row ({b}, {d}): {err:.3e}"
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_grad_backward_own_B_C(dtype):
     wl = WORKLOADS["vim_ti_224"].scaled(batch=2, dim=48, seqlen=70, dtype=dtype)
     inp = make_inputs(wl, seed=830)
