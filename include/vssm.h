@@ -279,7 +279,10 @@ int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len
 /* Workspace bytes of vssm_scan_grad: 16 bytes per token, channel and
  * direction for the state checkpoints (16 fp32 every 4 tokens), plus 12 bytes
  * per token and channel for the partial gradients exchanged between the two
- * directions (both directions only), channels rounded up to groups of 32. */
+ * directions (both directions only), channels rounded up to groups of 32.
+ * When there are too few 32-channel groups to fill the GPU, the rows are cut
+ * into token ranges for the adjoint, and 128 bytes per range, channel and
+ * direction hold the ranges' adjoint summaries. */
 int vssm_scan_grad_workspace_size(const vssm_scan_args *a, int seg_len, size_t *bytes);
 
 /*
