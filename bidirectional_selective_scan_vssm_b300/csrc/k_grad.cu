@@ -1,0 +1,87 @@
+// Launchers of the gradient kernels (scan_grad.cuh).
+#include <algorithm>
+
+#include "launch.h"
+
+namespace vssm {
+
+namespace {
+
+// Test of the bounded-wait path: one warp waits on a pair barrier whose
+// second arrival never comes, gives up after limit_ns and records a timeout
+// in the device error word as the kernels with bounded waits do.
+__global__ void selftest_wait_kernel(unsigned *err, uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 2);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0) mbar_arrive(&bar);
+    const bool met = mbar_wait(&bar, 0, limit_ns);
+    if (!__all_sync(0xffffffffu, met) && threadIdx.x == 0) atomicOr(err, kErrTimeout);
+}
+
+__global__ void zero_f32_kernel(float *p, long long n)
+{
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x)
+        p[i] = 0.f;
+}
+
+
+template <typename T, int DIRS>
+cudaError_t launch_dirs(const GradParams &p, long long ngroups, int nrange, cudaStream_t s)
+{
+    constexpr int NDIR = DIRS == 3 ? 2 : 1;
+    const long long units = (long long)NDIR * ngroups;
+    grad_ckpt_kernel<T, DIRS><<<(unsigned)((units + 3) / 4), 128, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (nrange > 1) {
+        const long long su = units * nrange;
+        grad_adj_summary_kernel<T, DIRS><<<(unsigned)((su + 3) / 4), 128, 0, s>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    const size_t smem = (size_t)NDIR * GradLayout<T, DIRS>::kWarpBytes;
+    auto kern = grad_adjoint_kernel<T, DIRS>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+        return e;
+    kern<<<(unsigned)(ngroups * nrange), NDIR * 32, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_typed(const GradParams &p, int dirs, long long ngroups, int nrange, cudaStream_t s)
+{
+    switch (dirs) {
+    case 1: return launch_dirs<T, 1>(p, ngroups, nrange, s);
+    case 2: return launch_dirs<T, 2>(p, ngroups, nrange, s);
+    default: return launch_dirs<T, 3>(p, ngroups, nrange, s);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_grad(const GradParams &p, int dirs, bool f32, long long ngroups, int nrange, cudaStream_t s)
+{
+    return f32 ? launch_typed<float>(p, dirs, ngroups, nrange, s)
+               : launch_typed<__nv_bfloat16>(p, dirs, ngroups, nrange, s);
+}
+
+cudaError_t launch_zero_f32(float *p, size_t n, cudaStream_t s)
+{
+    if (!p || n == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, 148 * 8);
+    zero_f32_kernel<<<blocks, 256, 0, s>>>(p, (long long)n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_wait(unsigned *err, uint64_t limit_ns, cudaStream_t s)
+{
+    selftest_wait_kernel<<<1, 32, 0, s>>>(err, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace vssm

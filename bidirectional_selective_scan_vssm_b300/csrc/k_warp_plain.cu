@@ -1,0 +1,6 @@
+// Warp-per-channel-group scan variants with SP = false, CONV = false.
+#include "k_warp_opts.cuh"
+
+namespace vssm {
+VSSM_WARP_OPTS_DEFINE(false, false)
+}  // namespace vssm

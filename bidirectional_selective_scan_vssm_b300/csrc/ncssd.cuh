@@ -37,7 +37,7 @@
 #include <stdint.h>
 
 #include "ptx.cuh"
-#include "scan_warp.cuh"
+#include "common.cuh"
 
 namespace vssm {
 

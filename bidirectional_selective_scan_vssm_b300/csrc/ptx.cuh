@@ -83,6 +83,12 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t 
                  : "memory");
 }
 
+// Per-thread 16-byte async copy global -> shared of a whole block.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
 // Store v to global memory when pred holds (a predicated store, no branch).
 // No memory clobber: the compiler may move other loads and stores across it;
 // it stays ordered with the other volatile asm, fences included.
@@ -185,6 +191,19 @@ __device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c)
     return d;
 }
 
+// In-place forms: the accumulator keeps its register pair (a loop-carried
+// state updated in place needs no copy at the loop's back edge).
+// acc = a * acc + c
+__device__ __forceinline__ void fma2_scale_acc(f2 &acc, f2 a, f2 c)
+{
+    asm("fma.rn.f32x2 %0, %1, %0, %2;" : "+l"(acc.v) : "l"(a.v), "l"(c.v));
+}
+// acc = a * b + acc
+__device__ __forceinline__ void fma2_acc(f2 &acc, f2 a, f2 b)
+{
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc.v) : "l"(a.v), "l"(b.v));
+}
+
 __device__ __forceinline__ f2 add2(f2 a, f2 b)
 {
     f2 d;
@@ -255,6 +274,23 @@ __device__ __forceinline__ float lg2_mufu(float x)
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Invalidate a 128-byte line of global memory in L2 without writing it back
+// (its contents become undefined). Used for scratch that has been read for
+// the last time.
+__device__ __forceinline__ void discard_l2(const void *p)
+{
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
+// Two fp32 values rounded (to nearest even) to bf16 and packed: lo in bits
+// 0..15, hi in bits 16..31.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 // softplus(v) = log(1 + exp(v)) = ln 2 * log2(1 + 2^(v * log2 e)) on the MUFU

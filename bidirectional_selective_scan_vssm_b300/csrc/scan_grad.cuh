@@ -43,7 +43,7 @@
 #include <stdint.h>
 
 #include "ptx.cuh"
-#include "scan_warp.cuh"
+#include "common.cuh"
 
 namespace vssm {
 
@@ -583,29 +583,6 @@ grad_adjoint_kernel(const GradParams p)
         }
         atomicAdd(p.dD[dir] + d, dD);
     }
-}
-
-// Test of the bounded-wait path: one warp waits on a pair barrier whose
-// second arrival never comes, gives up after limit_ns and records a timeout
-// in the device error word exactly as the scan kernels do.
-__global__ void selftest_wait_kernel(unsigned *err, uint64_t limit_ns)
-{
-    __shared__ uint64_t bar;
-    if (threadIdx.x == 0) {
-        mbar_init(&bar, 2);
-        fence_mbar_init();
-    }
-    __syncwarp();
-    if (threadIdx.x == 0) mbar_arrive(&bar);
-    const bool met = mbar_wait(&bar, 0, limit_ns);
-    if (!__all_sync(0xffffffffu, met) && threadIdx.x == 0) atomicOr(err, kErrTimeout);
-}
-
-__global__ void zero_f32_kernel(float *p, long long n)
-{
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-         i += (long long)gridDim.x * blockDim.x)
-        p[i] = 0.f;
 }
 
 }  // namespace vssm

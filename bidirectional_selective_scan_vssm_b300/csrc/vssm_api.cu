@@ -1,19 +1,15 @@
 // C ABI of the selective-scan library (declared in include/vssm.h):
-// argument validation, variant selection and launch on the caller's stream.
+// argument validation, planning and launch on the caller's stream.
 #include <algorithm>
-#include <atomic>
+#include <cmath>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 
-#include <mutex>
-
-#include "scan_kernel.cuh"
-#include "ncssd.cuh"
-#include "scan_grad.cuh"
-#include "scan_warp.cuh"
+#include "launch.h"
 #include "vssm.h"
 
 // Device error word written by kernels whose bounded waits expire (one per
@@ -41,6 +37,11 @@ int fail(int status, const char *fmt, ...)
     return status;
 }
 
+int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(VSSM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool overlaps(const void *a, size_t na, const void *b, size_t nb)
@@ -48,6 +49,32 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb)
     if (!a || !b || na == 0 || nb == 0) return false;
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
     return a0 < b0 + nb && b0 < a0 + na;
+}
+
+size_t al256(size_t n) { return (n + 255) / 256 * 256; }
+
+// Multiprocessors of the current device, queried once per device (148 on a
+// B300; the same figure when no device is visible, so that sizes reported
+// without a GPU match a B300).
+int sm_count()
+{
+    static std::mutex mu;
+    static int cnt[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return 148;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cnt[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+            cudaGetLastError();
+            v = 148;
+        }
+        cnt[dev] = v;
+    }
+    return cnt[dev];
 }
 
 // Launch plan for one call.
@@ -73,21 +100,15 @@ struct Plan {
 constexpr int kBidirR = 32, kBidirG = 2;     // 128 threads: 64 forward, 64 backward
 constexpr int kOneDirR = 64, kOneDirG = 2;   // 128 threads
 constexpr int kYSmemMaxBytes = 48 * 1024;    // shared y-buffer budget per CTA
-constexpr int kTargetCtas = 148 * 8;         // enough CTAs to fill 148 SMs
 
 // Folded sequences are cut into independent pieces (each starts on a reset):
-// aim for about three waves of 148 SMs x 14 resident warps, so that the last
-// wave is short.
-constexpr int kFoldTargetWarps = 148 * 48;
+// aim for about three waves of the SMs x 14 resident warps (48 warps per SM),
+// so that the last wave is short.
+constexpr int kFoldWarpsPerSm = 48;
 
-constexpr int warps_per_cta(int G) { return G == 4 ? 8 : (G == 2 ? 4 : 2); }
-#ifndef VSSM_CARRY_WARPS
-#define VSSM_CARRY_WARPS 1
-#endif
-constexpr int kCarryW = VSSM_CARRY_WARPS;    // warps per CTA of the summary kernel
+using vssm::kCarryW;
+using vssm::warps_per_cta;
 
-// Sub-partitions of the GPU (148 SMs x 4 schedulers).
-constexpr int kSubParts = 148 * 4;
 
 // Cost model of one call with each row cut into P ranges of lp tokens, in
 // microseconds. It is a least-squares fit to B300 timings of each kernel
@@ -105,11 +126,12 @@ struct KernelCost {
 constexpr KernelCost kScanCost{268.8, 189.2, 173.4, 5717.0, 3.7};
 constexpr KernelCost kSummaryCost{170.9, 130.3, 113.4, 620.0, 4.3};
 constexpr double kFoldUsPerRange = 0.2;
-constexpr double kClockMHz = 2032.0;
+constexpr double kClockMHz = 2032.0;   // B300 maximum SM clock (the fit's cycle counts are per clock)
 
 double kernel_us(const KernelCost &m, long long warps, long long lp, long long resident)
 {
     auto per_token = [&](double k) { return k <= 1.0 ? m.c1 : (k <= 2.0 ? m.c2 : m.c3); };
+    const long long kSubParts = 4LL * sm_count();   // schedulers of the GPU
     const long long full = warps / resident, rem = warps - full * resident;
     const double kf = (double)resident / kSubParts;
     double cyc = (double)full * kf * ((double)lp * per_token(kf) + m.start);
@@ -125,7 +147,7 @@ double kernel_us(const KernelCost &m, long long warps, long long lp, long long r
 long long resident_warps(size_t warp_bytes, int warps_per_cta)
 {
     const long long per_sm = (228 * 1024) / ((long long)warps_per_cta * warp_bytes + 1024);
-    return 148LL * std::max(1LL, std::min(32LL, per_sm)) * warps_per_cta;
+    return (long long)sm_count() * std::max(1LL, std::min(32LL, per_sm)) * warps_per_cta;
 }
 
 struct CarryShape {
@@ -221,7 +243,8 @@ void make_warp_plan(const vssm_scan_args *a, int seg_len, int pieces_req, Plan *
         pl->carry = true;
     } else if (seg_len > 0 && a->seqlen > 0) {
         const long long per_piece_warps = (long long)a->batch * pl->rgroups * ndir;
-        long long want = (kFoldTargetWarps + per_piece_warps - 1) / std::max<long long>(1, per_piece_warps);
+        const long long target = (long long)kFoldWarpsPerSm * sm_count();
+        long long want = (target + per_piece_warps - 1) / std::max<long long>(1, per_piece_warps);
         want = std::max<long long>(1, std::min<long long>(want, nseg));
         const long long per = (nseg + want - 1) / want;        // segments per piece
         pl->pieces = (int)((nseg + per - 1) / per);
@@ -257,7 +280,8 @@ int make_plan(const vssm_scan_args *a, int seg_len, int pieces_req, Plan *pl)
         // Split each folded row at segment boundaries so that the grid has
         // enough CTAs; every piece starts on a reset, so pieces are independent.
         const long long nseg = (a->seqlen + seg_len - 1) / seg_len;
-        long long want = (kTargetCtas + (long long)a->batch * dblocks - 1) /
+        const long long target = 8LL * sm_count();
+        long long want = (target + (long long)a->batch * dblocks - 1) /
                          std::max<long long>(1, (long long)a->batch * dblocks);
         want = std::max<long long>(1, std::min<long long>(want, nseg));
         const long long per = (nseg + want - 1) / want;        // segments per piece
@@ -350,23 +374,6 @@ int validate(const vssm_scan_args *a, int seg_len, bool folded, bool need_out = 
     return VSSM_OK;
 }
 
-template <typename T, int DIRS, int R, int G, bool YSMEM>
-int launch_variant(const vssm::ScanParams &p, const Plan &pl, cudaStream_t stream)
-{
-    constexpr int NDIR = DIRS == 3 ? 2 : 1;
-    const size_t smem = sizeof(float) * ((size_t)NDIR * vssm::DirBlock<R>::kFloats +
-                                         (YSMEM ? (size_t)R * p.ypitch : 0));
-    auto kern = vssm::scan_kernel<T, DIRS, R, G, YSMEM>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess)
-        return fail(VSSM_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    kern<<<(unsigned)pl.ctas, NDIR * R * G, smem, stream>>>(p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
-    return VSSM_OK;
-}
-
 // Address of this device's error word (looked up once per device).
 unsigned *device_error_word()
 {
@@ -409,80 +416,6 @@ void *noalloc_scratch()
     return addr[dev];
 }
 
-template <typename T, int DIRS, bool SP, bool CONV>
-int launch_carry(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t stream)
-{
-    constexpr int W = kCarryW;
-    const size_t smem = (size_t)W * vssm::WarpLayout<T, 1, false>::kWarpBytes;
-    auto kern = vssm::warp_carry_kernel<T, DIRS, W, SP, CONV>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 (int)cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess)
-        return fail(VSSM_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    kern<<<(unsigned)pl.summ_ctas, W * 32, smem, stream>>>(p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
-    return VSSM_OK;
-}
-
-template <typename T, int G, int DIRS, bool SP, bool CONV>
-int launch_warp_variant(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t stream)
-{
-    if (pl.carry) {
-        const int st = launch_carry<T, DIRS, SP, CONV>(p, pl, stream);
-        if (st != VSSM_OK) return st;
-    }
-    constexpr int W = warps_per_cta(G);
-    const size_t smem = (size_t)W * vssm::WarpLayout<T, G, DIRS == 3>::kWarpBytes;
-    auto kern = pl.carry ? vssm::warp_scan_kernel<T, G, DIRS, W, true, SP, CONV>
-                         : vssm::warp_scan_kernel<T, G, DIRS, W, false, SP, CONV>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess)   // all of the unified L1/shared array as shared memory: residency is smem-bound
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 (int)cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess)
-        return fail(VSSM_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    kern<<<(unsigned)pl.ctas, W * 32, smem, stream>>>(p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
-    return VSSM_OK;
-}
-
-template <typename T, int G, bool SP, bool CONV>
-int launch_warp_dirs(const vssm::WarpScanParams &p, const Plan &pl, cudaStream_t s)
-{
-    switch (pl.dirs) {
-    case 1: return launch_warp_variant<T, G, 1, SP, CONV>(p, pl, s);
-    case 2: return launch_warp_variant<T, G, 2, SP, CONV>(p, pl, s);
-    default: return launch_warp_variant<T, G, 3, SP, CONV>(p, pl, s);
-    }
-}
-
-template <typename T>
-int launch_warp(const vssm::WarpScanParams &p, const Plan &pl, bool softplus, bool conv,
-                cudaStream_t s)
-{
-    if (conv)
-        return softplus ? launch_warp_dirs<T, 1, true, true>(p, pl, s)
-                        : launch_warp_dirs<T, 1, false, true>(p, pl, s);
-    return softplus ? launch_warp_dirs<T, 1, true, false>(p, pl, s)
-                    : launch_warp_dirs<T, 1, false, false>(p, pl, s);
-}
-
-template <typename T>
-int launch_typed(const vssm::ScanParams &p, const Plan &pl, cudaStream_t s)
-{
-    switch (pl.dirs) {
-    case 1: return launch_variant<T, 1, kOneDirR, kOneDirG, false>(p, pl, s);
-    case 2: return launch_variant<T, 2, kOneDirR, kOneDirG, false>(p, pl, s);
-    default:
-        return pl.ysmem ? launch_variant<T, 3, kBidirR, kBidirG, true>(p, pl, s)
-                        : launch_variant<T, 3, kBidirR, kBidirG, false>(p, pl, s);
-    }
-}
-
 int run(const vssm_scan_args *a, int seg_len, bool folded, int pieces_req, void *stream)
 {
     int st = validate(a, seg_len, folded);
@@ -500,6 +433,7 @@ int run(const vssm_scan_args *a, int seg_len, bool folded, int pieces_req, void 
         return fail(VSSM_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", pl.workspace,
                     a->workspace ? a->workspace_bytes : (size_t)0);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool f32 = a->dtype == VSSM_F32;
     if (pl.warp) {
         vssm::WarpScanParams w{};
         w.x = a->x;
@@ -523,6 +457,7 @@ int run(const vssm_scan_args *a, int seg_len, bool folded, int pieces_req, void 
         w.D[1] = a->D_bwd;
         w.out = a->out;
         w.ybuf = pl.dirs == 3 ? static_cast<float *>(a->workspace) : nullptr;
+        w.discard_y = (reinterpret_cast<uintptr_t>(w.ybuf) & 127u) == 0 && vssm::WarpLayout<float, 1, true>::RPW == 32;
         w.summ = pl.carry ? reinterpret_cast<float *>(static_cast<char *>(a->workspace) + pl.summ_off)
                           : nullptr;
         w.err = device_error_word();
@@ -537,9 +472,10 @@ int run(const vssm_scan_args *a, int seg_len, bool folded, int pieces_req, void 
         w.rgroups = pl.rgroups;
         w.ngroups = pl.ngroups;
         w.srows = pl.srows;
-        const bool sp = a->delta_softplus != 0, cv = a->conv_k > 0;
-        return a->dtype == VSSM_F32 ? launch_warp<float>(w, pl, sp, cv, s)
-                                    : launch_warp<__nv_bfloat16>(w, pl, sp, cv, s);
+        const cudaError_t e = vssm::launch_warp(w, pl.dirs, a->dtype == VSSM_F32, pl.carry,
+                                                a->delta_softplus != 0, a->conv_k > 0, pl.ctas,
+                                                pl.summ_ctas, s);
+        return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "launch");
     }
     vssm::ScanParams p{};
     p.x = a->x;
@@ -572,10 +508,9 @@ int run(const vssm_scan_args *a, int seg_len, bool folded, int pieces_req, void 
     p.pieces = pl.pieces;
     p.piece_len = pl.piece_len;
     p.ypitch = pl.ypitch;
-    return a->dtype == VSSM_F32 ? launch_typed<float>(p, pl, s)
-                                : launch_typed<__nv_bfloat16>(p, pl, s);
+    const cudaError_t e = vssm::launch_general(p, pl.dirs, pl.ysmem, f32, pl.ctas, s);
+    return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "launch");
 }
-
 
 struct GradPlan {
     int ndir = 1, rgroups = 0, nch = 0;
@@ -588,11 +523,11 @@ struct GradPlan {
 // to fill the GPU (about two waves of the adjoint's two-warp CTAs at four
 // per SM), keeping at least 16 chunks (64 tokens) per range; the ranges are
 // joined by the adjoint summaries (grad_adj_summary_kernel).
-constexpr long long kGradTargetCtas = 148LL * 8;
 constexpr int kGradMaxRanges = 16, kGradMinRangeChunks = 16;
 
 GradPlan make_grad_plan(const vssm_scan_args *a)
 {
+    const long long kGradTargetCtas = 8LL * sm_count();
     GradPlan g;
     g.ndir = a->dir_flags == 3 ? 2 : 1;
     g.rgroups = (a->dim + 31) / 32;
@@ -615,49 +550,6 @@ GradPlan make_grad_plan(const vssm_scan_args *a)
     g.workspace = g.nrange > 1 ? g.summ_off + (size_t)g.ndir * g.ngroups * g.nrange * 1024 * sizeof(float)
                                : part_end;
     return g;
-}
-
-int zero_f32(float *p, size_t n, cudaStream_t s)
-{
-    if (!p || n == 0) return VSSM_OK;
-    const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, 148 * 8);
-    vssm::zero_f32_kernel<<<blocks, 256, 0, s>>>(p, (long long)n);
-    const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? VSSM_OK : fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
-}
-
-template <typename T, int DIRS>
-int launch_grad(const vssm::GradParams &p, const GradPlan &g, cudaStream_t s)
-{
-    constexpr int NDIR = DIRS == 3 ? 2 : 1;
-    const long long units = (long long)NDIR * g.ngroups;
-    vssm::grad_ckpt_kernel<T, DIRS><<<(unsigned)((units + 3) / 4), 128, 0, s>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
-    if (g.nrange > 1) {
-        const long long su = units * g.nrange;
-        vssm::grad_adj_summary_kernel<T, DIRS><<<(unsigned)((su + 3) / 4), 128, 0, s>>>(p);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
-    }
-    const size_t smem = (size_t)NDIR * vssm::GradLayout<T, DIRS>::kWarpBytes;
-    auto kern = vssm::grad_adjoint_kernel<T, DIRS>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    kern<<<(unsigned)(g.ngroups * g.nrange), NDIR * 32, smem, s>>>(p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
-    return VSSM_OK;
-}
-
-template <typename T>
-int launch_grad_dirs(const vssm::GradParams &p, const GradPlan &g, int dirs, cudaStream_t s)
-{
-    switch (dirs) {
-    case 1: return launch_grad<T, 1>(p, g, s);
-    case 2: return launch_grad<T, 2>(p, g, s);
-    default: return launch_grad<T, 3>(p, g, s);
-    }
 }
 
 
@@ -724,7 +616,6 @@ struct HostCut {
     size_t total = 0;
 };
 
-size_t al256(size_t n) { return (n + 255) / 256 * 256; }
 
 int host_cut(const vssm_scan_args *a, int seg_len, int slices, HostCut *c)
 {
@@ -893,50 +784,6 @@ int host_scan(const vssm_scan_args *a, int seg_len, int slices, void *stream)
     if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "pipeline join: %s", cudaGetErrorString(e));
     return VSSM_OK;
 }
-template <typename T, int Q, bool GATE, bool SKIP>
-void ncssd_launch_k(const vssm::NcssdParams &p, dim3 grid, cudaStream_t s)
-{
-    const dim3 block(vssm::kNcW * 32);
-    if (sizeof(T) == 2) vssm::ncssd_mma_kernel<Q, GATE, SKIP><<<grid, block, 0, s>>>(p);
-    else vssm::ncssd_kernel<float, Q, GATE, SKIP><<<grid, block, 0, s>>>(p);
-}
-
-template <typename T, int Q>
-void ncssd_launch_q(const vssm::NcssdParams &p, bool gate, bool skip, dim3 grid, cudaStream_t s)
-{
-    if (gate && skip) ncssd_launch_k<T, Q, true, true>(p, grid, s);
-    else if (gate) ncssd_launch_k<T, Q, true, false>(p, grid, s);
-    else if (skip) ncssd_launch_k<T, Q, false, true>(p, grid, s);
-    else ncssd_launch_k<T, Q, false, false>(p, grid, s);
-}
-
-template <bool GATE, bool SKIP>
-int ncssd_rows_launch(const vssm::NcssdParams &p, dim3 grid, cudaStream_t s)
-{
-    const vssm::NcRowsLayout lay(p.L, GATE);
-    auto kern = vssm::ncssd_rows_kernel<GATE, SKIP>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 (int)cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return fail(VSSM_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    kern<<<grid, vssm::kNcW * 32, lay.total, s>>>(p);
-    return VSSM_OK;
-}
-
-// The NC-SSD kernel with Q CTAs per cluster (1, 2, 4 or 8) and the z / D
-// options fixed at compile time: bf16 I/O on the tensor cores, fp32 I/O on
-// the FMA pipe.
-template <typename T>
-void ncssd_launch(const vssm::NcssdParams &p, int q, bool gate, bool skip, dim3 grid, cudaStream_t s)
-{
-    switch (q) {
-    case 1: ncssd_launch_q<T, 1>(p, gate, skip, grid, s); break;
-    case 2: ncssd_launch_q<T, 2>(p, gate, skip, grid, s); break;
-    case 4: ncssd_launch_q<T, 4>(p, gate, skip, grid, s); break;
-    default: ncssd_launch_q<T, 8>(p, gate, skip, grid, s); break;
-    }
-}
 
 }  // namespace
 
@@ -1065,26 +912,18 @@ int vssm_ncssd(const vssm_ncssd_args *a, void *stream)
     if (dtiles > 65535) return fail(VSSM_ERR_UNSUPPORTED, "dim=%d above 65535 x 32", a->dim);
     const long long base = (long long)a->batch * dtiles;
     int q = 1;
-    while (q < vssm::kNcMaxQ && base * q < 148LL * 7 && a->seqlen >= 2 * q * 64) q *= 2;
+    while (q < vssm::kNcMaxQ && base * q < 7LL * sm_count() && a->seqlen >= 2 * q * 64) q *= 2;
     p.rng = (a->seqlen + q - 1) / q;
     const dim3 grid((unsigned)q, (unsigned)dtiles, (unsigned)a->batch);
     const bool gate = a->z != nullptr, skip = a->D != nullptr;
-    if (a->dtype == VSSM_BF16 && q == 1 && a->dim % 8 == 0 && a->seqlen <= vssm::kNcRowsMaxL) {
-        // whole rows resident in shared memory, spans moved by bulk copies
+    // whole rows resident in shared memory, spans moved by bulk copies
+    const bool rows = a->dtype == VSSM_BF16 && q == 1 && a->dim % 8 == 0 && a->seqlen <= vssm::kNcRowsMaxL;
+    if (rows) {
         p.err = device_error_word();
         if (!p.err) return fail(VSSM_ERR_CUDA, "device error word unavailable");
-        const int st = gate ? (skip ? ncssd_rows_launch<true, true>(p, grid, s)
-                                    : ncssd_rows_launch<true, false>(p, grid, s))
-                            : (skip ? ncssd_rows_launch<false, true>(p, grid, s)
-                                    : ncssd_rows_launch<false, false>(p, grid, s));
-        if (st != VSSM_OK) return st;
-    } else if (a->dtype == VSSM_F32) {
-        ncssd_launch<float>(p, q, gate, skip, grid, s);
-    } else {
-        ncssd_launch<__nv_bfloat16>(p, q, gate, skip, grid, s);
     }
-    const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? VSSM_OK : fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    const cudaError_t e = vssm::launch_ncssd(p, rows, q, gate, skip, a->dtype == VSSM_F32, grid, s);
+    return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "launch");
 }
 
 int vssm_selftest_wait_timeout(unsigned limit_us, void *stream)
@@ -1093,10 +932,9 @@ int vssm_selftest_wait_timeout(unsigned limit_us, void *stream)
         return fail(VSSM_ERR_INVALID_ARG, "limit_us=%u outside 1..1000000", limit_us);
     unsigned *err = device_error_word();
     if (!err) return fail(VSSM_ERR_CUDA, "cannot locate the device error word");
-    vssm::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
-        err, (uint64_t)limit_us * 1000ull);
-    const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? VSSM_OK : fail(VSSM_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+    const cudaError_t e = vssm::launch_selftest_wait(err, (uint64_t)limit_us * 1000ull,
+                                                     static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "launch");
 }
 
 int vssm_scan_grad_workspace_size(const vssm_scan_args *a, int seg_len, size_t *bytes)
@@ -1209,16 +1047,15 @@ int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len
     // the reductions accumulate atomically: start them at zero
     const size_t nbcf = (size_t)a->batch * a->seqlen * a->dstate;
     float *zs[] = {g->dB, g->dC, g->dB_bwd, g->dC_bwd};
+    cudaError_t e = cudaSuccess;
     for (float *q : zs)
-        if ((st = zero_f32(q, nbcf, s)) != VSSM_OK) return st;
-    if ((dirs & 1) && ((st = zero_f32(g->dA_fwd, (size_t)a->dim * 16, s)) != VSSM_OK ||
-                       (st = zero_f32(g->dD_fwd, (size_t)a->dim, s)) != VSSM_OK))
-        return st;
-    if ((dirs & 2) && ((st = zero_f32(g->dA_bwd, (size_t)a->dim * 16, s)) != VSSM_OK ||
-                       (st = zero_f32(g->dD_bwd, (size_t)a->dim, s)) != VSSM_OK))
-        return st;
-    return a->dtype == VSSM_F32 ? launch_grad_dirs<float>(p, gl, (int)dirs, s)
-                                : launch_grad_dirs<__nv_bfloat16>(p, gl, (int)dirs, s);
+        if (e == cudaSuccess) e = vssm::launch_zero_f32(q, nbcf, s);
+    if ((dirs & 1) && e == cudaSuccess) e = vssm::launch_zero_f32(g->dA_fwd, (size_t)a->dim * 16, s);
+    if ((dirs & 1) && e == cudaSuccess) e = vssm::launch_zero_f32(g->dD_fwd, (size_t)a->dim, s);
+    if ((dirs & 2) && e == cudaSuccess) e = vssm::launch_zero_f32(g->dA_bwd, (size_t)a->dim * 16, s);
+    if ((dirs & 2) && e == cudaSuccess) e = vssm::launch_zero_f32(g->dD_bwd, (size_t)a->dim, s);
+    if (e == cudaSuccess) e = vssm::launch_grad(p, (int)dirs, a->dtype == VSSM_F32, gl.ngroups, gl.nrange, s);
+    return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "launch");
 }
 
 int vssm_scan_chunked(const vssm_scan_args *a, int seg_len, int pieces, void *stream)
