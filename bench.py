@@ -40,8 +40,7 @@ from workloads import (DIR_BOTH, DIR_BWD, DIR_FWD, ORDER, WORKLOADS,  # noqa: E4
 
 METRIC = "bidir selective-scan GB/s and Gtoken·ch/s, % of HBM roofline, 1×B300"
 L2_BYTES = 126 * 1024 * 1024
-SMS = 148
-MAX_SM_MHZ = 2032.0
+FALLBACK_MAX_SM_MHZ = 2032.0   # B300 maximum SM clock, used only when the driver reports none
 EX2_PER_CLK_SM = 32        # MUFU ex2.approx.f32 per clock per SM, measured on B300
 FMA_PER_CLK_SM = 128       # fp32 FMA-pipe lane operations per clock per SM
 FALLBACK_HBM_GBS = 6400.0
@@ -146,15 +145,61 @@ def aggregate(units_per_rank: float, world: int, max_seconds: float) -> float:
 
 # ------------------------------------------------------------------ clocks
 
+class _Nvml:
+    """Read-only NVML through ctypes (clock and clock-event-reason queries
+    only; nothing is ever set). Looks for the driver's libnvidia-ml in the
+    loader path and in the usual driver directories."""
+    SM = 1   # NVML_CLOCK_SM
+
+    def __init__(self, uuid: str):
+        import glob
+        names = ["libnvidia-ml.so.1", "libnvidia-ml.so"]
+        for d in ("/usr/lib/x86_64-linux-gnu", "/usr/lib64", "/usr/lib", "/usr/local/nvidia/lib64",
+                  "/usr/local/nvidia/lib", "/usr/lib/x86_64-linux-gnu/nvidia/current"):
+            names += sorted(glob.glob(os.path.join(d, "libnvidia-ml.so*")))
+        self.lib, err = None, None
+        for n in names:
+            try:
+                self.lib = ctypes.CDLL(n)
+                break
+            except OSError as e:
+                err = e
+        if self.lib is None:
+            raise OSError(f"libnvidia-ml not found ({err})")
+        init = getattr(self.lib, "nvmlInit_v2", None) or self.lib.nvmlInit
+        if init() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        get = getattr(self.lib, "nvmlDeviceGetHandleByUUID")
+        if get(uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise OSError(f"no NVML device with uuid {uuid}")
+        self._reasons = (getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+                         or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons)
+
+    def sm_mhz(self):
+        v = ctypes.c_uint()
+        return v.value if self.lib.nvmlDeviceGetClockInfo(self.h, self.SM, ctypes.byref(v)) == 0 else None
+
+    def max_sm_mhz(self):
+        v = ctypes.c_uint()
+        return v.value if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.SM, ctypes.byref(v)) == 0 else None
+
+    def reasons(self):
+        v = ctypes.c_ulonglong()
+        return int(v.value) if self._reasons(self.h, ctypes.byref(v)) == 0 else 0
+
+
 class ClockSampler:
     """Samples the SM clock and the clock-event reasons of one GPU during the
-    timed region, through NVML when importable, else a streaming nvidia-smi."""
+    timed region: NVML (read-only, through ctypes) every half millisecond when
+    the library can be loaded, else a streaming nvidia-smi at its shortest
+    period. It only reads clocks; it never sets them."""
     REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
                0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
                0x100: "display_clock_setting"}
 
-    def __init__(self, uuid: str, period_ms: int = 20):
+    def __init__(self, uuid: str, period_ms: float = 0.5):
         self.uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
         self.period_ms = period_ms
         self.samples = []
@@ -165,11 +210,8 @@ class ClockSampler:
         self._thread = None
         self._proc = None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByUUID(self.uuid)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.nv = _Nvml(self.uuid)
+            self.max_mhz = self.nv.max_sm_mhz()
             self.source = "nvml"
         except Exception as e:
             self.nv = None
@@ -180,12 +222,7 @@ class ClockSampler:
         return True
 
     def _nvml_sample(self):
-        nv = self.nv
-        try:
-            reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-        except AttributeError:
-            reasons = nv.nvmlDeviceGetCurrentClocksThrottleReasons(self.h)
-        self.samples.append((nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM), int(reasons)))
+        self.samples.append((self.nv.sm_mhz(), self.nv.reasons()))
 
     def _nvml_loop(self):
         while not self._stop.is_set():
@@ -211,6 +248,10 @@ class ClockSampler:
         """Begin sampling; returns once the first sample has arrived (or failed)."""
         if self.nv is not None:
             self._nvml_sample()
+            # the launching thread holds the interpreter most of the time: a
+            # short switch interval lets the sampler run every period
+            self._switch = sys.getswitchinterval()
+            sys.setswitchinterval(self.period_ms / 2000)
             self._thread = threading.Thread(target=self._nvml_loop, daemon=True)
             self._thread.start()
             return
@@ -219,7 +260,7 @@ class ClockSampler:
             self._proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.uuid,
                  "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
-                 "--format=csv,noheader,nounits", f"-lms={self.period_ms}"],
+                 "--format=csv,noheader,nounits", f"-lms={max(10, int(self.period_ms))}"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError as e:
             self.err = (self.err or "") + f"; nvidia-smi: {e!r}"
@@ -233,6 +274,8 @@ class ClockSampler:
 
     def stop(self):
         self._stop.set()
+        if getattr(self, "_switch", None):
+            sys.setswitchinterval(self._switch)
         if self._proc is not None:
             self._proc.terminate()
             try:
@@ -666,7 +709,9 @@ def run_ours(args):
     # (the summary pass's repeated ones are not credited).
     upd = exp_count(wl) * (2 if args.grad else 1)
     ach = upd / kern_avg_s / 1e9
-    peak_upd = EX2_PER_CLK_SM * SMS * MAX_SM_MHZ * 1e6 / 1e9
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    max_mhz = float(clocks.get("sm_max_mhz") or FALLBACK_MAX_SM_MHZ)
+    peak_upd = EX2_PER_CLK_SM * sms * max_mhz * 1e6 / 1e9
     kern_gbs = step_bytes / kern_avg_s / 1e9
     med = clocks.get("sm_mhz")
     roofline = {
@@ -675,8 +720,8 @@ def run_ours(args):
         "traffic": ncu_traffic(variant_key(wl) + ("+grad" if args.grad else "")),
         "update": "one (token, channel, state, direction) recurrence step: 1 MUFU ex2 + 4 fp32 FMA-pipe ops",
         "peak_basis": f"{EX2_PER_CLK_SM} ex2/clk/SM (and {FMA_PER_CLK_SM}/4 FMA-pipe updates/clk/SM) "
-                      f"x {SMS} SMs x {MAX_SM_MHZ:.0f} MHz max SM clock",
-        "frac_at_median_clock": round(ach / (peak_upd * med / MAX_SM_MHZ), 4) if med else None,
+                      f"x {sms} SMs x {max_mhz:.0f} MHz max SM clock",
+        "frac_at_median_clock": round(ach / (peak_upd * med / max_mhz), 4) if med else None,
         "kernel_avg_us": round(kern_avg_s * 1e6, 3),
         "launches_per_call": launches,
         "ranges_per_row": ranges,

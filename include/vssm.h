@@ -272,7 +272,10 @@ typedef struct {
  * vssm_scan_grad_workspace_size bytes and must not overlap any input or
  * output. Asynchronous on `stream`; the
  * pair rendezvous of the two directions is bounded as in the forward kernel
- * (vssm_device_error).
+ * (vssm_device_error). When that wait expires (vssm_device_error then
+ * returns VSSM_ERR_TIMEOUT), every gradient output of the call is undefined:
+ * the warps that gave up stop before their second half, so part of dB/dC was
+ * accumulated and part of dx/ddelta/dz, dA, dD was never written.
  */
 int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len, void *stream);
 
