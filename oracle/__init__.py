@@ -75,6 +75,9 @@ def load_library(path: str):
         ctypes.c_int, ctypes.c_long, ctypes.c_int]
     lib.oracle_scan_grad.restype = ctypes.c_int
     lib.oracle_scan_grad.argtypes = [dp] * 23 + [ctypes.c_long] * 4 + [ctypes.c_int, ctypes.c_long]
+    lib.oracle_scan_grad_ex.restype = ctypes.c_int
+    lib.oracle_scan_grad_ex.argtypes = ([dp] * 14 + [ctypes.c_int] + [dp] * 4 + [ctypes.c_long] +
+                                        [dp] * 19 + [ctypes.c_long] * 4 + [ctypes.c_int, ctypes.c_long])
     lib.oracle_ncssd.restype = ctypes.c_int
     lib.oracle_ncssd.argtypes = [dp] * 7 + [ctypes.c_long] * 4
     lib.oracle_conv_silu.restype = ctypes.c_int
@@ -213,36 +216,62 @@ def _scan_ex(lib, x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, B_bwd, C_bwd, d
 
 
 def scan_grad(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, dout=None,
-              B_bwd=None, C_bwd=None, dirs: int = DIR_BOTH, seg_len: int = 0, lib=None) -> dict:
-    """Gradients of L = sum(dout * scan(...)) (C oracle ``oracle_scan_grad``):
-    dict with dx, ddelta, dz (None without z), dB, dC, dB_bwd / dC_bwd (None
-    when the backward direction shares B / C), dA_fwd, dA_bwd, dD_fwd, dD_bwd
-    (None for a direction that is not run). float64."""
+              B_bwd=None, C_bwd=None, dirs: int = DIR_BOTH, seg_len: int = 0, lib=None,
+              delta_bwd=None, delta_bias=None, delta_bias_bwd=None, delta_softplus: bool = False,
+              conv_w=None, conv_b=None, conv_w_bwd=None, conv_b_bwd=None) -> dict:
+    """Gradients of L = sum(dout * scan(...)) (C oracle ``oracle_scan_grad_ex``),
+    for the plain scan or with the step options and the convolution of
+    ``scan``: dict with dx, ddelta, dz (None without z), dB, dC, dB_bwd / dC_bwd
+    (None when the backward direction shares B / C), dA_fwd, dA_bwd, dD_fwd,
+    dD_bwd (None for a direction that is not run), ddelta_bwd (with
+    delta_bwd), ddelta_bias / ddelta_bias_bwd (with softplus; the backward
+    one only with its own bias), dconv_w, dconv_b, dconv_w_bwd, dconv_b_bwd
+    (with the convolution; each only for a given parameter). float64. A
+    backward parameter that is not given is the forward one, and its
+    gradient is included in the forward one's."""
     lib = lib or _get_lib()
     x = np.asarray(x)
     batch, dim, L = x.shape
     N = np.asarray(B).shape[-1]
+    K = 0 if conv_w is None else np.asarray(conv_w).shape[-1]
     keep, ptrs = [], []
-    for a in (x, delta, z, B, C, B_bwd, C_bwd, A_fwd, A_bwd, D_fwd, D_bwd, dout):
+    for a in (x, delta, z, B, C, B_bwd, C_bwd, A_fwd, A_bwd, D_fwd, D_bwd, delta_bwd,
+              delta_bias, delta_bias_bwd):
         arr, p = _as_f64(a)
         keep.append(arr)
         ptrs.append(p)
+    cptrs = []
+    for a in (conv_w, conv_b, conv_w_bwd, conv_b_bwd):
+        arr, p = _as_f64(a)
+        keep.append(arr)
+        cptrs.append(p)
+    dout_arr, dout_p = _as_f64(dout)
     act = lambda: np.zeros((batch, dim, L))
     bc = lambda: np.zeros((batch, L, N))
+    sp = bool(delta_softplus)
     g = dict(dx=act(), ddelta=act(), dz=act() if z is not None else None, dB=bc(), dC=bc(),
              dB_bwd=bc() if B_bwd is not None else None, dC_bwd=bc() if C_bwd is not None else None,
              dA_fwd=np.zeros((dim, N)) if dirs & DIR_FWD else None,
              dA_bwd=np.zeros((dim, N)) if dirs & DIR_BWD else None,
              dD_fwd=np.zeros(dim) if dirs & DIR_FWD else None,
-             dD_bwd=np.zeros(dim) if dirs & DIR_BWD else None)
+             dD_bwd=np.zeros(dim) if dirs & DIR_BWD else None,
+             ddelta_bwd=act() if delta_bwd is not None else None,
+             ddelta_bias=np.zeros(dim) if sp else None,
+             ddelta_bias_bwd=np.zeros(dim) if sp and delta_bias_bwd is not None else None,
+             dconv_w=np.zeros((dim, K)) if K else None,
+             dconv_b=np.zeros(dim) if K and conv_b is not None else None,
+             dconv_w_bwd=np.zeros((dim, K)) if K and conv_w_bwd is not None else None,
+             dconv_b_bwd=np.zeros(dim) if K and conv_b_bwd is not None else None)
     outp = [_as_f64(g[k])[1] if g[k] is not None else None
             for k in ("dx", "ddelta", "dz", "dB", "dC", "dB_bwd", "dC_bwd", "dA_fwd", "dA_bwd",
-                      "dD_fwd", "dD_bwd")]
+                      "dD_fwd", "dD_bwd", "ddelta_bwd", "ddelta_bias", "ddelta_bias_bwd",
+                      "dconv_w", "dconv_b", "dconv_w_bwd", "dconv_b_bwd")]
     # _as_f64 returns the same array for float64 C-contiguous input, so the
     # pointers above write into g's arrays
-    rc = lib.oracle_scan_grad(*ptrs, *outp, batch, dim, L, N, int(dirs), int(seg_len))
+    rc = lib.oracle_scan_grad_ex(*ptrs, int(sp), *cptrs, K, dout_p, *outp, batch, dim, L, N,
+                                 int(dirs), int(seg_len))
     if rc != 0:
-        raise ValueError(f"oracle_scan_grad rejected its arguments (status {rc})")
+        raise ValueError(f"oracle_scan_grad_ex rejected its arguments (status {rc})")
     return g
 
 

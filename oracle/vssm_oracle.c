@@ -277,7 +277,8 @@ int oracle_scan_ex(const double *x, const double *delta, const double *z,
  *   g'(z) = sigma(z) * (1 + z * (1 - sigma(z)));
  *   ds_t = dout_t * g(z_t);   dz_t = dout_t * s_t * g'(z_t);
  *   per direction, walking the tokens against its scan order with the
- *   adjoint lambda_t = dL/dh_t (an N-vector):
+ *   adjoint lambda_t = dL/dh_t (an N-vector), where x_t and delta_t are that
+ *   direction's input and step:
  *     lambda_t = ds_t * C_t + abar_next * lambda_next      (0 past the end)
  *     dC_t    += ds_t * h_t;           dB_t += lambda_t * delta_t * x_t
  *     dx_t    += ds_t * D + sum_n lambda_t[n] * delta_t * B_t[n]
@@ -288,35 +289,88 @@ int oracle_scan_ex(const double *x, const double *delta, const double *z,
  *   exp(delta_t * A); at a folded reset abar_t is the constant 0, so neither
  *   ddelta nor dA gets a decay term there and lambda is not carried past it.
  *
- * Inputs as oracle_scan (steps used as given, shared x). z, D_fwd, D_bwd may
- * be NULL. Gradients are written (not accumulated): dx, ddelta, dz
- * [batch][dim][L] (dz ignored if z is NULL); dB, dC [batch][L][N]; when
- * B_bwd / C_bwd are given, the backward direction's go to dB_bwd / dC_bwd
- * (else into dB / dC); dA_fwd, dA_bwd [dim][N]; dD_fwd, dD_bwd [dim]
- * (NULL for a direction that is not run).
+ * With the step options and the convolution of oracle_scan_ex (the inputs
+ * below), each direction k's step and input are functions of the raw
+ * tensors, and the chain rule carries the per-direction gradients of the
+ * step (d step_k) and of the input (d u_k) back to them:
+ *   step_k = softplus(v_k + bias_k)  (use_softplus; v_k = delta or delta_bwd)
+ *            d v_k = d step_k * sigma(v_k + bias_k),  d bias_k = sum_t d v_k
+ *            (softplus'(v) = sigma(v)); otherwise step_k = v_k, d v_k = d step_k
+ *   u_k = silu(pre_k), pre_k[t] = cb_k + sum_j w_k[j] * x[tap_k(t, j)]  (K > 0)
+ *            d pre_k = d u_k * silu'(pre_k),  silu'(p) = sigma(p) + p sigma(p) (1 - sigma(p))
+ *            dx[tap] += w_k[j] * d pre_k,  d w_k[j] += d pre_k * x[tap],  d cb_k += d pre_k
+ *            with tap_k(t, j) = t - (K-1) + j forward, t + (K-1) - j backward
+ *            (taps outside the row or, folded, the segment read zero)
+ *   u_k = x otherwise, dx += d u_k.
+ * A backward parameter that is NULL is the forward one, and its gradient is
+ * added to the forward one's.
+ *
+ * Inputs as oracle_scan_ex (delta_bwd, bias_fwd, bias_bwd, use_softplus) plus
+ * the convolution (conv_w [dim][K], conv_b [dim], conv_w_bwd, conv_b_bwd;
+ * K = 0: none). z, D_fwd, D_bwd, B_bwd, C_bwd, delta_bwd, biases and conv_b*
+ * may be NULL. Gradients are written (not accumulated): dx, ddelta, dz
+ * [batch][dim][L] (dz ignored if z is NULL); ddelta_bwd (required iff
+ * delta_bwd is given); dB, dC [batch][L][N]; when B_bwd / C_bwd are given,
+ * the backward direction's go to dB_bwd / dC_bwd (else into dB / dC); dA_fwd,
+ * dA_bwd [dim][N]; dD_fwd, dD_bwd [dim] (each required iff its direction
+ * runs); dbias_fwd [dim] (required iff use_softplus), dbias_bwd (iff
+ * bias_bwd is given with use_softplus); dconv_w [dim][K] (iff K > 0),
+ * dconv_b (iff conv_b), dconv_w_bwd (iff conv_w_bwd), dconv_b_bwd (iff
+ * conv_b_bwd). Single-threaded.
  */
-int oracle_scan_grad(const double *x, const double *delta, const double *z,
-                     const double *B, const double *C,
-                     const double *B_bwd, const double *C_bwd,
-                     const double *A_fwd, const double *A_bwd,
-                     const double *D_fwd, const double *D_bwd,
-                     const double *dout,
-                     double *dx, double *ddelta, double *dz,
-                     double *dB, double *dC, double *dB_bwd, double *dC_bwd,
-                     double *dA_fwd, double *dA_bwd, double *dD_fwd, double *dD_bwd,
-                     long batch, long dim, long L, long N, int dirs, long seg_len)
+static double sigmoid(double v) { return 1.0 / (1.0 + exp(-v)); }
+
+/* silu'(p) = sigma(p) + p * sigma(p) * (1 - sigma(p)). */
+static double dsilu(double p)
+{
+    const double q = sigmoid(p);
+    return q + p * q * (1.0 - q);
+}
+
+/* Source token of convolution tap j for output token t (-1 when the tap
+ * reads zero: outside the row or, folded, outside t's segment). */
+static long conv_tap(long t, long j, long K, long L, long seg_len, int reverse)
+{
+    const long s = reverse ? t + (K - 1) - j : t - (K - 1) + j;
+    if (s < 0 || s >= L) return -1;
+    if (seg_len > 0 && s / seg_len != t / seg_len) return -1;
+    return s;
+}
+
+int oracle_scan_grad_ex(const double *x, const double *delta, const double *z,
+                        const double *B, const double *C,
+                        const double *B_bwd, const double *C_bwd,
+                        const double *A_fwd, const double *A_bwd,
+                        const double *D_fwd, const double *D_bwd,
+                        const double *delta_bwd, const double *bias_fwd, const double *bias_bwd,
+                        int use_softplus,
+                        const double *conv_w, const double *conv_b,
+                        const double *conv_w_bwd, const double *conv_b_bwd, long K,
+                        const double *dout,
+                        double *dx, double *ddelta, double *dz,
+                        double *dB, double *dC, double *dB_bwd, double *dC_bwd,
+                        double *dA_fwd, double *dA_bwd, double *dD_fwd, double *dD_bwd,
+                        double *ddelta_bwd, double *dbias_fwd, double *dbias_bwd,
+                        double *dconv_w, double *dconv_b, double *dconv_w_bwd, double *dconv_b_bwd,
+                        long batch, long dim, long L, long N, int dirs, long seg_len)
 {
     if (!x || !delta || !B || !C || !dout || !dx || !ddelta || !dB || !dC) return ORACLE_EINVAL;
-    if (batch < 0 || dim < 0 || L < 0 || N <= 0 || dirs < 1 || dirs > 3 || seg_len < 0)
+    if (batch < 0 || dim < 0 || L < 0 || N <= 0 || dirs < 1 || dirs > 3 || seg_len < 0 || K < 0)
         return ORACLE_EINVAL;
     if ((dirs & 1) && (!A_fwd || !dA_fwd || !dD_fwd)) return ORACLE_EINVAL;
     if ((dirs & 2) && (!A_bwd || !dA_bwd || !dD_bwd)) return ORACLE_EINVAL;
     if (seg_len > 0 && (dirs & 2) && L % seg_len != 0) return ORACLE_EINVAL;
     if ((B_bwd && !dB_bwd) || (C_bwd && !dC_bwd)) return ORACLE_EINVAL;
+    if (delta_bwd && !ddelta_bwd) return ORACLE_EINVAL;
+    if (use_softplus && (!dbias_fwd || (bias_bwd && !dbias_bwd))) return ORACLE_EINVAL;
+    if (K > 0 && (!conv_w || !dconv_w || (conv_b && !dconv_b) || (conv_w_bwd && !dconv_w_bwd) ||
+                  (conv_b_bwd && !dconv_b_bwd)))
+        return ORACLE_EINVAL;
     const long rows = batch * dim;
     for (long i = 0; i < rows * L; ++i) {
         dx[i] = 0.0;
         ddelta[i] = 0.0;
+        if (delta_bwd) ddelta_bwd[i] = 0.0;
         if (z && dz) dz[i] = 0.0;
     }
     for (long i = 0; i < batch * L * N; ++i) {
@@ -332,21 +386,61 @@ int oracle_scan_grad(const double *x, const double *delta, const double *z,
     for (long i = 0; i < dim; ++i) {
         if (dirs & 1) dD_fwd[i] = 0.0;
         if (dirs & 2) dD_bwd[i] = 0.0;
+        if (use_softplus) dbias_fwd[i] = 0.0;
+        if (use_softplus && bias_bwd) dbias_bwd[i] = 0.0;
+        if (K > 0 && conv_b) dconv_b[i] = 0.0;
+        if (K > 0 && conv_b_bwd) dconv_b_bwd[i] = 0.0;
     }
-    double *H = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * (size_t)N * 2);
-    double *Ab = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * (size_t)N * 2);
-    double *y = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * 2);
+    for (long i = 0; i < dim * K; ++i) {
+        dconv_w[i] = 0.0;
+        if (conv_w_bwd) dconv_w_bwd[i] = 0.0;
+    }
+    const size_t LL = (size_t)(L > 0 ? L : 1);
+    double *H = (double *)malloc(sizeof(double) * LL * (size_t)N * 2);
+    double *Ab = (double *)malloc(sizeof(double) * LL * (size_t)N * 2);
+    double *y = (double *)malloc(sizeof(double) * LL * 2);
     double *lam = (double *)malloc(sizeof(double) * (size_t)N);
-    if (!H || !Ab || !y || !lam) {
-        free(H); free(Ab); free(y); free(lam);
+    double *u = (double *)malloc(sizeof(double) * LL * 2);      /* each direction's input   */
+    double *pre = (double *)malloc(sizeof(double) * LL * 2);    /* ... its conv argument    */
+    double *st = (double *)malloc(sizeof(double) * LL * 2);     /* ... its step             */
+    double *du = (double *)malloc(sizeof(double) * LL * 2);     /* d input, per direction   */
+    double *dst = (double *)malloc(sizeof(double) * LL * 2);    /* d step, per direction    */
+    if (!H || !Ab || !y || !lam || !u || !pre || !st || !du || !dst) {
+        free(H); free(Ab); free(y); free(lam); free(u); free(pre); free(st); free(du); free(dst);
         return ORACLE_ENOMEM;
     }
     for (long r = 0; r < rows; ++r) {
         const long b = r / dim, d = r % dim;
-        const double *xr = x + r * L, *dtr = delta + r * L;
+        const double *xraw = x + r * L;
+        /* each direction's step and input */
+        for (int k = 0; k < 2; ++k) {
+            if (!(dirs & (1 << k))) continue;
+            const double *v = (k && delta_bwd ? delta_bwd : delta) + r * L;
+            const double *bk = k && bias_bwd ? bias_bwd : bias_fwd;
+            const double bias = bk ? bk[d] : 0.0;
+            const double *wk = k && conv_w_bwd ? conv_w_bwd : conv_w;
+            const double *cbk = k && conv_b_bwd ? conv_b_bwd : conv_b;
+            for (long t = 0; t < L; ++t) {
+                st[k * L + t] = use_softplus ? softplus(v[t] + bias) : v[t];
+                if (K > 0) {
+                    double a = cbk ? cbk[d] : 0.0;
+                    for (long j = 0; j < K; ++j) {
+                        const long sidx = conv_tap(t, j, K, L, seg_len, k);
+                        if (sidx >= 0) a += wk[d * K + j] * xraw[sidx];
+                    }
+                    pre[k * L + t] = a;
+                    u[k * L + t] = silu(a);
+                } else {
+                    u[k * L + t] = xraw[t];
+                }
+                du[k * L + t] = 0.0;
+                dst[k * L + t] = 0.0;
+            }
+        }
         /* forward states and outputs of each direction (k = 0 fwd, 1 bwd) */
         for (int k = 0; k < 2; ++k) {
             if (!(dirs & (1 << k))) continue;
+            const double *xr = u + k * L, *dtr = st + k * L;
             const double *Bk = (k && B_bwd ? B_bwd : B) + b * L * N;
             const double *Ck = (k && C_bwd ? C_bwd : C) + b * L * N;
             const double *Ak = (k ? A_bwd : A_fwd) + d * N;
@@ -369,6 +463,8 @@ int oracle_scan_grad(const double *x, const double *delta, const double *z,
         }
         for (int k = 0; k < 2; ++k) {
             if (!(dirs & (1 << k))) continue;
+            const double *xr = u + k * L, *dtr = st + k * L;
+            double *dur = du + k * L, *dstr = dst + k * L;
             const double *Bk = (k && B_bwd ? B_bwd : B) + b * L * N;
             const double *Ck = (k && C_bwd ? C_bwd : C) + b * L * N;
             double *dBk = (k && B_bwd ? dB_bwd : dB) + b * L * N;
@@ -398,8 +494,8 @@ int oracle_scan_grad(const double *x, const double *delta, const double *z,
                     dAk[n] += lam[n] * a * hp * dtr[t];
                     lam[n] = a * lam[n];
                 }
-                dx[r * L + t] += dxx;
-                ddelta[r * L + t] += ddt;
+                dur[t] += dxx;
+                dstr[t] += ddt;
             }
         }
         if (z && dz) {
@@ -412,12 +508,58 @@ int oracle_scan_grad(const double *x, const double *delta, const double *z,
                 dz[r * L + t] = dout[r * L + t] * s * sg * (1.0 + zt * (1.0 - sg));
             }
         }
+        /* chain rule back to the raw step, its bias, x and the taps */
+        for (int k = 0; k < 2; ++k) {
+            if (!(dirs & (1 << k))) continue;
+            const double *v = (k && delta_bwd ? delta_bwd : delta) + r * L;
+            double *dv = (k && delta_bwd ? ddelta_bwd : ddelta) + r * L;
+            const double *bk = k && bias_bwd ? bias_bwd : bias_fwd;
+            double *dbk = k && bias_bwd ? dbias_bwd : dbias_fwd;
+            const double bias = bk ? bk[d] : 0.0;
+            const double *wk = k && conv_w_bwd ? conv_w_bwd : conv_w;
+            double *dwk = k && conv_w_bwd ? dconv_w_bwd : dconv_w;
+            double *dcbk = k && conv_b_bwd ? dconv_b_bwd : (conv_b ? dconv_b : NULL);
+            for (long t = 0; t < L; ++t) {
+                const double g_step = dst[k * L + t] * (use_softplus ? sigmoid(v[t] + bias) : 1.0);
+                dv[t] += g_step;
+                if (use_softplus) dbk[d] += g_step;
+                if (K > 0) {
+                    const double dp = du[k * L + t] * dsilu(pre[k * L + t]);
+                    for (long j = 0; j < K; ++j) {
+                        const long sidx = conv_tap(t, j, K, L, seg_len, k);
+                        if (sidx < 0) continue;
+                        dx[r * L + sidx] += wk[d * K + j] * dp;
+                        dwk[d * K + j] += dp * xraw[sidx];
+                    }
+                    if (dcbk) dcbk[d] += dp;
+                } else {
+                    dx[r * L + t] += du[k * L + t];
+                }
+            }
+        }
     }
-    free(H);
-    free(Ab);
-    free(y);
-    free(lam);
+    free(H); free(Ab); free(y); free(lam); free(u); free(pre); free(st); free(du); free(dst);
     return ORACLE_OK;
+}
+
+/* The gradient with the steps used as given, shared by both directions, and
+ * no convolution (the inputs and outputs of oracle_scan). */
+int oracle_scan_grad(const double *x, const double *delta, const double *z,
+                     const double *B, const double *C,
+                     const double *B_bwd, const double *C_bwd,
+                     const double *A_fwd, const double *A_bwd,
+                     const double *D_fwd, const double *D_bwd,
+                     const double *dout,
+                     double *dx, double *ddelta, double *dz,
+                     double *dB, double *dC, double *dB_bwd, double *dC_bwd,
+                     double *dA_fwd, double *dA_bwd, double *dD_fwd, double *dD_bwd,
+                     long batch, long dim, long L, long N, int dirs, long seg_len)
+{
+    return oracle_scan_grad_ex(x, delta, z, B, C, B_bwd, C_bwd, A_fwd, A_bwd, D_fwd, D_bwd,
+                               NULL, NULL, NULL, 0, NULL, NULL, NULL, NULL, 0, dout,
+                               dx, ddelta, dz, dB, dC, dB_bwd, dC_bwd, dA_fwd, dA_bwd, dD_fwd, dD_bwd,
+                               NULL, NULL, NULL, NULL, NULL, NULL, NULL,
+                               batch, dim, L, N, dirs, seg_len);
 }
 
 /*

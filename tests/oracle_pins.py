@@ -411,6 +411,103 @@ def _grad_fd_ok(lib, rng, dirs, gate, seg_len, own_bc, L=6):
     return True
 
 
+def _grad_opts_fd_ok(lib, rng, dirs, seg_len, sp, own_step, own_bias, K, own_conv, L=7):
+    """As _grad_fd_ok, with the fused step (softplus(delta + bias), the
+    backward direction's own delta and bias) and the directional convolution
+    (own backward taps and bias or shared): every entry of every gradient,
+    the raw steps, biases and taps included, against a central finite
+    difference of the forward oracle with the same options."""
+    b, d, N = 1, 2, 3
+    p = _rand_problem(rng, b, d, L, N, gate=True)
+    p["delta"] = rng.normal(-1.0, 0.6, (b, d, L))            # raw step (pre-softplus when sp)
+    if not sp:
+        p["delta"] = np.abs(p["delta"]) * 0.5 + 0.05
+    if own_step:
+        p["delta_bwd"] = (rng.normal(-1.0, 0.6, (b, d, L)) if sp
+                          else rng.uniform(0.05, 0.6, (b, d, L)))
+    if sp:
+        p["delta_bias"] = rng.uniform(-0.5, 0.5, d)
+        if own_bias:
+            p["delta_bias_bwd"] = rng.uniform(-0.5, 0.5, d)
+    if K:
+        p["conv_w"] = rng.uniform(-0.8, 0.8, (d, K))
+        p["conv_b"] = rng.uniform(-0.3, 0.3, d)
+        if own_conv:
+            p["conv_w_bwd"] = rng.uniform(-0.8, 0.8, (d, K))
+            p["conv_b_bwd"] = rng.uniform(-0.3, 0.3, d)
+    dout = rng.standard_normal((b, d, L))
+    opt_keys = ("delta_bwd", "delta_bias", "delta_bias_bwd", "conv_w", "conv_b", "conv_w_bwd",
+                "conv_b_bwd")
+
+    def opts(q):
+        o = {k: q.get(k) for k in opt_keys}
+        o["delta_softplus"] = sp
+        return o
+
+    def loss(q):
+        out = oracle.scan(q["x"], q["delta"], q["A_fwd"], q["A_bwd"], q["B"], q["C"], q["D_fwd"],
+                          q["D_bwd"], q["z"], dirs=dirs, seg_len=seg_len, lib=lib, **opts(q))
+        return float(np.sum(dout * out))
+
+    g = oracle.scan_grad(p["x"], p["delta"], p["A_fwd"], p["A_bwd"], p["B"], p["C"], p["D_fwd"],
+                         p["D_bwd"], p["z"], dout, dirs=dirs, seg_len=seg_len, lib=lib, **opts(p))
+    names = {"x": "dx", "delta": "ddelta", "z": "dz", "B": "dB", "C": "dC", "A_fwd": "dA_fwd",
+             "A_bwd": "dA_bwd", "D_fwd": "dD_fwd", "D_bwd": "dD_bwd", "delta_bwd": "ddelta_bwd",
+             "delta_bias": "ddelta_bias", "delta_bias_bwd": "ddelta_bias_bwd", "conv_w": "dconv_w",
+             "conv_b": "dconv_b", "conv_w_bwd": "dconv_w_bwd", "conv_b_bwd": "dconv_b_bwd"}
+    eps = 1e-6
+    for k, name in names.items():
+        if p.get(k) is None:
+            continue
+        if k in ("A_fwd", "D_fwd") and not dirs & 1 or k in ("A_bwd", "D_bwd") and not dirs & 2:
+            continue
+        if g.get(name) is None:
+            return False
+        fd = np.zeros_like(p[k])
+        for idx in np.ndindex(p[k].shape):
+            q = {kk: (vv.copy() if isinstance(vv, np.ndarray) else vv) for kk, vv in p.items()}
+            q[k][idx] += eps
+            lp = loss(q)
+            q[k][idx] -= 2 * eps
+            fd[idx] = (lp - loss(q)) / (2 * eps)
+        if not _close(g[name], fd, 1e-6):
+            return False
+    return True
+
+
+def pin_gradient_step_options_fd(lib):
+    """The gradient through the fused step map softplus(delta + bias) (the
+    raw step and the bias), with a shared step, the backward direction's own
+    step, and its own bias, on plain and folded rows, against central finite
+    differences of the forward oracle."""
+    rng = np.random.default_rng(61)
+    ok = True
+    for dirs, seg, sp, own_step, own_bias in ((3, 0, True, False, False), (3, 0, True, True, True),
+                                              (3, 0, False, True, False), (2, 0, True, True, False),
+                                              (3, 4, True, True, True)):
+        ok = ok and _grad_opts_fd_ok(lib, rng, dirs, seg, sp, own_step, own_bias, 0, False,
+                                     L=2 * seg if seg else 7)
+    return ok
+
+
+def pin_gradient_conv_fd(lib):
+    """The gradient through the directional convolution + SiLU (x through
+    the taps of both directions, the taps and the biases, shared or per
+    direction), alone and with the fused step, on plain rows and on folded
+    rows whose taps stop at segment edges, against central finite
+    differences of the forward oracle."""
+    rng = np.random.default_rng(67)
+    ok = True
+    for dirs, seg, sp, own_step, K, own_conv in ((3, 0, False, False, 4, False),
+                                                 (3, 0, False, False, 3, True),
+                                                 (1, 0, False, False, 2, False),
+                                                 (3, 0, True, True, 4, True),
+                                                 (3, 4, False, False, 3, True)):
+        ok = ok and _grad_opts_fd_ok(lib, rng, dirs, seg, sp, own_step, False, K, own_conv,
+                                     L=2 * seg if seg else 7)
+    return ok
+
+
 def pin_gradient_finite_differences(lib):
     """The adjoint gradients (dx, ddelta, dz, dB, dC, per-direction dB/dC,
     dA, dD) equal central finite differences of the forward oracle, for each
@@ -475,7 +572,8 @@ PINS = [pin_worked_example, pin_quadratic_form, pin_A_zero_prefix_sum,
         pin_backward_is_flipped_forward, pin_folded_equals_segments,
         pin_reset_first_token, pin_gate, pin_linearity, pin_softplus_step,
         pin_per_direction_step, pin_conv_taps, pin_conv_feeds_each_direction,
-        pin_gradient_finite_differences, pin_ncssd_matrix_form, pin_ncssd_token_order]
+        pin_gradient_finite_differences, pin_gradient_step_options_fd, pin_gradient_conv_fd,
+        pin_ncssd_matrix_form, pin_ncssd_token_order]
 
 
 def failing_pins(lib):

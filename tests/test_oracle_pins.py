@@ -56,6 +56,20 @@ MUTANTS = {
     "grad_gate_derivative_sign": ("(1.0 + zt * (1.0 - sg))", "(1.0 - zt * (1.0 - sg))"),
     "grad_skip_dropped": ("double dxx = ds * Dk, ddt = 0.0;", "double dxx = 0.0, ddt = 0.0;"),
     "grad_dA_without_step": ("dAk[n] += lam[n] * a * hp * dtr[t];", "dAk[n] += lam[n] * a * hp;"),
+    "grad_softplus_derivative_dropped": (
+        "dst[k * L + t] * (use_softplus ? sigmoid(v[t] + bias) : 1.0)", "dst[k * L + t]"),
+    "grad_softplus_derivative_without_bias": ("sigmoid(v[t] + bias) : 1.0", "sigmoid(v[t]) : 1.0"),
+    "grad_bwd_bias_gradient_to_fwd": ("double *dbk = k && bias_bwd ? dbias_bwd : dbias_fwd;",
+                                      "double *dbk = dbias_fwd;"),
+    "grad_own_steps_swapped": ("double *dv = (k && delta_bwd ? ddelta_bwd : ddelta) + r * L;",
+                               "double *dv = (delta_bwd ? ddelta_bwd : ddelta) + r * L;"),
+    "grad_silu_derivative_is_sigmoid": ("return q + p * q * (1.0 - q);", "return q;"),
+    "grad_conv_transpose_to_output_token": ("dx[r * L + sidx] += wk[d * K + j] * dp;",
+                                            "dx[r * L + t] += wk[d * K + j] * dp;"),
+    "grad_conv_taps_read_output_token": ("dwk[d * K + j] += dp * xraw[sidx];",
+                                         "dwk[d * K + j] += dp * xraw[t];"),
+    "grad_conv_bias_gradient_dropped": ("if (dcbk) dcbk[d] += dp;", ""),
+    "grad_conv_recompute_without_bias": ("double a = cbk ? cbk[d] : 0.0;", "double a = 0.0;"),
     "ncssd_weight_dropped": ("h += mb[j] * Bb[j * N + n] * xb[d * L + j];",
                              "h += Bb[j * N + n] * xb[d * L + j];"),
     "ncssd_reads_C_for_B": ("h += mb[j] * Bb[j * N + n] * xb[d * L + j];",
