@@ -62,7 +62,8 @@ class GradArgs(ctypes.Structure):
     """Mirror of ``vssm_grad_args`` (include/vssm.h)."""
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "dout", "dx", "ddelta", "dz", "dB", "dC", "dB_bwd", "dC_bwd", "dA_fwd", "dA_bwd",
-        "dD_fwd", "dD_bwd")]
+        "dD_fwd", "dD_bwd", "ddelta_bwd", "ddelta_bias", "ddelta_bias_bwd", "dconv_w", "dconv_b",
+        "dconv_w_bwd", "dconv_b_bwd")]
 
 
 class NcssdArgs(ctypes.Structure):
@@ -335,17 +336,28 @@ def grad_workspace_size(a: ScanArgs, seg_len: int = 0) -> int:
 
 def scan_grad(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *, dout,
               dirs: int = DIR_BOTH, seg_len: int = 0, B_bwd=None, C_bwd=None,
-              stream: Optional[torch.cuda.Stream] = None, workspace=None) -> dict:
+              stream: Optional[torch.cuda.Stream] = None, workspace=None, **step) -> dict:
     """``vssm_scan_grad``: gradients of sum(dout * out) for the forward call
-    with these arguments (``seg_len`` > 0: the folded scan). Returns a dict
-    with dx, ddelta, dz (None without z) in x's dtype and float32 dB, dC,
-    dB_bwd, dC_bwd (None when shared), dA_fwd, dA_bwd, dD_fwd, dD_bwd (None
-    for a direction that is not run). Output tensors are allocated here."""
-    a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, None, B_bwd, C_bwd, dirs)
+    with these arguments (``seg_len`` > 0: the folded scan; ``step``: the step
+    options and the convolution of :func:`make_args`). Returns a dict with dx,
+    ddelta, dz (None without z) in x's dtype and float32 dB, dC, dB_bwd, dC_bwd
+    (None when shared), dA_fwd, dA_bwd, dD_fwd, dD_bwd (None for a direction
+    that is not run); with the options also ddelta_bwd (x's dtype),
+    ddelta_bias, ddelta_bias_bwd, dconv_w, dconv_b, dconv_w_bwd, dconv_b_bwd
+    (float32), each None unless the matching input is given. Output tensors
+    are allocated here."""
+    a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, None, B_bwd, C_bwd, dirs, **step)
     _dev_tensor("dout", dout, x.dtype, x.shape, x.device)
     batch, dim, L = x.shape
     N = B.shape[-1]
     f32 = dict(dtype=torch.float32, device=x.device)
+    sp = bool(step.get("delta_softplus"))
+    cw = step.get("conv_w")
+    K = int(cw.shape[1]) if cw is not None else 0
+
+    def given(name):
+        return step.get(name) is not None
+
     out = dict(dx=torch.empty_like(x), ddelta=torch.empty_like(x),
                dz=torch.empty_like(x) if z is not None else None,
                dB=torch.empty(batch, L, N, **f32), dC=torch.empty(batch, L, N, **f32),
@@ -354,7 +366,14 @@ def scan_grad(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *, d
                dA_fwd=torch.empty(dim, N, **f32) if dirs & DIR_FWD else None,
                dA_bwd=torch.empty(dim, N, **f32) if dirs & DIR_BWD else None,
                dD_fwd=torch.empty(dim, **f32) if dirs & DIR_FWD else None,
-               dD_bwd=torch.empty(dim, **f32) if dirs & DIR_BWD else None)
+               dD_bwd=torch.empty(dim, **f32) if dirs & DIR_BWD else None,
+               ddelta_bwd=torch.empty_like(x) if given("delta_bwd") else None,
+               ddelta_bias=torch.empty(dim, **f32) if sp and given("delta_bias") else None,
+               ddelta_bias_bwd=torch.empty(dim, **f32) if sp and given("delta_bias_bwd") else None,
+               dconv_w=torch.empty(dim, K, **f32) if K else None,
+               dconv_b=torch.empty(dim, **f32) if K and given("conv_b") else None,
+               dconv_w_bwd=torch.empty(dim, K, **f32) if K and given("conv_w_bwd") else None,
+               dconv_b_bwd=torch.empty(dim, **f32) if K and given("conv_b_bwd") else None)
     g = GradArgs()
     g.dout = dout.data_ptr()
     for k, v in out.items():

@@ -25,7 +25,7 @@ UNITS = ["vssm_api.cu", "k_warp.cu", "k_warp_plain.cu", "k_warp_sp.cu", "k_warp_
          "k_warp_spconv.cu", "k_general.cu", "k_grad.cu", "k_ncssd.cu"]
 SOURCES = [os.path.join(CSRC, f) for f in UNITS]
 HEADERS = [os.path.join(CSRC, f) for f in ("common.cuh", "scan_kernel.cuh", "scan_warp.cuh", "scan_grad.cuh",
-                                            "ncssd.cuh", "ptx.cuh", "launch.h", "k_warp_opts.cuh")] + [
+                                            "ncssd.cuh", "ptx.cuh", "launch.h", "k_warp_opts.cuh", "grad_ext.cuh")] + [
     os.path.join(ROOT, "include", "vssm.h")]
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,6 +1,7 @@
-// Launchers of the gradient kernels (scan_grad.cuh).
+// Launchers of the gradient kernels (scan_grad.cuh, grad_ext.cuh).
 #include <algorithm>
 
+#include "grad_ext.cuh"
 #include "launch.h"
 
 namespace vssm {
@@ -75,6 +76,37 @@ cudaError_t launch_zero_f32(float *p, size_t n, cudaStream_t s)
     if (!p || n == 0) return cudaSuccess;
     const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, 148 * 8);
     zero_f32_kernel<<<blocks, 256, 0, s>>>(p, (long long)n);
+    return cudaGetLastError();
+}
+
+unsigned stride_blocks(long long n)
+{
+    return (unsigned)std::min<long long>((n + 255) / 256, 148LL * 16);
+}
+
+cudaError_t launch_grad_ext_prep(const GradExtParams &p, bool f32, cudaStream_t s)
+{
+    const long long n = (long long)p.batch * p.dim * p.L;
+    if (n == 0) return cudaSuccess;
+    if (f32) grad_prep_kernel<float><<<stride_blocks(n), 256, 0, s>>>(p);
+    else grad_prep_kernel<__nv_bfloat16><<<stride_blocks(n), 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_widen_bf16(const void *src, float *dst, long long n, cudaStream_t s)
+{
+    if (n == 0) return cudaSuccess;
+    widen_f32_kernel<__nv_bfloat16><<<stride_blocks(n), 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(src), dst, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_grad_ext_post(const GradExtParams &p, bool f32, cudaStream_t s)
+{
+    const long long rows = (long long)p.batch * p.dim;
+    if (rows == 0 || p.L == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)((rows + 3) / 4);
+    if (f32) grad_post_kernel<float><<<blocks, 128, 0, s>>>(p);
+    else grad_post_kernel<__nv_bfloat16><<<blocks, 128, 0, s>>>(p);
     return cudaGetLastError();
 }
 

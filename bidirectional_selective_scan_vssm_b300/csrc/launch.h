@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 
+#include "grad_ext.cuh"
 #include "ncssd.cuh"
 #include "scan_grad.cuh"
 #include "scan_kernel.cuh"
@@ -32,6 +33,12 @@ cudaError_t launch_general(const ScanParams &p, int dirs, bool ysmem, bool f32, 
 cudaError_t launch_grad(const GradParams &p, int dirs, bool f32, long long ngroups, int nrange,
                         cudaStream_t s);
 cudaError_t launch_zero_f32(float *p, size_t n, cudaStream_t s);
+// Gradient with the step options and the convolution: the float32 inputs of
+// each direction, a bfloat16 -> float32 copy, and the chain rule to the raw
+// tensors.
+cudaError_t launch_grad_ext_prep(const GradExtParams &p, bool f32, cudaStream_t s);
+cudaError_t launch_widen_bf16(const void *src, float *dst, long long n, cudaStream_t s);
+cudaError_t launch_grad_ext_post(const GradExtParams &p, bool f32, cudaStream_t s);
 cudaError_t launch_selftest_wait(unsigned *err, uint64_t limit_ns, cudaStream_t s);
 
 // NC-SSD: rows kernel (bf16, whole rows in shared memory), else the tiled

@@ -785,6 +785,191 @@ int host_scan(const vssm_scan_args *a, int seg_len, int slices, void *stream)
     return VSSM_OK;
 }
 
+// ---- gradient
+
+bool grad_composed(const vssm_scan_args *a)
+{
+    return a->delta_softplus || a->delta_bwd || a->conv_k > 0;
+}
+
+// Workspace of the composed gradient (step options or convolution): float32
+// intermediates of each direction that runs, then the plain gradient's
+// workspace for one direction (the directions run one after the other and
+// reuse it). kNone marks an array that is not allocated: u then reads x, st
+// the raw step (float32 I/O without convolution / softplus).
+struct GradExtLayout {
+    static constexpr size_t kNone = ~(size_t)0;
+    size_t u[2] = {kNone, kNone}, pre[2] = {kNone, kNone}, st[2] = {kNone, kNone};
+    size_t du[2] = {kNone, kNone}, dst[2] = {kNone, kNone}, dz[2] = {kNone, kNone};
+    size_t B32[2] = {kNone, kNone}, C32[2] = {kNone, kNone};
+    size_t z32 = kNone, dout32 = kNone, core = 0, total = 0;
+    GradPlan gl;
+};
+
+GradExtLayout grad_ext_layout(const vssm_scan_args *a)
+{
+    GradExtLayout w;
+    const bool bf16 = a->dtype != VSSM_F32;
+    const size_t nf = (size_t)a->batch * a->dim * a->seqlen * sizeof(float);
+    const size_t nbc = (size_t)a->batch * a->seqlen * a->dstate * sizeof(float);
+    size_t cur = 0;
+    auto take = [&cur](size_t n) {
+        const size_t o = cur;
+        cur = al256(cur + n);
+        return o;
+    };
+    // both directions read the same step when neither the step nor its bias differ
+    const bool st_shared = !a->delta_bwd && !(a->delta_softplus && a->delta_bias_bwd);
+    for (int k = 0; k < 2; ++k) {
+        if (!(a->dir_flags & (1 << k))) continue;
+        const bool second = k == 1 && (a->dir_flags & 1);
+        if (a->conv_k > 0) {
+            w.u[k] = take(nf);
+            w.pre[k] = take(nf);
+        } else if (bf16) {
+            w.u[k] = second ? w.u[0] : take(nf);
+        }
+        if (a->delta_softplus || bf16) w.st[k] = (second && st_shared) ? w.st[0] : take(nf);
+        w.du[k] = take(nf);
+        w.dst[k] = take(nf);
+        if (a->z) w.dz[k] = take(nf);
+        if (bf16) {
+            w.B32[k] = (second && !a->B_bwd) ? w.B32[0] : take(nbc);
+            w.C32[k] = (second && !a->C_bwd) ? w.C32[0] : take(nbc);
+        }
+    }
+    if (bf16) {
+        if (a->z) w.z32 = take(nf);
+        w.dout32 = take(nf);
+    }
+    vssm_scan_args one = *a;
+    one.dir_flags = 1;
+    w.gl = make_grad_plan(&one);
+    w.core = take(w.gl.workspace);
+    w.total = cur;
+    return w;
+}
+
+size_t grad_workspace(const vssm_scan_args *a)
+{
+    if ((long long)a->batch * a->dim * a->seqlen == 0) return 0;
+    return grad_composed(a) ? grad_ext_layout(a).total : make_grad_plan(a).workspace;
+}
+
+// The plain gradient's parameters common to both paths.
+void grad_fill_sizes(vssm::GradParams &p, const vssm_scan_args *a, const GradPlan &gl, int seg_len)
+{
+    p.batch = a->batch;
+    p.dim = a->dim;
+    p.L = a->seqlen;
+    p.seg_len = seg_len;
+    p.rgroups = gl.rgroups;
+    p.nch = gl.nch;
+    p.nrange = gl.nrange;
+    p.rch = gl.rch;
+    p.ngroups = gl.ngroups;
+}
+
+// Composed gradient: float32 step and input of each direction (prep), the
+// plain gradient once per direction in float32, then the chain rule back to
+// the raw tensors (post). The accumulated outputs are zeroed by the caller.
+cudaError_t grad_composed_launch(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len,
+                                 unsigned *err, cudaStream_t s)
+{
+    const GradExtLayout w = grad_ext_layout(a);
+    char *ws = static_cast<char *>(a->workspace);
+    auto at = [ws](size_t off) -> float * {
+        return off == GradExtLayout::kNone ? nullptr : reinterpret_cast<float *>(ws + off);
+    };
+    const bool f32 = a->dtype == VSSM_F32;
+    const unsigned dirs = a->dir_flags;
+    vssm::GradExtParams q{};
+    q.x = a->x;
+    q.delta[0] = a->delta;
+    q.delta[1] = a->delta_bwd ? a->delta_bwd : a->delta;
+    q.z = a->z;
+    q.dout = g->dout;
+    q.bias[0] = a->delta_bias;
+    q.bias[1] = a->delta_bias_bwd ? a->delta_bias_bwd : a->delta_bias;
+    q.conv_w[0] = a->conv_w;
+    q.conv_w[1] = a->conv_w_bwd ? a->conv_w_bwd : a->conv_w;
+    q.conv_b[0] = a->conv_b;
+    q.conv_b[1] = a->conv_b_bwd ? a->conv_b_bwd : a->conv_b;
+    q.softplus = a->delta_softplus != 0;
+    q.K = a->conv_k;
+    q.batch = a->batch;
+    q.dim = a->dim;
+    q.L = a->seqlen;
+    q.seg_len = seg_len;
+    q.dirs = (int)dirs;
+    for (int k = 0; k < 2; ++k) {
+        if (!(dirs & (1u << k))) continue;
+        q.u[k] = w.u[k] != GradExtLayout::kNone ? at(w.u[k]) : const_cast<float *>(static_cast<const float *>(a->x));
+        q.pre[k] = at(w.pre[k]);
+        q.st[k] = w.st[k] != GradExtLayout::kNone ? at(w.st[k])
+                                                   : const_cast<float *>(static_cast<const float *>(q.delta[k]));
+        q.du[k] = at(w.du[k]);
+        q.dst[k] = at(w.dst[k]);
+        q.dz[k] = at(w.dz[k]);
+    }
+    q.z32 = at(w.z32);
+    q.dout32 = at(w.dout32);
+    q.dx = g->dx;
+    q.ddelta = g->ddelta;
+    q.ddelta_bwd = g->ddelta_bwd;
+    q.dzo = g->dz;
+    q.dbias[0] = g->ddelta_bias;
+    q.dbias[1] = a->delta_bias_bwd ? g->ddelta_bias_bwd : g->ddelta_bias;
+    q.dconv_w[0] = g->dconv_w;
+    q.dconv_w[1] = a->conv_w_bwd ? g->dconv_w_bwd : g->dconv_w;
+    q.dconv_b[0] = g->dconv_b;
+    q.dconv_b[1] = a->conv_b_bwd ? g->dconv_b_bwd : g->dconv_b;
+
+    cudaError_t e = vssm::launch_grad_ext_prep(q, f32, s);
+    const long long nbc = (long long)a->batch * a->seqlen * a->dstate;
+    for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
+        if (!(dirs & (1u << k)) || w.B32[k] == GradExtLayout::kNone) continue;
+        const bool own_b = k == 0 || !(dirs & 1) || w.B32[1] != w.B32[0];
+        const bool own_c = k == 0 || !(dirs & 1) || w.C32[1] != w.C32[0];
+        if (own_b) e = vssm::launch_widen_bf16(k && a->B_bwd ? a->B_bwd : a->B, at(w.B32[k]), nbc, s);
+        if (own_c && e == cudaSuccess)
+            e = vssm::launch_widen_bf16(k && a->C_bwd ? a->C_bwd : a->C, at(w.C32[k]), nbc, s);
+    }
+    for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
+        if (!(dirs & (1u << k))) continue;
+        vssm::GradParams p{};
+        p.x = q.u[k];
+        p.delta = q.st[k];
+        p.z = f32 ? a->z : q.z32;
+        p.dout = f32 ? g->dout : q.dout32;
+        const void *Bk = f32 ? (k && a->B_bwd ? a->B_bwd : a->B) : at(w.B32[k]);
+        const void *Ck = f32 ? (k && a->C_bwd ? a->C_bwd : a->C) : at(w.C32[k]);
+        p.B[0] = p.B[1] = Bk;
+        p.C[0] = p.C[1] = Ck;
+        p.A[0] = a->A_fwd;
+        p.A[1] = a->A_bwd;
+        p.D[0] = a->D_fwd;
+        p.D[1] = a->D_bwd;
+        p.dx = at(w.du[k]);
+        p.ddelta = at(w.dst[k]);
+        p.dz = at(w.dz[k]);
+        p.dB[0] = p.dB[1] = k && g->dB_bwd ? g->dB_bwd : g->dB;
+        p.dC[0] = p.dC[1] = k && g->dC_bwd ? g->dC_bwd : g->dC;
+        p.dA[0] = g->dA_fwd;
+        p.dA[1] = g->dA_bwd;
+        p.dD[0] = g->dD_fwd;
+        p.dD[1] = g->dD_bwd;
+        p.ckpt = at(w.core);
+        p.part = nullptr;
+        p.summ = w.gl.nrange > 1 ? reinterpret_cast<float *>(ws + w.core + w.gl.summ_off) : nullptr;
+        p.err = err;
+        grad_fill_sizes(p, a, w.gl, seg_len);
+        e = vssm::launch_grad(p, 1 << k, true, w.gl.ngroups, w.gl.nrange, s);
+    }
+    if (e == cudaSuccess) e = vssm::launch_grad_ext_post(q, f32, s);
+    return e;
+}
+
 }  // namespace
 
 extern "C" {
@@ -941,9 +1126,9 @@ int vssm_scan_grad_workspace_size(const vssm_scan_args *a, int seg_len, size_t *
 {
     if (!a || !bytes) return fail(VSSM_ERR_INVALID_ARG, "args or bytes is NULL");
     if (a->batch < 0 || a->dim < 0 || a->seqlen < 0 || a->dir_flags < 1 || a->dir_flags > 3 ||
-        seg_len < 0)
-        return fail(VSSM_ERR_INVALID_ARG, "invalid sizes or dir_flags");
-    *bytes = (long long)a->batch * a->dim * a->seqlen == 0 ? 0 : make_grad_plan(a).workspace;
+        seg_len < 0 || a->conv_k < 0 || a->conv_k > vssm::kMaxConv)
+        return fail(VSSM_ERR_INVALID_ARG, "invalid sizes, dir_flags or conv_k");
+    *bytes = grad_workspace(a);
     return VSSM_OK;
 }
 
@@ -957,9 +1142,17 @@ int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len
     if (a->dstate != vssm::kMaxState)
         return fail(VSSM_ERR_UNSUPPORTED, "the gradient needs dstate %d (got %d)", vssm::kMaxState,
                     a->dstate);
-    if (a->delta_softplus || a->delta_bwd || a->conv_k)
-        return fail(VSSM_ERR_UNSUPPORTED,
-                    "the gradient supports steps used as given, shared, without convolution");
+    const bool sp = a->delta_softplus != 0, conv = a->conv_k > 0;
+    struct { const void *out; bool want; const char *what; } pairs[] = {
+        {g->ddelta_bwd, a->delta_bwd != nullptr, "ddelta_bwd goes with delta_bwd"},
+        {g->ddelta_bias, sp && a->delta_bias, "ddelta_bias goes with delta_softplus and delta_bias"},
+        {g->ddelta_bias_bwd, sp && a->delta_bias_bwd, "ddelta_bias_bwd goes with delta_softplus and delta_bias_bwd"},
+        {g->dconv_w, conv, "dconv_w goes with conv_k > 0"},
+        {g->dconv_b, conv && a->conv_b, "dconv_b goes with conv_k > 0 and conv_b"},
+        {g->dconv_w_bwd, conv && a->conv_w_bwd, "dconv_w_bwd goes with conv_k > 0 and conv_w_bwd"},
+        {g->dconv_b_bwd, conv && a->conv_b_bwd, "dconv_b_bwd goes with conv_k > 0 and conv_b_bwd"}};
+    for (const auto &pr : pairs)
+        if ((pr.out != nullptr) != pr.want) return fail(VSSM_ERR_INVALID_ARG, "%s", pr.what);
     if ((long long)a->batch * a->dim * a->seqlen == 0) return VSSM_OK;
     const unsigned dirs = a->dir_flags;
     if (!g->dout || !g->dx || !g->ddelta || !g->dB || !g->dC)
@@ -972,26 +1165,33 @@ int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len
     if ((dirs & 2) && (!g->dA_bwd || !g->dD_bwd))
         return fail(VSSM_ERR_INVALID_ARG, "dA_bwd and dD_bwd are required for the backward direction");
     const void *gp[] = {g->dout, g->dx, g->ddelta, g->dz, g->dB, g->dC, g->dB_bwd, g->dC_bwd,
-                        g->dA_fwd, g->dA_bwd, g->dD_fwd, g->dD_bwd};
+                        g->dA_fwd, g->dA_bwd, g->dD_fwd, g->dD_bwd, g->ddelta_bwd, g->ddelta_bias,
+                        g->ddelta_bias_bwd, g->dconv_w, g->dconv_b, g->dconv_w_bwd, g->dconv_b_bwd};
     for (const void *q : gp)
         if (q && !aligned16(q)) return fail(VSSM_ERR_MISALIGNED, "gradient pointer %p is not 16-byte aligned", q);
-    const GradPlan gl = make_grad_plan(a);
-    if (!a->workspace || a->workspace_bytes < gl.workspace)
-        return fail(VSSM_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", gl.workspace,
+    const bool composed = grad_composed(a);
+    const GradPlan gl = composed ? grad_ext_layout(a).gl : make_grad_plan(a);
+    const size_t need = grad_workspace(a);
+    if (!a->workspace || a->workspace_bytes < need)
+        return fail(VSSM_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", need,
                     a->workspace ? a->workspace_bytes : (size_t)0);
     if (gl.ngroups * gl.nrange > 0x7fffffffLL) return fail(VSSM_ERR_UNSUPPORTED, "problem too large for one grid");
     const size_t es = a->dtype == VSSM_F32 ? 4 : 2;
     const size_t nact = (size_t)a->batch * a->dim * a->seqlen * es;
     const size_t nbc = (size_t)a->batch * a->seqlen * a->dstate * 4;
     const size_t npar = (size_t)a->dim * a->dstate * 4, nd = (size_t)a->dim * 4;
+    const size_t ncw = (size_t)a->dim * std::max(a->conv_k, 0) * 4;
     const struct { const void *p; size_t n; } outs[] = {
         {g->dx, nact}, {g->ddelta, nact}, {g->dz, nact}, {g->dB, nbc}, {g->dC, nbc},
         {g->dB_bwd, nbc}, {g->dC_bwd, nbc}, {g->dA_fwd, npar}, {g->dA_bwd, npar},
-        {g->dD_fwd, nd}, {g->dD_bwd, nd}};
+        {g->dD_fwd, nd}, {g->dD_bwd, nd}, {g->ddelta_bwd, nact}, {g->ddelta_bias, nd},
+        {g->ddelta_bias_bwd, nd}, {g->dconv_w, ncw}, {g->dconv_b, nd}, {g->dconv_w_bwd, ncw},
+        {g->dconv_b_bwd, nd}};
     const void *ins[] = {a->x, a->delta, a->z, a->B, a->C, a->B_bwd, a->C_bwd, a->A_fwd, a->A_bwd,
-                         a->D_fwd, a->D_bwd, g->dout};
+                         a->D_fwd, a->D_bwd, g->dout, a->delta_bwd, a->delta_bias, a->delta_bias_bwd,
+                         a->conv_w, a->conv_b, a->conv_w_bwd, a->conv_b_bwd};
     const size_t insz[] = {nact, nact, nact, nbc / 4 * es, nbc / 4 * es, nbc / 4 * es, nbc / 4 * es,
-                           npar, npar, nd, nd, nact};
+                           npar, npar, nd, nd, nact, nact, nd, nd, ncw, nd, ncw, nd};
     for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
         if (!outs[i].p) continue;
         if (overlaps(outs[i].p, outs[i].n, a->workspace, a->workspace_bytes))
@@ -1003,58 +1203,58 @@ int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len
             if (overlaps(outs[i].p, outs[i].n, outs[k].p, outs[k].n))
                 return fail(VSSM_ERR_INVALID_ARG, "two gradient outputs overlap");
     }
+    for (size_t k = 0; k < sizeof(ins) / sizeof(ins[0]); ++k)
+        if (overlaps(a->workspace, a->workspace_bytes, ins[k], insz[k]))
+            return fail(VSSM_ERR_INVALID_ARG, "the workspace overlaps an input");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    vssm::GradParams p{};
-    p.x = a->x;
-    p.delta = a->delta;
-    p.z = a->z;
-    p.dout = g->dout;
-    p.B[0] = a->B;
-    p.C[0] = a->C;
-    p.B[1] = a->B_bwd ? a->B_bwd : a->B;
-    p.C[1] = a->C_bwd ? a->C_bwd : a->C;
-    p.A[0] = a->A_fwd;
-    p.A[1] = a->A_bwd;
-    p.D[0] = a->D_fwd;
-    p.D[1] = a->D_bwd;
-    p.dx = g->dx;
-    p.ddelta = g->ddelta;
-    p.dz = g->dz;
-    p.dB[0] = g->dB;
-    p.dC[0] = g->dC;
-    p.dB[1] = g->dB_bwd ? g->dB_bwd : g->dB;
-    p.dC[1] = g->dC_bwd ? g->dC_bwd : g->dC;
-    p.dA[0] = g->dA_fwd;
-    p.dA[1] = g->dA_bwd;
-    p.dD[0] = g->dD_fwd;
-    p.dD[1] = g->dD_bwd;
-    p.ckpt = static_cast<float *>(a->workspace);
-    p.part = dirs == 3 ? reinterpret_cast<float *>(static_cast<char *>(a->workspace) + gl.part_off)
-                       : nullptr;
-    p.summ = gl.nrange > 1 ? reinterpret_cast<float *>(static_cast<char *>(a->workspace) + gl.summ_off)
-                           : nullptr;
-    p.err = device_error_word();
-    if (!p.err) return fail(VSSM_ERR_CUDA, "cannot locate the device error word");
-    p.batch = a->batch;
-    p.dim = a->dim;
-    p.L = a->seqlen;
-    p.seg_len = seg_len;
-    p.rgroups = gl.rgroups;
-    p.nch = gl.nch;
-    p.nrange = gl.nrange;
-    p.rch = gl.rch;
-    p.ngroups = gl.ngroups;
+    unsigned *err = device_error_word();
+    if (!err) return fail(VSSM_ERR_CUDA, "cannot locate the device error word");
     // the reductions accumulate atomically: start them at zero
     const size_t nbcf = (size_t)a->batch * a->seqlen * a->dstate;
-    float *zs[] = {g->dB, g->dC, g->dB_bwd, g->dC_bwd};
+    const struct { float *p; size_t n; } zs[] = {
+        {g->dB, nbcf}, {g->dC, nbcf}, {g->dB_bwd, nbcf}, {g->dC_bwd, nbcf},
+        {(dirs & 1) ? g->dA_fwd : nullptr, npar / 4}, {(dirs & 1) ? g->dD_fwd : nullptr, nd / 4},
+        {(dirs & 2) ? g->dA_bwd : nullptr, npar / 4}, {(dirs & 2) ? g->dD_bwd : nullptr, nd / 4},
+        {g->ddelta_bias, nd / 4}, {g->ddelta_bias_bwd, nd / 4}, {g->dconv_w, ncw / 4},
+        {g->dconv_b, nd / 4}, {g->dconv_w_bwd, ncw / 4}, {g->dconv_b_bwd, nd / 4}};
     cudaError_t e = cudaSuccess;
-    for (float *q : zs)
-        if (e == cudaSuccess) e = vssm::launch_zero_f32(q, nbcf, s);
-    if ((dirs & 1) && e == cudaSuccess) e = vssm::launch_zero_f32(g->dA_fwd, (size_t)a->dim * 16, s);
-    if ((dirs & 1) && e == cudaSuccess) e = vssm::launch_zero_f32(g->dD_fwd, (size_t)a->dim, s);
-    if ((dirs & 2) && e == cudaSuccess) e = vssm::launch_zero_f32(g->dA_bwd, (size_t)a->dim * 16, s);
-    if ((dirs & 2) && e == cudaSuccess) e = vssm::launch_zero_f32(g->dD_bwd, (size_t)a->dim, s);
-    if (e == cudaSuccess) e = vssm::launch_grad(p, (int)dirs, a->dtype == VSSM_F32, gl.ngroups, gl.nrange, s);
+    for (const auto &z : zs)
+        if (e == cudaSuccess) e = vssm::launch_zero_f32(z.p, z.n, s);
+    if (e == cudaSuccess && composed) e = grad_composed_launch(a, g, seg_len, err, s);
+    if (e == cudaSuccess && !composed) {
+        vssm::GradParams p{};
+        p.x = a->x;
+        p.delta = a->delta;
+        p.z = a->z;
+        p.dout = g->dout;
+        p.B[0] = a->B;
+        p.C[0] = a->C;
+        p.B[1] = a->B_bwd ? a->B_bwd : a->B;
+        p.C[1] = a->C_bwd ? a->C_bwd : a->C;
+        p.A[0] = a->A_fwd;
+        p.A[1] = a->A_bwd;
+        p.D[0] = a->D_fwd;
+        p.D[1] = a->D_bwd;
+        p.dx = g->dx;
+        p.ddelta = g->ddelta;
+        p.dz = g->dz;
+        p.dB[0] = g->dB;
+        p.dC[0] = g->dC;
+        p.dB[1] = g->dB_bwd ? g->dB_bwd : g->dB;
+        p.dC[1] = g->dC_bwd ? g->dC_bwd : g->dC;
+        p.dA[0] = g->dA_fwd;
+        p.dA[1] = g->dA_bwd;
+        p.dD[0] = g->dD_fwd;
+        p.dD[1] = g->dD_bwd;
+        p.ckpt = static_cast<float *>(a->workspace);
+        p.part = dirs == 3 ? reinterpret_cast<float *>(static_cast<char *>(a->workspace) + gl.part_off)
+                           : nullptr;
+        p.summ = gl.nrange > 1 ? reinterpret_cast<float *>(static_cast<char *>(a->workspace) + gl.summ_off)
+                               : nullptr;
+        p.err = err;
+        grad_fill_sizes(p, a, gl, seg_len);
+        e = vssm::launch_grad(p, (int)dirs, a->dtype == VSSM_F32, gl.ngroups, gl.nrange, s);
+    }
     return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "launch");
 }
 

@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define VSSM_VERSION 161 /* 1.6.1 */
+#define VSSM_VERSION 170 /* 1.7.0 */
 
 typedef enum {
     VSSM_OK = 0,
@@ -253,6 +253,20 @@ typedef struct {
     float *dA_fwd, *dA_bwd;  /* [dim][dstate] fp32, written; required for each
                                 direction the call runs                       */
     float *dD_fwd, *dD_bwd;  /* [dim] fp32, written; as dA                     */
+    /* Gradients of the step options and of the convolution (zero-initialise
+     * the struct to leave them unset; each is required exactly when the
+     * forward call has the corresponding input): */
+    void *ddelta_bwd;        /* [batch][dim][seqlen], dtype of x: d/d delta_bwd;
+                                iff delta_bwd is given (ddelta is then the
+                                forward direction's step only)                */
+    float *ddelta_bias;      /* [dim] fp32; iff delta_softplus and delta_bias
+                                (with a shared bias it holds both directions') */
+    float *ddelta_bias_bwd;  /* [dim] fp32; iff delta_softplus and delta_bias_bwd */
+    float *dconv_w, *dconv_b;          /* [dim][conv_k], [dim] fp32; dconv_w iff
+                                          conv_k > 0, dconv_b iff conv_b      */
+    float *dconv_w_bwd, *dconv_b_bwd;  /* iff conv_w_bwd / conv_b_bwd (else the
+                                          backward taps' gradients are added
+                                          to dconv_w / dconv_b)               */
 } vssm_grad_args;
 
 /*
@@ -266,11 +280,21 @@ typedef struct {
  * fp32 sums over batch, channels and tokens, computed with atomic additions
  * (their summation order, and so their last bits, can vary from run to run).
  *
- * Supported: dstate == 16, steps used as given and shared by both
- * directions, no convolution (delta_softplus == 0, delta_bwd == NULL,
- * conv_k == 0); anything else is VSSM_ERR_UNSUPPORTED. a->workspace must hold
- * vssm_scan_grad_workspace_size bytes and must not overlap any input or
- * output. Asynchronous on `stream`; the
+ * With the step options and the convolution (delta_softplus, delta_bwd,
+ * conv_k > 0) the derivatives reach the raw tensors through the chain rule:
+ * the step of direction k is s_k = softplus(v_k + bias_k) (or v_k), so
+ * d v_k = d s_k * sigmoid(v_k + bias_k) and d bias_k = sum over batch and
+ * tokens of d v_k; its input is u_k = silu(pre_k), pre_k the direction's
+ * depthwise convolution of x (causal forward, reversed backward, segment
+ * bounded when folded), so x, the taps and the bias get the transposed
+ * convolution of d pre_k = d u_k * silu'(pre_k). The call then runs the
+ * scan's gradient once per direction on float32 copies of that direction's
+ * step and input (the values the forward computes), and needs the larger
+ * workspace that vssm_scan_grad_workspace_size reports for it.
+ *
+ * Supported: dstate == 16; anything else is VSSM_ERR_UNSUPPORTED.
+ * a->workspace must hold vssm_scan_grad_workspace_size bytes and must not
+ * overlap any input or output. Asynchronous on `stream`; the
  * pair rendezvous of the two directions is bounded as in the forward kernel
  * (vssm_device_error). When that wait expires (vssm_device_error then
  * returns VSSM_ERR_TIMEOUT), every gradient output of the call is undefined:

@@ -39,7 +39,8 @@ def test_library_exports_every_declared_symbol(v):
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared in vssm.h but not exported"
     assert set(v.EXPORTS) <= set(declared_functions())
-    assert v.version() == 161
+    declared = re.search(r"#define\s+VSSM_VERSION\s+(\d+)", open(HEADER).read())
+    assert declared and v.version() == int(declared.group(1))
 
 
 def test_args_struct_layout_matches_header(v):
@@ -48,22 +49,26 @@ def test_args_struct_layout_matches_header(v):
     assert ctypes.sizeof(v.ScanArgs) == 208
 
 
-def test_args_struct_matches_c_header(v, tmp_path):
+@pytest.mark.parametrize("struct,cname", [("ScanArgs", "vssm_scan_args"),
+                                          ("GradArgs", "vssm_grad_args"),
+                                          ("NcssdArgs", "vssm_ncssd_args")])
+def test_args_struct_matches_c_header(v, tmp_path, struct, cname):
     """Compile a C program against include/vssm.h and compare the struct's
     size and field offsets with the ctypes mirror."""
+    mirror = getattr(v, struct)
     src = tmp_path / "layout.c"
-    fields = [f[0] for f in v.ScanArgs._fields_]
+    fields = [f[0] for f in mirror._fields_]
     src.write_text("#include <stdio.h>\n#include <stddef.h>\n#include \"vssm.h\"\n"
-                   "int main(void) {\n  printf(\"%zu\\n\", sizeof(vssm_scan_args));\n" +
-                   "".join(f"  printf(\"%zu\\n\", offsetof(vssm_scan_args, {f}));\n"
+                   f"int main(void) {{\n  printf(\"%zu\\n\", sizeof({cname}));\n" +
+                   "".join(f"  printf(\"%zu\\n\", offsetof({cname}, {f}));\n"
                            for f in fields) + "  return 0;\n}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-std=c11", "-I", os.path.dirname(HEADER), "-o", str(exe), str(src)],
                    check=True, capture_output=True)
     got = [int(t) for t in subprocess.run([str(exe)], check=True, capture_output=True,
                                           text=True).stdout.split()]
-    assert got[0] == ctypes.sizeof(v.ScanArgs)
-    assert got[1:] == [getattr(v.ScanArgs, f).offset for f in fields]
+    assert got[0] == ctypes.sizeof(mirror)
+    assert got[1:] == [getattr(mirror, f).offset for f in fields]
 
 
 def _args(v, **kw):
@@ -247,8 +252,15 @@ def test_grad_validation(v):
     def call(a, g, seg=0):
         return v.lib.vssm_scan_grad(ctypes.byref(a), ctypes.byref(g), seg, None)
     assert call(_args(v, dstate=8), _grad_args(v)) == -2
-    assert call(_args(v, delta_softplus=1), _grad_args(v)) == -2
-    assert call(_args(v, conv_k=4, conv_w=(1 << 20) * 13), _grad_args(v)) == -2
+    # the option gradients go exactly with their inputs
+    assert call(_args(v, delta_softplus=1), _grad_args(v)) == -6          # valid; no workspace
+    assert call(_args(v, delta_softplus=1), _grad_args(v, ddelta_bias=(1 << 20) * 20)) == -1
+    assert call(_args(v, delta_bwd=(1 << 20) * 12), _grad_args(v)) == -1  # ddelta_bwd missing
+    assert call(_args(v, conv_k=4, conv_w=(1 << 20) * 13), _grad_args(v)) == -1  # dconv_w missing
+    assert call(_args(v, conv_k=4, conv_w=(1 << 20) * 13),
+                _grad_args(v, dconv_w=(1 << 20) * 20, dconv_b=(1 << 20) * 21)) == -1  # no conv_b
+    assert call(_args(v, conv_k=4, conv_w=(1 << 20) * 13),
+                _grad_args(v, dconv_w=(1 << 20) * 20 + 4)) == -3
     assert call(_args(v), _grad_args(v, dout=None)) == -1
     assert call(_args(v), _grad_args(v, dz=None)) == -1          # the call has z
     assert call(_args(v, B_bwd=(1 << 20) * 14), _grad_args(v)) == -1  # dB_bwd missing
@@ -346,3 +358,32 @@ def test_host_pipeline_validation(v):
     assert _host_ws(v, _args(v), slices=-1)[0] == -1
     assert _host_ws(v, _args(v, batch=0))[1] == 0
     assert v.lib.vssm_scan_host(ctypes.byref(_args(v)), 0, 0, None) == -6      # no workspace
+
+
+def test_grad_workspace_sizes_with_options(v):
+    """The plain gradient: 16 x 32 fp32 checkpoints per 4-token chunk, channel
+    group of 32 and direction, plus 96 fp32 per token and channel group
+    exchanged between the directions. With the step options or the
+    convolution: float32 intermediates per direction (input, convolution
+    argument, step, the two token gradients, the gate's share), float32
+    copies of z, dout, B and C for bfloat16 I/O, then one direction's plain
+    workspace."""
+    n = ctypes.c_size_t(0)
+    a = _args(v, batch=2, dim=64, seqlen=40, dtype=0)            # float32, both directions
+    assert v.lib.vssm_scan_grad_workspace_size(ctypes.byref(a), 0, ctypes.byref(n)) == 0
+    ck = 2 * 2 * 2 * 10 * 512 * 4                       # dirs x batch x groups x 4-token chunks
+    part = 2 * 2 * 40 * 96 * 4
+    assert n.value == ck + part
+    one = ck // 2                                                 # one direction's checkpoints
+    tok = 2 * 64 * 40 * 4
+    r = lambda b: (b + 255) // 256 * 256
+    # float32, convolution: per direction u, pre, du, dst, dz (the raw step is read as given)
+    a = _args(v, batch=2, dim=64, seqlen=40, dtype=0, conv_k=2, conv_w=(1 << 20) * 13)
+    assert v.lib.vssm_scan_grad_workspace_size(ctypes.byref(a), 0, ctypes.byref(n)) == 0
+    assert n.value == 2 * 5 * r(tok) + r(one)
+    # bfloat16, softplus with one shared step: one u and one st for both directions, then
+    # du, dst, dz per direction, B and C copies (shared), z and dout copies
+    bc = 2 * 40 * 16 * 4
+    a = _args(v, batch=2, dim=64, seqlen=40, dtype=1, delta_softplus=1)
+    assert v.lib.vssm_scan_grad_workspace_size(ctypes.byref(a), 0, ctypes.byref(n)) == 0
+    assert n.value == (2 + 2 * 3 + 2) * r(tok) + 2 * r(bc) + r(one)
