@@ -235,7 +235,7 @@ struct GradLayout {
     // one ring stage: this lane's 16-byte blocks of delta, x, z, dout over the
     // chunk (row slots of SLOT bytes), B and C of the chunk (raw), the
     // chunk's checkpoint [16][32] fp32 and, both directions, the partner's
-    // partial gradients [kTG][3][32] fp32
+    // partial gradients [kTG][3][32] fp32 (copied in the last phase only)
     static constexpr int SLOT = ((16 - ES) + kTG * ES + 15) / 16 * 16;
     // rows staggered by 16 bytes every 8 rows so that lanes r and r + 8 read
     // different banks
@@ -245,14 +245,17 @@ struct GradLayout {
     static constexpr int sB = sROW + 4 * ROWS;
     static constexpr int sC = sB + kTG * 16 * ES;
     static constexpr int sCK = sC + kTG * 16 * ES;
-    static constexpr int kStage = sCK + 512 * 4;
+    static constexpr int sPT = sCK + 512 * 4;                 // partner's partials [kTG][3][32]
+    static constexpr int kStage = sPT + (BIDIR ? kTG * 3 * 32 * 4 : 0);
     // per warp: 2 stages, then
     //   hb  [kTG + 1][4][32 lanes][4] states (quarter q of a lane's 16 states;
     //                                 a warp's access to one quarter is 512
     //                                 contiguous bytes)
     //   bc  [kTG][32]                 B[16], C[16] of each token, fp32
-    //   tr  [32 lanes][kTP]           per-token dB, dC contributions, transposed
-    static constexpr int kTP = 36;
+    //   tr  [32 lanes][kTP]           dB, dC contributions of two consecutive
+    //                                 tokens of the walk ([token][B 16 | C 16]
+    //                                 per lane), reduced over the lanes together
+    static constexpr int kTP = 68;
     static constexpr int oHB = 2 * kStage;
     static constexpr int oBC = oHB + (kTG + 1) * 4 * 32 * 16;
     static constexpr int oTR = oBC + kTG * 32 * 4;              // two buffers
@@ -263,18 +266,31 @@ struct GradLayout {
     static constexpr int kMinBlocks = kPerSm < 1 ? 1 : (kPerSm > 8 ? 8 : kPerSm);
 };
 
-// Column `lane` of a [32][TP] buffer summed over its 32 rows (four partial
-// sums), added to dB (lanes 0-15) or dC (lanes 16-31) of token t.
+// The dB, dC contributions of two tokens summed over the warp's 32 channels:
+// row r of the [32][TP] buffer holds channel r's values for token slot 0
+// (columns 0..31: B 16, C 16) and slot 1 (columns 32..63). Lane l sums the
+// column pair 2(l mod 16), +1 of slot l / 16 over the rows (one 8-byte load
+// and one packed add per row) and adds it to dB / dC of that slot's token,
+// t[slot]; a slot whose token is -1 (the walk's last, unpaired token) is
+// skipped.
 template <int TP>
-__device__ __forceinline__ void column_sum_add(const float *buf, int lane, float *dB, float *dC,
-                                               long long bcrow, int t)
+__device__ __forceinline__ void column_pair_sum_add(const float *buf, int lane, float *dB, float *dC,
+                                                    long long bcrow, int t0, int t1)
 {
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    const int slot = lane >> 4, c = 2 * (lane & 15);
+    const float *col = buf + slot * 32 + c;
+    f2 acc[4] = {pack2(0.f, 0.f), pack2(0.f, 0.f), pack2(0.f, 0.f), pack2(0.f, 0.f)};
 #pragma unroll
-    for (int l = 0; l < 32; ++l) c[l & 3] += buf[l * TP + lane];
-    float *dst = lane < 16 ? dB + bcrow + (long long)t * 16 + lane
-                           : dC + bcrow + (long long)t * 16 + (lane - 16);
-    atomicAdd(dst, (c[0] + c[1]) + (c[2] + c[3]));
+    for (int r = 0; r < 32; ++r) {
+        const float2 v = *reinterpret_cast<const float2 *>(col + r * TP);
+        acc[r & 3] = add2(acc[r & 3], pack2(v.x, v.y));
+    }
+    const float2 sum = unpack2(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])));
+    const int t = slot ? t1 : t0;
+    if (t >= 0) {
+        float *dst = c < 16 ? dB + bcrow + (long long)t * 16 + c : dC + bcrow + (long long)t * 16 + (c - 16);
+        atomicAdd(reinterpret_cast<float2 *>(dst), sum);
+    }
 }
 
 template <typename T, int DIRS>
@@ -402,6 +418,14 @@ grad_adjoint_kernel(const GradParams p)
 #pragma unroll
             for (int m = 0; m < 4; ++m) cp_async16(sg + Lay::sCK + 16 * (lane + 32 * m), src + 16 * (lane + 32 * m), 16u);
         }
+        if (DIRS == 3 && fin) {   // the partner's partials of the chunk's tokens: len * 24 blocks
+            const char *src = reinterpret_cast<const char *>(p.part + (grp * p.L + t0) * 96);
+#pragma unroll
+            for (int m = 0; m < (kTG * 24 + 31) / 32; ++m) {
+                const int jj = lane + 32 * m;
+                cp_async16_if(sg + Lay::sPT + 16 * jj, src + 16 * jj, jj < len * 24);
+            }
+        }
         cp_async_commit();
     };
 
@@ -472,6 +496,7 @@ grad_adjoint_kernel(const GradParams p)
             f2 hn[8];
 #pragma unroll
             for (int q = 0; q < 4; ++q) lds2(my_h + (len * 4 + q) * 128, hn[2 * q], hn[2 * q + 1]);
+            int t_prev = -1;                      // the previous token of the walk (its pair's slot 0)
 #pragma unroll 1
             for (int k = len - 1; k >= 0; --k) {
                 const int i = dir == 0 ? k : len - 1 - k;
@@ -481,13 +506,13 @@ grad_adjoint_kernel(const GradParams p)
                 const float xv = act ? ld_as_f32(rowv[1] + i) : 0.f;
                 const float zv = (act && hasZ) ? ld_as_f32(rowv[2] + i) : 0.f;
                 const float go = act ? ld_as_f32(rowv[3] + i) : 0.f;
-                // the partner's partials of this token (phase 1), loaded early
+                // the partner's partials of this token (phase 1), staged with the chunk
                 float px = 0.f, pdt = 0.f, pz = 0.f;
-                if (DIRS == 3 && fin && act) {
-                    const float *pp = p.part + ((grp * p.L + t) * 3) * 32 + lane;
-                    px = __ldcg(pp);
-                    pdt = __ldcg(pp + 32);
-                    pz = __ldcg(pp + 64);
+                if (DIRS == 3 && fin) {
+                    const float *pp = reinterpret_cast<const float *>(sg + Lay::sPT) + i * 96 + lane;
+                    px = pp[0];
+                    pdt = pp[32];
+                    pz = pp[64];
                 }
                 float g = 1.f, gp = 0.f;
                 if (hasZ) {
@@ -501,7 +526,8 @@ grad_adjoint_kernel(const GradParams p)
                 const f2 lmd = rs ? pack2(-INFINITY, -INFINITY) : pack2(0.f, 0.f);
                 const float *Bt = bc + i * 32;
                 f2 yk2 = pack2(0.f, 0.f), sB2 = pack2(0.f, 0.f), sw2 = pack2(0.f, 0.f);
-                float *trow = tr + lane * TP;
+                const int pslot = (len - 1 - k) & 1;     // slot of this token in its pair
+                float *trow = tr + lane * TP + pslot * 32;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     f2 B0, B1, C0, C1, hp0, hp1;
@@ -532,11 +558,15 @@ grad_adjoint_kernel(const GradParams p)
                 float gx = fmaf(ds, Dk, dt * sB);
                 float gdt = fmaf(xv, sB, sw);
                 float gz = go * gp * yk;
-                // dB, dC of the token: sum of column `lane` over the warp's
-                // channels (rows of idle lanes hold zeros)
-                __syncwarp();
-                column_sum_add<TP>(tr, lane, dBk, dCk, bcrow, t);
-                __syncwarp();                     // the buffer is written again at the next token
+                // dB, dC of the pair's tokens once both are written (or the
+                // chunk's last token): sums over the warp's channels (rows of
+                // idle lanes hold zeros)
+                if (pslot == 1 || k == 0) {
+                    __syncwarp();
+                    column_pair_sum_add<TP>(tr, lane, dBk, dCk, bcrow, pslot ? t_prev : t, pslot ? t : -1);
+                    __syncwarp();                 // the buffer is written again by the next pair
+                }
+                t_prev = t;
                 // per-token gradients of x, delta, z
                 if (!fin) {
                     float *pp = p.part + ((grp * p.L + t) * 3) * 32 + lane;

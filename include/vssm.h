@@ -309,7 +309,16 @@ int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len
  * directions (both directions only), channels rounded up to groups of 32.
  * When there are too few 32-channel groups to fill the GPU, the rows are cut
  * into token ranges for the adjoint, and 128 bytes per range, channel and
- * direction hold the ranges' adjoint summaries. */
+ * direction hold the ranges' adjoint summaries.
+ * With the step options or the convolution the directions run one after the
+ * other and share one direction's workspace of the above, after float32
+ * intermediates of 4 bytes per token and channel each, per direction run:
+ * the gradients of its step and input and, with z, its share of dz; with the
+ * convolution its input and the convolution's argument; with softplus or
+ * bfloat16 I/O its step (one for both directions when they share step and
+ * bias); with bfloat16 I/O and no convolution one input copy; with bfloat16
+ * I/O float32 copies of z, dout and (per distinct tensor) B and C. Arrays
+ * start on 256-byte boundaries. */
 int vssm_scan_grad_workspace_size(const vssm_scan_args *a, int seg_len, size_t *bytes);
 
 /*
