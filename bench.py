@@ -64,8 +64,9 @@ def parse_args(argv=None):
                    help="pass per-direction steps before softplus, with biases (the kernel "
                         "applies softplus(delta + bias))")
     p.add_argument("--grad", action="store_true",
-                   help="time a training step: the forward scan plus its gradient "
-                        "(vssm_scan_grad) for a seeded upstream gradient")
+                   help="time a training step: the training forward (vssm_scan_train, "
+                        "which also stores the state checkpoints) plus the gradient "
+                        "(vssm_scan_grad) from them, for a seeded upstream gradient")
     p.add_argument("--ncssd", action="store_true",
                    help="time the NC-SSD global-state variant (vssm_ncssd) on the workload's "
                         "shapes instead of the scan")
@@ -623,16 +624,19 @@ def run_ours(args):
 
     grad_calls = []
     if args.grad:
-        # the training step adds the gradient of sum(dout * out): seeded dout,
-        # outputs and workspace allocated once
-        if wl.fused_step or wl.conv:
-            raise SystemExit("--grad covers the scan with steps as given and no convolution")
+        # the training step: the training forward (vssm_scan_train, which also
+        # stores the state checkpoints) and the gradient of sum(dout * out)
+        # from them, for a seeded dout; outputs, checkpoints and workspace
+        # allocated once
         gen = torch.Generator(device=dev)
         gen.manual_seed(1234 + rank)
         dout = torch.randn(base["x"].shape, device=dev, generator=gen).to(base["x"].dtype)
         gws = None
-        for s_, a in zip(sets, argsets):
+        ckpt_bytes = vssm.ckpt_size(argsets[0])
+        ckpts = [torch.empty(ckpt_bytes // 4, dtype=torch.float32, device=dev) for _ in range(nsets)]
+        for s_, a, ck in zip(sets, argsets, ckpts):
             batch, dim, L = s_["x"].shape
+            K = wl.conv
             f32 = dict(dtype=torch.float32, device=dev)
             outs_g = dict(dx=torch.empty_like(s_["x"]), ddelta=torch.empty_like(s_["x"]),
                           dz=torch.empty_like(s_["x"]), dB=torch.empty(batch, L, 16, **f32),
@@ -640,25 +644,36 @@ def run_ours(args):
                           dA_fwd=torch.empty(dim, 16, **f32) if wl.dirs & 1 else None,
                           dA_bwd=torch.empty(dim, 16, **f32) if wl.dirs & 2 else None,
                           dD_fwd=torch.empty(dim, **f32) if wl.dirs & 1 else None,
-                          dD_bwd=torch.empty(dim, **f32) if wl.dirs & 2 else None)
+                          dD_bwd=torch.empty(dim, **f32) if wl.dirs & 2 else None,
+                          ddelta_bwd=torch.empty_like(s_["x"]) if wl.fused_step else None,
+                          ddelta_bias=torch.empty(dim, **f32) if wl.fused_step else None,
+                          ddelta_bias_bwd=torch.empty(dim, **f32) if wl.fused_step else None,
+                          dconv_w=torch.empty(dim, K, **f32) if K else None,
+                          dconv_b=torch.empty(dim, **f32) if K else None,
+                          dconv_w_bwd=torch.empty(dim, K, **f32) if K else None,
+                          dconv_b_bwd=torch.empty(dim, **f32) if K else None)
             g = vssm.GradArgs()
             g.dout = dout.data_ptr()
             for k, v in outs_g.items():
                 setattr(g, k, v.data_ptr() if v is not None else None)
+            g.ckpt, g.ckpt_bytes = ck.data_ptr(), ckpt_bytes
             ga = vssm.ScanArgs.from_buffer_copy(a)
             need = vssm.grad_workspace_size(ga, seg)
             if gws is None:
                 gws = torch.empty(need, dtype=torch.uint8, device=dev)
             ga.workspace, ga.workspace_bytes = gws.data_ptr(), need
-            grad_calls.append((ga, g, outs_g))
-        launches += 8   # six zero-fills, the checkpoint pass and the adjoint
+            grad_calls.append((ga, g, outs_g, ck))
+        launches += vssm.grad_plan(grad_calls[0][0], grad_calls[0][1], seg)[1]
 
     def launch(i):
         a = ctypes.byref(argsets[i % nsets])
-        st = fn(a, seg, sptr) if seg else fn(a, sptr)
-        if st == 0 and grad_calls:
-            ga, g, _ = grad_calls[i % nsets]
-            st = vssm.lib.vssm_scan_grad(ctypes.byref(ga), ctypes.byref(g), seg, sptr)
+        if grad_calls:
+            ga, g, _, ck = grad_calls[i % nsets]
+            st = vssm.lib.vssm_scan_train(a, seg, ctypes.c_void_p(ck.data_ptr()), ck.numel() * 4, sptr)
+            if st == 0:
+                st = vssm.lib.vssm_scan_grad(ctypes.byref(ga), ctypes.byref(g), seg, sptr)
+        else:
+            st = fn(a, seg, sptr) if seg else fn(a, sptr)
         if st != 0:
             raise RuntimeError(vssm.lib.vssm_last_error().decode())
 

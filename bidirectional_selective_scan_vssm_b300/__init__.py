@@ -34,7 +34,8 @@ EXPORTS = ["vssm_scan_bidir", "vssm_scan_bidir_noalloc", "vssm_scan_folded",
            "vssm_scan_chunked", "vssm_scan_workspace_size", "vssm_scan_chunked_workspace_size",
            "vssm_scan_plan_query", "vssm_scan_grad", "vssm_scan_grad_workspace_size",
            "vssm_selftest_wait_timeout", "vssm_scan_host", "vssm_scan_host_workspace_size",
-           "vssm_ncssd", "vssm_ncssd_workspace_size",
+           "vssm_ncssd", "vssm_ncssd_workspace_size", "vssm_scan_train", "vssm_scan_ckpt_size",
+           "vssm_scan_grad_plan_query",
            "vssm_device_error", "vssm_status_string", "vssm_last_error", "vssm_version"]
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -63,7 +64,7 @@ class GradArgs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "dout", "dx", "ddelta", "dz", "dB", "dC", "dB_bwd", "dC_bwd", "dA_fwd", "dA_bwd",
         "dD_fwd", "dD_bwd", "ddelta_bwd", "ddelta_bias", "ddelta_bias_bwd", "dconv_w", "dconv_b",
-        "dconv_w_bwd", "dconv_b_bwd")]
+        "dconv_w_bwd", "dconv_b_bwd", "ckpt")] + [("ckpt_bytes", ctypes.c_size_t)]
 
 
 class NcssdArgs(ctypes.Structure):
@@ -109,6 +110,13 @@ def _load():
     lib.vssm_scan_plan_query.restype = ctypes.c_int
     lib.vssm_scan_grad.argtypes = [P, ctypes.POINTER(GradArgs), ctypes.c_int, ctypes.c_void_p]
     lib.vssm_scan_grad.restype = ctypes.c_int
+    lib.vssm_scan_train.argtypes = [P, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.vssm_scan_train.restype = ctypes.c_int
+    lib.vssm_scan_ckpt_size.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
+    lib.vssm_scan_ckpt_size.restype = ctypes.c_int
+    lib.vssm_scan_grad_plan_query.argtypes = [P, ctypes.POINTER(GradArgs), ctypes.c_int,
+                                              ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
+    lib.vssm_scan_grad_plan_query.restype = ctypes.c_int
     lib.vssm_scan_host.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
     lib.vssm_scan_host.restype = ctypes.c_int
     lib.vssm_scan_host_workspace_size.argtypes = [P, ctypes.c_int, ctypes.c_int,
@@ -238,6 +246,15 @@ def plan(a: ScanArgs, seg_len: int = 0, pieces: int = 0):
     return int(r.value), int(n.value)
 
 
+def grad_plan(a: ScanArgs, g: GradArgs, seg_len: int = 0):
+    """(adjoint token ranges per row, kernel launches) of the gradient call
+    (``vssm_scan_grad_plan_query``)."""
+    r, n = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib.vssm_scan_grad_plan_query(ctypes.byref(a), ctypes.byref(g), seg_len, ctypes.byref(r),
+                                         ctypes.byref(n)))
+    return int(r.value), int(n.value)
+
+
 _ws_cache = {}
 
 
@@ -314,6 +331,39 @@ def scan_folded(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *,
     return out
 
 
+def ckpt_size(a: ScanArgs) -> int:
+    """Bytes of the checkpoints ``vssm_scan_train`` stores for this call."""
+    n = ctypes.c_size_t(0)
+    _check(lib.vssm_scan_ckpt_size(ctypes.byref(a), ctypes.byref(n)))
+    return int(n.value)
+
+
+def scan_train(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *,
+               seg_len: int = 0, dirs: int = DIR_BOTH, out=None, ckpt=None, B_bwd=None, C_bwd=None,
+               stream: Optional[torch.cuda.Stream] = None, workspace=None, **step):
+    """``vssm_scan_train``: the forward scan (folded with ``seg_len`` > 0)
+    that also stores the gradient's state checkpoints. Returns (out, ckpt);
+    pass ckpt to :func:`scan_grad` for the same arguments. ``ckpt`` (float32,
+    at least ``ckpt_size`` bytes) is allocated here when not given."""
+    if out is None:
+        out = torch.empty_like(x)
+    a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, out, B_bwd, C_bwd, dirs, **step)
+    n = ckpt_size(a)
+    if ckpt is None:
+        ckpt = torch.empty(max(1, n // 4), dtype=torch.float32, device=x.device)
+    _dev_tensor("ckpt", ckpt, torch.float32, None, x.device)
+    stream = stream if stream is not None else torch.cuda.current_stream(x.device)
+    need = workspace_size(a, seg_len)
+    if workspace is None:
+        workspace = _workspace(x.device, stream, need)
+    if workspace is not None:
+        a.workspace = workspace.data_ptr()
+        a.workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.vssm_scan_train(ctypes.byref(a), int(seg_len), ctypes.c_void_p(ckpt.data_ptr()),
+                               ckpt.numel() * 4, ctypes.c_void_p(stream.cuda_stream)))
+    return out, ckpt
+
+
 def scan_chunked(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *,
                  pieces: int, seg_len: int = 0, dirs: int = DIR_BOTH, out=None, B_bwd=None,
                  C_bwd=None, stream: Optional[torch.cuda.Stream] = None,
@@ -336,7 +386,7 @@ def grad_workspace_size(a: ScanArgs, seg_len: int = 0) -> int:
 
 def scan_grad(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *, dout,
               dirs: int = DIR_BOTH, seg_len: int = 0, B_bwd=None, C_bwd=None,
-              stream: Optional[torch.cuda.Stream] = None, workspace=None, **step) -> dict:
+              stream: Optional[torch.cuda.Stream] = None, workspace=None, ckpt=None, **step) -> dict:
     """``vssm_scan_grad``: gradients of sum(dout * out) for the forward call
     with these arguments (``seg_len`` > 0: the folded scan; ``step``: the step
     options and the convolution of :func:`make_args`). Returns a dict with dx,
@@ -344,8 +394,9 @@ def scan_grad(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *, d
     (None when shared), dA_fwd, dA_bwd, dD_fwd, dD_bwd (None for a direction
     that is not run); with the options also ddelta_bwd (x's dtype),
     ddelta_bias, ddelta_bias_bwd, dconv_w, dconv_b, dconv_w_bwd, dconv_b_bwd
-    (float32), each None unless the matching input is given. Output tensors
-    are allocated here."""
+    (float32), each None unless the matching input is given. ``ckpt``: the
+    checkpoints :func:`scan_train` stored for the same arguments (None: the
+    gradient recomputes them). Output tensors are allocated here."""
     a = make_args(x, delta, A_fwd, A_bwd, B, C, D_fwd, D_bwd, z, None, B_bwd, C_bwd, dirs, **step)
     _dev_tensor("dout", dout, x.dtype, x.shape, x.device)
     batch, dim, L = x.shape
@@ -378,6 +429,9 @@ def scan_grad(x, delta, A_fwd, A_bwd, B, C, D_fwd=None, D_bwd=None, z=None, *, d
     g.dout = dout.data_ptr()
     for k, v in out.items():
         setattr(g, k, _ptr(v))
+    if ckpt is not None:
+        _dev_tensor("ckpt", ckpt, torch.float32, None, x.device)
+        g.ckpt, g.ckpt_bytes = ckpt.data_ptr(), ckpt.numel() * 4
     stream = stream if stream is not None else torch.cuda.current_stream(x.device)
     need = grad_workspace_size(a, seg_len)
     if workspace is None:

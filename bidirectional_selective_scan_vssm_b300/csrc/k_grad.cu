@@ -33,13 +33,15 @@ __global__ void zero_f32_kernel(float *p, long long n)
 
 
 template <typename T, int DIRS>
-cudaError_t launch_dirs(const GradParams &p, long long ngroups, int nrange, cudaStream_t s)
+cudaError_t launch_dirs(const GradParams &p, long long ngroups, int nrange, bool have_ckpt, cudaStream_t s)
 {
     constexpr int NDIR = DIRS == 3 ? 2 : 1;
     const long long units = (long long)NDIR * ngroups;
-    grad_ckpt_kernel<T, DIRS><<<(unsigned)((units + 3) / 4), 128, 0, s>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    if (!have_ckpt) {     // (else the training forward stored them)
+        grad_ckpt_kernel<T, DIRS><<<(unsigned)((units + 3) / 4), 128, 0, s>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     if (nrange > 1) {
         const long long su = units * nrange;
         grad_adj_summary_kernel<T, DIRS><<<(unsigned)((su + 3) / 4), 128, 0, s>>>(p);
@@ -54,21 +56,23 @@ cudaError_t launch_dirs(const GradParams &p, long long ngroups, int nrange, cuda
 }
 
 template <typename T>
-cudaError_t launch_typed(const GradParams &p, int dirs, long long ngroups, int nrange, cudaStream_t s)
+cudaError_t launch_typed(const GradParams &p, int dirs, long long ngroups, int nrange, bool have_ckpt,
+                         cudaStream_t s)
 {
     switch (dirs) {
-    case 1: return launch_dirs<T, 1>(p, ngroups, nrange, s);
-    case 2: return launch_dirs<T, 2>(p, ngroups, nrange, s);
-    default: return launch_dirs<T, 3>(p, ngroups, nrange, s);
+    case 1: return launch_dirs<T, 1>(p, ngroups, nrange, have_ckpt, s);
+    case 2: return launch_dirs<T, 2>(p, ngroups, nrange, have_ckpt, s);
+    default: return launch_dirs<T, 3>(p, ngroups, nrange, have_ckpt, s);
     }
 }
 
 }  // namespace
 
-cudaError_t launch_grad(const GradParams &p, int dirs, bool f32, long long ngroups, int nrange, cudaStream_t s)
+cudaError_t launch_grad(const GradParams &p, int dirs, bool f32, long long ngroups, int nrange, bool have_ckpt,
+                        cudaStream_t s)
 {
-    return f32 ? launch_typed<float>(p, dirs, ngroups, nrange, s)
-               : launch_typed<__nv_bfloat16>(p, dirs, ngroups, nrange, s);
+    return f32 ? launch_typed<float>(p, dirs, ngroups, nrange, have_ckpt, s)
+               : launch_typed<__nv_bfloat16>(p, dirs, ngroups, nrange, have_ckpt, s);
 }
 
 cudaError_t launch_zero_f32(float *p, size_t n, cudaStream_t s)

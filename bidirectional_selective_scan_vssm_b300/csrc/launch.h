@@ -29,8 +29,9 @@ constexpr int kCarryW = VSSM_CARRY_WARPS;
 cudaError_t launch_general(const ScanParams &p, int dirs, bool ysmem, bool f32, long long ctas,
                            cudaStream_t s);
 
-// Gradient: checkpoints, optional adjoint summaries (nrange > 1), adjoint.
-cudaError_t launch_grad(const GradParams &p, int dirs, bool f32, long long ngroups, int nrange,
+// Gradient: checkpoints (unless have_ckpt: stored by the training forward),
+// optional adjoint summaries (nrange > 1), adjoint.
+cudaError_t launch_grad(const GradParams &p, int dirs, bool f32, long long ngroups, int nrange, bool have_ckpt,
                         cudaStream_t s);
 cudaError_t launch_zero_f32(float *p, size_t n, cudaStream_t s);
 // Gradient with the step options and the convolution: the float32 inputs of

@@ -66,6 +66,10 @@ struct WarpScanParams {
     float *ybuf;                 // [ngroups][piece_len][RPW] floats (both directions only)
     int discard_y;               // ybuf is 128-byte aligned: its rows are dropped from L2 once read
     float *summ;                 // carry summaries [slot][srows][pieces][kSummFloats], or null
+    float *ckpt;                 // training forward: [slot][srows][nch][16][32], the state
+                                 // entering every 4-token chunk in each direction's scan
+                                 // order (the gradient's checkpoints), or null
+    int nch;                     // 4-token chunks per row (ckpt)
                                  // when every piece starts from a zero state
     unsigned *err;               // device error word
     long long total;             // batch * dim * L elements
@@ -140,6 +144,7 @@ struct WarpScan {
     long long lane_erow;         // element index of (b, d0+r, 0)
     const char *rowp[3];         // this lane's row (b, d0+r, 0) of delta, x, z
     T *out_row0;                 // output row (b, d0, 0)
+    float *ck_row;               // this warp's checkpoint row (b, d0 .. d0+31, slot), or null
 
     __device__ WarpScan(const WarpScanParams &p_) : p(p_) {}
 
@@ -170,6 +175,8 @@ struct WarpScan {
         rowp[1] = static_cast<const char *>(p.x) + lane_erow * ES;
         rowp[2] = p.z ? static_cast<const char *>(p.z) + lane_erow * ES : rowp[1];
         out_row0 = static_cast<T *>(p.out) + e0;
+        ck_row = p.ckpt ? p.ckpt + (((long long)slot * p.srows + (long long)b * p.rgroups + rg) * p.nch) * 512 + lane
+                        : nullptr;
     }
 
     __device__ __forceinline__ unsigned char *stage(int s) const { return wsm + s * Lay::kStageBytes; }
@@ -275,7 +282,10 @@ struct WarpScan {
     // SEG: folded sequence (segment-start decay forced to 0). Tokens past len
     // up to the unroll multiple read delta = x = 0 (zero_tail), which leaves
     // h unchanged.
-    template <int DIR, bool FIN, bool SEG, bool GATE>
+    // CK: store the state entering every 4-token chunk of the row, in this
+    // direction's scan order, before the chunk's first token in that order
+    // (the gradient's checkpoints; G == 1).
+    template <int DIR, bool FIN, bool SEG, bool GATE, bool CK>
     __device__ __forceinline__ void scan_chunk(f2 (&h)[NS / 2], const f2 (&Ap)[NS / 2], float Dsum,
                                                float (&xh)[3], int s, int c0, int len,
                                                uint32_t rmask)
@@ -295,6 +305,23 @@ struct WarpScan {
 #pragma unroll
             for (int j = 0; j < kUnroll; ++j) {
                 const int i = (DIR == 0) ? (k0 + j) : (n4 - 1 - k0 - j);
+                if (CK) {
+                    static_assert(!CK || G == 1, "checkpoints hold one channel per lane");
+                    const int t = c0 + i;
+                    const bool first = DIR == 0 ? (t & 3) == 0 : ((t & 3) == 3 || t == p.L - 1);
+                    if (i < len && first) {
+                        // (lanes past the last channel hold zeros: their staged
+                        // rows are not copied, so their states are undefined)
+                        const bool act = d0 + r < p.dim;
+                        float *dst = ck_row + (long long)(t >> 2) * 512;
+#pragma unroll
+                        for (int q = 0; q < NS / 2; ++q) {
+                            const float2 v = unpack2(h[q]);
+                            dst[(2 * q) * 32] = act ? v.x : 0.f;
+                            dst[(2 * q + 1) * 32] = act ? v.y : 0.f;
+                        }
+                    }
+                }
                 float dtv = ld_as_f32(rd + i);
                 if (SP) dtv = softplus_f32(dtv + dbias_l);
                 const float xv = conv_input<SEG>(ld_as_f32(rx + i), xh, i, len, rmask);
@@ -385,13 +412,33 @@ struct WarpScan {
         }
     }
 
-    template <bool FIN, bool SEG, bool GATE>
-    __device__ __forceinline__ void scan_dispatch(f2 (&h)[NS / 2], const f2 (&Ap)[NS / 2], float Dsum,
-                                                  float (&xh)[3], int s, int c0, int len,
-                                                  uint32_t rmask)
+    template <bool FIN, bool SEG, bool GATE, bool CK>
+    __device__ __forceinline__ void scan_dir(f2 (&h)[NS / 2], const f2 (&Ap)[NS / 2], float Dsum,
+                                             float (&xh)[3], int s, int c0, int len, uint32_t rmask)
     {
-        if (dir == 0) scan_chunk<0, FIN, SEG, GATE>(h, Ap, Dsum, xh, s, c0, len, rmask);
-        else scan_chunk<1, FIN, SEG, GATE>(h, Ap, Dsum, xh, s, c0, len, rmask);
+        if (dir == 0) scan_chunk<0, FIN, SEG, GATE, CK>(h, Ap, Dsum, xh, s, c0, len, rmask);
+        else scan_chunk<1, FIN, SEG, GATE, CK>(h, Ap, Dsum, xh, s, c0, len, rmask);
+    }
+
+    // The scan_chunk instance for this chunk: last phase or not, folded,
+    // gate, checkpoints (the gate only matters in the last phase).
+    __device__ __forceinline__ void scan_dispatch(bool fin, bool seg, bool gate, bool ck, f2 (&h)[NS / 2],
+                                                  const f2 (&Ap)[NS / 2], float Dsum, float (&xh)[3], int s,
+                                                  int c0, int len, uint32_t rmask)
+    {
+#define VSSM_SCAN_CASE(F, S, Z)                                                          \
+        if (ck) scan_dir<F, S, Z, (G == 1)>(h, Ap, Dsum, xh, s, c0, len, rmask);        \
+        else scan_dir<F, S, Z, false>(h, Ap, Dsum, xh, s, c0, len, rmask);
+        if (fin) {
+            if (seg) {
+                if (gate) { VSSM_SCAN_CASE(true, true, true) } else { VSSM_SCAN_CASE(true, true, false) }
+            } else {
+                if (gate) { VSSM_SCAN_CASE(true, false, true) } else { VSSM_SCAN_CASE(true, false, false) }
+            }
+        } else {
+            if (seg) { VSSM_SCAN_CASE(false, true, false) } else { VSSM_SCAN_CASE(false, false, false) }
+        }
+#undef VSSM_SCAN_CASE
     }
 
     // History of the convolution at the first token t0 this warp visits in
@@ -617,6 +664,7 @@ struct WarpScan {
         }
         const bool hasZ = p.z != nullptr;
         const bool seg = p.seg_len > 0;
+        const bool ck = ck_row != nullptr;
 
         const int Lv = tb - ta;
         const int H = (DIRS == 3) ? (Lv + 1) / 2 : Lv;
@@ -660,19 +708,8 @@ struct WarpScan {
                 zero_tail(s, c0, len);
                 widen_bc(s, len);
                 const uint32_t rmask = reset_mask(c0, len);
-                if (fin) {
-                    if (seg) {
-                        if (hasZ) scan_dispatch<true, true, true>(h, Ap, Dsum, xh, s, c0, len, rmask);
-                        else scan_dispatch<true, true, false>(h, Ap, Dsum, xh, s, c0, len, rmask);
-                    } else {
-                        if (hasZ) scan_dispatch<true, false, true>(h, Ap, Dsum, xh, s, c0, len, rmask);
-                        else scan_dispatch<true, false, false>(h, Ap, Dsum, xh, s, c0, len, rmask);
-                    }
-                    store_out(c0, c1);
-                } else {
-                    if (seg) scan_dispatch<false, true, false>(h, Ap, Dsum, xh, s, c0, len, rmask);
-                    else scan_dispatch<false, false, false>(h, Ap, Dsum, xh, s, c0, len, rmask);
-                }
+                scan_dispatch(fin, seg, hasZ, ck, h, Ap, Dsum, xh, s, c0, len, rmask);
+                if (fin) store_out(c0, c1);
                 if (k + kStages < nk) {
                     int n0, n1;
                     chunk_range(k + kStages, lo, hi, n0, n1);

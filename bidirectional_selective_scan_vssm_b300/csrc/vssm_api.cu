@@ -416,10 +416,39 @@ void *noalloc_scratch()
     return addr[dev];
 }
 
-int run(const vssm_scan_args *a, int seg_len, bool folded, int pieces_req, void *stream)
+// Bytes of the gradient's state checkpoints for this call: 16 fp32 per
+// 4-token chunk, channel (in groups of 32) and direction.
+size_t ckpt_bytes(const vssm_scan_args *a)
+{
+    const size_t ndir = a->dir_flags == 3 ? 2 : 1;
+    const size_t rgroups = ((size_t)a->dim + 31) / 32, nch = ((size_t)a->seqlen + 3) / 4;
+    return ndir * (size_t)a->batch * rgroups * nch * 512 * sizeof(float);
+}
+
+// ckpt: the training forward also stores the gradient's checkpoints there
+// (dstate 16 only).
+int run(const vssm_scan_args *a, int seg_len, bool folded, int pieces_req, void *stream,
+        float *ckpt = nullptr, size_t ckpt_size = 0)
 {
     int st = validate(a, seg_len, folded);
     if (st != VSSM_OK) return st;
+    if (ckpt) {
+        if (a->dstate != vssm::kMaxState)
+            return fail(VSSM_ERR_UNSUPPORTED, "checkpoints need dstate %d (got %d)", vssm::kMaxState, a->dstate);
+        if (!aligned16(ckpt)) return fail(VSSM_ERR_MISALIGNED, "ckpt is not 16-byte aligned");
+        const size_t need = ckpt_bytes(a);
+        if (ckpt_size < need)
+            return fail(VSSM_ERR_INVALID_ARG, "ckpt of %zu bytes required, %zu given", need, ckpt_size);
+        const size_t es = a->dtype == VSSM_F32 ? 4 : 2;
+        const size_t nact = (size_t)a->batch * a->dim * a->seqlen * es;
+        const size_t nbc = (size_t)a->batch * a->seqlen * a->dstate * es;
+        const void *bufs[] = {a->x, a->delta, a->z, a->out, a->delta_bwd, a->B, a->C, a->B_bwd, a->C_bwd,
+                              a->workspace};
+        const size_t sz[] = {nact, nact, nact, nact, nact, nbc, nbc, nbc, nbc, a->workspace_bytes};
+        for (size_t i = 0; i < sizeof(bufs) / sizeof(bufs[0]); ++i)
+            if (overlaps(ckpt, need, bufs[i], sz[i]))
+                return fail(VSSM_ERR_INVALID_ARG, "ckpt overlaps an input, the output or the workspace");
+    }
     if (pieces_req < 0) return fail(VSSM_ERR_INVALID_ARG, "pieces=%d must be >= 0", pieces_req);
     if (pieces_req > 1 && a->dstate != vssm::kMaxState)
         return fail(VSSM_ERR_UNSUPPORTED, "pieces joined by the carry need dstate %d (got %d)",
@@ -472,6 +501,8 @@ int run(const vssm_scan_args *a, int seg_len, bool folded, int pieces_req, void 
         w.rgroups = pl.rgroups;
         w.ngroups = pl.ngroups;
         w.srows = pl.srows;
+        w.ckpt = ckpt;
+        w.nch = (a->seqlen + 3) / 4;
         const cudaError_t e = vssm::launch_warp(w, pl.dirs, a->dtype == VSSM_F32, pl.carry,
                                                 a->delta_softplus != 0, a->conv_k > 0, pl.ctas,
                                                 pl.summ_ctas, s);
@@ -959,12 +990,14 @@ cudaError_t grad_composed_launch(const vssm_scan_args *a, const vssm_grad_args *
         p.dA[1] = g->dA_bwd;
         p.dD[0] = g->dD_fwd;
         p.dD[1] = g->dD_bwd;
-        p.ckpt = at(w.core);
+        p.ckpt = g->ckpt ? const_cast<float *>(g->ckpt) + (dirs == 3 ? (size_t)k : 0) * (size_t)w.gl.ngroups *
+                                                         w.gl.nch * 512
+                         : at(w.core);
         p.part = nullptr;
         p.summ = w.gl.nrange > 1 ? reinterpret_cast<float *>(ws + w.core + w.gl.summ_off) : nullptr;
         p.err = err;
         grad_fill_sizes(p, a, w.gl, seg_len);
-        e = vssm::launch_grad(p, 1 << k, true, w.gl.ngroups, w.gl.nrange, s);
+        e = vssm::launch_grad(p, 1 << k, true, w.gl.ngroups, w.gl.nrange, g->ckpt != nullptr, s);
     }
     if (e == cudaSuccess) e = vssm::launch_grad_ext_post(q, f32, s);
     return e;
@@ -1023,6 +1056,23 @@ int vssm_scan_plan_query(const vssm_scan_args *a, int seg_len, int pieces, int *
 }
 
 int vssm_scan_bidir(const vssm_scan_args *a, void *stream) { return run(a, 0, false, 0, stream); }
+
+int vssm_scan_ckpt_size(const vssm_scan_args *a, size_t *bytes)
+{
+    if (!a || !bytes) return fail(VSSM_ERR_INVALID_ARG, "args or bytes is NULL");
+    if (a->batch < 0 || a->dim < 0 || a->seqlen < 0 || a->dir_flags < 1 || a->dir_flags > 3)
+        return fail(VSSM_ERR_INVALID_ARG, "invalid sizes or dir_flags");
+    *bytes = ckpt_bytes(a);
+    return VSSM_OK;
+}
+
+int vssm_scan_train(const vssm_scan_args *a, int seg_len, float *ckpt, size_t ckpt_size, void *stream)
+{
+    if (seg_len < 0) return fail(VSSM_ERR_INVALID_ARG, "seg_len=%d must be >= 0", seg_len);
+    if (!ckpt && a && (long long)a->batch * a->dim * a->seqlen > 0)
+        return fail(VSSM_ERR_INVALID_ARG, "ckpt is NULL");
+    return run(a, seg_len, seg_len > 0, 0, stream, ckpt, ckpt_size);
+}
 
 int vssm_scan_host_workspace_size(const vssm_scan_args *a, int seg_len, int slices, size_t *bytes)
 {
@@ -1169,6 +1219,11 @@ int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len
                         g->ddelta_bias_bwd, g->dconv_w, g->dconv_b, g->dconv_w_bwd, g->dconv_b_bwd};
     for (const void *q : gp)
         if (q && !aligned16(q)) return fail(VSSM_ERR_MISALIGNED, "gradient pointer %p is not 16-byte aligned", q);
+    if (g->ckpt) {
+        if (!aligned16(g->ckpt)) return fail(VSSM_ERR_MISALIGNED, "ckpt is not 16-byte aligned");
+        if (g->ckpt_bytes < ckpt_bytes(a))
+            return fail(VSSM_ERR_INVALID_ARG, "ckpt of %zu bytes required, %zu given", ckpt_bytes(a), g->ckpt_bytes);
+    }
     const bool composed = grad_composed(a);
     const GradPlan gl = composed ? grad_ext_layout(a).gl : make_grad_plan(a);
     const size_t need = grad_workspace(a);
@@ -1189,9 +1244,10 @@ int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len
         {g->dconv_b_bwd, nd}};
     const void *ins[] = {a->x, a->delta, a->z, a->B, a->C, a->B_bwd, a->C_bwd, a->A_fwd, a->A_bwd,
                          a->D_fwd, a->D_bwd, g->dout, a->delta_bwd, a->delta_bias, a->delta_bias_bwd,
-                         a->conv_w, a->conv_b, a->conv_w_bwd, a->conv_b_bwd};
+                         a->conv_w, a->conv_b, a->conv_w_bwd, a->conv_b_bwd, g->ckpt};
     const size_t insz[] = {nact, nact, nact, nbc / 4 * es, nbc / 4 * es, nbc / 4 * es, nbc / 4 * es,
-                           npar, npar, nd, nd, nact, nact, nd, nd, ncw, nd, ncw, nd};
+                           npar, npar, nd, nd, nact, nact, nd, nd, ncw, nd, ncw, nd,
+                           g->ckpt ? ckpt_bytes(a) : 0};
     for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
         if (!outs[i].p) continue;
         if (overlaps(outs[i].p, outs[i].n, a->workspace, a->workspace_bytes))
@@ -1246,16 +1302,58 @@ int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len
         p.dA[1] = g->dA_bwd;
         p.dD[0] = g->dD_fwd;
         p.dD[1] = g->dD_bwd;
-        p.ckpt = static_cast<float *>(a->workspace);
+        p.ckpt = g->ckpt ? const_cast<float *>(g->ckpt) : static_cast<float *>(a->workspace);
         p.part = dirs == 3 ? reinterpret_cast<float *>(static_cast<char *>(a->workspace) + gl.part_off)
                            : nullptr;
         p.summ = gl.nrange > 1 ? reinterpret_cast<float *>(static_cast<char *>(a->workspace) + gl.summ_off)
                                : nullptr;
         p.err = err;
         grad_fill_sizes(p, a, gl, seg_len);
-        e = vssm::launch_grad(p, (int)dirs, a->dtype == VSSM_F32, gl.ngroups, gl.nrange, s);
+        e = vssm::launch_grad(p, (int)dirs, a->dtype == VSSM_F32, gl.ngroups, gl.nrange, g->ckpt != nullptr, s);
     }
     return e == cudaSuccess ? VSSM_OK : cuda_fail(e, "launch");
+}
+
+int vssm_scan_grad_plan_query(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len,
+                              int *ranges_per_row, int *launches)
+{
+    if (!a || !g || !ranges_per_row || !launches) return fail(VSSM_ERR_INVALID_ARG, "NULL argument");
+    if (a->batch < 0 || a->dim < 0 || a->seqlen < 0 || a->dir_flags < 1 || a->dir_flags > 3 ||
+        seg_len < 0 || a->conv_k < 0 || a->conv_k > vssm::kMaxConv)
+        return fail(VSSM_ERR_INVALID_ARG, "invalid sizes, dir_flags or conv_k");
+    if (a->dstate != vssm::kMaxState)
+        return fail(VSSM_ERR_UNSUPPORTED, "the gradient needs dstate %d (got %d)", vssm::kMaxState, a->dstate);
+    *ranges_per_row = 0;
+    *launches = 0;
+    if ((long long)a->batch * a->dim * a->seqlen == 0) return VSSM_OK;
+    const unsigned dirs = a->dir_flags;
+    // zero-fills of the accumulated outputs (as vssm_scan_grad)
+    const void *zs[] = {g->dB, g->dC, g->dB_bwd, g->dC_bwd, (dirs & 1) ? g->dA_fwd : nullptr,
+                        (dirs & 1) ? g->dD_fwd : nullptr, (dirs & 2) ? g->dA_bwd : nullptr,
+                        (dirs & 2) ? g->dD_bwd : nullptr, g->ddelta_bias, g->ddelta_bias_bwd,
+                        g->dconv_w, g->dconv_b, g->dconv_w_bwd, g->dconv_b_bwd};
+    int n = 0;
+    for (const void *z : zs) n += z != nullptr;
+    const int per_dir_extra = g->ckpt ? 0 : 1;   // the checkpoint pass
+    if (grad_composed(a)) {
+        const GradExtLayout w = grad_ext_layout(a);
+        n += 2;                                  // prep, post
+        for (int k = 0; k < 2; ++k) {
+            if (!(dirs & (1u << k))) continue;
+            if (w.B32[k] != GradExtLayout::kNone) {
+                n += (k == 0 || !(dirs & 1) || w.B32[1] != w.B32[0]) ? 1 : 0;
+                n += (k == 0 || !(dirs & 1) || w.C32[1] != w.C32[0]) ? 1 : 0;
+            }
+            n += per_dir_extra + (w.gl.nrange > 1 ? 1 : 0) + 1;
+        }
+        *ranges_per_row = w.gl.nrange;
+    } else {
+        const GradPlan gl = make_grad_plan(a);
+        n += per_dir_extra + (gl.nrange > 1 ? 1 : 0) + 1;
+        *ranges_per_row = gl.nrange;
+    }
+    *launches = n;
+    return VSSM_OK;
 }
 
 int vssm_scan_chunked(const vssm_scan_args *a, int seg_len, int pieces, void *stream)

@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define VSSM_VERSION 170 /* 1.7.0 */
+#define VSSM_VERSION 180 /* 1.8.0 */
 
 typedef enum {
     VSSM_OK = 0,
@@ -267,6 +267,10 @@ typedef struct {
     float *dconv_w_bwd, *dconv_b_bwd;  /* iff conv_w_bwd / conv_b_bwd (else the
                                           backward taps' gradients are added
                                           to dconv_w / dconv_b)               */
+    /* State checkpoints stored by vssm_scan_train for this same forward call
+     * (NULL = recompute them: one more pass over the inputs). Read only. */
+    const float *ckpt;
+    size_t ckpt_bytes;       /* bytes available at ckpt (>= vssm_scan_ckpt_size) */
 } vssm_grad_args;
 
 /*
@@ -320,6 +324,43 @@ int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len
  * I/O float32 copies of z, dout and (per distinct tensor) B and C. Arrays
  * start on 256-byte boundaries. */
 int vssm_scan_grad_workspace_size(const vssm_scan_args *a, int seg_len, size_t *bytes);
+
+/*
+ * Training forward: the scan of vssm_scan_bidir (seg_len == 0) or
+ * vssm_scan_folded (seg_len >= 1), with the same output, that also stores
+ * the states vssm_scan_grad needs as checkpoints: per direction run, channel
+ * and 4-token chunk of the row, the state h (16 fp32) entering the chunk in
+ * that direction's scan order (VSSD page §4.2.1.3: the recurrence the
+ * gradient walks back through), zero when the chunk's first token in that
+ * order starts a folded segment (the recurrence restarts there). Layout [direction slot][batch][channel group
+ * of 32][chunk][16][32] fp32 (slot 0 = forward, 1 = backward when both run;
+ * slot 0 alone for one direction). Passing the buffer to vssm_scan_grad
+ * (vssm_grad_args.ckpt) saves the gradient its checkpoint pass, a full
+ * recurrence over the inputs, for 64 bytes per 4 tokens, channel and
+ * direction written here. ckpt is caller-owned device memory of at least
+ * vssm_scan_ckpt_size bytes, 16-byte aligned, overlapping no other tensor
+ * of the call. dstate must be 16 (else VSSM_ERR_UNSUPPORTED); other errors
+ * as the plain calls, VSSM_ERR_INVALID_ARG for a NULL or short ckpt.
+ */
+int vssm_scan_train(const vssm_scan_args *a, int seg_len, float *ckpt, size_t ckpt_bytes, void *stream);
+
+/*
+ * How vssm_scan_grad(a, g, seg_len, ...) would run: *ranges_per_row receives
+ * the token ranges each row's adjoint is cut into (joined by the adjoint
+ * summaries when more than 1), *launches the number of kernel launches of
+ * the call (zero-fills of the accumulated outputs, the checkpoint pass unless
+ * g->ckpt is given, the summaries, the adjoint; with the step options or the
+ * convolution also the float32 preparation, bfloat16 widening of B and C and
+ * the chain rule, and the passes once per direction). Reads only sizes,
+ * dstate, dir_flags, the option fields of `a` and which pointers of `g` are
+ * set; touches no device. 0 and 0 for an empty problem.
+ */
+int vssm_scan_grad_plan_query(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len,
+                              int *ranges_per_row, int *launches);
+
+/* Bytes of the checkpoints of vssm_scan_train:
+ * 64 * directions * batch * ceil(dim / 32) * 32 * ceil(seqlen / 4). */
+int vssm_scan_ckpt_size(const vssm_scan_args *a, size_t *bytes);
 
 /*
  * Synchronises `stream`, then reads and clears this device's error word.
