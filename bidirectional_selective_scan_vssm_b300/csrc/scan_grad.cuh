@@ -233,9 +233,10 @@ struct GradLayout {
     static constexpr int ES = (int)sizeof(T);
     static constexpr bool BIDIR = DIRS == 3;
     // one ring stage: this lane's 16-byte blocks of delta, x, z, dout over the
-    // chunk (row slots of SLOT bytes), B and C of the chunk (raw), the
-    // chunk's checkpoint [16][32] fp32 and, both directions, the partner's
-    // partial gradients [kTG][3][32] fp32 (copied in the last phase only)
+    // chunk (row slots of SLOT bytes), B and C of the chunk (raw). The chunk's
+    // checkpoint and the partner's partial gradients go to registers instead
+    // (prefetched), which keeps a warp's shared memory small enough for four
+    // two-warp CTAs per SM.
     static constexpr int SLOT = ((16 - ES) + kTG * ES + 15) / 16 * 16;
     // rows staggered by 16 bytes every 8 rows so that lanes r and r + 8 read
     // different banks
@@ -244,11 +245,10 @@ struct GradLayout {
     static constexpr int sROW = 0;
     static constexpr int sB = sROW + 4 * ROWS;
     static constexpr int sC = sB + kTG * 16 * ES;
-    static constexpr int sCK = sC + kTG * 16 * ES;
-    static constexpr int sPT = sCK + 512 * 4;                 // partner's partials [kTG][3][32]
-    static constexpr int kStage = sPT + (BIDIR ? kTG * 3 * 32 * 4 : 0);
+    static constexpr int kStage = (sC + kTG * 16 * ES + 15) / 16 * 16;
     // per warp: 2 stages, then
-    //   hb  [kTG + 1][4][32 lanes][4] states (quarter q of a lane's 16 states;
+    //   hb  [kTG][4][32 lanes][4] states entering each token of the chunk
+    //                                 (quarter q of a lane's 16 states;
     //                                 a warp's access to one quarter is 512
     //                                 contiguous bytes)
     //   bc  [kTG][32]                 B[16], C[16] of each token, fp32
@@ -257,7 +257,7 @@ struct GradLayout {
     //                                 per lane), reduced over the lanes together
     static constexpr int kTP = 68;
     static constexpr int oHB = 2 * kStage;
-    static constexpr int oBC = oHB + (kTG + 1) * 4 * 32 * 16;
+    static constexpr int oBC = oHB + kTG * 4 * 32 * 16;
     static constexpr int oTR = oBC + kTG * 32 * 4;              // two buffers
     static constexpr int kWarpBytes = oTR + 32 * kTP * 4 + 16;   // + pair barrier
     static_assert(kStage % 16 == 0 && oHB % 16 == 0 && oTR % 16 == 0, "alignment");
@@ -413,20 +413,13 @@ grad_adjoint_kernel(const GradParams p)
                 cp_async16_if(sg + Lay::sC + 16 * jj, srcC + 16 * jj, jj < nb);
             }
         }
-        {   // the checkpoint entering the chunk: 512 floats
-            const char *src = reinterpret_cast<const char *>(ck + (long long)j * 512);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) cp_async16(sg + Lay::sCK + 16 * (lane + 32 * m), src + 16 * (lane + 32 * m), 16u);
-        }
-        if (DIRS == 3 && fin) {   // the partner's partials of the chunk's tokens: len * 24 blocks
-            const char *src = reinterpret_cast<const char *>(p.part + (grp * p.L + t0) * 96);
-#pragma unroll
-            for (int m = 0; m < (kTG * 24 + 31) / 32; ++m) {
-                const int jj = lane + 32 * m;
-                cp_async16_if(sg + Lay::sPT + 16 * jj, src + 16 * jj, jj < len * 24);
-            }
-        }
         cp_async_commit();
+    };
+    // the checkpoint entering chunk j, this lane's 16 states
+    auto load_ckpt = [&](int j, f2 (&c)[8]) {
+        const float *src = ck + (long long)j * 512 + lane;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) c[q] = pack2(__ldcg(src + (2 * q) * 32), __ldcg(src + (2 * q + 1) * 32));
     };
 
     bool ok = true;
@@ -439,12 +432,38 @@ grad_adjoint_kernel(const GradParams p)
             if (chunk_of(phase, s, j)) issue((ring + s) & 1, j, fin);
             else cp_async_commit();
         }
+        f2 ckn[8];                                // the next chunk's checkpoint
+        {
+            int j0;
+            if (chunk_of(phase, 0, j0)) load_ckpt(j0, ckn);
+        }
         for (int s = 0; s < nk; ++s, ++ring) {
             const int st = ring & 1;
             unsigned char *sg = wsm + st * Lay::kStage;
             int j;
             chunk_of(phase, s, j);
             const int t0 = j * kTG, t1 = min(p.L, t0 + kTG), len = t1 - t0;
+            // this chunk's checkpoint; the next one's is fetched during this chunk
+            f2 h[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) h[q] = ckn[q];
+            {
+                int jn1;
+                if (chunk_of(phase, s + 1, jn1)) load_ckpt(jn1, ckn);
+            }
+            // the partner's partials of the chunk's tokens (last phase), in walk order
+            float ppx[kTG], ppd[kTG], ppz[kTG];
+#pragma unroll
+            for (int m = 0; m < kTG; ++m) {
+                ppx[m] = ppd[m] = ppz[m] = 0.f;
+                if (DIRS == 3 && fin && m < len) {
+                    const int i = dir == 0 ? len - 1 - m : m;
+                    const float *pp = p.part + ((grp * p.L + t0 + i) * 3) * 32 + lane;
+                    ppx[m] = __ldcg(pp);
+                    ppd[m] = __ldcg(pp + 32);
+                    ppz[m] = __ldcg(pp + 64);
+                }
+            }
             cp_async_wait<1>();
             __syncwarp();
             const uint32_t lead = (uint32_t)(((erow + t0) * ES) & 15);
@@ -462,16 +481,11 @@ grad_adjoint_kernel(const GradParams p)
                     for (int i = 0; i < 8; ++i) dst[i] = ld_as_f32(src + i);
                 }
             }
-            // recompute the chunk's states: slot 0 = entering state, slot
-            // k + 1 = state after the token at scan position k
-            f2 h[8];
-            {
-                const float *cj = reinterpret_cast<const float *>(sg + Lay::sCK);
+            // recompute the chunk's states: slot k = state entering the token
+            // at scan position k (slot 0 the checkpoint); the state after the
+            // last token stays in registers
 #pragma unroll
-                for (int q = 0; q < 8; ++q) h[q] = pack2(cj[(2 * q) * 32 + lane], cj[(2 * q + 1) * 32 + lane]);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) sts2(my_h + q * 128, h[2 * q], h[2 * q + 1]);
-            }
+            for (int q = 0; q < 4; ++q) sts2(my_h + q * 128, h[2 * q], h[2 * q + 1]);
             __syncwarp();
 #pragma unroll 1
             for (int k = 0; k < len; ++k) {
@@ -488,17 +502,20 @@ grad_adjoint_kernel(const GradParams p)
                     lds2(Bt + 4 * q, B0, B1);
                     h[2 * q] = fma2(ex2_fma2(dd, Ap[2 * q], lmd), h[2 * q], mul2(uu, B0));
                     h[2 * q + 1] = fma2(ex2_fma2(dd, Ap[2 * q + 1], lmd), h[2 * q + 1], mul2(uu, B1));
-                    sts2(my_h + ((k + 1) * 4 + q) * 128, h[2 * q], h[2 * q + 1]);
+                    if (k + 1 < len) sts2(my_h + ((k + 1) * 4 + q) * 128, h[2 * q], h[2 * q + 1]);
                 }
             }
             __syncwarp();
-            // adjoint, against the scan order; hn = state after the current token
+            // adjoint, against the scan order (walk step m at scan position
+            // k = len - 1 - m); hn = state after the current token
             f2 hn[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) lds2(my_h + (len * 4 + q) * 128, hn[2 * q], hn[2 * q + 1]);
+            for (int q = 0; q < 8; ++q) hn[q] = h[q];
             int t_prev = -1;                      // the previous token of the walk (its pair's slot 0)
-#pragma unroll 1
-            for (int k = len - 1; k >= 0; --k) {
+#pragma unroll
+            for (int m = 0; m < kTG; ++m) {
+                if (m >= len) break;
+                const int k = len - 1 - m;
                 const int i = dir == 0 ? k : len - 1 - k;
                 const int t = t0 + i;
                 const bool rs = reset_at(t, p.seg_len, dir);
@@ -506,14 +523,8 @@ grad_adjoint_kernel(const GradParams p)
                 const float xv = act ? ld_as_f32(rowv[1] + i) : 0.f;
                 const float zv = (act && hasZ) ? ld_as_f32(rowv[2] + i) : 0.f;
                 const float go = act ? ld_as_f32(rowv[3] + i) : 0.f;
-                // the partner's partials of this token (phase 1), staged with the chunk
-                float px = 0.f, pdt = 0.f, pz = 0.f;
-                if (DIRS == 3 && fin) {
-                    const float *pp = reinterpret_cast<const float *>(sg + Lay::sPT) + i * 96 + lane;
-                    px = pp[0];
-                    pdt = pp[32];
-                    pz = pp[64];
-                }
+                // the partner's partials of this token (last phase)
+                const float px = ppx[m], pdt = ppd[m], pz = ppz[m];
                 float g = 1.f, gp = 0.f;
                 if (hasZ) {
                     const float sgm = __frcp_rn(1.f + ex2_mufu(-kLog2e * zv));
@@ -526,7 +537,7 @@ grad_adjoint_kernel(const GradParams p)
                 const f2 lmd = rs ? pack2(-INFINITY, -INFINITY) : pack2(0.f, 0.f);
                 const float *Bt = bc + i * 32;
                 f2 yk2 = pack2(0.f, 0.f), sB2 = pack2(0.f, 0.f), sw2 = pack2(0.f, 0.f);
-                const int pslot = (len - 1 - k) & 1;     // slot of this token in its pair
+                const int pslot = m & 1;                 // slot of this token in its pair
                 float *trow = tr + lane * TP + pslot * 32;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
