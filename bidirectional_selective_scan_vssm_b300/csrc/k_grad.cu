@@ -39,10 +39,11 @@ cudaError_t launch_dirs(const GradParams &p, long long ngroups, int nrange, bool
     const long long units = (long long)NDIR * ngroups;
     cudaError_t e = cudaSuccess;
     if (!have_ckpt) {     // (else the training forward stored them)
-        grad_ckpt_kernel<T, DIRS><<<(unsigned)((units + 3) / 4), 128, 0, s>>>(p);
+        const long long walks = units * (p.summ ? 1 : nrange);   // independent ranges walk apart
+        grad_ckpt_kernel<T, DIRS><<<(unsigned)((walks + 3) / 4), 128, 0, s>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    if (nrange > 1) {
+    if (nrange > 1 && p.summ) {     // (ranges at folded segment starts need no summaries)
         const long long su = units * nrange;
         grad_adj_summary_kernel<T, DIRS><<<(unsigned)((su + 3) / 4), 128, 0, s>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;

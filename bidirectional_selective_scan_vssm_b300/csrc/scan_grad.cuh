@@ -61,7 +61,8 @@ struct GradParams {
     float *dA[2], *dD[2];
     float *ckpt;                        // [slot][ngroups][nch][16][32]
     float *part;                        // [ngroups][L][3][32] (both directions only)
-    float *summ;                        // [slot][ngroups][nrange][P 16 | q 16][32] (nrange > 1)
+    float *summ;                        // [slot][ngroups][nrange][P 16 | q 16][32] when ranges are
+                                        // joined by summaries; null when uncut or independent
     unsigned *err;
     int batch, dim, L, seg_len, rgroups, nch;
     int nrange, rch;                    // token ranges per row, chunks per range
@@ -81,15 +82,22 @@ __device__ __forceinline__ bool reset_at(int t, int seg_len, int dir)
     return dir == 0 ? ph == 0 : ph == seg_len - 1;
 }
 
-// Checkpoints: the state entering each 8-token chunk in this direction's
-// scan order.
+// Checkpoints: the state entering each kTG-token chunk in this direction's
+// scan order. One warp per (direction, group) walks the whole row; when the
+// ranges are independent (folded rows cut at segment starts, no summaries)
+// one warp per (direction, group, range) walks its range from zero, which is
+// exact because the range starts on a reset in either direction.
 template <typename T, int DIRS>
 __global__ void __launch_bounds__(128) grad_ckpt_kernel(const GradParams p)
 {
     constexpr int NDIR = (DIRS == 3) ? 2 : 1;
     const int lane = threadIdx.x & 31;
-    const long long u = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
-    if (u >= NDIR * p.ngroups) return;
+    const int nr = p.summ ? 1 : p.nrange;             // walks per row
+    const long long uu = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (uu >= (long long)NDIR * p.ngroups * nr) return;
+    const int rr = (int)(uu % nr);
+    const long long u = uu / nr;
+    const int clo = nr > 1 ? rr * p.rch : 0, chi = nr > 1 ? min(p.nch, clo + p.rch) : p.nch;
     const int slot = (int)(u / p.ngroups);
     const long long grp = u % p.ngroups;
     const int dir = (DIRS == 3) ? slot : (DIRS == 1 ? 0 : 1);
@@ -108,12 +116,13 @@ __global__ void __launch_bounds__(128) grad_ckpt_kernel(const GradParams p)
     float *ck = p.ckpt + ((long long)slot * p.ngroups + grp) * p.nch * 512;
     // steps and inputs of chunk s in scan order (independent loads, issued one
     // chunk ahead so that their latency overlaps the current chunk's work)
+    const int ncr = chi - clo;                                // chunks this warp walks
     auto fetch = [&](int s, float (&dtv)[kTG], float (&xv)[kTG]) {
-        const int j = dir == 0 ? s : p.nch - 1 - s;
+        const int j = dir == 0 ? clo + s : chi - 1 - s;
         const int t0 = j * kTG, t1 = min(p.L, t0 + kTG), len = t1 - t0;
 #pragma unroll
         for (int k = 0; k < kTG; ++k) {
-            const bool in = act && s < p.nch && k < len;
+            const bool in = act && s < ncr && k < len;
             const long long e = row + (dir == 0 ? t0 + k : t1 - 1 - k);
             dtv[k] = in ? gload<T>(p.delta, e) : 0.f;
             xv[k] = in ? gload<T>(p.x, e) : 0.f;
@@ -121,8 +130,8 @@ __global__ void __launch_bounds__(128) grad_ckpt_kernel(const GradParams p)
     };
     float ndt[kTG], nxv[kTG];
     fetch(0, ndt, nxv);
-    for (int s = 0; s < p.nch; ++s) {
-        const int j = dir == 0 ? s : p.nch - 1 - s;          // chunk in scan order
+    for (int s = 0; s < ncr; ++s) {
+        const int j = dir == 0 ? clo + s : chi - 1 - s;      // chunk in scan order
         float *cj = ck + (long long)j * 512;
 #pragma unroll
         for (int n = 0; n < 16; ++n) cj[n * 32 + lane] = h[n];
@@ -369,7 +378,7 @@ grad_adjoint_kernel(const GradParams p)
     // the lam entering this range, from the summaries of the ranges before it
     // in walk order (the forward direction walks right to left, the backward
     // one left to right), nearest last
-    if (p.nrange > 1 && act) {
+    if (p.summ && act) {
         const float *sg = p.summ + ((long long)slot * p.ngroups + grp) * p.nrange * 1024 + lane;
         const int n_before = dir == 0 ? p.nrange - 1 - rr : rr;
         for (int k = 0; k < n_before; ++k) {

@@ -1,6 +1,7 @@
 // C ABI of the selective-scan library (declared in include/vssm.h):
 // argument validation, planning and launch on the caller's stream.
 #include <algorithm>
+#include <numeric>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
@@ -546,6 +547,7 @@ int run(const vssm_scan_args *a, int seg_len, bool folded, int pieces_req, void 
 struct GradPlan {
     int ndir = 1, rgroups = 0, nch = 0;
     int nrange = 1, rch = 0;          // token ranges per row for the adjoint, chunks per range
+    bool summaries = false;           // ranges joined by the adjoint summaries (else independent)
     long long ngroups = 0;
     size_t ckpt_bytes = 0, part_off = 0, summ_off = 0, workspace = 0;
 };
@@ -553,10 +555,13 @@ struct GradPlan {
 // Rows are cut into ranges for the adjoint when there are too few of them
 // to fill the GPU (about two waves of the adjoint's two-warp CTAs at four
 // per SM), keeping at least 16 chunks (64 tokens) per range; the ranges are
-// joined by the adjoint summaries (grad_adj_summary_kernel).
-constexpr int kGradMaxRanges = 16, kGradMinRangeChunks = 16;
+// joined by the adjoint summaries (grad_adj_summary_kernel). Folded rows are
+// cut at segment starts instead, where the reset cuts the adjoint in both
+// directions (the decay that would carry lambda across is 0), so their
+// ranges are independent: no summaries, and as many as fill the GPU.
+constexpr int kGradMaxRanges = 16, kGradMinRangeChunks = 16, kGradMaxIndepRanges = 4096;
 
-GradPlan make_grad_plan(const vssm_scan_args *a)
+GradPlan make_grad_plan(const vssm_scan_args *a, int seg_len)
 {
     const long long kGradTargetCtas = 8LL * sm_count();
     GradPlan g;
@@ -565,12 +570,25 @@ GradPlan make_grad_plan(const vssm_scan_args *a)
     g.ngroups = (long long)a->batch * g.rgroups;
     g.nch = (a->seqlen + vssm::kTG - 1) / vssm::kTG;
     g.rch = g.nch;
-    if (g.ngroups > 0 && g.ngroups < kGradTargetCtas) {
+    // chunks per step of segment-aligned ranges: seg_len / gcd(seg_len, kTG)
+    const int unit = seg_len > 0 ? seg_len / std::gcd(seg_len, vssm::kTG) : 0;
+    if (unit > 0 && unit < g.nch && g.ngroups > 0 && g.ngroups < 2 * kGradTargetCtas) {
+        const long long want = std::min<long long>(kGradMaxIndepRanges,
+                                                   (2 * kGradTargetCtas + g.ngroups - 1) / g.ngroups);
+        long long rch = (g.nch + want - 1) / want;
+        rch = std::max<long long>(unit, (rch + unit - 1) / unit * unit);
+        const int r = (int)((g.nch + rch - 1) / rch);
+        if (r > 1) {
+            g.rch = (int)rch;
+            g.nrange = r;
+        }
+    } else if (g.ngroups > 0 && g.ngroups < kGradTargetCtas) {
         const long long want = std::min<long long>(kGradMaxRanges, (kGradTargetCtas + g.ngroups - 1) / g.ngroups);
         const int r = (int)std::min<long long>(want, g.nch / kGradMinRangeChunks);
         if (r > 1) {
             g.rch = (g.nch + r - 1) / r;
             g.nrange = (g.nch + g.rch - 1) / g.rch;
+            g.summaries = true;
         }
     }
     g.ckpt_bytes = (size_t)g.ndir * g.ngroups * g.nch * 512 * sizeof(float);
@@ -578,8 +596,8 @@ GradPlan make_grad_plan(const vssm_scan_args *a)
     const size_t part_end = a->dir_flags == 3 ? g.part_off + (size_t)g.ngroups * a->seqlen * 96 * sizeof(float)
                                               : g.ckpt_bytes;
     g.summ_off = (part_end + 255) / 256 * 256;
-    g.workspace = g.nrange > 1 ? g.summ_off + (size_t)g.ndir * g.ngroups * g.nrange * 1024 * sizeof(float)
-                               : part_end;
+    g.workspace = g.summaries ? g.summ_off + (size_t)g.ndir * g.ngroups * g.nrange * 1024 * sizeof(float)
+                              : part_end;
     return g;
 }
 
@@ -837,7 +855,7 @@ struct GradExtLayout {
     GradPlan gl;
 };
 
-GradExtLayout grad_ext_layout(const vssm_scan_args *a)
+GradExtLayout grad_ext_layout(const vssm_scan_args *a, int seg_len)
 {
     GradExtLayout w;
     const bool bf16 = a->dtype != VSSM_F32;
@@ -875,16 +893,16 @@ GradExtLayout grad_ext_layout(const vssm_scan_args *a)
     }
     vssm_scan_args one = *a;
     one.dir_flags = 1;
-    w.gl = make_grad_plan(&one);
+    w.gl = make_grad_plan(&one, seg_len);
     w.core = take(w.gl.workspace);
     w.total = cur;
     return w;
 }
 
-size_t grad_workspace(const vssm_scan_args *a)
+size_t grad_workspace(const vssm_scan_args *a, int seg_len)
 {
     if ((long long)a->batch * a->dim * a->seqlen == 0) return 0;
-    return grad_composed(a) ? grad_ext_layout(a).total : make_grad_plan(a).workspace;
+    return grad_composed(a) ? grad_ext_layout(a, seg_len).total : make_grad_plan(a, seg_len).workspace;
 }
 
 // The plain gradient's parameters common to both paths.
@@ -907,7 +925,7 @@ void grad_fill_sizes(vssm::GradParams &p, const vssm_scan_args *a, const GradPla
 cudaError_t grad_composed_launch(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len,
                                  unsigned *err, cudaStream_t s)
 {
-    const GradExtLayout w = grad_ext_layout(a);
+    const GradExtLayout w = grad_ext_layout(a, seg_len);
     char *ws = static_cast<char *>(a->workspace);
     auto at = [ws](size_t off) -> float * {
         return off == GradExtLayout::kNone ? nullptr : reinterpret_cast<float *>(ws + off);
@@ -994,7 +1012,7 @@ cudaError_t grad_composed_launch(const vssm_scan_args *a, const vssm_grad_args *
                                                          w.gl.nch * 512
                          : at(w.core);
         p.part = nullptr;
-        p.summ = w.gl.nrange > 1 ? reinterpret_cast<float *>(ws + w.core + w.gl.summ_off) : nullptr;
+        p.summ = w.gl.summaries ? reinterpret_cast<float *>(ws + w.core + w.gl.summ_off) : nullptr;
         p.err = err;
         grad_fill_sizes(p, a, w.gl, seg_len);
         e = vssm::launch_grad(p, 1 << k, true, w.gl.ngroups, w.gl.nrange, g->ckpt != nullptr, s);
@@ -1178,7 +1196,7 @@ int vssm_scan_grad_workspace_size(const vssm_scan_args *a, int seg_len, size_t *
     if (a->batch < 0 || a->dim < 0 || a->seqlen < 0 || a->dir_flags < 1 || a->dir_flags > 3 ||
         seg_len < 0 || a->conv_k < 0 || a->conv_k > vssm::kMaxConv)
         return fail(VSSM_ERR_INVALID_ARG, "invalid sizes, dir_flags or conv_k");
-    *bytes = grad_workspace(a);
+    *bytes = grad_workspace(a, seg_len);
     return VSSM_OK;
 }
 
@@ -1225,8 +1243,8 @@ int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len
             return fail(VSSM_ERR_INVALID_ARG, "ckpt of %zu bytes required, %zu given", ckpt_bytes(a), g->ckpt_bytes);
     }
     const bool composed = grad_composed(a);
-    const GradPlan gl = composed ? grad_ext_layout(a).gl : make_grad_plan(a);
-    const size_t need = grad_workspace(a);
+    const GradPlan gl = composed ? grad_ext_layout(a, seg_len).gl : make_grad_plan(a, seg_len);
+    const size_t need = grad_workspace(a, seg_len);
     if (!a->workspace || a->workspace_bytes < need)
         return fail(VSSM_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given", need,
                     a->workspace ? a->workspace_bytes : (size_t)0);
@@ -1305,7 +1323,7 @@ int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len
         p.ckpt = g->ckpt ? const_cast<float *>(g->ckpt) : static_cast<float *>(a->workspace);
         p.part = dirs == 3 ? reinterpret_cast<float *>(static_cast<char *>(a->workspace) + gl.part_off)
                            : nullptr;
-        p.summ = gl.nrange > 1 ? reinterpret_cast<float *>(static_cast<char *>(a->workspace) + gl.summ_off)
+        p.summ = gl.summaries ? reinterpret_cast<float *>(static_cast<char *>(a->workspace) + gl.summ_off)
                                : nullptr;
         p.err = err;
         grad_fill_sizes(p, a, gl, seg_len);
@@ -1336,7 +1354,7 @@ int vssm_scan_grad_plan_query(const vssm_scan_args *a, const vssm_grad_args *g, 
     for (const void *z : zs) n += z != nullptr;
     const int per_dir_extra = g->ckpt ? 0 : 1;   // the checkpoint pass
     if (grad_composed(a)) {
-        const GradExtLayout w = grad_ext_layout(a);
+        const GradExtLayout w = grad_ext_layout(a, seg_len);
         n += 2;                                  // prep, post
         for (int k = 0; k < 2; ++k) {
             if (!(dirs & (1u << k))) continue;
@@ -1344,12 +1362,12 @@ int vssm_scan_grad_plan_query(const vssm_scan_args *a, const vssm_grad_args *g, 
                 n += (k == 0 || !(dirs & 1) || w.B32[1] != w.B32[0]) ? 1 : 0;
                 n += (k == 0 || !(dirs & 1) || w.C32[1] != w.C32[0]) ? 1 : 0;
             }
-            n += per_dir_extra + (w.gl.nrange > 1 ? 1 : 0) + 1;
+            n += per_dir_extra + (w.gl.summaries ? 1 : 0) + 1;
         }
         *ranges_per_row = w.gl.nrange;
     } else {
-        const GradPlan gl = make_grad_plan(a);
-        n += per_dir_extra + (gl.nrange > 1 ? 1 : 0) + 1;
+        const GradPlan gl = make_grad_plan(a, seg_len);
+        n += per_dir_extra + (gl.summaries ? 1 : 0) + 1;
         *ranges_per_row = gl.nrange;
     }
     *launches = n;

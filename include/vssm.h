@@ -313,7 +313,9 @@ int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len
  * directions (both directions only), channels rounded up to groups of 32.
  * When there are too few 32-channel groups to fill the GPU, the rows are cut
  * into token ranges for the adjoint, and 128 bytes per range, channel and
- * direction hold the ranges' adjoint summaries.
+ * direction hold the ranges' adjoint summaries; folded rows (seg_len > 0) are
+ * cut at segment starts instead, into ranges the reset makes independent,
+ * which need no summaries.
  * With the step options or the convolution the directions run one after the
  * other and share one direction's workspace of the above, after float32
  * intermediates of 4 bytes per token and channel each, per direction run:

@@ -110,14 +110,28 @@ def test_grad_long_rows_cut_into_ranges(dtype, dirs):
 
 
 @pytest.mark.parametrize("dirs", [DIR_FWD, DIR_BWD, DIR_BOTH])
-def test_grad_long_folded_rows_cut_into_ranges(dirs):
-    """Folded rows of 20 segments of 51 tokens, cut into ranges that start and
-    end inside segments: the resets must cut the adjoint carry between ranges."""
-    wl = WORKLOADS["sf_folded"].scaled(batch=1, dim=40, seqlen=51 * 20, seg_len=51, dtype="f32",
+@pytest.mark.parametrize("seg,nseg", [(51, 20), (5, 200), (1, 700)])
+def test_grad_long_folded_rows_cut_into_ranges(dirs, seg, nseg):
+    """Folded rows with few channel groups: the adjoint (and the checkpoint
+    pass) cut each row into independent ranges at segment starts, where the
+    reset stops the adjoint in both directions. Ranges are multiples of
+    lcm(seg, 4) tokens: 204 for 51-token segments, 20 for 5, 4 for 1."""
+    wl = WORKLOADS["sf_folded"].scaled(batch=1, dim=40, seqlen=seg * nseg, seg_len=seg, dtype="f32",
                                        dirs=dirs)
-    inp = make_inputs(wl, seed=850)
-    got, ref = _run(inp, dirs, seg_len=51)
-    _compare(got, ref, "f32", "folded ranges")
+    inp = make_inputs(wl, seed=850 + seg)
+    got, ref = _run(inp, dirs, seg_len=seg)
+    _compare(got, ref, "f32", f"folded ranges seg={seg}")
+
+
+def test_grad_folded_row_shorter_than_a_segment_uses_summaries():
+    """A forward-only folded call whose one (partial) segment is longer than
+    the row: no segment start to cut at, so the ranges are joined by the
+    adjoint summaries, with the reset only at token 0."""
+    wl = WORKLOADS["sf_folded"].scaled(batch=1, dim=40, seqlen=1001, seg_len=4096, dtype="f32",
+                                       dirs=DIR_FWD)
+    inp = make_inputs(wl, seed=855)
+    got, ref = _run(inp, DIR_FWD, seg_len=4096)
+    _compare(got, ref, "f32", "folded, summaries")
 
 
 def test_grad_long_workload_sampled():
