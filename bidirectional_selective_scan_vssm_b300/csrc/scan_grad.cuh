@@ -431,6 +431,14 @@ grad_adjoint_kernel(const GradParams p)
         for (int q = 0; q < 8; ++q) c[q] = pack2(__ldcg(src + (2 * q) * 32), __ldcg(src + (2 * q + 1) * 32));
     };
 
+    if (!act) {   // an idle lane's row slots are never copied into: zero them once
+#pragma unroll 1
+        for (int st = 0; st < 2; ++st)
+            for (int a = 0; a < 4; ++a) {
+                uint4 *r = reinterpret_cast<uint4 *>(wsm + st * Lay::kStage + Lay::sROW + Lay::row_off(a, lane));
+                for (int k = 0; k < Lay::SLOT / 16; ++k) r[k] = make_uint4(0u, 0u, 0u, 0u);
+            }
+    }
     bool ok = true;
     int ring = 0;
     for (int phase = 0; phase < nphase && ok; ++phase) {
@@ -496,11 +504,11 @@ grad_adjoint_kernel(const GradParams p)
 #pragma unroll
             for (int q = 0; q < 4; ++q) sts2(my_h + q * 128, h[2 * q], h[2 * q + 1]);
             __syncwarp();
-#pragma unroll 1
-            for (int k = 0; k < len; ++k) {
+            // (rows of idle lanes hold zeros: every per-token value below is 0 there)
+            auto rec_step = [&](int k, bool store) {
                 const int i = dir == 0 ? k : len - 1 - k;
-                const float dt = act ? ld_as_f32(rowv[0] + i) : 0.f;
-                const float ux = act ? dt * ld_as_f32(rowv[1] + i) : 0.f;
+                const float dt = ld_as_f32(rowv[0] + i);
+                const float ux = dt * ld_as_f32(rowv[1] + i);
                 const bool rs = reset_at(t0 + i, p.seg_len, dir);
                 const f2 dd = pack2(dt, dt), uu = pack2(ux, ux);
                 const f2 lmd = rs ? pack2(-INFINITY, -INFINITY) : pack2(0.f, 0.f);
@@ -511,29 +519,22 @@ grad_adjoint_kernel(const GradParams p)
                     lds2(Bt + 4 * q, B0, B1);
                     h[2 * q] = fma2(ex2_fma2(dd, Ap[2 * q], lmd), h[2 * q], mul2(uu, B0));
                     h[2 * q + 1] = fma2(ex2_fma2(dd, Ap[2 * q + 1], lmd), h[2 * q + 1], mul2(uu, B1));
-                    if (k + 1 < len) sts2(my_h + ((k + 1) * 4 + q) * 128, h[2 * q], h[2 * q + 1]);
+                    if (store) sts2(my_h + ((k + 1) * 4 + q) * 128, h[2 * q], h[2 * q + 1]);
                 }
-            }
-            __syncwarp();
+            };
             // adjoint, against the scan order (walk step m at scan position
             // k = len - 1 - m); hn = state after the current token
             f2 hn[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) hn[q] = h[q];
             int t_prev = -1;                      // the previous token of the walk (its pair's slot 0)
-#pragma unroll
-            for (int m = 0; m < kTG; ++m) {
-                if (m >= len) break;
+            auto adj_step = [&](int m, float px, float pdt, float pz) {
                 const int k = len - 1 - m;
                 const int i = dir == 0 ? k : len - 1 - k;
                 const int t = t0 + i;
                 const bool rs = reset_at(t, p.seg_len, dir);
-                const float dt = act ? ld_as_f32(rowv[0] + i) : 0.f;
-                const float xv = act ? ld_as_f32(rowv[1] + i) : 0.f;
-                const float zv = (act && hasZ) ? ld_as_f32(rowv[2] + i) : 0.f;
-                const float go = act ? ld_as_f32(rowv[3] + i) : 0.f;
-                // the partner's partials of this token (last phase)
-                const float px = ppx[m], pdt = ppd[m], pz = ppz[m];
+                const float dt = ld_as_f32(rowv[0] + i);
+                const float xv = ld_as_f32(rowv[1] + i);
+                const float zv = hasZ ? ld_as_f32(rowv[2] + i) : 0.f;
+                const float go = ld_as_f32(rowv[3] + i);
                 float g = 1.f, gp = 0.f;
                 if (hasZ) {
                     const float sgm = __frcp_rn(1.f + ex2_mufu(-kLog2e * zv));
@@ -601,6 +602,33 @@ grad_adjoint_kernel(const GradParams p)
                     st_from_f32(static_cast<T *>(p.dx) + e, gx);
                     st_from_f32(static_cast<T *>(p.ddelta) + e, gdt);
                     if (hasZ) st_from_f32(static_cast<T *>(p.dz) + e, gz);
+                }
+            };
+            if (len == kTG) {                     // a whole chunk: straight-line code
+#pragma unroll
+                for (int k = 0; k < kTG; ++k) rec_step(k, k + 1 < kTG);
+                __syncwarp();
+#pragma unroll
+                for (int q = 0; q < 8; ++q) hn[q] = h[q];
+#pragma unroll
+                for (int m = 0; m < kTG; ++m) adj_step(m, ppx[m], ppd[m], ppz[m]);
+            } else {                              // the row's last, partial chunk
+#pragma unroll 1
+                for (int k = 0; k < len; ++k) rec_step(k, k + 1 < len);
+                __syncwarp();
+#pragma unroll
+                for (int q = 0; q < 8; ++q) hn[q] = h[q];
+#pragma unroll 1
+                for (int m = 0; m < len; ++m) {
+                    float px = ppx[0], pdt = ppd[0], pz = ppz[0];
+#pragma unroll
+                    for (int u = 1; u < kTG; ++u)
+                        if (m == u) {
+                            px = ppx[u];
+                            pdt = ppd[u];
+                            pz = ppz[u];
+                        }
+                    adj_step(m, px, pdt, pz);
                 }
             }
             __syncwarp();
