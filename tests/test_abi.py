@@ -387,3 +387,68 @@ def test_grad_workspace_sizes_with_options(v):
     a = _args(v, batch=2, dim=64, seqlen=40, dtype=1, delta_softplus=1)
     assert v.lib.vssm_scan_grad_workspace_size(ctypes.byref(a), 0, ctypes.byref(n)) == 0
     assert n.value == (2 + 2 * 3 + 2) * r(tok) + 2 * r(bc) + r(one)
+
+
+def test_checkpoint_size(v):
+    """vssm_scan_ckpt_size: 16 fp32 per 4-token chunk, 32-channel group lane
+    and direction: 64 * directions * batch * ceil(dim / 32) * 32 * ceil(L / 4)."""
+    n = ctypes.c_size_t(0)
+    a = _args(v, batch=3, dim=40, seqlen=9)                      # both directions
+    assert v.lib.vssm_scan_ckpt_size(ctypes.byref(a), ctypes.byref(n)) == 0
+    assert n.value == 64 * 2 * 3 * 2 * 32 * 3
+    a = _args(v, batch=3, dim=40, seqlen=9, dir_flags=2)
+    assert v.lib.vssm_scan_ckpt_size(ctypes.byref(a), ctypes.byref(n)) == 0
+    assert n.value == 64 * 1 * 3 * 2 * 32 * 3
+    assert v.lib.vssm_scan_ckpt_size(ctypes.byref(_args(v, dir_flags=0)), ctypes.byref(n)) == -1
+
+
+def test_train_validation(v):
+    """The training forward validates its checkpoint buffer before launching
+    (fake device addresses: nothing is launched)."""
+    a = _args(v)                                                  # 1 x 4 x 8, both directions
+    n = ctypes.c_size_t(0)
+    assert v.lib.vssm_scan_ckpt_size(ctypes.byref(a), ctypes.byref(n)) == 0
+    ck = (1 << 20) * 30
+    assert v.lib.vssm_scan_train(ctypes.byref(a), 0, None, n.value, None) == -1        # NULL
+    assert v.lib.vssm_scan_train(ctypes.byref(a), 0, ck, n.value - 4, None) == -1     # short
+    assert v.lib.vssm_scan_train(ctypes.byref(a), 0, ck + 8, n.value, None) == -3     # misaligned
+    assert v.lib.vssm_scan_train(ctypes.byref(a), 0, (1 << 20) * 10, n.value, None) == -1  # on out
+    assert v.lib.vssm_scan_train(ctypes.byref(_args(v, dstate=8)), 0, ck, n.value, None) == -2
+    assert v.lib.vssm_scan_train(ctypes.byref(a), -1, ck, n.value, None) == -1
+
+
+def test_grad_plan_query(v):
+    """Launch counts of the gradient for given arguments (no device touched):
+    the zero-fills of the accumulated outputs, the checkpoint pass unless
+    checkpoints are given, the summaries when rows are cut and joined, the
+    adjoint; with the step options also the preparation, the bf16 widening
+    of B and C and the chain rule, and the passes once per direction."""
+    r, n = ctypes.c_int(0), ctypes.c_int(0)
+
+    def query(a, g, seg=0):
+        assert v.lib.vssm_scan_grad_plan_query(ctypes.byref(a), ctypes.byref(g), seg, ctypes.byref(r),
+                                               ctypes.byref(n)) == 0
+        return r.value, n.value
+
+    # 128 x 768 x 197 both directions: enough groups, whole rows. Zero-fills of
+    # dB, dC, dA_fwd, dA_bwd, dD_fwd, dD_bwd (6), checkpoints, adjoint
+    a = _args(v, batch=128, dim=768, seqlen=197)
+    g = _grad_args(v)
+    assert query(a, g) == (1, 8)
+    g.ckpt = (1 << 20) * 30
+    assert query(a, g) == (1, 7)
+    # few groups, long rows: ranges joined by the summaries (one more launch)
+    a = _args(v, batch=1, dim=384, seqlen=197)
+    g = _grad_args(v)
+    assert query(a, g) == (3, 9)
+    # folded rows with few groups: independent ranges at segment starts, no summaries
+    a = _args(v, batch=1, dim=40, seqlen=51 * 20)
+    ranges, launches = query(a, g, seg=51)
+    assert ranges > 1 and launches == 8
+    # bf16 with softplus, shared step and B/C: 6 zero-fills + ddelta_bias, prep,
+    # widen B and C once, per direction checkpoints + adjoint, post
+    a = _args(v, batch=128, dim=768, seqlen=197, dtype=1, delta_softplus=1, delta_bias=(1 << 20) * 11)
+    g = _grad_args(v, ddelta_bias=(1 << 20) * 20)
+    assert query(a, g) == (1, 7 + 1 + 2 + 2 * 2 + 1)
+    # empty problem
+    assert query(_args(v, batch=0), _grad_args(v)) == (0, 0)
