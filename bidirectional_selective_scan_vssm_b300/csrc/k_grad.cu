@@ -45,7 +45,11 @@ cudaError_t launch_dirs(const GradParams &p, long long ngroups, int nrange, bool
     }
     if (nrange > 1 && p.summ) {     // (ranges at folded segment starts need no summaries)
         const long long su = units * nrange;
-        grad_adj_summary_kernel<T, DIRS><<<(unsigned)((su + 3) / 4), 128, 0, s>>>(p);
+        const size_t ssmem = 4 * SummLayout<T>::kWarpBytes;
+        auto skern = grad_adj_summary_kernel<T, DIRS>;
+        if ((e = cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem)) != cudaSuccess)
+            return e;
+        skern<<<(unsigned)((su + 3) / 4), 128, ssmem, s>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     const size_t smem = (size_t)NDIR * GradLayout<T, DIRS>::kWarpBytes;

@@ -161,6 +161,23 @@ __global__ void __launch_bounds__(128) grad_ckpt_kernel(const GradParams p)
     }
 }
 
+// Staging of the adjoint summaries: per warp a two-stage ring of kSC-token
+// chunks; each lane copies the 16-byte blocks that cover its own row's span of
+// delta, dout (and z) into a row slot, and the chunk's C rows are copied one
+// block per lane, so that no load in the walk touches more than one line per
+// lane and token.
+template <typename T>
+struct SummLayout {
+    static constexpr int kSC = 16;                                  // tokens per chunk
+    static constexpr int ES = (int)sizeof(T);
+    static constexpr int SLOT = ((16 - ES) + kSC * ES + 15) / 16 * 16;
+    static constexpr int ROWS = 32 * SLOT + 16 * 3;                // one array's 32 rows
+    __device__ static constexpr int row_off(int a, int r) { return a * ROWS + r * SLOT + 16 * (r >> 3); }
+    static constexpr int sC = 3 * ROWS;
+    static constexpr int kStage = (sC + kSC * 16 * ES + 15) / 16 * 16;
+    static constexpr int kWarpBytes = 2 * kStage;
+};
+
 // Adjoint range summaries, for rows cut into nrange ranges of rch chunks. The
 // adjoint of a direction runs against its scan order, l_t = ds_t C_t + lam
 // and then lam = a_t l_t (a_t = exp(delta_t A), 0 at a folded reset), so a
@@ -173,9 +190,13 @@ __global__ void __launch_bounds__(128) grad_ckpt_kernel(const GradParams p)
 template <typename T, int DIRS>
 __global__ void __launch_bounds__(128) grad_adj_summary_kernel(const GradParams p)
 {
+    using Lay = SummLayout<T>;
     constexpr int NDIR = (DIRS == 3) ? 2 : 1;
+    constexpr int kSC = Lay::kSC, ES = Lay::ES;
     constexpr float kLog2e = 1.4426950408889634f;
+    extern __shared__ __align__(128) unsigned char ssm[];
     const int lane = threadIdx.x & 31;
+    unsigned char *wsm = ssm + (threadIdx.x >> 5) * Lay::kWarpBytes;
     const long long u = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
     if (u >= (long long)NDIR * p.ngroups * p.nrange) return;
     const int rr = (int)(u % p.nrange);
@@ -193,36 +214,107 @@ __global__ void __launch_bounds__(128) grad_adj_summary_kernel(const GradParams 
         Al2[n] = act ? p.A[dir][(long long)d * 16 + n] * kLog2e : 0.f;
         lam[n] = 0.f;
     }
-    const long long row = ((long long)b * p.dim + (act ? d : d0)) * p.L;
+    const long long total = (long long)p.batch * p.dim * p.L;
+    const long long erow = ((long long)b * p.dim + (act ? d : d0)) * p.L;   // element of (b, d, 0)
     const T *Cb = static_cast<const T *>(p.C[dir]) + (long long)b * p.L * 16;
     const bool hasZ = p.z != nullptr;
+    const void *arr[3] = {p.delta, p.dout, hasZ ? p.z : p.delta};
+    if (!act) {   // an idle lane's row slots are never copied into: zero them once
+        for (int st = 0; st < 2; ++st)
+            for (int a = 0; a < 3; ++a) {
+                uint4 *r = reinterpret_cast<uint4 *>(wsm + st * Lay::kStage + Lay::row_off(a, lane));
+                for (int k = 0; k < Lay::SLOT / 16; ++k) r[k] = make_uint4(0u, 0u, 0u, 0u);
+            }
+    }
+    // chunk c of the walk (against the scan order) covers tokens [c0, c1)
+    const int n = tb - ta, nc = (n + kSC - 1) / kSC;
+    auto span = [&](int c, int &c0, int &c1) {
+        if (dir == 0) {
+            c1 = tb - c * kSC;
+            c0 = max(ta, c1 - kSC);
+        } else {
+            c0 = ta + c * kSC;
+            c1 = min(tb, c0 + kSC);
+        }
+    };
+    auto issue = [&](int st, int c) {
+        unsigned char *sg = wsm + st * Lay::kStage;
+        int c0, c1;
+        span(c, c0, c1);
+        const int len = c1 - c0;
+        if (act) {
+            const uint32_t lead = (uint32_t)(((erow + c0) * ES) & 15);
+            const int nblk = (int)((lead + (uint32_t)(len * ES) + 15u) >> 4);
+            const long long avail = (total - erow - c0) * ES + lead;
+            const long long off = (long long)c0 * ES - lead;
+            for (int a = 0; a < (hasZ ? 3 : 2); ++a) {
+                const char *src = static_cast<const char *>(arr[a]) + erow * ES + off;
+                unsigned char *dst = sg + Lay::row_off(a, lane);
+                for (int k = 0; k < nblk; ++k) {
+                    const long long rem = avail - 16 * k;
+                    cp_async16(dst + 16 * k, src + 16 * k, rem >= 16 ? 16u : (uint32_t)rem);
+                }
+            }
+        }
+        const int nb = len * ES;                                    // 16-byte blocks of C rows
+        const char *srcC = reinterpret_cast<const char *>(Cb + (long long)c0 * 16);
+#pragma unroll
+        for (int m = 0; m < (kSC * ES + 31) / 32; ++m) {
+            const int jj = lane + 32 * m;
+            cp_async16_if(sg + Lay::sC + 16 * jj, srcC + 16 * jj, jj < nb);
+        }
+        cp_async_commit();
+    };
     float sdt = 0.f;
     bool cut = false;
-    for (int k = 0; k < tb - ta; ++k) {
-        const int t = dir == 0 ? tb - 1 - k : ta + k;            // against the scan order
-        const float dt = act ? gload<T>(p.delta, row + t) : 0.f;
-        const float go = act ? gload<T>(p.dout, row + t) : 0.f;
-        float ds = go;
-        if (hasZ) {
-            const float zv = act ? gload<T>(p.z, row + t) : 0.f;
-            ds = go * (zv * __frcp_rn(1.f + ex2_mufu(-kLog2e * zv)));
-        }
-        float Cv[16];
-        load16_f32(Cb + (long long)t * 16, Cv);
-        const bool rs = reset_at(t, p.seg_len, dir);
-        cut = cut || rs;
-        sdt += dt;
-#pragma unroll
-        for (int n = 0; n < 16; ++n) {
-            const float l = fmaf(ds, Cv[n], lam[n]);
-            lam[n] = (rs ? 0.f : ex2_mufu(dt * Al2[n])) * l;
-        }
+    for (int c = 0; c < 2; ++c) {
+        if (c < nc) issue(c, c);
+        else cp_async_commit();
     }
+    for (int c = 0; c < nc; ++c) {
+        const int st = c & 1;
+        const unsigned char *sg = wsm + st * Lay::kStage;
+        int c0, c1;
+        span(c, c0, c1);
+        const int len = c1 - c0;
+        cp_async_wait<1>();
+        __syncwarp();
+        const uint32_t lead = (uint32_t)(((erow + c0) * ES) & 15);
+        const T *rdt = reinterpret_cast<const T *>(sg + Lay::row_off(0, lane) + lead);
+        const T *rgo = reinterpret_cast<const T *>(sg + Lay::row_off(1, lane) + lead);
+        const T *rz = reinterpret_cast<const T *>(sg + Lay::row_off(2, lane) + lead);
+        const T *cs = reinterpret_cast<const T *>(sg + Lay::sC);
+#pragma unroll 2
+        for (int k = 0; k < len; ++k) {
+            const int i = dir == 0 ? len - 1 - k : k;                // against the scan order
+            const int t = c0 + i;
+            const float dt = ld_as_f32(rdt + i);
+            float ds = ld_as_f32(rgo + i);
+            if (hasZ) {
+                const float zv = ld_as_f32(rz + i);
+                ds = ds * (zv * __frcp_rn(1.f + ex2_mufu(-kLog2e * zv)));
+            }
+            float Cv[16];
+            load16_f32(cs + i * 16, Cv);
+            const bool rs = reset_at(t, p.seg_len, dir);
+            cut = cut || rs;
+            sdt += dt;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const float l = fmaf(ds, Cv[q], lam[q]);
+                lam[q] = (rs ? 0.f : ex2_mufu(dt * Al2[q])) * l;
+            }
+        }
+        __syncwarp();                                               // the stage is read
+        if (c + 2 < nc) issue(st, c + 2);
+        else cp_async_commit();
+    }
+    cp_async_wait<0>();
     float *sm = p.summ + (((long long)slot * p.ngroups + grp) * p.nrange + rr) * 1024;
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
-        sm[n * 32 + lane] = cut ? 0.f : ex2_mufu(sdt * Al2[n]);
-        sm[(16 + n) * 32 + lane] = lam[n];
+    for (int q = 0; q < 16; ++q) {
+        sm[q * 32 + lane] = cut ? 0.f : ex2_mufu(sdt * Al2[q]);
+        sm[(16 + q) * 32 + lane] = lam[q];
     }
 }
 
