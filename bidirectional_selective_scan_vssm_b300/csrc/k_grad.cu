@@ -40,7 +40,11 @@ cudaError_t launch_dirs(const GradParams &p, long long ngroups, int nrange, bool
     cudaError_t e = cudaSuccess;
     if (!have_ckpt) {     // (else the training forward stored them)
         const long long walks = units * (p.summ ? 1 : nrange);   // independent ranges walk apart
-        grad_ckpt_kernel<T, DIRS><<<(unsigned)((walks + 3) / 4), 128, 0, s>>>(p);
+        const size_t csmem = 4 * SummLayout<T>::kWarpBytes;
+        auto ckern = grad_ckpt_kernel<T, DIRS>;
+        if ((e = cudaFuncSetAttribute(ckern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem)) != cudaSuccess)
+            return e;
+        ckern<<<(unsigned)((walks + 3) / 4), 128, csmem, s>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (nrange > 1 && p.summ) {     // (ranges at folded segment starts need no summaries)

@@ -82,6 +82,24 @@ __device__ __forceinline__ bool reset_at(int t, int seg_len, int dir)
     return dir == 0 ? ph == 0 : ph == seg_len - 1;
 }
 
+// Staging of the checkpoint pass and of the adjoint summaries: per warp a
+// two-stage ring of kSC-token chunks; each lane copies the 16-byte blocks that
+// cover its own row's span of the inputs it walks (delta and x, or delta,
+// dout and z) into row slots, and the chunk's B or C rows are copied one block
+// per lane, so that no load in the walk touches more than one line per lane
+// and token.
+template <typename T>
+struct SummLayout {
+    static constexpr int kSC = 16;                                  // tokens per chunk
+    static constexpr int ES = (int)sizeof(T);
+    static constexpr int SLOT = ((16 - ES) + kSC * ES + 15) / 16 * 16;
+    static constexpr int ROWS = 32 * SLOT + 16 * 3;                // one array's 32 rows
+    __device__ static constexpr int row_off(int a, int r) { return a * ROWS + r * SLOT + 16 * (r >> 3); }
+    static constexpr int sC = 3 * ROWS;
+    static constexpr int kStage = (sC + kSC * 16 * ES + 15) / 16 * 16;
+    static constexpr int kWarpBytes = 2 * kStage;
+};
+
 // Checkpoints: the state entering each kTG-token chunk in this direction's
 // scan order. One warp per (direction, group) walks the whole row; when the
 // ranges are independent (folded rows cut at segment starts, no summaries)
@@ -111,72 +129,109 @@ __global__ void __launch_bounds__(128) grad_ckpt_kernel(const GradParams p)
         Al2[n] = act ? p.A[dir][(long long)d * 16 + n] * kLog2e : 0.f;
         h[n] = 0.f;
     }
-    const long long row = ((long long)b * p.dim + (act ? d : d0)) * p.L;
-    const char *Bb = static_cast<const char *>(p.B[dir]) + (long long)b * p.L * 16 * sizeof(T);
-    float *ck = p.ckpt + ((long long)slot * p.ngroups + grp) * p.nch * 512;
-    // steps and inputs of chunk s in scan order (independent loads, issued one
-    // chunk ahead so that their latency overlaps the current chunk's work)
-    const int ncr = chi - clo;                                // chunks this warp walks
-    auto fetch = [&](int s, float (&dtv)[kTG], float (&xv)[kTG]) {
-        const int j = dir == 0 ? clo + s : chi - 1 - s;
-        const int t0 = j * kTG, t1 = min(p.L, t0 + kTG), len = t1 - t0;
-#pragma unroll
-        for (int k = 0; k < kTG; ++k) {
-            const bool in = act && s < ncr && k < len;
-            const long long e = row + (dir == 0 ? t0 + k : t1 - 1 - k);
-            dtv[k] = in ? gload<T>(p.delta, e) : 0.f;
-            xv[k] = in ? gload<T>(p.x, e) : 0.f;
+    float *ck = p.ckpt + ((long long)slot * p.ngroups + grp) * p.nch * 512 + lane;
+    // the walk over tokens [T0, T1) in scan order, in staged chunks of kSC
+    // tokens (the inputs' row spans as 16-byte blocks into a two-stage ring,
+    // as in grad_adj_summary_kernel); the state is stored before the first
+    // token, in scan order, of every kTG-token chunk
+    using Lay = SummLayout<T>;
+    constexpr int kSC = Lay::kSC, ES = Lay::ES;
+    extern __shared__ __align__(128) unsigned char csm[];
+    unsigned char *wsm = csm + (threadIdx.x >> 5) * Lay::kWarpBytes;
+    const long long total = (long long)p.batch * p.dim * p.L;
+    const long long erow = ((long long)b * p.dim + (act ? d : d0)) * p.L;
+    const T *Bg = static_cast<const T *>(p.B[dir]) + (long long)b * p.L * 16;
+    const void *arr[2] = {p.delta, p.x};
+    if (!act) {   // an idle lane's row slots are never copied into: zero them once
+        for (int st = 0; st < 2; ++st)
+            for (int a = 0; a < 2; ++a) {
+                uint4 *r = reinterpret_cast<uint4 *>(wsm + st * Lay::kStage + Lay::row_off(a, lane));
+                for (int k = 0; k < Lay::SLOT / 16; ++k) r[k] = make_uint4(0u, 0u, 0u, 0u);
+            }
+    }
+    const int T0 = clo * kTG, T1 = min(p.L, chi * kTG);
+    const int nc = (T1 - T0 + kSC - 1) / kSC;
+    auto span = [&](int c, int &c0, int &c1) {
+        if (dir == 0) {
+            c0 = T0 + c * kSC;
+            c1 = min(T1, c0 + kSC);
+        } else {
+            c1 = T1 - c * kSC;
+            c0 = max(T0, c1 - kSC);
         }
     };
-    float ndt[kTG], nxv[kTG];
-    fetch(0, ndt, nxv);
-    for (int s = 0; s < ncr; ++s) {
-        const int j = dir == 0 ? clo + s : chi - 1 - s;      // chunk in scan order
-        float *cj = ck + (long long)j * 512;
-#pragma unroll
-        for (int n = 0; n < 16; ++n) cj[n * 32 + lane] = h[n];
-        const int t0 = j * kTG, t1 = min(p.L, t0 + kTG), len = t1 - t0;
-        float dtv[kTG], xv[kTG];
-#pragma unroll
-        for (int k = 0; k < kTG; ++k) {
-            dtv[k] = ndt[k];
-            xv[k] = nxv[k];
-        }
-        fetch(s + 1, ndt, nxv);
-#pragma unroll
-        for (int k = 0; k < kTG; ++k) {
-            if (k < len) {
-                const int t = dir == 0 ? t0 + k : t1 - 1 - k;
-                const bool rs = reset_at(t, p.seg_len, dir);
-                float Bv[16];                                   // B_t: 32 or 64 aligned bytes
-                load16_f32(reinterpret_cast<const T *>(Bb) + (long long)t * 16, Bv);
-                const float ux = dtv[k] * xv[k];
-#pragma unroll
-                for (int n = 0; n < 16; ++n) {
-                    const float a = rs ? 0.f : ex2_mufu(dtv[k] * Al2[n]);
-                    h[n] = fmaf(a, h[n], ux * Bv[n]);
+    auto issue = [&](int st, int c) {
+        unsigned char *sg = wsm + st * Lay::kStage;
+        int c0, c1;
+        span(c, c0, c1);
+        const int len = c1 - c0;
+        if (act) {
+            const uint32_t lead = (uint32_t)(((erow + c0) * ES) & 15);
+            const int nblk = (int)((lead + (uint32_t)(len * ES) + 15u) >> 4);
+            const long long avail = (total - erow - c0) * ES + lead;
+            const long long off = (long long)c0 * ES - lead;
+            for (int a = 0; a < 2; ++a) {
+                const char *src = static_cast<const char *>(arr[a]) + erow * ES + off;
+                unsigned char *dst = sg + Lay::row_off(a, lane);
+                for (int k = 0; k < nblk; ++k) {
+                    const long long rem = avail - 16 * k;
+                    cp_async16(dst + 16 * k, src + 16 * k, rem >= 16 ? 16u : (uint32_t)rem);
                 }
             }
         }
+        const int nb = len * ES;                                    // 16-byte blocks of B rows
+        const char *srcB = reinterpret_cast<const char *>(Bg + (long long)c0 * 16);
+#pragma unroll
+        for (int m = 0; m < (kSC * ES + 31) / 32; ++m) {
+            const int jj = lane + 32 * m;
+            cp_async16_if(sg + Lay::sC + 16 * jj, srcB + 16 * jj, jj < nb);
+        }
+        cp_async_commit();
+    };
+    for (int c = 0; c < 2; ++c) {
+        if (c < nc) issue(c, c);
+        else cp_async_commit();
     }
+    for (int c = 0; c < nc; ++c) {
+        const int st = c & 1;
+        const unsigned char *sg = wsm + st * Lay::kStage;
+        int c0, c1;
+        span(c, c0, c1);
+        const int len = c1 - c0;
+        cp_async_wait<1>();
+        __syncwarp();
+        const uint32_t lead = (uint32_t)(((erow + c0) * ES) & 15);
+        const T *rdt = reinterpret_cast<const T *>(sg + Lay::row_off(0, lane) + lead);
+        const T *rx = reinterpret_cast<const T *>(sg + Lay::row_off(1, lane) + lead);
+        const T *bs = reinterpret_cast<const T *>(sg + Lay::sC);
+#pragma unroll 2
+        for (int k = 0; k < len; ++k) {
+            const int i = dir == 0 ? k : len - 1 - k;               // scan order
+            const int t = c0 + i;
+            const bool first = dir == 0 ? (t % kTG) == 0 : ((t % kTG) == kTG - 1 || t == p.L - 1);
+            if (first) {
+                float *cj = ck + (long long)(t / kTG) * 512;
+#pragma unroll
+                for (int n = 0; n < 16; ++n) cj[n * 32] = h[n];
+            }
+            const bool rs = reset_at(t, p.seg_len, dir);
+            const float dt = ld_as_f32(rdt + i);
+            const float ux = dt * ld_as_f32(rx + i);
+            float Bv[16];
+            load16_f32(bs + i * 16, Bv);
+#pragma unroll
+            for (int n = 0; n < 16; ++n) {
+                const float a = rs ? 0.f : ex2_mufu(dt * Al2[n]);
+                h[n] = fmaf(a, h[n], ux * Bv[n]);
+            }
+        }
+        __syncwarp();                                               // the stage is read
+        if (c + 2 < nc) issue(st, c + 2);
+        else cp_async_commit();
+    }
+    cp_async_wait<0>();
 }
 
-// Staging of the adjoint summaries: per warp a two-stage ring of kSC-token
-// chunks; each lane copies the 16-byte blocks that cover its own row's span of
-// delta, dout (and z) into a row slot, and the chunk's C rows are copied one
-// block per lane, so that no load in the walk touches more than one line per
-// lane and token.
-template <typename T>
-struct SummLayout {
-    static constexpr int kSC = 16;                                  // tokens per chunk
-    static constexpr int ES = (int)sizeof(T);
-    static constexpr int SLOT = ((16 - ES) + kSC * ES + 15) / 16 * 16;
-    static constexpr int ROWS = 32 * SLOT + 16 * 3;                // one array's 32 rows
-    __device__ static constexpr int row_off(int a, int r) { return a * ROWS + r * SLOT + 16 * (r >> 3); }
-    static constexpr int sC = 3 * ROWS;
-    static constexpr int kStage = (sC + kSC * 16 * ES + 15) / 16 * 16;
-    static constexpr int kWarpBytes = 2 * kStage;
-};
 
 // Adjoint range summaries, for rows cut into nrange ranges of rch chunks. The
 // adjoint of a direction runs against its scan order, l_t = ds_t C_t + lam
