@@ -317,8 +317,10 @@ struct WarpScan {
 #pragma unroll
                         for (int q = 0; q < NS / 2; ++q) {
                             const float2 v = unpack2(h[q]);
-                            dst[(2 * q) * 32] = act ? v.x : 0.f;
-                            dst[(2 * q + 1) * 32] = act ? v.y : 0.f;
+                            // (streaming stores: the adjoint reads them after this
+                            // kernel, long after they would have left L2 anyway)
+                            __stcs(dst + (2 * q) * 32, act ? v.x : 0.f);
+                            __stcs(dst + (2 * q + 1) * 32, act ? v.y : 0.f);
                         }
                     }
                 }
