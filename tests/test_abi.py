@@ -452,3 +452,32 @@ def test_grad_plan_query(v):
     assert query(a, g) == (1, 7 + 1 + 2 + 2 * 2 + 1)
     # empty problem
     assert query(_args(v, batch=0), _grad_args(v)) == (0, 0)
+
+
+def test_train_and_grad_empty_problems(v):
+    """An empty problem is a no-op: the training forward needs no checkpoint
+    buffer, the sizes are 0, and nothing is launched."""
+    a = _args(v, batch=0)
+    n = ctypes.c_size_t(123)
+    assert v.lib.vssm_scan_ckpt_size(ctypes.byref(a), ctypes.byref(n)) == 0 and n.value == 0
+    assert v.lib.vssm_scan_train(ctypes.byref(a), 0, None, 0, None) == 0
+    assert v.lib.vssm_scan_grad_workspace_size(ctypes.byref(a), 0, ctypes.byref(n)) == 0 and n.value == 0
+
+
+def test_grad_workspace_folded_rows_need_no_summaries(v):
+    """Folded rows with few channel groups are cut at segment starts into
+    independent ranges: the workspace is the checkpoints and the partial
+    gradients only (no range summaries), whatever the number of ranges."""
+    n = ctypes.c_size_t(0)
+    L = 51 * 20
+    a = _args(v, batch=1, dim=40, seqlen=L, dtype=0)            # both directions, 2 groups
+    assert v.lib.vssm_scan_grad_workspace_size(ctypes.byref(a), 51, ctypes.byref(n)) == 0
+    nch = (L + 3) // 4
+    ck = 2 * 2 * nch * 512 * 4
+    part = 2 * L * 96 * 4
+    r = lambda b: (b + 255) // 256 * 256
+    assert n.value == r(ck) + part
+    # the same rows unfolded are cut and joined by summaries: more workspace
+    m = ctypes.c_size_t(0)
+    assert v.lib.vssm_scan_grad_workspace_size(ctypes.byref(a), 0, ctypes.byref(m)) == 0
+    assert m.value > n.value
