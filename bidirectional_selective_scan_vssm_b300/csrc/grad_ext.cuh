@@ -18,9 +18,20 @@
 //    sigmoid), d b_k = sum_t d v_k; d pre_k = d u_k * silu'(pre_k) with
 //    silu'(p) = sigmoid(p) (1 + p (1 - sigmoid(p))); dx gathers d pre_k of
 //    the output tokens whose taps read it (the transposed convolution), and
-//    the taps' and biases' gradients sum d pre_k * x and d pre_k. One warp per
-//    (batch, channel) row; the per-channel sums are reduced over the warp and
-//    added atomically.
+//    the taps' and biases' gradients sum d pre_k * x and d pre_k. pre_k is
+//    recomputed from x rather than stored.
+//
+// Both kernels take one (batch, channel) row and a tile of 256 TPT tokens per
+// block, TPT tokens per thread (strided by the block, so that loads coalesce;
+// TPT = 4 for rows of 1024 tokens or more, else 1), with the tile's x and its halo of up to 2 (K - 1) tokens staged in
+// shared memory: the convolution's taps and the neighbours' d pre_k come from
+// there, zero outside the row, so that a tap only tests the segment (a
+// select, no branch; the tap count K is a template parameter). The step,
+// softplus and silu are the forward kernel's own functions,
+// the taps summed in its order, so that s_k and u_k are the values the forward
+// used. The per-channel sums are reduced over the block (a warp
+// reduce-scatter, then shared memory) and added with one atomic per sum and
+// block.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -28,6 +39,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace vssm {
 
@@ -39,7 +51,6 @@ struct GradExtParams {
     int batch, dim, L, seg_len, dirs;
     // float32 intermediates (workspace); null for a direction that is not run
     float *u[2];                           // input of each direction (may alias x when x is float32)
-    float *pre[2];                         // convolution argument of each direction (K > 0)
     float *st[2];                          // step of each direction (may alias the raw step)
     float *z32, *dout32;                   // float32 copies (bfloat16 I/O), else null
     const float *du[2], *dst[2], *dz[2];   // the plain gradient's outputs per direction
@@ -49,55 +60,164 @@ struct GradExtParams {
     float *dconv_w[2], *dconv_b[2];        // [dim][K], [dim]; [1] == [0] when shared, null = none
 };
 
-__device__ __forceinline__ float sigmoid_acc(float v) { return 1.f / (1.f + expf(-v)); }
-
-__device__ __forceinline__ float softplus_acc(float v)
+// sigmoid(v) = 1 / (1 + 2^(-v log2 e)); tends to 0 and 1 at the ends.
+__device__ __forceinline__ float sigmoid_f32(float v)
 {
-    return v > 20.f ? v : log1pf(expf(v));
+    return __fdividef(1.0f, 1.0f + ex2_mufu(-1.4426950408889634f * v));
 }
 
-// Source token of convolution tap j for output token t, or -1 when the tap
-// reads zero (outside the row or, folded, outside t's segment).
-__device__ __forceinline__ int conv_src(int t, int j, int K, int L, int seg_len, int rev)
+// silu'(p) = sigmoid(p) (1 + p (1 - sigmoid(p))).
+__device__ __forceinline__ float silu_grad(float p)
 {
-    const int s = rev ? t + (K - 1) - j : t - (K - 1) + j;
-    if (s < 0 || s >= L) return -1;
-    if (seg_len > 0 && s / seg_len != t / seg_len) return -1;
-    return s;
+    const float sg = sigmoid_f32(p);
+    return fmaf(p * sg, 1.f - sg, sg);
 }
 
-template <typename T>
-__global__ void __launch_bounds__(256) grad_prep_kernel(const GradExtParams p)
+// Threads per block of the preparation and chain-rule kernels, the tokens per
+// thread of long rows, and the largest halo the chain rule stages
+// (2 (K - 1) for K <= 4).
+constexpr int kExtThreads = 256;
+constexpr int kExtLongTPT = 4;
+constexpr int kExtHalo = 6;
+
+// Block -> (row, first token of the tile, tokens of the tile).
+template <int TILE>
+__device__ __forceinline__ void ext_tile(int L, long long &row, int &t0, int &tl)
 {
-    const long long n = (long long)p.batch * p.dim * p.L;
-    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
-         e += (long long)gridDim.x * blockDim.x) {
-        const long long row = e / p.L;
-        const int t = (int)(e - row * p.L);
-        const int d = (int)(row % p.dim);
-        const T *xr = static_cast<const T *>(p.x) + row * p.L;
+    const int ntile = (L + TILE - 1) / TILE;
+    row = (long long)blockIdx.x / ntile;
+    t0 = (int)((long long)blockIdx.x - row * ntile) * TILE;
+    tl = min(TILE, L - t0);
+}
+
+// Place in its segment of token t, then of t + kExtThreads, ... : one modulo
+// (t mod seg_len in [0, seg_len), also for the halo before the row, t < 0),
+// then a step of kExtThreads mod seg_len with one wrap (not folded: t itself,
+// with a segment longer than any row).
+struct SegPos {
+    int pos, step, seg;
+    __device__ __forceinline__ SegPos(int t, int seg_len)
+        : pos(t), step(kExtThreads), seg(0x7fffffff)
+    {
+        if (seg_len > 0) {
+            pos = t % seg_len;
+            if (pos < 0) pos += seg_len;
+            step = kExtThreads % seg_len;
+            seg = seg_len;
+        }
+    }
+    __device__ __forceinline__ void next()
+    {
+        pos += step;
+        if (pos >= seg) pos -= seg;
+    }
+};
+
+// Stage x[t0 - h, t0 + tl + h) of row xr as float32, zero outside the row
+// (at most R passes of the block).
+template <int R, typename T>
+__device__ __forceinline__ void stage_x(float *xs, const T *xr, int t0, int tl, int h, int L)
+{
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int i = threadIdx.x + r * kExtThreads, t = t0 - h + i;
+        if (i < tl + 2 * h) xs[i] = (t >= 0 && t < L) ? ld_as_f32(xr + t) : 0.f;
+    }
+}
+
+// The convolution argument of a token in direction k: bias + sum over the K
+// taps of w_j x_s, s = t - m (k = 0) or t + m (k = 1), m = K - 1 - j, summed
+// from the token's own tap outwards as the forward kernel does. xc points at
+// x_t in the staged tile, which reads zero outside the row; a tap outside
+// the token's segment (pos: its place in it) gets weight zero (FOLD: folded
+// rows; otherwise the staged zeros are the only bound).
+template <int K, bool FOLD>
+__device__ __forceinline__ float conv_arg(const float *xc, const float (&w)[4], float b, int k, int pos,
+                                          int seg)
+{
+    float a = b;
+#pragma unroll
+    for (int m = 0; m < K; ++m) {
+        const bool ok = !FOLD || (k ? (pos + m < seg) : (pos >= m));
+        a = fmaf(ok ? w[K - 1 - m] : 0.f, xc[k ? m : -m], a);
+    }
+    return a;
+}
+
+// Taps and biases of channel d for the directions that run.
+template <int K>
+__device__ __forceinline__ void ext_weights(const GradExtParams &p, int d, float (&w)[2][4], float (&cb)[2],
+                                            float (&sb)[2])
+{
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        w[k][0] = w[k][1] = w[k][2] = w[k][3] = 0.f;
+        cb[k] = sb[k] = 0.f;
+        if (!(p.dirs & (1 << k))) continue;
+#pragma unroll
+        for (int j = 0; j < K; ++j) w[k][j] = p.conv_w[k][(long long)d * K + j];
+        if (K > 0 && p.conv_b[k]) cb[k] = p.conv_b[k][d];
+        if (p.softplus && p.bias[k]) sb[k] = p.bias[k][d];
+    }
+}
+
+template <typename T, int TPT, int K, bool FOLD>
+__global__ void __launch_bounds__(kExtThreads) grad_prep_kernel(const GradExtParams p)
+{
+    constexpr int kTile = kExtThreads * TPT;
+    constexpr int H = K > 0 ? K - 1 : 0;
+    __shared__ float xs[kTile + 2 * H + 1];
+    long long row;
+    int t0, tl;
+    ext_tile<kTile>(p.L, row, t0, tl);
+    const int d = (int)(row % p.dim);
+    const long long base = row * p.L;
+    const T *xr = static_cast<const T *>(p.x) + base;
+    float w[2][4], cb[2], sb[2];
+    ext_weights<K>(p, d, w, cb, sb);
+    // this thread's tokens: loads first (the stores below may alias them for
+    // all the compiler knows), then x staged, then the step and input maps
+    const bool own_st1 = p.st[1] != p.st[0], own_u1 = p.u[1] != p.u[0];
+    // (the thread's r-th token is eb + r kExtThreads: constant offsets)
+    const long long eb = base + t0 + threadIdx.x;
+    float gv[2][TPT], gz[TPT], go[TPT], gx[TPT];
+#pragma unroll
+    for (int r = 0; r < TPT; ++r) {
+        const int o = r * kExtThreads;
+        const bool in = (int)threadIdx.x + o < tl;
+        gz[r] = go[r] = gx[r] = 0.f;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            gv[k][r] = 0.f;
+            if (in && (p.dirs & (1 << k)) && (p.softplus || sizeof(T) == 2) && (k == 0 || own_st1))
+                gv[k][r] = ld_as_f32(static_cast<const T *>(p.delta[k]) + eb + o);
+        }
+        if (in && p.z32) gz[r] = ld_as_f32(static_cast<const T *>(p.z) + eb + o);
+        if (in && p.dout32) go[r] = ld_as_f32(static_cast<const T *>(p.dout) + eb + o);
+        if (in && K == 0 && sizeof(T) == 2) gx[r] = ld_as_f32(static_cast<const T *>(p.x) + eb + o);
+    }
+    if (K > 0) {
+        stage_x<TPT + 1>(xs, xr, t0, tl, H, p.L);
+        __syncthreads();
+    }
+    SegPos sp(t0 + (int)threadIdx.x, FOLD ? p.seg_len : 0);
+#pragma unroll
+    for (int r = 0; r < TPT; ++r, sp.next()) {
+        const int o = r * kExtThreads, i = (int)threadIdx.x + o;
+        if (i >= tl) break;
+        const long long e = eb + o;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             if (!(p.dirs & (1 << k))) continue;
-            if ((p.softplus || sizeof(T) == 2) && (k == 0 || p.st[1] != p.st[0])) {
-                float v = ld_as_f32(static_cast<const T *>(p.delta[k]) + e);
-                if (p.softplus) v = softplus_acc(v + (p.bias[k] ? p.bias[k][d] : 0.f));
-                p.st[k][e] = v;
-            }
-            if (p.K > 0) {
-                float a = p.conv_b[k] ? p.conv_b[k][d] : 0.f;
-                for (int j = 0; j < p.K; ++j) {
-                    const int s = conv_src(t, j, p.K, p.L, p.seg_len, k);
-                    if (s >= 0) a = fmaf(p.conv_w[k][(long long)d * p.K + j], ld_as_f32(xr + s), a);
-                }
-                p.pre[k][e] = a;
-                p.u[k][e] = a * sigmoid_acc(a);
-            } else if (sizeof(T) == 2 && (k == 0 || p.u[1] != p.u[0])) {
-                p.u[k][e] = ld_as_f32(xr + t);
-            }
+            if ((p.softplus || sizeof(T) == 2) && (k == 0 || own_st1))
+                p.st[k][e] = p.softplus ? softplus_f32(gv[k][r] + sb[k]) : gv[k][r];
+            if (K > 0)
+                p.u[k][e] = silu_f32<T>(conv_arg<K, FOLD>(xs + H + i, w[k], cb[k], k, sp.pos, sp.seg));
+            else if (sizeof(T) == 2 && (k == 0 || own_u1))
+                p.u[k][e] = gx[r];
         }
-        if (p.z32) p.z32[e] = ld_as_f32(static_cast<const T *>(p.z) + e);
-        if (p.dout32) p.dout32[e] = ld_as_f32(static_cast<const T *>(p.dout) + e);
+        if (p.z32) p.z32[e] = gz[r];
+        if (p.dout32) p.dout32[e] = go[r];
     }
 }
 
@@ -109,57 +229,122 @@ __global__ void __launch_bounds__(256) widen_f32_kernel(const T *src, float *dst
         dst[i] = ld_as_f32(src + i);
 }
 
-template <typename T>
-__global__ void __launch_bounds__(128) grad_post_kernel(const GradExtParams p)
+// Per-channel sums of a direction: the step bias, the convolution bias and the
+// K <= 4 taps (slots 6, 7 unused).
+constexpr int kExtSums = 8;
+
+// Reduce-scatter of 16 values over the warp: on return lane l's v[0] holds the
+// warp's total of value l / 2 (each halving step sends one half of the values
+// to the partner lane and keeps the other; a last step adds the lane pair).
+__device__ __forceinline__ float warp_reduce_scatter16(float (&v)[16], int lane)
 {
-    const int lane = threadIdx.x & 31;
-    const long long row = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
-    if (row >= (long long)p.batch * p.dim) return;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const int half = 8 >> s, o = 16 >> s;
+        const bool up = lane & o;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (i >= half) break;
+            const float send = up ? v[i] : v[i + half];
+            const float keep = up ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
+template <typename T, int TPT, int K, bool FOLD>
+__global__ void __launch_bounds__(kExtThreads) grad_post_kernel(const GradExtParams p)
+{
+    constexpr int kTile = kExtThreads * TPT;
+    constexpr int H = K > 0 ? K - 1 : 0;
+    __shared__ float xs[kTile + 4 * H + 1];
+    __shared__ float dps[2][kTile + 2 * H + 1];   // d pre_k of tokens t0 - H ...
+    __shared__ float red[kExtThreads / 32][2 * kExtSums];
+    long long row;
+    int t0, tl;
+    ext_tile<kTile>(p.L, row, t0, tl);
     const int d = (int)(row % p.dim);
+    const int tid = threadIdx.x, lane = tid & 31;
     const long long base = row * p.L;
     const T *xr = static_cast<const T *>(p.x) + base;
-    const int K = p.K;
-    float accb[2] = {0.f, 0.f}, acccb[2] = {0.f, 0.f};
-    float accw[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    float bias[2];
+    float w[2][4], cb[2], sb[2];
+    ext_weights<K>(p, d, w, cb, sb);
+    // this thread's tokens: loads first (before the staging, to overlap it)
+    // (the thread's r-th token is eb + r kExtThreads: constant offsets)
+    const long long eb = base + t0 + tid;
+    float gs[2][TPT], gv[2][TPT], gz[TPT], gu[TPT];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) bias[k] = (p.softplus && p.bias[k]) ? p.bias[k][d] : 0.f;
-    for (int t = lane; t < p.L; t += 32) {
-        const long long e = base + t;
-        float dv[2] = {0.f, 0.f}, dxv = 0.f;
+    for (int r = 0; r < TPT; ++r) {
+        const int o = r * kExtThreads;
+        const bool in = tid + o < tl;
+        gz[r] = gu[r] = 0.f;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            gs[k][r] = gv[k][r] = 0.f;
+            if (!(p.dirs & (1 << k)) || !in) continue;
+            gs[k][r] = p.dst[k][eb + o];
+            if (p.softplus) gv[k][r] = ld_as_f32(static_cast<const T *>(p.delta[k]) + eb + o);
+            if (p.dzo) gz[r] += p.dz[k][eb + o];
+            if (K == 0) gu[r] += p.du[k][eb + o];
+        }
+    }
+    if (K > 0) {
+        // x over [t0 - 2H, t0 + tl + 2H), then d pre_k over [t0 - H, t0 + tl + H)
+        // (zero outside the row, where the direction's gradient d u_k is read as zero)
+        stage_x<TPT + 1>(xs, xr, t0, tl, 2 * H, p.L);
+        __syncthreads();
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             if (!(p.dirs & (1 << k))) continue;
-            float g = p.dst[k][e];
-            if (p.softplus) g *= sigmoid_acc(ld_as_f32(static_cast<const T *>(p.delta[k]) + e) + bias[k]);
+            const float *dur = p.du[k] + base;
+            float duv[TPT + 1];
+#pragma unroll
+            for (int r = 0; r <= TPT; ++r) {
+                const int i = tid + r * kExtThreads, tt = t0 - H + i;
+                duv[r] = (i < tl + 2 * H && tt >= 0 && tt < p.L) ? dur[tt] : 0.f;
+            }
+            SegPos sp(t0 - H + tid, FOLD ? p.seg_len : 0);
+#pragma unroll
+            for (int r = 0; r <= TPT; ++r, sp.next()) {
+                const int i = tid + r * kExtThreads;
+                if (i < tl + 2 * H)
+                    dps[k][i] = duv[r] * silu_grad(conv_arg<K, FOLD>(xs + H + i, w[k], cb[k], k, sp.pos, sp.seg));
+            }
+        }
+        __syncthreads();
+    }
+    float sums[2][kExtSums] = {};
+    SegPos sp(t0 + tid, FOLD ? p.seg_len : 0);
+#pragma unroll
+    for (int r = 0; r < TPT; ++r, sp.next()) {
+        const int o = r * kExtThreads, i = tid + o;
+        if (i >= tl) break;
+        const long long e = eb + o;
+        const int pos = sp.pos;
+        float dv[2] = {0.f, 0.f}, dxv = gu[r];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            if (!(p.dirs & (1 << k))) continue;
+            float g = gs[k][r];
+            if (p.softplus) g *= sigmoid_f32(gv[k][r] + sb[k]);
             dv[k] = g;
-            accb[k] += g;
+            sums[k][0] += g;
             if (K > 0) {
-                // taps of this token's own output (the weights' and bias's sums)
-                const float pr = p.pre[k][e];
-                const float sg = sigmoid_acc(pr);
-                const float dp = p.du[k][e] * (sg + pr * sg * (1.f - sg));
-                acccb[k] += dp;
+                const float dp = dps[k][H + i];
+                const float *xc = xs + 2 * H + i;   // x_t
+                sums[k][1] += dp;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if (j >= K) break;
-                    const int s = conv_src(t, j, K, p.L, p.seg_len, k);
-                    if (s >= 0) accw[k][j] = fmaf(dp, ld_as_f32(xr + s), accw[k][j]);
+                for (int j = 0; j < K; ++j) {
+                    const int m = K - 1 - j;
+                    // tap j of token t reads x at t -/+ m (zero outside the row)
+                    const bool tap = !FOLD || (k ? (pos + m < sp.seg) : (pos >= m));
+                    sums[k][2 + j] = fmaf(tap ? dp : 0.f, xc[k ? m : -m], sums[k][2 + j]);
+                    // output token t +/- m reads x_t with tap j (transposed
+                    // convolution; its d pre is zero outside the row)
+                    const bool out = !FOLD || (k ? (pos >= m) : (pos + m < sp.seg));
+                    dxv = fmaf(out ? w[k][j] : 0.f, dps[k][H + i + (k ? -m : m)], dxv);
                 }
-                // the output tokens whose taps read x_t (the transposed convolution)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if (j >= K) break;
-                    const int to = k ? t - (K - 1) + j : t + (K - 1) - j;
-                    if (to < 0 || to >= p.L) continue;
-                    if (p.seg_len > 0 && to / p.seg_len != t / p.seg_len) continue;
-                    const long long eo = base + to;
-                    const float po = p.pre[k][eo];
-                    const float so = sigmoid_acc(po);
-                    dxv = fmaf(p.conv_w[k][(long long)d * K + j], p.du[k][eo] * (so + po * so * (1.f - so)), dxv);
-                }
-            } else {
-                dxv += p.du[k][e];
             }
         }
         st_from_f32(static_cast<T *>(p.dx) + e, dxv);
@@ -169,33 +354,30 @@ __global__ void __launch_bounds__(128) grad_post_kernel(const GradExtParams p)
         } else {
             st_from_f32(static_cast<T *>(p.ddelta) + e, dv[0] + dv[1]);
         }
-        if (p.dzo) {
-            float s = 0.f;
-            if (p.dirs & 1) s += p.dz[0][e];
-            if (p.dirs & 2) s += p.dz[1][e];
-            st_from_f32(static_cast<T *>(p.dzo) + e, s);
-        }
+        if (p.dzo) st_from_f32(static_cast<T *>(p.dzo) + e, gz[r]);
     }
-    // per-channel sums: over the warp, then one atomic add per row
+    // per-channel sums: over the warp, then over the block, one atomic each
+    if (!p.softplus && K == 0) return;
+    float v[16];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        if (!(p.dirs & (1 << k))) continue;
-        float vb = accb[k], vc = acccb[k];
-        float vw[4] = {accw[k][0], accw[k][1], accw[k][2], accw[k][3]};
+    for (int q = 0; q < kExtSums; ++q) {
+        v[q] = sums[0][q];
+        v[kExtSums + q] = sums[1][q];
+    }
+    const float tot = warp_reduce_scatter16(v, lane);
+    if (!(lane & 1)) red[tid >> 5][lane >> 1] = tot;
+    __syncthreads();
+    if (tid < 2 * kExtSums) {
+        const int k = tid / kExtSums, q = tid % kExtSums;
+        if (!(p.dirs & (1 << k))) return;
+        float s = 0.f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            vb += __shfl_xor_sync(0xffffffffu, vb, o);
-            vc += __shfl_xor_sync(0xffffffffu, vc, o);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) vw[j] += __shfl_xor_sync(0xffffffffu, vw[j], o);
-        }
-        if (lane == 0) {
-            if (p.softplus && p.dbias[k]) atomicAdd(p.dbias[k] + d, vb);
-            if (K > 0) {
-                if (p.dconv_b[k]) atomicAdd(p.dconv_b[k] + d, vc);
-                for (int j = 0; j < K; ++j) atomicAdd(p.dconv_w[k] + (long long)d * K + j, vw[j]);
-            }
-        }
+        for (int wi = 0; wi < kExtThreads / 32; ++wi) s += red[wi][tid];
+        float *dst = nullptr;
+        if (q == 0) dst = (p.softplus && p.dbias[k]) ? p.dbias[k] + d : nullptr;
+        else if (q == 1) dst = (K > 0 && p.dconv_b[k]) ? p.dconv_b[k] + d : nullptr;
+        else if (q - 2 < K) dst = p.dconv_w[k] + (long long)d * K + (q - 2);
+        if (dst) atomicAdd(dst, s);
     }
 }
 

@@ -97,12 +97,58 @@ unsigned stride_blocks(long long n)
     return (unsigned)std::min<long long>((n + 255) / 256, 148LL * 16);
 }
 
+// One block per (row, tile of 256 TPT tokens); 4 tokens per thread on rows of
+// 1024 tokens or more; the tap count and whether rows are folded as template
+// parameters.
+template <template <typename, int, int, bool> class KL, typename T, int TPT>
+void ext_launch_k(unsigned blocks, const GradExtParams &p, cudaStream_t s)
+{
+    const bool fold = p.seg_len > 0;
+    switch (p.K) {
+    case 0: KL<T, TPT, 0, false>::run(blocks, p, s); break;
+    case 1: fold ? KL<T, TPT, 1, true>::run(blocks, p, s) : KL<T, TPT, 1, false>::run(blocks, p, s); break;
+    case 2: fold ? KL<T, TPT, 2, true>::run(blocks, p, s) : KL<T, TPT, 2, false>::run(blocks, p, s); break;
+    case 3: fold ? KL<T, TPT, 3, true>::run(blocks, p, s) : KL<T, TPT, 3, false>::run(blocks, p, s); break;
+    default: fold ? KL<T, TPT, 4, true>::run(blocks, p, s) : KL<T, TPT, 4, false>::run(blocks, p, s); break;
+    }
+}
+
+template <template <typename, int, int, bool> class KL>
+void ext_launch(const GradExtParams &p, bool f32, cudaStream_t s)
+{
+    const long long rows = (long long)p.batch * p.dim;
+    if (p.L >= kExtThreads * kExtLongTPT) {
+        constexpr int tile = kExtThreads * kExtLongTPT;
+        const unsigned blocks = (unsigned)(rows * ((p.L + tile - 1) / tile));
+        if (f32) ext_launch_k<KL, float, kExtLongTPT>(blocks, p, s);
+        else ext_launch_k<KL, __nv_bfloat16, kExtLongTPT>(blocks, p, s);
+    } else {
+        const unsigned blocks = (unsigned)(rows * ((p.L + kExtThreads - 1) / kExtThreads));
+        if (f32) ext_launch_k<KL, float, 1>(blocks, p, s);
+        else ext_launch_k<KL, __nv_bfloat16, 1>(blocks, p, s);
+    }
+}
+
+template <typename T, int TPT, int K, bool FOLD>
+struct PrepLaunch {
+    static void run(unsigned blocks, const GradExtParams &p, cudaStream_t s)
+    {
+        grad_prep_kernel<T, TPT, K, FOLD><<<blocks, kExtThreads, 0, s>>>(p);
+    }
+};
+
+template <typename T, int TPT, int K, bool FOLD>
+struct PostLaunch {
+    static void run(unsigned blocks, const GradExtParams &p, cudaStream_t s)
+    {
+        grad_post_kernel<T, TPT, K, FOLD><<<blocks, kExtThreads, 0, s>>>(p);
+    }
+};
+
 cudaError_t launch_grad_ext_prep(const GradExtParams &p, bool f32, cudaStream_t s)
 {
-    const long long n = (long long)p.batch * p.dim * p.L;
-    if (n == 0) return cudaSuccess;
-    if (f32) grad_prep_kernel<float><<<stride_blocks(n), 256, 0, s>>>(p);
-    else grad_prep_kernel<__nv_bfloat16><<<stride_blocks(n), 256, 0, s>>>(p);
+    if ((long long)p.batch * p.dim * p.L == 0) return cudaSuccess;
+    ext_launch<PrepLaunch>(p, f32, s);
     return cudaGetLastError();
 }
 
@@ -115,11 +161,8 @@ cudaError_t launch_widen_bf16(const void *src, float *dst, long long n, cudaStre
 
 cudaError_t launch_grad_ext_post(const GradExtParams &p, bool f32, cudaStream_t s)
 {
-    const long long rows = (long long)p.batch * p.dim;
-    if (rows == 0 || p.L == 0) return cudaSuccess;
-    const unsigned blocks = (unsigned)((rows + 3) / 4);
-    if (f32) grad_post_kernel<float><<<blocks, 128, 0, s>>>(p);
-    else grad_post_kernel<__nv_bfloat16><<<blocks, 128, 0, s>>>(p);
+    if ((long long)p.batch * p.dim * p.L == 0) return cudaSuccess;
+    ext_launch<PostLaunch>(p, f32, s);
     return cudaGetLastError();
 }
 

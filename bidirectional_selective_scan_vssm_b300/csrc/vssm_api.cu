@@ -848,7 +848,7 @@ bool grad_composed(const vssm_scan_args *a)
 // the raw step (float32 I/O without convolution / softplus).
 struct GradExtLayout {
     static constexpr size_t kNone = ~(size_t)0;
-    size_t u[2] = {kNone, kNone}, pre[2] = {kNone, kNone}, st[2] = {kNone, kNone};
+    size_t u[2] = {kNone, kNone}, st[2] = {kNone, kNone};
     size_t du[2] = {kNone, kNone}, dst[2] = {kNone, kNone}, dz[2] = {kNone, kNone};
     size_t B32[2] = {kNone, kNone}, C32[2] = {kNone, kNone};
     size_t z32 = kNone, dout32 = kNone, core = 0, total = 0;
@@ -874,7 +874,6 @@ GradExtLayout grad_ext_layout(const vssm_scan_args *a, int seg_len)
         const bool second = k == 1 && (a->dir_flags & 1);
         if (a->conv_k > 0) {
             w.u[k] = take(nf);
-            w.pre[k] = take(nf);
         } else if (bf16) {
             w.u[k] = second ? w.u[0] : take(nf);
         }
@@ -954,7 +953,6 @@ cudaError_t grad_composed_launch(const vssm_scan_args *a, const vssm_grad_args *
     for (int k = 0; k < 2; ++k) {
         if (!(dirs & (1u << k))) continue;
         q.u[k] = w.u[k] != GradExtLayout::kNone ? at(w.u[k]) : const_cast<float *>(static_cast<const float *>(a->x));
-        q.pre[k] = at(w.pre[k]);
         q.st[k] = w.st[k] != GradExtLayout::kNone ? at(w.st[k])
                                                    : const_cast<float *>(static_cast<const float *>(q.delta[k]));
         q.du[k] = at(w.du[k]);

@@ -320,7 +320,7 @@ int vssm_scan_grad(const vssm_scan_args *a, const vssm_grad_args *g, int seg_len
  * other and share one direction's workspace of the above, after float32
  * intermediates of 4 bytes per token and channel each, per direction run:
  * the gradients of its step and input and, with z, its share of dz; with the
- * convolution its input and the convolution's argument; with softplus or
+ * convolution its input; with softplus or
  * bfloat16 I/O its step (one for both directions when they share step and
  * bias); with bfloat16 I/O and no convolution one input copy; with bfloat16
  * I/O float32 copies of z, dout and (per distinct tensor) B and C. Arrays

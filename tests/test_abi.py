@@ -364,8 +364,8 @@ def test_grad_workspace_sizes_with_options(v):
     """The plain gradient: 16 x 32 fp32 checkpoints per 4-token chunk, channel
     group of 32 and direction, plus 96 fp32 per token and channel group
     exchanged between the directions. With the step options or the
-    convolution: float32 intermediates per direction (input, convolution
-    argument, step, the two token gradients, the gate's share), float32
+    convolution: float32 intermediates per direction (input, step, the two
+    token gradients, the gate's share), float32
     copies of z, dout, B and C for bfloat16 I/O, then one direction's plain
     workspace."""
     n = ctypes.c_size_t(0)
@@ -377,10 +377,10 @@ def test_grad_workspace_sizes_with_options(v):
     one = ck // 2                                                 # one direction's checkpoints
     tok = 2 * 64 * 40 * 4
     r = lambda b: (b + 255) // 256 * 256
-    # float32, convolution: per direction u, pre, du, dst, dz (the raw step is read as given)
+    # float32, convolution: per direction u, du, dst, dz (the raw step is read as given)
     a = _args(v, batch=2, dim=64, seqlen=40, dtype=0, conv_k=2, conv_w=(1 << 20) * 13)
     assert v.lib.vssm_scan_grad_workspace_size(ctypes.byref(a), 0, ctypes.byref(n)) == 0
-    assert n.value == 2 * 5 * r(tok) + r(one)
+    assert n.value == 2 * 4 * r(tok) + r(one)
     # bfloat16, softplus with one shared step: one u and one st for both directions, then
     # du, dst, dz per direction, B and C copies (shared), z and dout copies
     bc = 2 * 40 * 16 * 4
