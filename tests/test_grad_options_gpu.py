@@ -191,6 +191,33 @@ def test_grad_options_long_rows_cut_into_ranges(dirs):
     _compare(got, ref, "bf16", "ranges")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dirs", [DIR_FWD, DIR_BWD, DIR_BOTH])
+@pytest.mark.parametrize("L,seg,K", [(2100, 0, 4), (1024, 0, 2), (2100, 7, 4), (2100, 300, 4),
+                                     (1024, 1, 4), (1530, 51, 1)], ids=str)
+def test_grad_options_long_tiles(dtype, dirs, L, seg, K):
+    """Rows of 1024 tokens or more, where the preparation and chain-rule
+    kernels take four tokens per thread in 1024-token tiles: halos across
+    tile edges, a ragged last tile, segments that do not divide the
+    256-token thread stride (7, 51), segments longer than it (300) and
+    one-token segments."""
+    wl = _workload(dtype, (1, 40, L), conv=K, seg_len=seg, dirs=dirs,
+                   name="sf_folded" if seg else "vim_ti_224")
+    inp = make_inputs(wl, seed=970 + L + seg + K)
+    got, ref = _run(inp, dirs, seg_len=seg)
+    _compare(got, ref, dtype, f"L={L} seg={seg} K={K}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_grad_options_long_tiles_partial_segment(dtype):
+    """Forward only (a backward reset needs whole segments): a 2101-token
+    folded row of 300 segments of 7 tokens and one of 1, in 1024-token tiles."""
+    wl = _workload(dtype, (1, 40, 2101), conv=3, seg_len=7, dirs=DIR_FWD, name="sf_folded")
+    inp = make_inputs(wl, seed=990)
+    got, ref = _run(inp, DIR_FWD, seg_len=7)
+    _compare(got, ref, dtype, "partial segment")
+
+
 def test_grad_options_workload_size_sampled():
     """Vim-S 224² (128 x 197 tokens x 768 channels, bfloat16) with own steps,
     biases and 4 taps per direction: the token gradients of one batch entry,
@@ -222,6 +249,36 @@ def test_grad_options_workload_size_sampled():
                             dout[:, dsl], delta_softplus=True, **chan)
     for k in ("dA_fwd", "dA_bwd", "dD_fwd", "dD_bwd", "ddelta_bias", "ddelta_bias_bwd",
               "dconv_w", "dconv_b", "dconv_w_bwd", "dconv_b_bwd"):
+        err = normwise_rel(got[k][dsl].cpu().numpy(), refc[k])
+        assert err <= SUM_TOL["bf16"], f"{k}: {err:.3e}"
+
+
+def test_grad_options_folded_workload_sampled():
+    """The SF-Mamba batch-folded shape (1024 segments of 51 tokens in one
+    52 224-token row, 1024 channels, bfloat16, forward only) with its own
+    step, bias and 4 taps, in the launch configuration of the training
+    step: a channel's token gradients and per-channel sums depend only on its
+    own parameters and the shared B and C, so a two-channel slice of the
+    oracle checks them exactly."""
+    wl = WORKLOADS["sf_folded"].scaled(fused_step=True, conv=4)
+    inp = make_inputs(wl, seed=0)
+    t = to_device(inp)
+    dout_t, dout = _dout(inp, 6)
+    got = vssm.scan_grad(t["x"], t["delta"], t["A_fwd"], t["A_bwd"], t["B"], t["C"], t["D_fwd"],
+                         t["D_bwd"], t["z"], dout=dout_t, dirs=wl.dirs, seg_len=wl.seg_len,
+                         **_options(t))
+    opts = _options(inp)
+    dsl = slice(700, 702)
+    chan = {k: (v[:, dsl] if k == "delta_bwd" else v[dsl]) for k, v in opts.items()
+            if k != "delta_softplus"}
+    refc = oracle.scan_grad(inp.x[:, dsl], inp.delta[:, dsl], inp.A_fwd[dsl], inp.A_bwd[dsl],
+                            inp.B, inp.C, inp.D_fwd[dsl], inp.D_bwd[dsl], inp.z[:, dsl],
+                            dout[:, dsl], dirs=wl.dirs, seg_len=wl.seg_len, delta_softplus=True,
+                            **chan)
+    for k in ("dx", "ddelta", "dz"):
+        err = normwise_rel(got[k][:, dsl].float().cpu().numpy(), refc[k])
+        assert err <= TOL["bf16"], f"{k} of channels 700-701: {err:.3e}"
+    for k in ("dA_fwd", "dD_fwd", "ddelta_bias", "dconv_w", "dconv_b"):
         err = normwise_rel(got[k][dsl].cpu().numpy(), refc[k])
         assert err <= SUM_TOL["bf16"], f"{k}: {err:.3e}"
 
