@@ -87,14 +87,14 @@ cudaError_t launch_grad(const GradParams &p, int dirs, bool f32, long long ngrou
 cudaError_t launch_zero_f32(float *p, size_t n, cudaStream_t s)
 {
     if (!p || n == 0) return cudaSuccess;
-    const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, 148 * 8);
+    const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)sm_count() * 8);
     zero_f32_kernel<<<blocks, 256, 0, s>>>(p, (long long)n);
     return cudaGetLastError();
 }
 
 unsigned stride_blocks(long long n)
 {
-    return (unsigned)std::min<long long>((n + 255) / 256, 148LL * 16);
+    return (unsigned)std::min<long long>((n + 255) / 256, 16LL * sm_count());
 }
 
 // One block per (row, tile of 256 TPT tokens); 4 tokens per thread on rows of

@@ -33,6 +33,9 @@ cudaError_t launch_general(const ScanParams &p, int dirs, bool ysmem, bool f32, 
 // optional adjoint summaries (nrange > 1), adjoint.
 cudaError_t launch_grad(const GradParams &p, int dirs, bool f32, long long ngroups, int nrange, bool have_ckpt,
                         cudaStream_t s);
+// Multiprocessors of the current device (queried once per device).
+int sm_count();
+
 cudaError_t launch_zero_f32(float *p, size_t n, cudaStream_t s);
 // Gradient with the step options and the convolution: the float32 inputs of
 // each direction, a bfloat16 -> float32 copy, and the chain rule to the raw

@@ -22,6 +22,34 @@ __device__ unsigned g_vssm_device_error;
 // exits; host code reaches it only through noalloc_scratch() below.
 static __device__ __align__(256) unsigned char g_vssm_noalloc_scratch[VSSM_NOALLOC_SCRATCH_BYTES];
 
+namespace vssm {
+
+// Multiprocessors of the current device, queried once per device (148 on a
+// B300; the same figure when no device is visible, so that sizes reported
+// without a GPU match a B300).
+int sm_count()
+{
+    static std::mutex mu;
+    static int cnt[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return 148;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cnt[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+            cudaGetLastError();
+            v = 148;
+        }
+        cnt[dev] = v;
+    }
+    return cnt[dev];
+}
+
+}  // namespace vssm
+
 namespace {
 
 thread_local std::string g_last_error;
@@ -54,29 +82,7 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb)
 
 size_t al256(size_t n) { return (n + 255) / 256 * 256; }
 
-// Multiprocessors of the current device, queried once per device (148 on a
-// B300; the same figure when no device is visible, so that sizes reported
-// without a GPU match a B300).
-int sm_count()
-{
-    static std::mutex mu;
-    static int cnt[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-        cudaGetLastError();
-        return 148;
-    }
-    std::lock_guard<std::mutex> lock(mu);
-    if (!cnt[dev]) {
-        int v = 0;
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
-            cudaGetLastError();
-            v = 148;
-        }
-        cnt[dev] = v;
-    }
-    return cnt[dev];
-}
+using vssm::sm_count;
 
 // Launch plan for one call.
 struct Plan {
