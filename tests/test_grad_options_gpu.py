@@ -193,19 +193,21 @@ def test_grad_options_long_rows_cut_into_ranges(dirs):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("dirs", [DIR_FWD, DIR_BWD, DIR_BOTH])
-@pytest.mark.parametrize("L,seg,K", [(2100, 0, 4), (1024, 0, 2), (2100, 7, 4), (2100, 300, 4),
-                                     (1024, 1, 4), (1530, 51, 1)], ids=str)
-def test_grad_options_long_tiles(dtype, dirs, L, seg, K):
+@pytest.mark.parametrize("b,L,seg,K", [(1, 2100, 0, 4), (1, 1024, 0, 2), (1, 2100, 7, 4),
+                                       (1, 2100, 300, 4), (1, 1024, 1, 4), (1, 1530, 51, 1),
+                                       (2, 1100, 0, 0), (2, 1100, 50, 2)], ids=str)
+def test_grad_options_long_tiles(dtype, dirs, b, L, seg, K):
     """Rows of 1024 tokens or more, where the preparation and chain-rule
     kernels take four tokens per thread in 1024-token tiles: halos across
     tile edges, a ragged last tile, segments that do not divide the
-    256-token thread stride (7, 51), segments longer than it (300) and
-    one-token segments."""
-    wl = _workload(dtype, (1, 40, L), conv=K, seg_len=seg, dirs=dirs,
+    256-token thread stride (7, 51), segments longer than it (300),
+    one-token segments, the fused step alone (K = 0) and two batch
+    entries."""
+    wl = _workload(dtype, (b, 40, L), conv=K, seg_len=seg, dirs=dirs,
                    name="sf_folded" if seg else "vim_ti_224")
-    inp = make_inputs(wl, seed=970 + L + seg + K)
-    got, ref = _run(inp, dirs, seg_len=seg)
-    _compare(got, ref, dtype, f"L={L} seg={seg} K={K}")
+    inp = make_inputs(wl, seed=970 + b + L + seg + K)
+    got, ref = _run(inp, dirs, seg_len=seg, conv=K > 0)
+    _compare(got, ref, dtype, f"b={b} L={L} seg={seg} K={K}")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
