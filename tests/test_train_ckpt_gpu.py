@@ -143,25 +143,33 @@ def test_grad_from_train_checkpoints(dtype, dirs, shape, seg):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_grad_from_train_checkpoints_with_options(dtype):
+@pytest.mark.parametrize("shape,seg,dirs", [((2, 40, 70), 0, DIR_BOTH), ((1, 40, 2100), 0, DIR_BOTH),
+                                            ((1, 40, 2100), 7, DIR_BOTH), ((1, 40, 2101), 7, DIR_FWD)],
+                         ids=str)
+def test_grad_from_train_checkpoints_with_options(dtype, shape, seg, dirs):
     """The composed gradient (own steps with softplus and biases, 4 taps per
-    direction) reads each direction's checkpoints from the training forward."""
-    wl = WORKLOADS["vim_ti_224"].scaled(batch=2, dim=40, seqlen=70, dtype=dtype, fused_step=True,
-                                        conv=4)
-    inp = make_inputs(wl, seed=1300)
+    direction) reads each direction's checkpoints from the training forward:
+    short rows; 2100-token rows of two channel groups, which the forward
+    cuts into carry-joined ranges (the convolution's history and the
+    checkpoints continue across them); folded rows of 7-token segments,
+    whole (both directions) and with a partial last one (forward only)."""
+    b, d, L = shape
+    wl = WORKLOADS["vim_ti_224"].scaled(batch=b, dim=d, seqlen=L, dtype=dtype, fused_step=True,
+                                        conv=4, dirs=dirs)
+    inp = make_inputs(wl, seed=1300 + L + seg)
     t = to_device(inp)
     opts = dict(delta_bwd=t["delta_bwd"], delta_bias=t["delta_bias"],
                 delta_bias_bwd=t["delta_bias_bwd"], delta_softplus=True, conv_w=t["conv_w"],
                 conv_b=t["conv_b"], conv_w_bwd=t["conv_w_bwd"], conv_b_bwd=t["conv_b_bwd"])
     dout_t, dout = _dout(inp, 7)
-    _, ckpt = vssm.scan_train(*_args(t), **opts)
-    got = vssm.scan_grad(*_args(t), dout=dout_t, ckpt=ckpt, **opts)
+    _, ckpt = vssm.scan_train(*_args(t), seg_len=seg, dirs=dirs, **opts)
+    got = vssm.scan_grad(*_args(t), dout=dout_t, seg_len=seg, dirs=dirs, ckpt=ckpt, **opts)
     ref = oracle.scan_grad(inp.x, inp.delta, inp.A_fwd, inp.A_bwd, inp.B, inp.C, inp.D_fwd,
-                           inp.D_bwd, inp.z, dout, delta_bwd=inp.delta_bwd,
+                           inp.D_bwd, inp.z, dout, dirs=dirs, seg_len=seg, delta_bwd=inp.delta_bwd,
                            delta_bias=inp.delta_bias, delta_bias_bwd=inp.delta_bias_bwd,
                            delta_softplus=True, conv_w=inp.conv_w, conv_b=inp.conv_b,
                            conv_w_bwd=inp.conv_w_bwd, conv_b_bwd=inp.conv_b_bwd)
-    _compare(got, ref, dtype, "options")
+    _compare(got, ref, dtype, f"options {shape} seg={seg} dirs={dirs}")
 
 
 def test_train_rejects_short_or_missing_checkpoints():
