@@ -23,15 +23,16 @@
 //
 // Both kernels take one (batch, channel) row and a tile of 256 TPT tokens per
 // block, TPT tokens per thread (strided by the block, so that loads coalesce;
-// TPT = 4 for rows of 1024 tokens or more, else 1), with the tile's x and its halo of up to 2 (K - 1) tokens staged in
-// shared memory: the convolution's taps and the neighbours' d pre_k come from
-// there, zero outside the row, so that a tap only tests the segment (a
-// select, no branch; the tap count K is a template parameter). The step,
-// softplus and silu are the forward kernel's own functions,
-// the taps summed in its order, so that s_k and u_k are the values the forward
-// used. The per-channel sums are reduced over the block (a warp
-// reduce-scatter, then shared memory) and added with one atomic per sum and
-// block.
+// TPT = 4 for rows of 1024 tokens or more, else 1). The tile's x and its halo
+// of up to 2 (K - 1) tokens are staged in shared memory, and so are the
+// neighbours' d pre_k, both zero outside the row: a tap then needs no row
+// test, and on folded rows only a segment test (a select, not a branch). The
+// tap count K and the folding are template parameters. The step, softplus
+// and silu are the forward kernel's own functions, the taps summed in its
+// order, so that s_k and u_k are the values the forward used. Each thread
+// issues its loads before its stores. The per-channel sums are reduced over
+// the block (a warp reduce-scatter, then shared memory) and added with one
+// atomic per sum and block.
 #pragma once
 
 #include <cuda_bf16.h>
