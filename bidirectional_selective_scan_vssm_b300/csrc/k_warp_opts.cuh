@@ -32,6 +32,15 @@ cudaError_t warp_launch_dirs(const WarpScanParams &p, bool carry, long long ctas
         sk<<<(unsigned)summ_ctas, WC * 32, smem, s>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
+    if constexpr (DIRS == 3) {
+        if (!carry && p.L <= kOneStageMaxL) {   // short rows: a one-deep copy ring
+            const size_t smem1 = (size_t)W * WarpLayout<T, G, true, 1>::kWarpBytes;
+            auto k1 = warp_scan_kernel<T, G, DIRS, W, false, SP, CONV, 1>;
+            if ((e = warp_set_smem(k1, smem1)) != cudaSuccess) return e;
+            k1<<<(unsigned)ctas, W * 32, smem1, s>>>(p);
+            return cudaGetLastError();
+        }
+    }
     const size_t smem = (size_t)W * WarpLayout<T, G, DIRS == 3>::kWarpBytes;
     auto kern = carry ? warp_scan_kernel<T, G, DIRS, W, true, SP, CONV> : warp_scan_kernel<T, G, DIRS, W, false, SP, CONV>;
     if ((e = warp_set_smem(kern, smem)) != cudaSuccess) return e;

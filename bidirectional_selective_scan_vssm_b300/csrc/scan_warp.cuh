@@ -22,7 +22,8 @@
 //
 // Data movement per warp and chunk of kTC tokens: every lane copies the
 // 16-byte blocks that cover its own channel's delta, x (and z) span into a
-// row slot of a kStages-deep shared-memory ring with per-thread async copies
+// row slot of an NST-deep shared-memory ring (two chunks; one on short rows,
+// where the smaller footprint buys more warps) with per-thread async copies
 // (the tensor's final partial block is zero-filled past its end); B_t, C_t and
 // the partner's y are copied the same way, one block per lane. The scan lanes
 // read delta/x/z straight from their row slots (rows staggered across banks);
@@ -49,7 +50,12 @@ constexpr int kTC = 16;          // tokens per chunk
 #ifndef VSSM_SCAN_STAGES
 #define VSSM_SCAN_STAGES 2
 #endif
-constexpr int kStages = VSSM_SCAN_STAGES;   // depth of the copy ring
+constexpr int kStages = VSSM_SCAN_STAGES;   // depth of the copy ring (default)
+// Uncut rows of both directions and at most this many tokens use a one-deep
+// ring: their chunks are few, and the smaller footprint fits 16 warps per SM
+// instead of 12, which hides more of the per-token latency than the lost
+// copy/compute overlap costs (measured on Vim-S 224^2; longer rows lose).
+constexpr int kOneStageMaxL = 256;
 #ifndef VSSM_SCAN_UNROLL
 #define VSSM_SCAN_UNROLL 2
 #endif
@@ -85,7 +91,7 @@ struct WarpScanParams {
 constexpr int kSummFloats = 17 * 32;
 constexpr uint32_t kCutBits = 0xffffffffu;
 
-template <typename T, int G, bool BIDIR>
+template <typename T, int G, bool BIDIR, int NST = kStages>
 struct WarpLayout {
     static constexpr int RPW = 32 / G;            // channels per warp
     static constexpr int NS = 16 / G;             // states per lane
@@ -105,7 +111,7 @@ struct WarpLayout {
     static constexpr int oPY = oC + kTC * 16 * ES;
     static constexpr int kStageBytes = (oPY + (BIDIR ? kTC * RPW * 4 : 0) + 15) / 16 * 16;
     // one warp's region (bytes)
-    static constexpr int oBC = kStages * kStageBytes;   // fp32 [kTC][32]: B[16], C[16]
+    static constexpr int oBC = NST * kStageBytes;       // fp32 [kTC][32]: B[16], C[16]
     // output tile [RPW][OTP] in the output type; the pitch makes the scan's
     // column writes (one row per lane) land on distinct banks
     static constexpr int OTP = ES == 2 ? kTC + 2 : kTC + 1;
@@ -123,9 +129,9 @@ struct WarpLayout {
 // input is silu of the direction's depthwise convolution of x, computed from
 // a three-token history of x that each lane carries in registers.
 template <typename T, int G, int DIRS, int W, bool CARRY = false, bool SP = false,
-          bool CONV = false>
+          bool CONV = false, int NST = kStages>
 struct WarpScan {
-    using Lay = WarpLayout<T, G, DIRS == 3>;
+    using Lay = WarpLayout<T, G, DIRS == 3, NST>;
     static constexpr int RPW = Lay::RPW, NS = Lay::NS, ES = Lay::ES;
     static constexpr int NDIR = (DIRS == 3) ? 2 : 1;
 
@@ -599,7 +605,7 @@ struct WarpScan {
         bool cut = false;
         const bool seg = p.seg_len > 0;
         const int nk = (tb - ta + kTC - 1) / kTC;
-        for (int k = 0; k < kStages; ++k) {
+        for (int k = 0; k < NST; ++k) {
             if (k < nk) {
                 int c0, c1;
                 chunk_range(k, ta, tb, c0, c1);
@@ -609,10 +615,10 @@ struct WarpScan {
             }
         }
         for (int k = 0; k < nk; ++k) {
-            const int s = k % kStages;
+            const int s = k % NST;
             int c0, c1;
             chunk_range(k, ta, tb, c0, c1);
-            cp_async_wait<kStages - 1>();
+            cp_async_wait<NST - 1>();
             __syncwarp();
             const int len = c1 - c0;
             zero_tail(s, c0, len);
@@ -626,9 +632,9 @@ struct WarpScan {
                 if (seg) summary_chunk<1, true>(h, Ap, S, xh, s, c0, len, rmask);
                 else summary_chunk<1, false>(h, Ap, S, xh, s, c0, len, rmask);
             }
-            if (k + kStages < nk) {
+            if (k + NST < nk) {
                 int n0, n1;
-                chunk_range(k + kStages, ta, tb, n0, n1);
+                chunk_range(k + NST, ta, tb, n0, n1);
                 issue(s, n0, n1, false);
             } else {
                 cp_async_commit();
@@ -686,20 +692,20 @@ struct WarpScan {
             const int nk = (hi - lo + kTC - 1) / kTC;
             // One copy group per ring slot in flight (empty groups past the end
             // keep the group count uniform).
-            for (int k = 0; k < kStages; ++k) {
+            for (int k = 0; k < NST; ++k) {
                 if (k < nk) {
                     int c0, c1;
                     chunk_range(k, lo, hi, c0, c1);
-                    issue((kk + k) % kStages, c0, c1, fin);
+                    issue((kk + k) % NST, c0, c1, fin);
                 } else {
                     cp_async_commit();
                 }
             }
             for (int k = 0; k < nk; ++k, ++kk) {
-                const int s = kk % kStages;
+                const int s = kk % NST;
                 int c0, c1;
                 chunk_range(k, lo, hi, c0, c1);
-                cp_async_wait<kStages - 1>();
+                cp_async_wait<NST - 1>();
                 __syncwarp();
                 const int len = c1 - c0;
                 if (DIRS == 3 && fin && p.discard_y && lane < len) {
@@ -712,9 +718,9 @@ struct WarpScan {
                 const uint32_t rmask = reset_mask(c0, len);
                 scan_dispatch(fin, seg, hasZ, ck, h, Ap, Dsum, xh, s, c0, len, rmask);
                 if (fin) store_out(c0, c1);
-                if (k + kStages < nk) {
+                if (k + NST < nk) {
                     int n0, n1;
-                    chunk_range(k + kStages, lo, hi, n0, n1);
+                    chunk_range(k + NST, lo, hi, n0, n1);
                     issue(s, n0, n1, fin);
                 } else {
                     cp_async_commit();
@@ -739,26 +745,27 @@ struct WarpScan {
 
 // CTAs per SM that the shared-memory footprint allows; used as the register
 // budget hint so that registers never limit residency below it.
-template <typename T, int G, int DIRS, int W>
+template <typename T, int G, int DIRS, int W, int NST = kStages>
 constexpr int warp_scan_min_blocks()
 {
     // 228 KB of shared memory per SM, 1 KB of it reserved per CTA
-    constexpr int kb = W * WarpLayout<T, G, DIRS == 3>::kWarpBytes + 1024;
+    constexpr int kb = W * WarpLayout<T, G, DIRS == 3, NST>::kWarpBytes + 1024;
     return (228 * 1024) / kb < 1 ? 1 : ((228 * 1024) / kb > 8 ? 8 : (228 * 1024) / kb);
 }
 
 // CARRY: the row is cut into ranges that start from the state carried in by
-// warp_carry_kernel's summaries (else every range starts from zero).
-template <typename T, int G, int DIRS, int W, bool CARRY, bool SP, bool CONV>
-__global__ void __launch_bounds__(W * 32, (warp_scan_min_blocks<T, G, DIRS, W>()))
+// warp_carry_kernel's summaries (else every range starts from zero). NST:
+// depth of the copy ring.
+template <typename T, int G, int DIRS, int W, bool CARRY, bool SP, bool CONV, int NST = kStages>
+__global__ void __launch_bounds__(W * 32, (warp_scan_min_blocks<T, G, DIRS, W, NST>()))
 warp_scan_kernel(const WarpScanParams p)
 {
-    using Lay = WarpLayout<T, G, DIRS == 3>;
+    using Lay = WarpLayout<T, G, DIRS == 3, NST>;
     constexpr int NDIR = (DIRS == 3) ? 2 : 1;
     static_assert(W % NDIR == 0, "whole pairs per CTA");
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int warp = threadIdx.x >> 5;
-    WarpScan<T, G, DIRS, W, CARRY, SP, CONV> ws(p);
+    WarpScan<T, G, DIRS, W, CARRY, SP, CONV, NST> ws(p);
     ws.lane = threadIdx.x & 31;
     ws.r = ws.lane / G;
     ws.g = ws.lane % G;
