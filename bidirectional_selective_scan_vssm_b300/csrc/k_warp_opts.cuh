@@ -42,6 +42,14 @@ cudaError_t warp_launch_dirs(const WarpScanParams &p, bool carry, long long ctas
         }
     }
     const size_t smem = (size_t)W * WarpLayout<T, G, DIRS == 3>::kWarpBytes;
+    if constexpr (!(CONV && DIRS == 3)) {
+        if (!carry && p.L > kOneStageMaxL && p.ckpt == nullptr) {   // long uncut rows: wider unroll
+            auto k4 = warp_scan_kernel<T, G, DIRS, W, false, SP, CONV, kStages, kLongRowUnroll>;
+            if ((e = warp_set_smem(k4, smem)) != cudaSuccess) return e;
+            k4<<<(unsigned)ctas, W * 32, smem, s>>>(p);
+            return cudaGetLastError();
+        }
+    }
     auto kern = carry ? warp_scan_kernel<T, G, DIRS, W, true, SP, CONV> : warp_scan_kernel<T, G, DIRS, W, false, SP, CONV>;
     if ((e = warp_set_smem(kern, smem)) != cudaSuccess) return e;
     kern<<<(unsigned)ctas, W * 32, smem, s>>>(p);

@@ -60,6 +60,11 @@ constexpr int kOneStageMaxL = 256;
 #define VSSM_SCAN_UNROLL 2
 #endif
 constexpr int kUnroll = VSSM_SCAN_UNROLL;   // tokens per unrolled scan step
+// Uncut rows longer than kOneStageMaxL unroll more tokens: each warp walks
+// many chunks, and the extra independent work per step hides more latency.
+// Not taken with the convolution in both directions, nor when the training
+// forward writes checkpoints: there it measured slower (register pressure).
+constexpr int kLongRowUnroll = 4;
 
 struct WarpScanParams {
     const void *x, *delta[2], *z;  // delta: [0] forward, [1] backward step
@@ -129,7 +134,7 @@ struct WarpLayout {
 // input is silu of the direction's depthwise convolution of x, computed from
 // a three-token history of x that each lane carries in registers.
 template <typename T, int G, int DIRS, int W, bool CARRY = false, bool SP = false,
-          bool CONV = false, int NST = kStages>
+          bool CONV = false, int NST = kStages, int UNR = kUnroll>
 struct WarpScan {
     using Lay = WarpLayout<T, G, DIRS == 3, NST>;
     static constexpr int RPW = Lay::RPW, NS = Lay::NS, ES = Lay::ES;
@@ -305,11 +310,11 @@ struct WarpScan {
         const T *rd = reinterpret_cast<const T *>(st + Lay::oD + Lay::row_off(r) + lead);
         const T *rx = reinterpret_cast<const T *>(st + Lay::oX + Lay::row_off(r) + lead);
         const T *rz = reinterpret_cast<const T *>(st + Lay::oZ + Lay::row_off(r) + lead);
-        const int n4 = (len + kUnroll - 1) / kUnroll * kUnroll;   // len rounded up to the unroll
+        const int n4 = (len + UNR - 1) / UNR * UNR;   // len rounded up to the unroll
 #pragma unroll 1
-        for (int k0 = 0; k0 < n4; k0 += kUnroll) {
+        for (int k0 = 0; k0 < n4; k0 += UNR) {
 #pragma unroll
-            for (int j = 0; j < kUnroll; ++j) {
+            for (int j = 0; j < UNR; ++j) {
                 const int i = (DIR == 0) ? (k0 + j) : (n4 - 1 - k0 - j);
                 if (CK) {
                     static_assert(!CK || G == 1, "checkpoints hold one channel per lane");
@@ -378,7 +383,7 @@ struct WarpScan {
     // delta is -inf, whose softplus is exactly 0.
     __device__ void zero_tail(int s, int c0, int len)
     {
-        const int n4 = (len + kUnroll - 1) / kUnroll * kUnroll;
+        const int n4 = (len + UNR - 1) / UNR * UNR;
         if (n4 != len && (G == 1 || g == 0)) {
             unsigned char *st = stage(s);
             const uint32_t lead = lead_of(lane_emod, c0);
@@ -561,11 +566,11 @@ struct WarpScan {
         const uint32_t lead = lead_of(lane_emod, c0);
         const T *rd = reinterpret_cast<const T *>(st + Lay::oD + Lay::row_off(r) + lead);
         const T *rx = reinterpret_cast<const T *>(st + Lay::oX + Lay::row_off(r) + lead);
-        const int n4 = (len + kUnroll - 1) / kUnroll * kUnroll;
+        const int n4 = (len + UNR - 1) / UNR * UNR;
 #pragma unroll 1
-        for (int k0 = 0; k0 < n4; k0 += kUnroll) {
+        for (int k0 = 0; k0 < n4; k0 += UNR) {
 #pragma unroll
-            for (int j = 0; j < kUnroll; ++j) {
+            for (int j = 0; j < UNR; ++j) {
                 const int i = (DIR == 0) ? (k0 + j) : (n4 - 1 - k0 - j);
                 float dtv = ld_as_f32(rd + i);
                 if (SP) dtv = softplus_f32(dtv + dbias_l);
@@ -756,7 +761,8 @@ constexpr int warp_scan_min_blocks()
 // CARRY: the row is cut into ranges that start from the state carried in by
 // warp_carry_kernel's summaries (else every range starts from zero). NST:
 // depth of the copy ring.
-template <typename T, int G, int DIRS, int W, bool CARRY, bool SP, bool CONV, int NST = kStages>
+template <typename T, int G, int DIRS, int W, bool CARRY, bool SP, bool CONV, int NST = kStages,
+          int UNR = kUnroll>
 __global__ void __launch_bounds__(W * 32, (warp_scan_min_blocks<T, G, DIRS, W, NST>()))
 warp_scan_kernel(const WarpScanParams p)
 {
@@ -765,7 +771,7 @@ warp_scan_kernel(const WarpScanParams p)
     static_assert(W % NDIR == 0, "whole pairs per CTA");
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int warp = threadIdx.x >> 5;
-    WarpScan<T, G, DIRS, W, CARRY, SP, CONV, NST> ws(p);
+    WarpScan<T, G, DIRS, W, CARRY, SP, CONV, NST, UNR> ws(p);
     ws.lane = threadIdx.x & 31;
     ws.r = ws.lane / G;
     ws.g = ws.lane % G;
