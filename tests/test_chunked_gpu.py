@@ -101,6 +101,43 @@ def test_one_piece_equals_unsplit_bitwise():
     assert torch.equal(got, ref)
 
 
+def _step_opts(src, sp, conv):
+    get = (lambda k: src[k]) if isinstance(src, dict) else (lambda k: getattr(src, k))
+    kw = {}
+    if sp:
+        kw.update(delta_bwd=get("delta_bwd"), delta_bias=get("delta_bias"),
+                  delta_bias_bwd=get("delta_bias_bwd"), delta_softplus=True)
+    if conv:
+        kw.update(conv_w=get("conv_w"), conv_b=get("conv_b"), conv_w_bwd=get("conv_w_bwd"),
+                  conv_b_bwd=get("conv_b_bwd"))
+    return kw
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dirs", [DIR_FWD, DIR_BWD, DIR_BOTH])
+@pytest.mark.parametrize("L,sp,conv,seg", [(257, False, False, 0), (1001, False, False, 0),
+                                           (1030, True, False, 0), (1001, False, True, 0),
+                                           (1001, True, True, 0), (1020, False, False, 51)],
+                         ids=str)
+def test_uncut_long_rows(dtype, dirs, L, sp, conv, seg):
+    """Rows longer than 256 tokens forced uncut (pieces = 1): the forward
+    kernel's wider-unroll variant, element by element, with ragged tails
+    (L mod 4 = 1, 2), the fused step, the convolution (single directions
+    take the wider unroll with it; both directions keep the narrow one), and
+    folded rows."""
+    name = "sf_folded" if seg else "vim_ti_224"
+    wl = WORKLOADS[name].scaled(batch=2, dim=40, seqlen=L, dtype=dtype, dirs=dirs,
+                                fused_step=sp, conv=4 if conv else 0)
+    inp = make_inputs(wl, seed=310 + L + 2 * sp + conv)
+    t = to_device(inp)
+    got = vssm.scan_chunked(t["x"], t["delta"], t["A_fwd"], t["A_bwd"], t["B"], t["C"],
+                            t["D_fwd"], t["D_bwd"], t["z"], pieces=1, seg_len=seg, dirs=dirs,
+                            **_step_opts(t, sp, conv))
+    ref = oracle.scan(inp.x, inp.delta, inp.A_fwd, inp.A_bwd, inp.B, inp.C, inp.D_fwd,
+                      inp.D_bwd, inp.z, dirs=dirs, seg_len=seg, **_step_opts(inp, sp, conv))
+    _check(got, ref, dtype, f"L={L} sp={sp} conv={conv} seg={seg} dirs={dirs}")
+
+
 @pytest.mark.parametrize("workload", ["vim_ti_224", "vim_s_1024"])
 def test_library_choice_for_few_rows(workload):
     """The default entry point cuts few long rows by itself; its result
