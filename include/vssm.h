@@ -158,8 +158,10 @@ int vssm_scan_bidir(const vssm_scan_args *a, void *stream);
  * GPU idle; vssm_scan_bidir chooses the count itself.
  *
  * pieces: 0 = the library's choice (what vssm_scan_bidir / vssm_scan_folded
- * do); 1 = rows are not cut for the carry (a folded call may still be split
- * at segment starts, which needs no carry); P > 1 = rows are cut into
+ * do; a folded call is split at segment starts into as many independent
+ * ranges of whole segments as fill two waves of the warps resident at once);
+ * 1 = rows are not cut for the carry (a folded call may still be split at
+ * segment starts, which needs no carry); P > 1 = rows are cut into
  * ceil(seqlen / ceil(seqlen / P)) ranges of ceil(seqlen / P) tokens (the last
  * one shorter). P > 1 needs dstate == 16, else VSSM_ERR_UNSUPPORTED. The
  * workspace must hold vssm_scan_chunked_workspace_size bytes: the partial
