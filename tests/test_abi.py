@@ -217,6 +217,19 @@ def test_plan_query(v):
     assert _plan(v, _args(v, dstate=8), 0, 2)[0] == -2
 
 
+@pytest.mark.parametrize("b,d,nseg,seg,dirs,dt", [(1, 1024, 1024, 51, 1, 1), (2, 40, 20, 51, 3, 1),
+                                                  (8, 768, 64, 51, 3, 0), (1, 64, 300, 7, 1, 0),
+                                                  (4, 256, 1, 197, 3, 1), (1, 32, 4096, 1, 2, 1)])
+def test_folded_plan_whole_segments(v, b, d, nseg, seg, dirs, dt):
+    """The default folded plan cuts each row into independent ranges of whole
+    segments (the last one possibly shorter), one launch, at least one range
+    and at most one per segment."""
+    st, r, n = _plan(v, _args(v, batch=b, dim=d, seqlen=nseg * seg, dir_flags=dirs, dtype=dt), seg)
+    assert st == 0 and n == 1 and 1 <= r <= nseg
+    per = -(-nseg // r)                                  # segments per range
+    assert -(-nseg // per) == r
+
+
 def _grad_args(v, **kw):
     g = v.GradArgs()
     base = 1 << 30                      # fake, aligned, far from the inputs of _args
